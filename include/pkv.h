@@ -1,0 +1,203 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache attention library.
+ *
+ * Decode-phase attention over a paged KV cache, plus the cache writes that feed it:
+ *
+ *   pkv_kv_append               scatter new tokens' K/V into cache slots (slot_mapping)
+ *   pkv_kv_block_copy           copy whole blocks (copy-on-write of shared blocks)
+ *   pkv_paged_decode_attention  one query per sequence against its paged cache,
+ *                               GQA groups sharing each K/V tile, split-K with a
+ *                               log-sum-exp merge for long contexts
+ *   pkv_prefill_attention       varlen causal attention over cu_seqlens that also
+ *                               writes the cache
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Cache layout: k_cache and v_cache are each [NB][Hkv][bs][d] row-major (NB physical
+ *   blocks, Hkv KV heads, bs tokens per block, head_dim d).  The K (or V) row of the
+ *   token stored in slot s for KV head h starts at element
+ *   ((s / bs) * Hkv + h) * bs * d + (s % bs) * d.
+ *   A slot is a physical block id times bs plus the offset inside the block: logical
+ *   position pos of a sequence lives in slot block_table[pos / bs] * bs + pos % bs
+ *   (plumephp.com "KV Cache 优化与注意力机制加速：FlashAttention / PagedAttention"
+ *   §4.2-§4.3, BlockTable.get_kv).
+ * Element types: PKV_F32 (fp32) or PKV_BF16 (bf16).  Queries of decode are fp32;
+ *   outputs and lse are fp32.
+ * GQA: query head i reads KV head floor(i / m), m = Hq / Hkv consecutive query heads per
+ *   group (limoncc.com "大语言模型研究15——注意力机制优化之KV缓存" §3.3).  MHA is
+ *   Hkv == Hq, MQA is Hkv == 1.
+ * Pointers: every array argument is a DEVICE pointer on the current CUDA device unless
+ *   stated otherwise.  The caller owns all memory; the library allocates no device
+ *   memory in any call (split-K scratch is the caller's workspace).  The only library
+ *   state is one device error word per device (a static device variable).
+ * Streams: every call only enqueues work on `stream` and returns; nothing is
+ *   synchronised except in pkv_get_device_error.  NULL is the legacy default stream.
+ * Errors: arguments are validated on the host before any launch; a bad argument
+ *   returns PKV_ERR_INVALID_ARG (or PKV_ERR_UNSUPPORTED / PKV_ERR_WORKSPACE) and
+ *   enqueues nothing.  A failed launch returns PKV_ERR_CUDA.  Values that live in
+ *   device memory (slots, block ids, lengths, cu_seqlens) are checked by the kernels:
+ *   an out-of-range value skips the access it would make and sets a bit of the device
+ *   error word (PKV_DEVERR_*), read with pkv_get_device_error.  No kernel traps or
+ *   waits without a bound.  pkv_last_error() gives a message for the last failing call
+ *   of the calling thread.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,  /* null pointer, bad size, Hq % Hkv != 0, ... */
+    PKV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. an element type) */
+    PKV_ERR_WORKSPACE = 3,    /* split-K workspace missing or too small */
+    PKV_ERR_CUDA = 4          /* a CUDA runtime call or kernel launch failed */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_SLOT        1u   /* slot_mapping entry >= NB * bs (write skipped) */
+#define PKV_DEVERR_BLOCK       2u   /* block_table entry outside [0, NB) (block read as zeros) */
+#define PKV_DEVERR_LEN         4u   /* context length < 0 or > MBS * bs (sequence treated as empty) */
+#define PKV_DEVERR_CU_SEQLENS  8u   /* cu_seqlens decreasing, > T, or a sequence > max_seqlen */
+#define PKV_DEVERR_PAIR       16u   /* kv_block_copy pair outside [0, NB) (pair skipped) */
+#define PKV_DEVERR_TIMEOUT    32u   /* a bounded wait for an asynchronous copy gave up */
+
+/* Static description of a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* Message describing the last failing call on the calling thread ("" if none). */
+const char *pkv_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+/*
+ * pkv_kv_append -- write T new tokens' K and V rows into the cache.
+ *
+ * For every token t with slot_mapping[t] >= 0 and every KV head h:
+ *   K row of (slot_mapping[t], h) = k_new[t][h][:],  V row likewise from v_new.
+ * Compute only the new token's K/V and add it to the cache (limoncc.com
+ * "大语言模型研究15——注意力机制优化之KV缓存" §2; zwjcode.cn "KV Cache 的增量解码" §04,
+ * §10: write into a preallocated slot instead of concatenating).
+ *
+ *   k_new, v_new   [T][Hkv][d], element type dt (the cache's; the copy is bit-exact)
+ *   k_cache, v_cache  [NB][Hkv][bs][d] of type dt
+ *   slot_mapping   int64 [T]; a negative entry is padding (token skipped); an entry
+ *                  >= NB * bs sets PKV_DEVERR_SLOT and is skipped
+ *   T >= 0 (T == 0 enqueues nothing), Hkv >= 1, d >= 1, bs >= 1, NB >= 1.
+ * Two tokens naming the same slot race (the result is one of them).
+ */
+pkv_status pkv_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         pkv_dtype dt, const int64_t *slot_mapping, int T, int Hkv, int d,
+                         int bs, int NB, pkv_stream_t stream);
+
+/*
+ * pkv_kv_block_copy -- copy-on-write support: copy whole physical blocks.
+ *
+ * For each pair p: block pairs[p][1] of k_cache (all Hkv heads, all bs slots) becomes
+ * a copy of block pairs[p][0]; the same for v_cache.  Before a sequence writes into a
+ * block whose reference count is above one, the block is copied and the writer gets
+ * the copy (plumephp.com "KV Cache 优化与注意力机制加速" §4.3; 0539edu.com
+ * "从KV cache共享到批量调度…" §3.2, §5.2: check the count before the write).
+ *
+ *   pairs  int32 [n][2] (src, dst), device memory.  The copies run concurrently: a
+ *          block may not be the dst of two pairs, nor both a src and a dst.  A
+ *          block id outside [0, NB) sets PKV_DEVERR_PAIR and the pair is skipped.
+ *   n >= 0 (0 enqueues nothing).
+ */
+pkv_status pkv_kv_block_copy(void *k_cache, void *v_cache, pkv_dtype dt, const int32_t *pairs,
+                             int n, int Hkv, int d, int bs, int NB, pkv_stream_t stream);
+
+/*
+ * Bytes of split-K workspace pkv_paged_decode_attention needs for these sizes and
+ * num_splits on the current device (0 when the call runs in one pass).  The split
+ * count chosen for num_splits == 0 depends on the device's SM count.
+ */
+size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS, int num_splits);
+
+/*
+ * pkv_paged_decode_attention -- one new query per sequence against its cached K/V.
+ *
+ * For sequence b, query head i, KV head j = floor(i / m), len = context_lens[b]:
+ *   s_t = scale * q[b][i] . K_t      for the len tokens t of sequence b, K_t read
+ *                                   from slot block_table[b][t / bs] * bs + t % bs
+ *   out[b][i] = sum_t softmax(s)_t V_t,   lse[b][i] = log sum_t exp(s_t)
+ * (softmax(qK^T/sqrt(d))V: limoncc.com §3.1, §3.3; online softmax and the statistic
+ * L = m + log l: plumephp.com §2.2-§2.3).  Long contexts are split into chunks of
+ * whole blocks whose partial results merge by log-sum-exp.
+ *
+ *   out          fp32 [B][Hq][d]
+ *   lse          fp32 [B][Hq] (natural log) or NULL
+ *   q            fp32 [B][Hq][d]
+ *   k_cache, v_cache  [NB][Hkv][bs][d], element type dt
+ *   block_table  int32 [B][MBS]; entries past a sequence's last block are not read
+ *   context_lens int32 [B]: tokens in the cache, counting the token just appended;
+ *                0 gives out = 0 and lse = -inf
+ *   scale        score scale (1/sqrt(d) for a standard layer)
+ *   num_splits   0: chosen by the library; 1: one pass; k > 1: at most k chunks per
+ *                sequence (chunk = ceil(MBS / k) blocks)
+ *   workspace    device scratch of at least pkv_decode_workspace_bytes(...) bytes
+ *                (may be NULL when that is 0); its contents need no initialisation
+ *                and are overwritten.  Calls that share a workspace must not overlap.
+ *   Requires Hq % Hkv == 0, B >= 0, d >= 1, bs >= 1, MBS >= 1.
+ *   bf16 caches with d in {64, 128, 256}, bs in {16, 32}, 16-byte aligned caches use
+ *   the tensor-core path; other shapes use a CUDA-core path with the same results.
+ */
+pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, const void *k_cache,
+                                      const void *v_cache, pkv_dtype dt,
+                                      const int32_t *block_table, const int32_t *context_lens,
+                                      int B, int Hq, int Hkv, int d, int bs, int MBS, int NB,
+                                      float scale, int num_splits, void *workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * pkv_prefill_attention -- varlen causal attention of whole prompts, writing the cache.
+ *
+ * Sequences are packed: sequence b owns tokens [cu_seqlens[b], cu_seqlens[b+1]) of
+ * q/k/v (0539edu.com "从KV cache共享到批量调度…" §3.3).  Token t of a sequence (0-based)
+ * attends to tokens 0..t of the same sequence with the GQA head mapping:
+ *   out[tok][i] = softmax_{u <= t}(scale * q[tok][i] . k[u][j]) v[u][j],  j = floor(i/m)
+ * (causal prefill: zwjcode.cn "KV Cache 的增量解码" §05, §13).  When slot_mapping is not
+ * NULL, every token's k/v rows are also written to the cache exactly as pkv_kv_append
+ * does with the same slot_mapping.
+ *
+ *   out         fp32 [T][Hq][d];  lse fp32 [T][Hq] or NULL
+ *   q           [T][Hq][d];  k, v [T][Hkv][d]; all of element type dt
+ *   cu_seqlens  int32 [B+1], non-decreasing, cu_seqlens[0] = 0, cu_seqlens[B] = T;
+ *               zero-length sequences are allowed.  Violations set
+ *               PKV_DEVERR_CU_SEQLENS and the offending sequence is skipped.
+ *   max_seqlen  host-side upper bound of every sequence length (sizes the grid); a
+ *               longer sequence sets PKV_DEVERR_CU_SEQLENS and its rows past
+ *               max_seqlen are not computed
+ *   k_cache, v_cache, slot_mapping, bs, NB: as pkv_kv_append; the caches may be NULL
+ *               when slot_mapping is NULL
+ *   bf16 with d in {64, 128} uses the tensor-core path; other inputs a CUDA-core path.
+ */
+pkv_status pkv_prefill_attention(float *out, float *lse, const void *q, const void *k,
+                                 const void *v, pkv_dtype dt, const int32_t *cu_seqlens, int B,
+                                 int T, int max_seqlen, int Hq, int Hkv, int d, float scale,
+                                 void *k_cache, void *v_cache, const int64_t *slot_mapping,
+                                 int bs, int NB, pkv_stream_t stream);
+
+/*
+ * pkv_get_device_error -- synchronise `stream`, then read and clear the device error
+ * word of the current device.  *code receives the OR of the PKV_DEVERR_* bits raised
+ * since the last clear (0: none).  code is a HOST pointer.
+ */
+pkv_status pkv_get_device_error(int *code, pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

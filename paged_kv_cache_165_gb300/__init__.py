@@ -1,0 +1,29 @@
+"""GB300 (sm_103a) paged KV-cache attention.
+
+The compute lives in libpkv.so (C ABI: include/pkv.h).  This package holds the
+thin ctypes binding with the ABI's names, the host-side block manager, and the
+build step.  Importing it does not load the library; the first call does, and
+raises if the library was not built.
+"""
+from ._binding import (  # noqa: F401
+    DEVERR,
+    PKV_BF16,
+    PKV_F32,
+    PkvError,
+    decode_workspace_bytes,
+    get_device_error,
+    header_functions,
+    kv_append,
+    kv_block_copy,
+    lib,
+    library_path,
+    paged_decode_attention,
+    prefill_attention,
+)
+from .blocks import BlockManager, OutOfBlocks  # noqa: F401
+
+
+def build(force: bool = False) -> str:
+    """Compile libpkv.so for sm_103a in-tree (nvcc) and return its path."""
+    from . import _build
+    return _build.build(force=force)

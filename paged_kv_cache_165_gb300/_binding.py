@@ -1,0 +1,215 @@
+"""ctypes binding of libpkv.so (the C ABI in include/pkv.h).
+
+Argument marshalling only: each function checks that the torch tensors it is
+given have the device, dtype, contiguity and shapes the C call expects, then
+passes raw pointers, sizes and the current CUDA stream.  All computation runs in
+the library's kernels; there is no fallback when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import _build
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+PKV_F32, PKV_BF16 = 0, 1
+
+DEVERR = {
+    "slot": 1, "block": 2, "len": 4, "cu_seqlens": 8, "pair": 16, "timeout": 32,
+}
+
+_DTYPES = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"pkv status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpkv.so with argument types set.  Raises if it was never built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first with "
+                           "paged_kv_cache_165_gb300._build.build() (needs nvcc)")
+    L = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.pkv_status_string.argtypes = [I]
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_last_error.argtypes = []
+    L.pkv_last_error.restype = ctypes.c_char_p
+    L.pkv_version.argtypes = []
+    L.pkv_version.restype = I
+    L.pkv_kv_append.argtypes = [P, P, P, P, I, P, I, I, I, I, I, P]
+    L.pkv_kv_append.restype = I
+    L.pkv_kv_block_copy.argtypes = [P, P, I, P, I, I, I, I, I, P]
+    L.pkv_kv_block_copy.restype = I
+    L.pkv_decode_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    L.pkv_decode_workspace_bytes.restype = Z
+    L.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P,
+                                             Z, P]
+    L.pkv_paged_decode_attention.restype = I
+    L.pkv_prefill_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, P, P, P, I, I, P]
+    L.pkv_prefill_attention.restype = I
+    L.pkv_get_device_error.argtypes = [ctypes.POINTER(I), P]
+    L.pkv_get_device_error.restype = I
+    _lib = L
+    return L
+
+
+def header_functions() -> list:
+    """Names of the functions include/pkv.h declares."""
+    with open(os.path.join(_build.INCLUDE, "pkv.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------------ helpers
+
+def _check(status: int) -> None:
+    if status != PKV_OK:
+        raise PkvError(status, lib().pkv_last_error().decode(errors="replace"))
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _cuda(name, t, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _dtype(t) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported element type {t.dtype} (fp32 or bf16)")
+    return _DTYPES[t.dtype]
+
+
+# --------------------------------------------------------------------- ABI
+
+def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    """k_new/v_new [T][Hkv][d] -> cache slots slot_mapping[t] (int64, <0 skipped)."""
+    _cuda("k_cache", k_cache)
+    dt = _dtype(k_cache)
+    _cuda("v_cache", v_cache, k_cache.dtype)
+    _cuda("k_new", k_new, k_cache.dtype)
+    _cuda("v_new", v_new, k_cache.dtype)
+    _cuda("slot_mapping", slot_mapping, torch.int64)
+    NB, Hkv, bs, d = k_cache.shape
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, Hkv, d) or tuple(v_new.shape) != (T, Hkv, d) or slot_mapping.numel() != T:
+        raise ValueError("kv_append: shapes do not match [T][Hkv][d] / [T]")
+    _check(lib().pkv_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), dt,
+                               _ptr(slot_mapping), T, Hkv, d, bs, NB, _stream(stream)))
+
+
+def kv_block_copy(k_cache, v_cache, pairs, stream=None) -> None:
+    """Copy whole blocks: for each (src, dst) row of int32 pairs [n][2]."""
+    _cuda("k_cache", k_cache)
+    dt = _dtype(k_cache)
+    _cuda("v_cache", v_cache, k_cache.dtype)
+    _cuda("pairs", pairs, torch.int32)
+    NB, Hkv, bs, d = k_cache.shape
+    n = pairs.numel() // 2
+    _check(lib().pkv_kv_block_copy(_ptr(k_cache), _ptr(v_cache), dt, _ptr(pairs), n, Hkv, d, bs,
+                                   NB, _stream(stream)))
+
+
+def decode_workspace_bytes(B, Hq, Hkv, d, bs, MBS, num_splits=0) -> int:
+    return int(lib().pkv_decode_workspace_bytes(B, Hq, Hkv, d, bs, MBS, num_splits))
+
+
+def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, scale, lse=None,
+                           num_splits=0, workspace=None, stream=None) -> None:
+    """out [B][Hq][d] fp32 = attention of q [B][Hq][d] fp32 over the paged cache."""
+    _cuda("k_cache", k_cache)
+    dt = _dtype(k_cache)
+    _cuda("v_cache", v_cache, k_cache.dtype)
+    _cuda("q", q, torch.float32)
+    _cuda("out", out, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    if lse is not None:
+        _cuda("lse", lse, torch.float32)
+    NB, Hkv, bs, d = k_cache.shape
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d) or block_table.dim() != 2 or \
+            block_table.shape[0] != B or context_lens.numel() != B or \
+            (lse is not None and lse.numel() != B * Hq):
+        raise ValueError("paged_decode_attention: shapes do not match")
+    MBS = block_table.shape[1]
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_decode_attention(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table),
+        _ptr(context_lens), B, Hq, Hkv, d, bs, MBS, NB, float(scale), int(num_splits),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def prefill_attention(out, q, k, v, cu_seqlens, max_seqlen, scale, lse=None, k_cache=None,
+                      v_cache=None, slot_mapping=None, stream=None) -> None:
+    """Varlen causal attention of packed q [T][Hq][d], k/v [T][Hkv][d]; optional cache write."""
+    _cuda("q", q)
+    dt = _dtype(q)
+    _cuda("k", k, q.dtype)
+    _cuda("v", v, q.dtype)
+    _cuda("out", out, torch.float32)
+    _cuda("cu_seqlens", cu_seqlens, torch.int32)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    if tuple(k.shape) != (T, Hkv, d) or tuple(v.shape) != (T, Hkv, d) or tuple(out.shape) != (T, Hq, d):
+        raise ValueError("prefill_attention: shapes do not match")
+    if lse is not None:
+        _cuda("lse", lse, torch.float32)
+    bs = NB = 0
+    if slot_mapping is not None:
+        _cuda("slot_mapping", slot_mapping, torch.int64)
+        _cuda("k_cache", k_cache, q.dtype)
+        _cuda("v_cache", v_cache, q.dtype)
+        NB, _, bs, _ = k_cache.shape
+    _check(lib().pkv_prefill_attention(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k), _ptr(v), dt, _ptr(cu_seqlens), B, T,
+        int(max_seqlen), Hq, Hkv, d, float(scale), _ptr(k_cache), _ptr(v_cache),
+        _ptr(slot_mapping), bs, NB, _stream(stream)))
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream; return and clear the device error bits."""
+    code = ctypes.c_int(0)
+    _check(lib().pkv_get_device_error(ctypes.byref(code), _stream(stream)))
+    return code.value

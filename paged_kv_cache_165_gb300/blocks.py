@@ -1,0 +1,164 @@
+"""Host-side block manager: physical block pool, per-sequence block tables,
+reference counts, fork and copy-on-write.
+
+This is the bookkeeping that sits above the C ABI and produces its inputs
+(block tables, slot mappings, copy pairs); nothing here runs on the GPU.
+
+* Blocks of ``block_size`` tokens are handed out on demand from a free pool; a
+  sequence's logical block j maps to a physical block through its table
+  (plumephp.com "KV Cache 优化与注意力机制加速" §4.2-§4.3, BlockTable.allocate /
+  get_kv).
+* ``fork`` gives a new sequence the same table and increments every block's
+  reference count (§4.3, BlockTable.fork).
+* Before a sequence writes into a block whose count is above one, the block is
+  copied to a fresh block which the writer takes over; the old block loses one
+  reference (copy-on-write; 0539edu.com "从KV cache共享到批量调度…" §3.2, §5.2: the
+  count is checked before the write).
+* ``audit`` checks the invariant that every block's count equals the number of
+  table entries that reference it (0539edu.com §5.2 suggests logging and checking
+  every cache read/write per request).
+"""
+from __future__ import annotations
+
+from collections import deque
+from typing import Dict, Iterable, List, Optional, Sequence, Tuple
+
+import torch
+
+
+class OutOfBlocks(RuntimeError):
+    pass
+
+
+class BlockManager:
+    def __init__(self, num_blocks: int, block_size: int = 16, order: Optional[Sequence[int]] = None):
+        """``order``: the order in which free blocks are handed out (default 0..NB-1)."""
+        if num_blocks < 1 or block_size < 1:
+            raise ValueError("num_blocks and block_size must be positive")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        ids = list(range(num_blocks)) if order is None else [int(x) for x in order]
+        if sorted(ids) != list(range(num_blocks)):
+            raise ValueError("order must be a permutation of the block ids")
+        self._free = deque(ids)
+        self.refcount = [0] * num_blocks
+        self.tables: Dict[int, List[int]] = {}
+        self.lengths: Dict[int, int] = {}
+
+    # ------------------------------------------------------------ pool
+    @property
+    def num_free(self) -> int:
+        return len(self._free)
+
+    def _alloc(self) -> int:
+        if not self._free:
+            raise OutOfBlocks("no free physical block")
+        blk = self._free.popleft()
+        self.refcount[blk] = 1
+        return blk
+
+    def _release(self, blk: int) -> None:
+        self.refcount[blk] -= 1
+        if self.refcount[blk] < 0:
+            raise AssertionError(f"block {blk} released more often than referenced")
+        if self.refcount[blk] == 0:
+            self._free.append(blk)
+
+    # ------------------------------------------------------- sequences
+    def add_sequence(self, seq: int, num_tokens: int = 0) -> List[int]:
+        """New sequence holding ``num_tokens`` tokens: ceil(n / bs) fresh blocks."""
+        if seq in self.tables:
+            raise KeyError(f"sequence {seq} exists")
+        need = -(-num_tokens // self.block_size)
+        if need > self.num_free:
+            raise OutOfBlocks(f"sequence {seq} needs {need} blocks, {self.num_free} free")
+        self.tables[seq] = [self._alloc() for _ in range(need)]
+        self.lengths[seq] = num_tokens
+        return list(self.tables[seq])
+
+    def fork(self, parent: int, child: int) -> None:
+        """``child`` shares all of ``parent``'s blocks (each count + 1)."""
+        if child in self.tables:
+            raise KeyError(f"sequence {child} exists")
+        table = list(self.tables[parent])
+        for blk in table:
+            self.refcount[blk] += 1
+        self.tables[child] = table
+        self.lengths[child] = self.lengths[parent]
+
+    def free_sequence(self, seq: int) -> None:
+        for blk in self.tables.pop(seq):
+            self._release(blk)
+        del self.lengths[seq]
+
+    def slot(self, seq: int, pos: int) -> int:
+        """Cache slot of logical position ``pos``: table[pos // bs] * bs + pos % bs."""
+        table = self.tables[seq]
+        return table[pos // self.block_size] * self.block_size + pos % self.block_size
+
+    def append_slot(self, seq: int) -> Tuple[int, Optional[Tuple[int, int]]]:
+        """Reserve the slot of the next token of ``seq``.
+
+        Returns (slot, copy) where ``copy`` is a (src, dst) block pair that must be
+        copied before the token is written (copy-on-write), or None.
+        """
+        pos = self.lengths[seq]
+        table = self.tables[seq]
+        copy = None
+        if pos % self.block_size == 0:
+            table.append(self._alloc())
+        else:
+            last = table[-1]
+            if self.refcount[last] > 1:
+                new = self._alloc()
+                self._release(last)
+                table[-1] = new
+                copy = (last, new)
+        self.lengths[seq] = pos + 1
+        return self.slot(seq, pos), copy
+
+    def append_step(self, seqs: Iterable[int]) -> Tuple[List[int], List[Tuple[int, int]]]:
+        """One decode step: a slot for every sequence, plus the COW copies to run first."""
+        slots, copies = [], []
+        for s in seqs:
+            slot, copy = self.append_slot(s)
+            slots.append(slot)
+            if copy is not None:
+                copies.append(copy)
+        return slots, copies
+
+    # ---------------------------------------------------------- tensors
+    def block_table(self, seqs: Sequence[int], max_blocks: Optional[int] = None,
+                    pad: int = -1) -> torch.Tensor:
+        mbs = max_blocks if max_blocks is not None else max(1, max(len(self.tables[s]) for s in seqs))
+        out = torch.full((len(seqs), mbs), pad, dtype=torch.int32)
+        for r, s in enumerate(seqs):
+            t = self.tables[s]
+            if len(t) > mbs:
+                raise ValueError(f"sequence {s} has {len(t)} blocks > max_blocks {mbs}")
+            if t:
+                out[r, :len(t)] = torch.tensor(t, dtype=torch.int32)
+        return out
+
+    def context_lens(self, seqs: Sequence[int]) -> torch.Tensor:
+        return torch.tensor([self.lengths[s] for s in seqs], dtype=torch.int32)
+
+    def slot_mapping(self, seq: int, positions: Iterable[int]) -> torch.Tensor:
+        return torch.tensor([self.slot(seq, p) for p in positions], dtype=torch.int64)
+
+    # ----------------------------------------------------------- checks
+    def audit(self) -> None:
+        """Every block's count equals its table references; free blocks have count 0."""
+        refs = [0] * self.num_blocks
+        for table in self.tables.values():
+            for blk in table:
+                refs[blk] += 1
+        if refs != self.refcount:
+            bad = [b for b in range(self.num_blocks) if refs[b] != self.refcount[b]][:8]
+            raise AssertionError(f"refcount mismatch at blocks {bad}")
+        free = set(self._free)
+        if len(free) != len(self._free):
+            raise AssertionError("a block is on the free list twice")
+        for b in range(self.num_blocks):
+            if (b in free) != (self.refcount[b] == 0):
+                raise AssertionError(f"block {b}: free-list membership disagrees with its count")

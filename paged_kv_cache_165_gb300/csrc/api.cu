@@ -1,0 +1,257 @@
+// api.cu -- the extern "C" entry points declared in include/pkv.h.
+//
+// Every entry point validates its host-side arguments before enqueueing anything,
+// maps CUDA failures to PKV_ERR_CUDA, and records a message for pkv_last_error().
+// Per-device state is limited to the SM count and the address of the device error
+// word (a static __device__ variable: nothing is allocated).
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+__device__ unsigned g_device_error;   // OR of PKV_DEVERR_* bits, one word per device
+
+thread_local char t_last_error[256] = "";
+
+pkv_status fail(pkv_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(PKV_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    unsigned *err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+// State of the current device, set up on first use.
+pkv_status device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    DeviceState &st = g_devices[dev];
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!st.ready) {
+        e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err), g_device_error);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+        st.ready = true;
+    }
+    *out = &st;
+    return PKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool elem_size(pkv_dtype dt, int *bytes) {
+    if (dt == PKV_F32) { *bytes = 4; return true; }
+    if (dt == PKV_BF16) { *bytes = 2; return true; }
+    return false;
+}
+
+bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+}  // namespace
+
+bool encode_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                     const uint64_t *strides_bytes, const uint32_t *box) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode == nullptr) return false;
+    cuuint64_t gdim[5];
+    cuuint64_t gstride[4];
+    cuuint32_t bdim[5], estride[5];
+    for (int r = 0; r < rank; ++r) {
+        gdim[r] = dims[r];
+        bdim[r] = box[r];
+        estride[r] = 1;
+        if (r + 1 < rank) gstride[r] = strides_bytes[r];
+    }
+    const CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                                  const_cast<void *>(base), gdim, gstride, bdim, estride,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char *pkv_status_string(pkv_status status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+const char *pkv_last_error(void) { return t_last_error; }
+
+int pkv_version(void) { return 10000; }
+
+pkv_status pkv_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         pkv_dtype dt, const int64_t *slot_mapping, int T, int Hkv, int d, int bs,
+                         int NB, pkv_stream_t stream) {
+    int eb = 0;
+    if (!elem_size(dt, &eb)) return fail(PKV_ERR_UNSUPPORTED, "kv_append: element type %d", dt);
+    if (T < 0 || Hkv < 1 || d < 1 || bs < 1 || NB < 1)
+        return fail(PKV_ERR_INVALID_ARG, "kv_append: T=%d Hkv=%d d=%d bs=%d NB=%d", T, Hkv, d, bs, NB);
+    if (T == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping)
+        return fail(PKV_ERR_INVALID_ARG, "kv_append: null pointer");
+    DeviceState *st = nullptr;
+    pkv_status s = device_state(&st);
+    if (s != PKV_OK) return s;
+    cudaError_t e = launch_kv_append(k_new, v_new, k_cache, v_cache, eb, slot_mapping, T, Hkv, d,
+                                     bs, NB, st->err, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_append launch");
+}
+
+pkv_status pkv_kv_block_copy(void *k_cache, void *v_cache, pkv_dtype dt, const int32_t *pairs,
+                             int n, int Hkv, int d, int bs, int NB, pkv_stream_t stream) {
+    int eb = 0;
+    if (!elem_size(dt, &eb)) return fail(PKV_ERR_UNSUPPORTED, "kv_block_copy: element type %d", dt);
+    if (n < 0 || Hkv < 1 || d < 1 || bs < 1 || NB < 1)
+        return fail(PKV_ERR_INVALID_ARG, "kv_block_copy: n=%d Hkv=%d d=%d bs=%d NB=%d", n, Hkv, d, bs, NB);
+    if (n == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !pairs) return fail(PKV_ERR_INVALID_ARG, "kv_block_copy: null pointer");
+    DeviceState *st = nullptr;
+    pkv_status s = device_state(&st);
+    if (s != PKV_OK) return s;
+    cudaError_t e = launch_kv_block_copy(k_cache, v_cache, eb, pairs, n, Hkv, d, bs, NB, st->err, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_block_copy launch");
+}
+
+static pkv_status check_decode_sizes(int B, int Hq, int Hkv, int d, int bs, int MBS) {
+    if (B < 0 || B > 65535 || Hq < 1 || Hq > 65535 || Hkv < 1 || Hq % Hkv != 0 || d < 1 ||
+        d > 256 || bs < 1 || MBS < 1)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "paged_decode_attention: B=%d Hq=%d Hkv=%d d=%d bs=%d MBS=%d (need 0<=B<=65535, "
+                    "Hq %% Hkv == 0, 1<=d<=256, bs>=1, MBS>=1)",
+                    B, Hq, Hkv, d, bs, MBS);
+    return PKV_OK;
+}
+
+size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS, int num_splits) {
+    if (check_decode_sizes(B, Hq, Hkv, d, bs, MBS) != PKV_OK || num_splits < 0) return 0;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != PKV_OK) return 0;
+    // the plan's split count does not depend on the element type or NB
+    return plan_decode(B, Hq, Hkv, d, bs, MBS, 1, PKV_BF16, num_splits, st->sm_count, true)
+        .workspace_bytes;
+}
+
+pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, const void *k_cache,
+                                      const void *v_cache, pkv_dtype dt, const int32_t *block_table,
+                                      const int32_t *context_lens, int B, int Hq, int Hkv, int d,
+                                      int bs, int MBS, int NB, float scale, int num_splits,
+                                      void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    int eb = 0;
+    if (!elem_size(dt, &eb)) return fail(PKV_ERR_UNSUPPORTED, "paged_decode_attention: element type %d", dt);
+    pkv_status s = check_decode_sizes(B, Hq, Hkv, d, bs, MBS);
+    if (s != PKV_OK) return s;
+    if (NB < 1 || num_splits < 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attention: NB=%d num_splits=%d", NB, num_splits);
+    if (B == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attention: null pointer");
+    if (reinterpret_cast<uintptr_t>(q) % 8 != 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attention: q must be 8-byte aligned");
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != PKV_OK) return s;
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count,
+                                        aligned16(k_cache) && aligned16(v_cache));
+    if (plan.workspace_bytes > 0 &&
+        (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
+         reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+        return fail(PKV_ERR_WORKSPACE,
+                    "paged_decode_attention: needs %zu bytes of 16-byte aligned workspace, got %zu",
+                    plan.workspace_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
+    DecodeArgs a{out, lse, q, k_cache, v_cache, block_table, context_lens,
+                 B, Hq, Hkv, d, bs, MBS, NB, scale, workspace, st->err};
+    cudaError_t e = launch_decode(a, plan, dt, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_decode_attention launch");
+}
+
+pkv_status pkv_prefill_attention(float *out, float *lse, const void *q, const void *k, const void *v,
+                                 pkv_dtype dt, const int32_t *cu_seqlens, int B, int T,
+                                 int max_seqlen, int Hq, int Hkv, int d, float scale,
+                                 void *k_cache, void *v_cache, const int64_t *slot_mapping, int bs,
+                                 int NB, pkv_stream_t stream) {
+    int eb = 0;
+    if (!elem_size(dt, &eb)) return fail(PKV_ERR_UNSUPPORTED, "prefill_attention: element type %d", dt);
+    if (B < 0 || B > 65535 || T < 0 || max_seqlen < 0 || Hq < 1 || Hq > 65535 || Hkv < 1 ||
+        Hq % Hkv != 0 || d < 1 || d > 256)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "prefill_attention: B=%d T=%d max_seqlen=%d Hq=%d Hkv=%d d=%d", B, T, max_seqlen,
+                    Hq, Hkv, d);
+    if (slot_mapping != nullptr && (bs < 1 || NB < 1 || !k_cache || !v_cache))
+        return fail(PKV_ERR_INVALID_ARG, "prefill_attention: cache write needs caches, bs and NB");
+    if (B == 0 || T == 0) return PKV_OK;
+    if (!out || !q || !k || !v || !cu_seqlens)
+        return fail(PKV_ERR_INVALID_ARG, "prefill_attention: null pointer");
+    DeviceState *st = nullptr;
+    pkv_status s = device_state(&st);
+    if (s != PKV_OK) return s;
+    cudaError_t e;
+    if (slot_mapping != nullptr) {
+        e = launch_kv_append(k, v, k_cache, v_cache, eb, slot_mapping, T, Hkv, d, bs, NB, st->err,
+                             stream);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill_attention cache write");
+    }
+    PrefillArgs a{out, lse, q, k, v, cu_seqlens, B, T, max_seqlen, Hq, Hkv, d, scale, st->err};
+    e = launch_prefill(a, dt, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "prefill_attention launch");
+}
+
+pkv_status pkv_get_device_error(int *code, pkv_stream_t stream) {
+    if (code == nullptr) return fail(PKV_ERR_INVALID_ARG, "get_device_error: null code");
+    DeviceState *st = nullptr;
+    pkv_status s = device_state(&st);
+    if (s != PKV_OK) return s;
+    unsigned host = 0;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&host, st->err, sizeof host, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(st->err, 0, sizeof host, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "get_device_error");
+    *code = static_cast<int>(host);
+    return PKV_OK;
+}
+
+}  // extern "C"

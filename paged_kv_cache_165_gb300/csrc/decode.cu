@@ -1,0 +1,587 @@
+// decode.cu -- paged decode attention: one query per sequence against its cached K/V.
+//
+// What is computed (for sequence b, query head i, KV head j = floor(i/m)):
+//   out[b][i] = softmax_t(scale * q[b][i] . K_t) V_t over the context_lens[b] cached
+//   tokens, gathered through block_table[b] (limoncc.com "大语言模型研究15——注意力机制
+//   优化之KV缓存" §3.1, §3.3; plumephp.com "KV Cache 优化与注意力机制加速" §4.2-§4.3).
+// The softmax is taken online, block by block, keeping a running max m and running sum
+// l (plumephp.com §2.2, online_softmax_update), and each chunk of blocks yields the
+// log-sum-exp statistic m + log l (§2.3) by which chunk partials merge (split-K).
+//
+// Tensor-core path (bf16 cache, d in {64,128,256}, bs in {16,32}):
+//   * one CTA per (sequence, KV head, group of up to 8 query heads, chunk of blocks);
+//     its warps take the chunk's blocks round-robin, each warp with a private ring of
+//     shared-memory stages filled by TMA (one K and one V tile of bs x d per block,
+//     128-byte swizzled, completion on an mbarrier with a bounded wait);
+//   * the m query heads of a GQA group share every K/V tile read from HBM: scores are
+//     one m16n8k16 bf16 MMA tile per 8 tokens whose 16 rows are the group's heads
+//     twice -- rows 0-7 the bf16 "hi" part of q, rows 8-15 the bf16 "lo" remainder --
+//     so q (fp32) enters the tensor core to ~2^-16 relative and hi+lo rows sum in fp32;
+//     the softmax weights P are split the same way for P.V, whose output rows 0-7 and
+//     8-15 again sum to one fp32 result;
+//   * per-warp running (m, l, O) merge across warps in shared memory at the end.
+// CUDA-core path: any d <= 256, fp32 or bf16 cache; one warp per (sequence, head, chunk).
+// With more than one chunk per sequence both paths write (o, lse) partials to the
+// caller's workspace and a merge kernel combines them by log-sum-exp.
+#include <algorithm>
+#include <atomic>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct DecodeKParams {
+    float *out;
+    float *lse;
+    float *ws_o;     // [B*Hq][splits][d]
+    float *ws_lse;   // [B*Hq][splits], log2 domain
+    const float *q;
+    const int32_t *block_table;
+    const int32_t *context_lens;
+    unsigned *err;
+    int B, Hq, Hkv, m, MBS, NB;
+    int head_tiles;   // ceil(m / 8): CTAs per KV head along grid.y
+    int chunk_pages;
+    int splits;
+    float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
+};
+
+// Sequence length after validation; an invalid length counts as empty.
+__device__ __forceinline__ int checked_len(const DecodeKParams &p, int b, int bs, bool report) {
+    int len = __ldg(p.context_lens + b);
+    if (len < 0 || (long long)len > (long long)p.MBS * bs) {
+        if (report) raise_error(p.err, PKV_DEVERR_LEN);
+        len = 0;
+    }
+    return len;
+}
+
+// =============================================================== tensor-core path
+
+template <int D, int BS, int NW, int ST>
+struct MmaCfg {
+    static constexpr int kPageBytes = BS * D * 2;             // one K (or V) tile of a block
+    static constexpr int kStageBytes = 2 * kPageBytes;        // K tile then V tile
+    static constexpr int kStagesBytes = NW * ST * kStageBytes;
+    static constexpr int kMergeBytes = NW * (16 + 8 * D) * 4;
+    static constexpr int kSmemBytes = 1024 + kStagesBytes + NW * ST * 8;
+    static_assert(kMergeBytes <= kStagesBytes, "merge scratch reuses the stage buffers");
+    static_assert(D % 64 == 0 && BS % 16 == 0, "tile shape");
+};
+
+template <int D, int BS, int NW, int ST>
+__global__ void __launch_bounds__(NW * 32)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const DecodeKParams p) {
+    using Cfg = MmaCfg<D, BS, NW, ST>;
+    constexpr int NT = BS / 8;    // 8-token score tiles per block
+    constexpr int KT = BS / 16;   // 16-token k-steps of P.V per block
+    constexpr int KS = D / 16;    // 16-wide k-steps of q.K
+    constexpr int ONT = D / 8;    // 8-wide output tiles
+    constexpr int PANELS = D / 64;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kStagesBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y / p.head_tiles;
+    const int head0 = kvh * p.m + (blockIdx.y % p.head_tiles) * 8;
+    const int nheads = min(8, (kvh + 1) * p.m - head0);
+    const int b = blockIdx.z;
+
+    const int len = checked_len(p, b, BS, threadIdx.x == 0 && split == 0 && blockIdx.y == 0);
+    const int n_pages = (len + BS - 1) / BS;
+    const int pg0 = split * p.chunk_pages;
+    const int pg1 = min(n_pages, pg0 + p.chunk_pages);
+    if (pg0 >= pg1) {
+        // Nothing to read.  With one chunk this is an empty sequence: out = 0, lse = -inf.
+        // With several, the merge kernel knows from the length that this chunk is absent.
+        if (p.splits == 1) {
+            for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32)
+                p.out[(static_cast<size_t>(b) * p.Hq + head0 + idx / D) * D + idx % D] = 0.f;
+            if (p.lse != nullptr && threadIdx.x < nheads)
+                p.lse[static_cast<size_t>(b) * p.Hq + head0 + threadIdx.x] = -INFINITY;
+        }
+        return;
+    }
+
+    if (lane == 0) {
+        for (int s = 0; s < ST; ++s) mbar_init(smem_addr(&bars[warp * ST + s]), 1);
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 0) {
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+    }
+    __syncwarp();
+
+    // q fragments (A operand, 16 rows x D): row g = hi part of head head0+g, row g+8 =
+    // its lo remainder; rows of heads outside this CTA's group are zero.
+    uint32_t qa[KS][4];
+    {
+        const bool row_ok = g < nheads;
+        const float *qrow = p.q + (static_cast<size_t>(b) * p.Hq + head0 + (row_ok ? g : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
+            if (row_ok) {
+                x0 = *reinterpret_cast<const float2 *>(qrow + kk * 16 + 2 * t4);
+                x1 = *reinterpret_cast<const float2 *>(qrow + kk * 16 + 8 + 2 * t4);
+            }
+            split_bf16x2(x0.x, x0.y, qa[kk][0], qa[kk][1]);
+            split_bf16x2(x1.x, x1.y, qa[kk][2], qa[kk][3]);
+        }
+    }
+
+    // This warp's blocks: pg0 + warp + NW*k, k = 0 .. n_my-1.  Block-table entries are
+    // fetched 32 at a time (one per lane) ahead of the copies that need them.
+    const int pages = pg1 - pg0;
+    const int n_my = pages > warp ? (pages - warp + NW - 1) / NW : 0;
+    const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + pg0 + warp;
+    int tcur = lane < n_my ? __ldg(tbl + static_cast<size_t>(lane) * NW) : 0;
+    int tnext = 32 + lane < n_my ? __ldg(tbl + static_cast<size_t>(32 + lane) * NW) : 0;
+    int tbase = 0;
+    const int oob_row = p.NB * p.Hkv * BS;   // a row past the end: TMA fills zeros
+
+    auto issue = [&](int k) {   // whole warp (shuffle); lane 0 issues the copies
+        while (k >= tbase + 32) {
+            tcur = tnext;
+            tbase += 32;
+            const int kn = tbase + 32 + lane;
+            tnext = kn < n_my ? __ldg(tbl + static_cast<size_t>(kn) * NW) : 0;
+        }
+        const int phys = __shfl_sync(kFull, tcur, k & 31);
+        if (lane == 0) {
+            int row;
+            if (phys < 0 || phys >= p.NB) {
+                raise_error(p.err, PKV_DEVERR_BLOCK);
+                row = oob_row;
+            } else {
+                row = (phys * p.Hkv + kvh) * BS;
+            }
+            const int st = warp * ST + k % ST;
+            const uint32_t bar = smem_addr(&bars[st]);
+            const uint32_t dst = smem_addr(smem + static_cast<size_t>(st) * Cfg::kStageBytes);
+            mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
+#pragma unroll
+            for (int pn = 0; pn < PANELS; ++pn) {
+                tma_load_2d(dst + pn * BS * 128, &tm_k, pn * 64, row, bar);
+                tma_load_2d(dst + Cfg::kPageBytes + pn * BS * 128, &tm_v, pn * 64, row, bar);
+            }
+        }
+    };
+
+    float o[ONT][4];
+#pragma unroll
+    for (int nt = 0; nt < ONT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    int issued = min(ST, n_my);
+    for (int k = 0; k < issued; ++k) issue(k);
+
+    int k = 0;
+    for (; k < n_my; ++k) {
+        const int st = warp * ST + k % ST;
+        const bool arrived = mbar_wait_bounded(smem_addr(&bars[st]), (k / ST) & 1);
+        if (!__all_sync(kFull, arrived)) {
+            if (lane == 0) raise_error(p.err, PKV_DEVERR_TIMEOUT);
+            break;
+        }
+        uint8_t *stage = smem + static_cast<size_t>(st) * Cfg::kStageBytes;
+        const uint32_t k_s = smem_addr(stage), v_s = k_s + Cfg::kPageBytes;
+        const int pg = pg0 + warp + k * NW;
+        const int valid = min(BS, len - pg * BS);
+        if (valid < BS) {
+            // V rows past the end of the sequence may hold anything (NaN, Inf): zero them
+            // so that their zero weights contribute exactly zero.
+            for (int idx = lane; idx < (BS - valid) * (D / 8); idx += 32) {
+                const int r = valid + idx / (D / 8), c16 = idx % (D / 8);
+                *reinterpret_cast<uint4 *>(stage + Cfg::kPageBytes + (c16 >> 3) * BS * 128 +
+                                           r * 128 + (c16 & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // ---- scores S^T: (2 x group heads) x BS tokens, fp32 accumulate
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                const int mi = lane >> 3, r8 = lane & 7;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(k_s + swz128(BS, np * 16 + (mi >> 1) * 8 + r8, kk * 16 + (mi & 1) * 8),
+                        b0, b1, b2, b3);
+                mma_bf16_16816(s[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                mma_bf16_16816(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+            }
+        }
+
+        // ---- online softmax (base 2) for head g: rows g (hi) + g+8 (lo) of each tile
+        float sc[NT][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tok = nt * 8 + 2 * t4 + e;
+                const float v = (s[nt][e] + s[nt][2 + e]) * p.scale_log2;
+                sc[nt][e] = tok < valid ? v : -INFINITY;
+                mx = fmaxf(mx, sc[nt][e]);
+            }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2f(m_run - m_new);
+        float psum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                sc[nt][e] = exp2f(sc[nt][e] - m_new);
+                psum += sc[nt][e];
+            }
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+#pragma unroll
+        for (int nt = 0; nt < ONT; ++nt) {
+            o[nt][0] *= alpha;
+            o[nt][1] *= alpha;
+            o[nt][2] *= alpha;
+            o[nt][3] *= alpha;
+        }
+
+        // ---- O += P V with P = P_hi (rows 0-7) + P_lo (rows 8-15)
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+            uint32_t a0, a1, a2, a3;
+            split_bf16x2(sc[2 * kt][0], sc[2 * kt][1], a0, a1);
+            split_bf16x2(sc[2 * kt + 1][0], sc[2 * kt + 1][1], a2, a3);
+#pragma unroll
+            for (int np = 0; np < D / 16; ++np) {
+                const int mi = lane >> 3, r8 = lane & 7;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(v_s + swz128(BS, kt * 16 + (mi & 1) * 8 + r8, np * 16 + (mi >> 1) * 8),
+                              b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_bf16_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        __syncwarp();
+        if (k + ST < n_my) {
+            issue(k + ST);
+            issued = k + ST + 1;
+        }
+    }
+    if (k < n_my) {
+        // A copy did not arrive in time: wait (bounded) for the copies still in flight
+        // so that none lands after the block exits.
+        for (int kk = k; kk < issued; ++kk)
+            mbar_wait_bounded(smem_addr(&bars[warp * ST + kk % ST]), (kk / ST) & 1);
+    }
+
+    l_run += __shfl_xor_sync(kFull, l_run, 1);
+    l_run += __shfl_xor_sync(kFull, l_run, 2);
+
+    // ---- merge the warps' (m, l, O) through shared memory (stage buffers are free now)
+    __syncthreads();
+    float *mw = reinterpret_cast<float *>(smem);
+    float *lw = mw + NW * 8;
+    float *ow = lw + NW * 8;
+    if (t4 == 0) {
+        mw[warp * 8 + g] = m_run;
+        lw[warp * 8 + g] = l_run;
+    }
+#pragma unroll
+    for (int nt = 0; nt < ONT; ++nt) {
+        float2 v = make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
+        *reinterpret_cast<float2 *>(ow + (warp * 8 + g) * D + nt * 8 + 2 * t4) = v;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32) {
+        const int h = idx / D, c = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mw[w * 8 + h]);
+        float L = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = exp2f(mw[w * 8 + h] - M);
+            L += lw[w * 8 + h] * f;
+            acc += ow[(w * 8 + h) * D + c] * f;
+        }
+        const size_t bi = static_cast<size_t>(b) * p.Hq + head0 + h;
+        if (p.splits == 1) {
+            p.out[bi * D + c] = acc / L;
+            if (c == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
+        } else {
+            p.ws_o[(bi * p.splits + split) * D + c] = acc / L;
+            if (c == 0) p.ws_lse[bi * p.splits + split] = M + log2f(L);
+        }
+    }
+}
+
+// ================================================================ CUDA-core path
+
+template <typename T>
+__device__ __forceinline__ float load_f32(const T *p);
+template <>
+__device__ __forceinline__ float load_f32<float>(const float *p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
+}
+
+// One warp per (chunk, query head, sequence); lanes own head-dim elements lane + 32*j.
+template <typename T, int J>
+__global__ void __launch_bounds__(32)
+    decode_simt_kernel(const T *__restrict__ kc, const T *__restrict__ vc, const DecodeKParams p,
+                       int d, int bs) {
+    const int lane = threadIdx.x;
+    const int split = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
+    const int kvh = i / p.m;
+    const int len = checked_len(p, b, bs, lane == 0 && split == 0 && i == 0);
+    const int n_pages = (len + bs - 1) / bs;
+    const int pg0 = split * p.chunk_pages;
+    const int pg1 = min(n_pages, pg0 + p.chunk_pages);
+    const size_t bi = static_cast<size_t>(b) * p.Hq + i;
+    if (pg0 >= pg1) {
+        if (p.splits == 1) {
+            for (int e = lane; e < d; e += 32) p.out[bi * d + e] = 0.f;
+            if (lane == 0 && p.lse != nullptr) p.lse[bi] = -INFINITY;
+        }
+        return;
+    }
+    float qv[J], acc[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        qv[j] = e < d ? p.q[bi * d + e] : 0.f;
+        acc[j] = 0.f;
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int pg = pg0; pg < pg1; ++pg) {
+        const int phys = __ldg(p.block_table + static_cast<size_t>(b) * p.MBS + pg);
+        const bool bad = phys < 0 || phys >= p.NB;
+        if (bad && lane == 0) raise_error(p.err, PKV_DEVERR_BLOCK);
+        const int valid = min(bs, len - pg * bs);
+        for (int off = 0; off < valid; ++off) {
+            const size_t base =
+                bad ? 0 : ((static_cast<size_t>(phys) * p.Hkv + kvh) * bs + off) * d;
+            float dot = 0.f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int e = lane + 32 * j;
+                if (e < d && !bad) dot += qv[j] * load_f32(kc + base + e);
+            }
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(kFull, dot, sh);
+            const float s = dot * p.scale_log2;
+            const float m_new = fmaxf(m_run, s);
+            const float alpha = exp2f(m_run - m_new);
+            const float w = exp2f(s - m_new);
+            l_run = l_run * alpha + w;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int e = lane + 32 * j;
+                const float v = (e < d && !bad) ? load_f32(vc + base + e) : 0.f;
+                acc[j] = acc[j] * alpha + w * v;
+            }
+            m_run = m_new;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        if (e >= d) continue;
+        if (p.splits == 1)
+            p.out[bi * d + e] = acc[j] / l_run;
+        else
+            p.ws_o[(bi * p.splits + split) * d + e] = acc[j] / l_run;
+    }
+    if (lane == 0) {
+        if (p.splits == 1) {
+            if (p.lse != nullptr) p.lse[bi] = (m_run + log2f(l_run)) * kLn2;
+        } else {
+            p.ws_lse[bi * p.splits + split] = m_run + log2f(l_run);
+        }
+    }
+}
+
+// ==================================================================== LSE merge
+
+// One block per (sequence, query head): lse = log2 sum_c 2^{lse_c},
+// out = sum_c 2^{lse_c - lse} o_c over the chunks that hold tokens.
+__global__ void __launch_bounds__(128)
+    decode_merge_kernel(const DecodeKParams p, int d, int bs) {
+    const size_t bi = blockIdx.x;
+    const int b = static_cast<int>(bi / p.Hq);
+    const int len = checked_len(p, b, bs, false);
+    const int n_pages = (len + bs - 1) / bs;
+    const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
+    const float *ls = p.ws_lse + bi * p.splits;
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, ls[c]);
+    float L = 0.f;
+    for (int c = 0; c < nc; ++c) L += exp2f(ls[c] - M);
+    for (int e = threadIdx.x; e < d; e += blockDim.x) {
+        float acc = 0.f;
+        for (int c = 0; c < nc; ++c) acc += exp2f(ls[c] - M) * p.ws_o[(bi * p.splits + c) * d + e];
+        p.out[bi * d + e] = nc > 0 ? acc / L : 0.f;
+    }
+    if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bi] = nc > 0 ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+// ====================================================================== launch
+
+template <int D, int BS, int NW, int ST>
+cudaError_t launch_mma(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv,
+                       dim3 grid, cudaStream_t stream) {
+    using Cfg = MmaCfg<D, BS, NW, ST>;
+    auto kernel = decode_mma_kernel<D, BS, NW, ST>;
+    static std::atomic<unsigned long long> attr_set{0};   // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(bit);
+    }
+    kernel<<<grid, NW * 32, Cfg::kSmemBytes, stream>>>(tk, tv, kp);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_simt(const DecodeArgs &a, const DecodeKParams &kp, dim3 grid,
+                        cudaStream_t stream) {
+    const T *kc = static_cast<const T *>(a.k_cache);
+    const T *vc = static_cast<const T *>(a.v_cache);
+    const int J = (a.d + 31) / 32;
+    switch (J) {
+#define PKV_SIMT_CASE(n)                                                                  \
+    case n:                                                                               \
+        decode_simt_kernel<T, n><<<grid, 32, 0, stream>>>(kc, vc, kp, a.d, a.bs);          \
+        break;
+        PKV_SIMT_CASE(1)
+        PKV_SIMT_CASE(2)
+        PKV_SIMT_CASE(3)
+        PKV_SIMT_CASE(4)
+        PKV_SIMT_CASE(5)
+        PKV_SIMT_CASE(6)
+        PKV_SIMT_CASE(7)
+        PKV_SIMT_CASE(8)
+#undef PKV_SIMT_CASE
+        default:
+            return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
+                       int num_splits, int sm_count, bool caches_aligned) {
+    DecodePlan plan{};
+    plan.tensor_core = dt == PKV_BF16 && (d == 64 || d == 128 || d == 256) &&
+                       (bs == 16 || bs == 32) && caches_aligned &&
+                       static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31);
+    // (sequence, KV head, group of up to 8 query heads) units; the same count for both
+    // paths, so that the workspace size depends only on the shapes
+    const int m = Hq / Hkv;
+    const long long units = static_cast<long long>(B) * Hkv * ((m + 7) / 8);
+    int chunk = MBS;
+    if (num_splits == 1) {
+        chunk = MBS;
+    } else if (num_splits > 1) {
+        chunk = (MBS + num_splits - 1) / num_splits;
+    } else {
+        // Enough (sequence, head-group, chunk) units for several waves of two CTAs per SM,
+        // without making chunks shorter than 16 blocks.
+        const long long target = 8ll * std::max(sm_count, 1);
+        while (chunk > 16 && units * ((MBS + chunk - 1) / chunk) < target)
+            chunk = (chunk + 1) / 2;
+    }
+    chunk = std::max(chunk, 1);
+    plan.chunk_pages = chunk;
+    plan.splits = (MBS + chunk - 1) / chunk;
+    plan.workspace_bytes = plan.splits > 1 ? static_cast<size_t>(B) * Hq * plan.splits *
+                                                 (static_cast<size_t>(d) + 1) * sizeof(float)
+                                           : 0;
+    return plan;
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
+                          cudaStream_t stream) {
+    if (a.B == 0) return cudaSuccess;
+    DecodeKParams kp{};
+    kp.out = a.out;
+    kp.lse = a.lse;
+    kp.q = a.q;
+    kp.block_table = a.block_table;
+    kp.context_lens = a.context_lens;
+    kp.err = a.err;
+    kp.B = a.B;
+    kp.Hq = a.Hq;
+    kp.Hkv = a.Hkv;
+    kp.m = a.Hq / a.Hkv;
+    kp.MBS = a.MBS;
+    kp.NB = a.NB;
+    kp.head_tiles = (kp.m + 7) / 8;
+    kp.chunk_pages = plan.chunk_pages;
+    kp.splits = plan.splits;
+    kp.scale_log2 = a.scale * kLog2e;
+    if (plan.splits > 1) {
+        kp.ws_o = static_cast<float *>(a.workspace);
+        kp.ws_lse = kp.ws_o + static_cast<size_t>(a.B) * a.Hq * plan.splits * a.d;
+    }
+
+    cudaError_t e;
+    if (plan.tensor_core) {
+        CUtensorMap tk, tv;
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.d),
+                                  static_cast<uint64_t>(a.NB) * a.Hkv * a.bs};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.d) * 2};
+        const uint32_t box[2] = {64, static_cast<uint32_t>(a.bs)};
+        if (!encode_map_bf16(&tk, a.k_cache, 2, dims, strides, box) ||
+            !encode_map_bf16(&tv, a.v_cache, 2, dims, strides, box))
+            return cudaErrorInvalidValue;
+        const dim3 grid(plan.splits, a.Hkv * kp.head_tiles, a.B);
+        if (a.bs == 16) {
+            if (a.d == 64) e = launch_mma<64, 16, 4, 6>(kp, tk, tv, grid, stream);
+            else if (a.d == 128) e = launch_mma<128, 16, 4, 3>(kp, tk, tv, grid, stream);
+            else e = launch_mma<256, 16, 4, 2>(kp, tk, tv, grid, stream);
+        } else {
+            if (a.d == 64) e = launch_mma<64, 32, 4, 3>(kp, tk, tv, grid, stream);
+            else if (a.d == 128) e = launch_mma<128, 32, 4, 2>(kp, tk, tv, grid, stream);
+            else e = launch_mma<256, 32, 2, 2>(kp, tk, tv, grid, stream);
+        }
+    } else {
+        const dim3 grid(plan.splits, a.Hq, a.B);
+        e = dt == PKV_F32 ? launch_simt<float>(a, kp, grid, stream)
+                          : launch_simt<__nv_bfloat16>(a, kp, grid, stream);
+    }
+    if (e != cudaSuccess || plan.splits == 1) return e;
+    decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, stream>>>(kp, a.d, a.bs);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

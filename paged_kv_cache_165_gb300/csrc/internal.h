@@ -1,0 +1,76 @@
+// internal.h -- declarations shared by the library's translation units (not the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// ------------------------------------------------------------- host helpers
+
+// Encode a 2-D / 3-D bf16 tiled tensor map with 128-byte swizzle.  dims[0] is the
+// innermost (contiguous) dimension; strides are the byte strides of dims 1.. .
+bool encode_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                     const uint64_t *strides_bytes, const uint32_t *box);
+
+// ---------------------------------------------------------------- cache ops
+
+cudaError_t launch_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             int elem_bytes, const int64_t *slot_mapping, int T, int Hkv, int d,
+                             int bs, int NB, unsigned *err, cudaStream_t stream);
+
+cudaError_t launch_kv_block_copy(void *k_cache, void *v_cache, int elem_bytes,
+                                 const int32_t *pairs, int n, int Hkv, int d, int bs, int NB,
+                                 unsigned *err, cudaStream_t stream);
+
+// ------------------------------------------------------------------ decode
+
+struct DecodePlan {
+    bool tensor_core;   // bf16 TMA + mma path; otherwise the CUDA-core path
+    int splits;         // chunks per sequence (1: one pass, no workspace)
+    int chunk_pages;    // blocks per chunk
+    size_t workspace_bytes;
+};
+
+DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
+                       int num_splits, int sm_count, bool caches_aligned);
+
+struct DecodeArgs {
+    float *out;
+    float *lse;
+    const float *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_table;
+    const int32_t *context_lens;
+    int B, Hq, Hkv, d, bs, MBS, NB;
+    float scale;
+    void *workspace;
+    unsigned *err;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
+                          cudaStream_t stream);
+
+// ----------------------------------------------------------------- prefill
+
+struct PrefillArgs {
+    float *out;
+    float *lse;
+    const void *q, *k, *v;
+    const int32_t *cu_seqlens;
+    int B, T, max_seqlen, Hq, Hkv, d;
+    float scale;
+    unsigned *err;
+};
+
+bool prefill_tensor_core_ok(pkv_dtype dt, int d, const void *q, const void *k, const void *v,
+                            int T, int Hq, int Hkv);
+
+cudaError_t launch_prefill(const PrefillArgs &a, pkv_dtype dt, cudaStream_t stream);
+
+}  // namespace pkv

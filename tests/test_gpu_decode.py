@@ -1,0 +1,192 @@
+"""paged_decode_attention on the GPU against the fp64 oracle: small ragged cases,
+every path (tensor-core bf16, CUDA-core fp32/bf16), one pass and split-K."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_165_gb300 as pkv
+from paged_kv_cache_165_gb300 import _build
+from workloads import gen
+
+from conftest import GOLDEN
+from helpers import ATTN_ATOL, assert_attn_close, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    _build.build()
+    pkv.lib()
+    pkv.get_device_error()
+
+
+def run_decode(q, kc, vc, table, lens, scale, num_splits=0, with_lse=True):
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    out = torch.full((B, Hq, d), float("nan"), device="cuda")
+    lse = torch.full((B, Hq), float("nan"), device="cuda") if with_lse else None
+    ws_bytes = pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, table.shape[1], num_splits)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    pkv.paged_decode_attention(out, dev(q), dev(kc), dev(vc), dev(table), dev(lens), scale, lse=lse,
+                               num_splits=num_splits, workspace=ws)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def random_case(seed, lens, hq, hkv, d, bs, dtype, spare=4, poison=False):
+    g = gen.generator(seed)
+    per_seq = [gen.blocks_needed(n, bs) for n in lens]
+    nb = sum(per_seq) + spare
+    table = gen.block_table_from_order(gen.permutation(g, nb), per_seq)
+    kc = gen.randn(g, (nb, hkv, bs, d), dtype)
+    vc = gen.randn(g, (nb, hkv, bs, d), dtype)
+    q = gen.randn(g, (len(lens), hq, d))
+    if poison:   # unwritten slots past each length hold NaN / Inf: they must stay invisible
+        for b, n in enumerate(lens):
+            for pos in range(n, per_seq[b] * bs):
+                s = oracle.slot_of(table[b], pos, bs)
+                kc[s // bs, :, s % bs] = float("nan")
+                vc[s // bs, :, s % bs] = float("inf")
+        for blk in range(nb):
+            if blk not in set(table.flatten().tolist()):
+                kc[blk] = float("nan")
+                vc[blk] = float("nan")
+    return q, kc, vc, table, torch.tensor(lens, dtype=torch.int32)
+
+
+def check(q, kc, vc, table, lens, scale, num_splits=0, what=""):
+    out, lse = run_decode(q, kc, vc, table, lens, scale, num_splits)
+    assert pkv.get_device_error() == 0
+    ref, ref_lse = oracle.paged_decode(q, kc, vc, table, lens, scale)
+    e1 = assert_attn_close(out, ref, what + " out")
+    e2 = assert_attn_close(lse, ref_lse, what + " lse")
+    return e1, e2
+
+
+RAGGED = [1, 15, 16, 17, 31, 32, 33, 100, 0, 257]
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (16, 2), (12, 2), (32, 2), (16, 1)])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("num_splits", [1, 3, 0])
+def test_tensor_core_path_ragged(hq, hkv, d, num_splits):
+    q, kc, vc, table, lens = random_case(hq * 1000 + d + num_splits, RAGGED, hq, hkv, d, 16, torch.bfloat16)
+    check(q, kc, vc, table, lens, 1 / math.sqrt(d), num_splits, f"hq={hq} hkv={hkv} d={d} s={num_splits}")
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_block_sizes_and_poisoned_unwritten_slots(bs):
+    q, kc, vc, table, lens = random_case(40 + bs, RAGGED, 16, 2, 128, bs, torch.bfloat16, poison=True)
+    for s in (1, 2, 0):
+        check(q, kc, vc, table, lens, 0.0884, s, f"bs={bs} s={s}")
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.float32, 128), (torch.bfloat16, 96),
+                                     (torch.float32, 40), (torch.bfloat16, 128)])
+@pytest.mark.parametrize("bs", [8, 16])
+def test_cuda_core_path(dtype, d, bs):
+    # fp32 caches, head dims outside {64,128,256} and bs == 8 take the CUDA-core path
+    q, kc, vc, table, lens = random_case(7 + d + bs, RAGGED, 8, 2, d, bs, dtype, poison=True)
+    for s in (1, 0, 4):
+        check(q, kc, vc, table, lens, 1 / math.sqrt(d), s, f"{dtype} d={d} bs={bs} s={s}")
+
+
+def test_tiny_config_append_then_decode():
+    """Tiny workload: batch 2, 8 q / 2 kv heads, d 64, lengths {17, 40} + 1 appended, fp32."""
+    inp = gen.tiny_inputs()
+    spec = inp.spec
+    kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
+    slots = torch.tensor([oracle.slot_of(inp.block_table[b], n, spec.block_size)
+                          for b, n in enumerate(inp.cached)], dtype=torch.int64)
+    gk, gv = dev(kc), dev(vc)
+    pkv.kv_append(dev(inp.k_new[0]), dev(inp.v_new[0]), gk, gv, dev(slots))
+    oracle.kv_append(kc, vc, inp.k_new[0], inp.v_new[0], slots)
+    lens = torch.tensor([n + 1 for n in inp.cached], dtype=torch.int32)
+    for s in (1, 0):
+        out = torch.empty((spec.batch, spec.q_heads, spec.head_dim), device="cuda")
+        lse = torch.empty((spec.batch, spec.q_heads), device="cuda")
+        pkv.paged_decode_attention(out, dev(inp.q[0]), gk, gv, dev(inp.block_table), dev(lens),
+                                   spec.scale, lse=lse, num_splits=s,
+                                   workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+        ref, ref_lse = oracle.paged_decode(inp.q[0], kc, vc, inp.block_table, lens, spec.scale)
+        assert_attn_close(out, ref, "tiny out")
+        assert_attn_close(lse, ref_lse, "tiny lse")
+    assert torch.equal(gk.cpu(), kc) and torch.equal(gv.cpu(), vc)
+    assert pkv.get_device_error() == 0
+
+
+def _d1_golden():
+    with open(os.path.join(GOLDEN, "d1_worked_example.json")) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 1), (torch.bfloat16, 64)])
+def test_d1_worked_example_on_gpu(dtype, d):
+    """zwjcode.cn "KV Cache 的增量解码" §04: cache [1,2] / [10,20], append (0, 30), q = 1 -> 18.45.
+
+    d = 1 runs on the CUDA-core path; the bf16 case embeds the one-dimensional head
+    in the first lane of a 64-wide head (zeros elsewhere) to run the tensor-core path.
+    """
+    g = _d1_golden()
+    bs = 16
+    kc = torch.zeros((2, 1, bs, d), dtype=dtype)
+    vc = torch.zeros_like(kc)
+    table = torch.tensor([[1]], dtype=torch.int32)
+    kc[1, 0, 0, 0], kc[1, 0, 1, 0] = g["K_before_append"]
+    vc[1, 0, 0, 0], vc[1, 0, 1, 0] = g["V_before_append"]
+    gk, gv = dev(kc), dev(vc)
+    k3 = torch.zeros((1, 1, d), dtype=dtype)
+    v3 = torch.zeros((1, 1, d), dtype=dtype)
+    k3[0, 0, 0], v3[0, 0, 0] = g["k3"], g["v3"]
+    pkv.kv_append(dev(k3), dev(v3), gk, gv, dev(torch.tensor([oracle.slot_of(table[0], 2, bs)])))
+    q = torch.zeros((1, 1, d))
+    q[0, 0, 0] = g["q3"]
+    out, lse = run_decode(q, gk.cpu(), gv.cpu(), table, torch.tensor([3], dtype=torch.int32), g["scale"], 1)
+    assert round(float(out[0, 0, 0]), g["o3_printed_decimals"]) == g["o3_printed"]
+    oracle.kv_append(kc, vc, k3, v3, torch.tensor([oracle.slot_of(table[0], 2, bs)]))
+    ref, ref_lse = oracle.paged_decode(q, kc, vc, table, torch.tensor([3], dtype=torch.int32), g["scale"])
+    assert_attn_close(out, ref, "d1 out")
+    assert_attn_close(lse, ref_lse, "d1 lse")
+
+
+def test_lse_optional_and_empty_batch():
+    q, kc, vc, table, lens = random_case(77, [5, 0, 40], 8, 2, 128, 16, torch.bfloat16)
+    out, _ = run_decode(q, kc, vc, table, lens, 0.1, 0, with_lse=False)
+    ref, _ = oracle.paged_decode(q, kc, vc, table, lens, 0.1)
+    assert_attn_close(out, ref, "no-lse out")
+    assert torch.all(out[1] == 0)
+    empty = torch.empty((0, 8, 128), device="cuda")
+    pkv.paged_decode_attention(empty, empty.clone(), dev(kc), dev(vc),
+                               torch.empty((0, 4), dtype=torch.int32, device="cuda"),
+                               torch.empty((0,), dtype=torch.int32, device="cuda"), 0.1)
+
+
+def test_workspace_too_small_is_rejected():
+    q, kc, vc, table, lens = random_case(78, [300, 300], 8, 2, 128, 16, torch.bfloat16)
+    out = torch.empty((2, 8, 128), device="cuda")
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.paged_decode_attention(out, dev(q), dev(kc), dev(vc), dev(table), dev(lens), 0.1,
+                                   num_splits=4, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert ei.value.status == 3
+
+
+def test_bad_lengths_and_block_ids_raise_device_errors():
+    q, kc, vc, table, lens = random_case(79, [20, 40], 8, 2, 128, 16, torch.bfloat16)
+    bad_len = torch.tensor([20, 10_000], dtype=torch.int32)
+    out, lse = run_decode(q, kc, vc, table, bad_len, 0.1, 1)
+    assert pkv.get_device_error() & pkv.DEVERR["len"]
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    ref, _ = oracle.paged_decode(q[:1], kc, vc, table[:1], lens[:1], 0.1)
+    assert_attn_close(out[:1], ref, "valid sequence next to a bad one")
+    bad_table = table.clone()
+    bad_table[1, 1] = kc.shape[0] + 3
+    for s in (1, 0):
+        out, _ = run_decode(q, kc, vc, bad_table, lens, 0.1, s)
+        assert pkv.get_device_error() & pkv.DEVERR["block"]
+        assert torch.isfinite(out).all()
