@@ -1,0 +1,533 @@
+"""Benchmark of the paged KV-cache decode path on GB300.
+
+Default workload: Llama-2-70B-shaped GQA decode, one layer -- batch 64, 64 query /
+8 KV heads (m = 8), head_dim 128, cached lengths uniform in [512, 8192], bf16
+K/V, block size 16, shuffled physical blocks, a cycle of 32 consecutive decode
+steps that each append one token per sequence.  One bench step = one decode step
+of the whole path: kv_append of the 64 new tokens, then paged_decode_attention
+(split-K partials + log-sum-exp merge) for all 64 x 64 heads.
+
+Metric: KV-cache bytes read per second (logical bytes: every cached token's K and
+V of every KV head, 2 bytes each), with tokens/s per layer beside it.  Other
+workloads (--workload) print the same line for the 7B MHA, long-context GQA/MQA
+and varlen-prefill configurations.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun every rank runs the same per-GPU workload (weak scaling, no
+collective on the data path); rank 0 prints one JSON line with the max time over
+ranks.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import gen  # noqa: E402
+
+METRIC = "paged GQA decode: KV-cache read GB/s (% of HBM peak); tokens/s per layer"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------- utilities
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_cache_165_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary_name, source_hash):
+    """DRAM bytes per launch recorded in a profile summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_val or m_hash.group(1) != source_hash:
+        return None
+    return float(m_val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU is under load."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].strip() not in ("", "[N/A]"))}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ------------------------------------------------------------------ workloads
+
+class DecodeWorkload:
+    """Decode steps over a paged cache: append one token per sequence, then attend."""
+
+    def __init__(self, spec, lengths, cycle, label):
+        self.spec, self.lengths, self.cycle, self.label = spec, list(lengths), cycle, label
+
+    # bytes of K and V read by one step c of the cycle (every cached token, every KV head)
+    def kv_bytes(self, c):
+        elt = 2 if self.spec.cache_dtype == torch.bfloat16 else 4
+        return sum(n + c + 1 for n in self.lengths) * self.spec.kv_heads * self.spec.head_dim * 2 * elt
+
+    def describe(self):
+        s = self.spec
+        return {"workload": self.label, "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads,
+                "head_dim": s.head_dim, "block_size": s.block_size, "cache_dtype": "bf16",
+                "q_dtype": "fp32", "mean_cached_len": sum(self.lengths) / len(self.lengths),
+                "decode_steps_cycle": self.cycle,
+                "kv_gb_per_step": self.kv_bytes(self.cycle // 2) / 1e9,
+                "l2": "inputs larger than L2: each step reads %.2f GB of K/V vs 129 MB L2"
+                      % (self.kv_bytes(0) / 1e9)}
+
+    def setup(self, device):
+        import paged_kv_cache_165_gb300 as pkv
+        s = self.spec
+        bs = s.block_size
+        g = gen.generator(s.seed)
+        nb = sum(gen.blocks_needed(n + self.cycle, bs) for n in self.lengths)
+        bm = pkv.BlockManager(nb, bs, order=gen.permutation(g, nb))
+        for b, n in enumerate(self.lengths):
+            bm.add_sequence(b, n)
+        slots, clens = [], []
+        for c in range(self.cycle):
+            sl, copies = bm.append_step(range(s.batch))
+            assert not copies
+            slots.append(torch.tensor(sl, dtype=torch.int64))
+            clens.append(bm.context_lens(range(s.batch)))
+        self.nb = nb
+        self.table = bm.block_table(range(s.batch)).to(device)
+        self.slots_h = [t.pin_memory() for t in slots]
+        self.clens_h = [t.pin_memory() for t in clens]
+        self.slots = [t.to(device) for t in slots]
+        self.clens = [t.to(device) for t in clens]
+        cg = torch.Generator(device=device)
+        cg.manual_seed(s.seed)
+        shape = (nb, s.kv_heads, bs, s.head_dim)
+        self.k_cache = torch.randn(shape, generator=cg, device=device, dtype=torch.float32).to(s.cache_dtype)
+        self.v_cache = torch.randn(shape, generator=cg, device=device, dtype=torch.float32).to(s.cache_dtype)
+        B, Hq, Hkv, d = s.batch, s.q_heads, s.kv_heads, s.head_dim
+        self.q = torch.randn((self.cycle, B, Hq, d), generator=cg, device=device)
+        self.k_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(s.cache_dtype)
+        self.v_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(s.cache_dtype)
+        self.out = torch.empty((B, Hq, d), device=device)
+        self.lse = torch.empty((B, Hq), device=device)
+        ws = pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, self.table.shape[1], 0)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        self.splits = 1 if ws == 0 else None
+        # pinned host copies of the per-step inputs and the output (end-to-end arm)
+        self.q_h = self.q.cpu().pin_memory()
+        self.k_new_h = self.k_new.cpu().pin_memory()
+        self.v_new_h = self.v_new.cpu().pin_memory()
+        self.out_h = torch.empty((B, Hq, d)).pin_memory()
+        self.q_d = torch.empty_like(self.q[0])
+        self.k_d = torch.empty_like(self.k_new[0])
+        self.v_d = torch.empty_like(self.v_new[0])
+        self.s_d = torch.empty_like(self.slots[0])
+        self.c_d = torch.empty_like(self.clens[0])
+        self.pkv = pkv
+        self.launches_per_step = 2 + (1 if ws > 0 else 0)   # append, decode split, merge
+
+    def append(self, c):
+        self.pkv.kv_append(self.k_new[c], self.v_new[c], self.k_cache, self.v_cache, self.slots[c])
+
+    def attend(self, c):
+        self.pkv.paged_decode_attention(self.out, self.q[c], self.k_cache, self.v_cache, self.table,
+                                        self.clens[c], self.spec.scale, lse=self.lse, workspace=self.ws)
+
+    def e2e_step(self, c):
+        """The same step through the public API from pinned host buffers and back."""
+        self.q_d.copy_(self.q_h[c], non_blocking=True)
+        self.k_d.copy_(self.k_new_h[c], non_blocking=True)
+        self.v_d.copy_(self.v_new_h[c], non_blocking=True)
+        self.s_d.copy_(self.slots_h[c], non_blocking=True)
+        self.c_d.copy_(self.clens_h[c], non_blocking=True)
+        self.pkv.kv_append(self.k_d, self.v_d, self.k_cache, self.v_cache, self.s_d)
+        self.pkv.paged_decode_attention(self.out, self.q_d, self.k_cache, self.v_cache, self.table,
+                                        self.c_d, self.spec.scale, workspace=self.ws)
+        self.out_h.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        h2d = sum(t[0].numel() * t[0].element_size() for t in (self.q_h, self.k_new_h, self.v_new_h))
+        h2d += self.slots_h[0].numel() * 8 + self.clens_h[0].numel() * 4
+        return h2d, self.out_h.numel() * 4
+
+    # ---- CPU oracle on a bounded sample (same shapes and distribution, own draws)
+    def oracle_sample(self, n_seq, steps=1):
+        import oracle
+        s = self.spec
+        sub = gen.DecodeSpec(s.name + "_sample", s.seed + 77, n_seq, s.q_heads, s.kv_heads, s.head_dim,
+                             s.cache_dtype, s.block_size, steps)
+        inp = gen.decode_inputs(sub, self.lengths[:n_seq], steps=steps)
+        bs = s.block_size
+        threads = os.cpu_count() or 1
+
+        def run(c):
+            slots = torch.tensor([oracle.slot_of(inp.block_table[b], n + c, bs)
+                                  for b, n in enumerate(inp.cached)])
+            oracle.kv_append(inp.k_cache, inp.v_cache, inp.k_new[c], inp.v_new[c], slots)
+            lens = torch.tensor([n + c + 1 for n in inp.cached], dtype=torch.int32)
+            oracle.paged_decode(inp.q[c], inp.k_cache, inp.v_cache, inp.block_table, lens, s.scale,
+                                nthreads=threads)
+            elt = 2 if s.cache_dtype == torch.bfloat16 else 4
+            return int(lens.sum()) * s.kv_heads * s.head_dim * 2 * elt
+        return run, threads
+
+
+class PrefillWorkload:
+    """Varlen causal prefill of 8 prompts (lengths uniform in [256, 4096]) writing the cache."""
+
+    def __init__(self):
+        self.lengths = gen.long_prefill_lengths()
+        self.hq, self.hkv, self.d, self.bs = 64, 8, 128, 16
+        self.label = "long-context prefill: 8 prompts U[256,4096], 64 q / 8 kv heads, d 128, bf16"
+
+    def flops(self):
+        # causal: sum_b L(L+1)/2 query-key pairs x Hq x (2d for q.k + 2d for p.v)
+        return sum(n * (n + 1) // 2 for n in self.lengths) * self.hq * 4 * self.d
+
+    def describe(self):
+        return {"workload": self.label, "prompt_lengths": self.lengths, "q_heads": self.hq,
+                "kv_heads": self.hkv, "head_dim": self.d, "tflop_per_step": self.flops() / 1e12,
+                "l2": "K/V of all prompts (%.0f MB) re-read from L2 across query tiles"
+                      % (sum(self.lengths) * self.hkv * self.d * 4 / 1e6)}
+
+    def setup(self, device):
+        import paged_kv_cache_165_gb300 as pkv
+        self.pkv = pkv
+        p = gen.prefill_inputs(self.lengths, self.hq, self.hkv, self.d, torch.bfloat16, seed=4)
+        self.p = p
+        self.q, self.k, self.v = p.q.to(device), p.k.to(device), p.v.to(device)
+        self.cu = p.cu_seqlens.to(device)
+        nb = sum(gen.blocks_needed(n) for n in self.lengths)
+        bm = pkv.BlockManager(nb, self.bs, order=gen.permutation(gen.generator(4), nb))
+        for s, n in enumerate(self.lengths):
+            bm.add_sequence(s, n)
+        self.slots = torch.cat([bm.slot_mapping(s, range(n)) for s, n in enumerate(self.lengths)]).to(device)
+        self.kc = torch.zeros((nb, self.hkv, self.bs, self.d), dtype=torch.bfloat16, device=device)
+        self.vc = torch.zeros_like(self.kc)
+        self.out = torch.empty((p.q.shape[0], self.hq, self.d), device=device)
+        self.launches_per_step = 2
+
+    def step(self, c):
+        self.pkv.prefill_attention(self.out, self.q, self.k, self.v, self.cu, max(self.lengths),
+                                   1 / math.sqrt(self.d), k_cache=self.kc, v_cache=self.vc,
+                                   slot_mapping=self.slots)
+
+
+WORKLOADS = {
+    "gqa70b": lambda: DecodeWorkload(gen.GQA_70B, gen.gqa_70b_lengths(), 32,
+                                     "llama2-70b-shaped GQA decode: batch 64, 64 q / 8 kv heads, d 128, "
+                                     "lengths U[512,8192], 32-step append+attend cycle, bs 16, bf16 KV"),
+    "mha7b": lambda: DecodeWorkload(gen.MHA_7B, [gen.MHA_7B_LENGTH] * gen.MHA_7B.batch, 1,
+                                    "llama2-7b-shaped MHA decode: batch 32, 32 q = 32 kv heads, d 128, "
+                                    "2048 cached tokens, one append+attend step, bs 16, bf16 KV"),
+    "long_gqa": lambda: DecodeWorkload(gen.LONG_GQA, [gen.LONG_LENGTH] * 4, 1,
+                                       "long-context split-K GQA decode: batch 4, 64 q / 8 kv heads, d 128, "
+                                       "131072 cached tokens, bs 16, bf16 KV"),
+    "long_mqa": lambda: DecodeWorkload(gen.LONG_MQA, [gen.LONG_LENGTH] * 4, 1,
+                                       "long-context split-K MQA decode: batch 4, 64 q / 1 kv head, d 128, "
+                                       "131072 cached tokens, bs 16, bf16 KV"),
+    "prefill": PrefillWorkload,
+}
+
+
+# ------------------------------------------------------------------- our arm
+
+def bench_ours(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    import paged_kv_cache_165_gb300 as pkv
+    from paged_kv_cache_165_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pkv.lib()
+
+    wl = WORKLOADS[args.workload]()
+    wl.setup(device)
+    is_decode = isinstance(wl, DecodeWorkload)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        c = i % wl.cycle if is_decode else 0
+        if is_decode:
+            wl.append(c)
+            wl.attend(c)
+        else:
+            wl.step(c)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # soak (untimed) so that clocks settle and the sampler sees the GPU under load
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    t_end = time.time() + args.soak
+    i = args.warmup
+    while time.time() < t_end:
+        step(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps, events on the launching stream
+    first = i
+    n_ev = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        c = (first + k) % wl.cycle if is_decode else 0
+        if is_decode:
+            wl.append(c)
+            ev_a[k].record(stream)
+            wl.attend(c)
+            ev_b[k].record(stream)
+        else:
+            ev_a[k].record(stream)
+            wl.step(c)
+            ev_b[k].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    kernel_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+    max_ms = elapsed_ms
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        max_ms = float(t.item())
+
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+    ms_per_step = max_ms / args.steps
+    res = {"metric": METRIC, "impl": "ours"}
+    if is_decode:
+        step_bytes = [wl.kv_bytes((first + k) % wl.cycle) for k in range(args.steps)]
+        total_bytes = sum(step_bytes) * world
+        value = total_bytes / (max_ms / 1e3) / 1e9
+        kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
+        achieved = (sum(step_bytes) / len(step_bytes)) / (kern_avg_ms / 1e3) / 1e9
+        src = kernel_source_hash(["decode.cu", "common.cuh"])
+        traffic = profiled_traffic(f"decode_{args.workload}.md", src)
+        res.update({
+            "value": value, "unit": "GB/s", "pct_hbm_peak": 100 * value / hbm,
+            "tokens_per_s_per_layer": wl.spec.batch * world / (ms_per_step / 1e3),
+            "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (split-K partials + LSE merge)",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s",
+                         "algorithmic_bytes_per_launch": sum(step_bytes) / len(step_bytes),
+                         "avg_launch_ms": kern_avg_ms,
+                         "traffic": traffic, "kernel_source_sha256_16": src},
+        })
+    else:
+        flops = wl.flops()
+        value = flops * world * args.steps / (max_ms / 1e3) / 1e12
+        kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
+        achieved = flops / (kern_avg_ms / 1e3) / 1e12
+        src = kernel_source_hash(["prefill.cu", "common.cuh"])
+        res.update({
+            "metric": "varlen causal prefill TFLOP/s (4*Hq*d per causal query-key pair)",
+            "value": value, "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "kernel": "prefill_attention (cache write + attention)",
+                         "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
+                         "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                         "avg_launch_ms": kern_avg_ms,
+                         "traffic": profiled_traffic("prefill.md", src), "kernel_source_sha256_16": src},
+        })
+    res.update({
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "accumulate": "fp32", "data": "synthetic (seeded N(0,1), shuffled blocks)",
+        "config": dict(wl.describe(), parallelism=f"replicas x{world} (independent batches)",
+                       soak_s=args.soak),
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "clocks": clocks,
+    })
+
+    # ---- end to end through the public API with pinned host buffers
+    if is_decode:
+        for k in range(3):
+            wl.e2e_step(k % wl.cycle)
+        torch.cuda.synchronize()
+        e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        for k in range(args.steps):
+            wl.e2e_step((first + k) % wl.cycle)
+        e_stop.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e_start.elapsed_time(e_stop)
+        if world > 1:
+            t = torch.tensor([e_ms], device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d, d2h = wl.e2e_bytes()
+        res["e2e"] = {"value": sum(step_bytes) * world / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+                      "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h}
+
+    # ---- CPU oracle baseline (rank 0, one GPU only)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and is_decode:
+        run, threads = wl.oracle_sample(min(args.cpu_seqs, wl.spec.batch))
+        t0 = time.perf_counter()
+        nbytes = run(0)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads,
+                               "kind": "oracle",
+                               "sample": f"one append+attend step of {min(args.cpu_seqs, wl.spec.batch)} of the {wl.spec.batch} "
+                                         f"sequences (same lengths and shapes, own seeded draws), "
+                                         f"fp64 C oracle, {threads} threads, {dt:.2f} s"}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+# ------------------------------------------------------------ reference arm
+
+def bench_reference(args):
+    """The fp64 CPU oracle as the reference arm, on a bounded sample per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]()
+    if not isinstance(wl, DecodeWorkload):
+        print(json.dumps({"impl": "reference", "unavailable": "reference arm covers the decode workloads"}))
+        return
+    run, threads = wl.oracle_sample(args.ref_seqs, steps=wl.cycle)
+    for k in range(args.warmup):
+        run(k % wl.cycle)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for k in range(args.steps):
+        nbytes += run((args.warmup + k) % wl.cycle)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    sample = (f"each step: one append+attend step of {args.ref_seqs} of the {wl.spec.batch} sequences "
+              f"(same lengths and shapes, own seeded draws), fp64 C oracle, {threads} threads")
+    print(json.dumps({
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": wl.describe(),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gqa70b", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--soak", type=float, default=1.5, help="untimed seconds before the timed steps")
+    ap.add_argument("--cpu-seqs", type=int, default=64,
+                    help="sequences in the CPU-baseline sample (one step)")
+    ap.add_argument("--ref-seqs", type=int, default=8,
+                    help="sequences per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup_requested = args.warmup
+    args.warmup = max(args.warmup, 3)     # at least three untimed warm-up steps
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()
