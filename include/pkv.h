@@ -161,6 +161,38 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
                                       size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_paged_decode_attention_noalloc -- pkv_paged_decode_attention without a workspace.
+ *
+ * The paper has no counterpart for this entry point: it exists for callers that cannot
+ * call cudaMalloc -- a plugin or extension running inside a host application that owns
+ * every byte of device memory and hands out none, or a latency-critical decode loop that
+ * must not allocate or free device memory in the middle of a step because cudaFree (and
+ * often cudaMalloc) synchronises the whole device.
+ *
+ * Arguments, layouts and results are those of pkv_paged_decode_attention, minus
+ * `workspace` and `workspace_bytes`.  The split-K partials go to a scratch array built
+ * into the library: a static device array of PKV_NOALLOC_SCRATCH_BYTES bytes that every
+ * GPU which loads the library holds until the process exits.
+ *   - Sizes whose partials need more than PKV_NOALLOC_SCRATCH_BYTES (the value
+ *     pkv_decode_workspace_bytes returns for the same arguments) are rejected with
+ *     PKV_ERR_WORKSPACE before anything is enqueued; num_splits = 1 needs no scratch.
+ *   - The first call on each device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents.  Calls
+ *     that overlap on the GPU (other streams, other host threads) race on it: the
+ *     caller must order them.  Nothing in the array has to start at zero.
+ *   - No call allocates or frees device memory.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+pkv_status pkv_paged_decode_attention_noalloc(float *out, float *lse, const float *q,
+                                              const void *k_cache, const void *v_cache,
+                                              pkv_dtype dt, const int32_t *block_table,
+                                              const int32_t *context_lens, int B, int Hq, int Hkv,
+                                              int d, int bs, int MBS, int NB, float scale,
+                                              int num_splits, pkv_stream_t stream);
+
+/*
  * pkv_prefill_attention -- varlen causal attention of whole prompts, writing the cache.
  *
  * Sequences are packed: sequence b owns tokens [cu_seqlens[b], cu_seqlens[b+1]) of

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     lib,
     library_path,
     paged_decode_attention,
+    paged_decode_attention_noalloc,
     prefill_attention,
 )
 from .blocks import BlockManager, OutOfBlocks  # noqa: F401

@@ -64,6 +64,9 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P,
                                              Z, P]
     L.pkv_paged_decode_attention.restype = I
+    L.pkv_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I,
+                                                     F, I, P]
+    L.pkv_paged_decode_attention_noalloc.restype = I
     L.pkv_prefill_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, P, P, P, I, I, P]
     L.pkv_prefill_attention.restype = I
     L.pkv_get_device_error.argtypes = [ctypes.POINTER(I), P]
@@ -178,6 +181,30 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table),
         _ptr(context_lens), B, Hq, Hkv, d, bs, MBS, NB, float(scale), int(num_splits),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_table, context_lens, scale,
+                                   lse=None, num_splits=0, stream=None) -> None:
+    """paged_decode_attention with the library's built-in split-K scratch (no workspace)."""
+    _cuda("k_cache", k_cache)
+    dt = _dtype(k_cache)
+    _cuda("v_cache", v_cache, k_cache.dtype)
+    _cuda("q", q, torch.float32)
+    _cuda("out", out, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    if lse is not None:
+        _cuda("lse", lse, torch.float32)
+    NB, Hkv, bs, d = k_cache.shape
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d) or block_table.dim() != 2 or \
+            block_table.shape[0] != B or context_lens.numel() != B or \
+            (lse is not None and lse.numel() != B * Hq):
+        raise ValueError("paged_decode_attention_noalloc: shapes do not match")
+    _check(lib().pkv_paged_decode_attention_noalloc(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table),
+        _ptr(context_lens), B, Hq, Hkv, d, bs, block_table.shape[1], NB, float(scale),
+        int(num_splits), _stream(stream)))
 
 
 def prefill_attention(out, q, k, v, cu_seqlens, max_seqlen, scale, lse=None, k_cache=None,

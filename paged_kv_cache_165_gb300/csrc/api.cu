@@ -102,6 +102,19 @@ bool encode_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_
     return res == CUDA_SUCCESS;
 }
 
+pkv_status current_device_info(int *sm_count, unsigned **err) {
+    DeviceState *st = nullptr;
+    const pkv_status s = device_state(&st);
+    if (s != PKV_OK) return s;
+    *sm_count = st->sm_count;
+    *err = st->err;
+    return PKV_OK;
+}
+
+pkv_status record_error(pkv_status status, const char *message) {
+    return fail(status, "%s", message);
+}
+
 }  // namespace pkv
 
 using namespace pkv;

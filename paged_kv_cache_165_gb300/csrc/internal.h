@@ -17,6 +17,11 @@ namespace pkv {
 bool encode_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                      const uint64_t *strides_bytes, const uint32_t *box);
 
+// Per-device state of the current device (SM count, device error word), set up on
+// first use; and recording of the calling thread's pkv_last_error() message.
+pkv_status current_device_info(int *sm_count, unsigned **err);
+pkv_status record_error(pkv_status status, const char *message);
+
 // ---------------------------------------------------------------- cache ops
 
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
