@@ -133,6 +133,7 @@ class DecodeWorkload:
 
     def __init__(self, spec, lengths, cycle, label):
         self.spec, self.lengths, self.cycle, self.label = spec, list(lengths), cycle, label
+        self.num_splits = 0
 
     # bytes of K and V read by one step c of the cycle (every cached token, every KV head)
     def kv_bytes(self, c):
@@ -181,8 +182,8 @@ class DecodeWorkload:
         self.v_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(s.cache_dtype)
         self.out = torch.empty((B, Hq, d), device=device)
         self.lse = torch.empty((B, Hq), device=device)
-        ws = pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, self.table.shape[1], 0)
-        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        ws = pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, self.table.shape[1], self.num_splits)
+        self.ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)   # zeroed once
         self.splits = 1 if ws == 0 else None
         # pinned host copies of the per-step inputs and the output (end-to-end arm)
         self.q_h = self.q.cpu().pin_memory()
@@ -202,7 +203,8 @@ class DecodeWorkload:
 
     def attend(self, c):
         self.pkv.paged_decode_attention(self.out, self.q[c], self.k_cache, self.v_cache, self.table,
-                                        self.clens[c], self.spec.scale, lse=self.lse, workspace=self.ws)
+                                        self.clens[c], self.spec.scale, lse=self.lse,
+                                        num_splits=self.num_splits, workspace=self.ws)
 
     def e2e_step(self, c):
         """The same step through the public API from pinned host buffers and back."""
@@ -213,7 +215,8 @@ class DecodeWorkload:
         self.c_d.copy_(self.clens_h[c], non_blocking=True)
         self.pkv.kv_append(self.k_d, self.v_d, self.k_cache, self.v_cache, self.s_d)
         self.pkv.paged_decode_attention(self.out, self.q_d, self.k_cache, self.v_cache, self.table,
-                                        self.c_d, self.spec.scale, workspace=self.ws)
+                                        self.c_d, self.spec.scale, num_splits=self.num_splits,
+                                        workspace=self.ws)
         self.out_h.copy_(self.out, non_blocking=True)
 
     def e2e_bytes(self):
@@ -321,6 +324,8 @@ def bench_ours(args):
     pkv.lib()
 
     wl = WORKLOADS[args.workload]()
+    if hasattr(wl, "num_splits"):
+        wl.num_splits = args.num_splits
     wl.setup(device)
     is_decode = isinstance(wl, DecodeWorkload)
     stream = torch.cuda.current_stream()
@@ -429,7 +434,7 @@ def bench_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "accumulate": "fp32", "data": "synthetic (seeded N(0,1), shuffled blocks)",
         "config": dict(wl.describe(), parallelism=f"replicas x{world} (independent batches)",
-                       soak_s=args.soak),
+                       soak_s=args.soak, num_splits=args.num_splits),
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clocks,
     })
@@ -514,6 +519,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="gqa70b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="decode split-K chunks per sequence (0: the library's plan)")
     ap.add_argument("--soak", type=float, default=1.5, help="untimed seconds before the timed steps")
     ap.add_argument("--cpu-seqs", type=int, default=64,
                     help="sequences in the CPU-baseline sample (one step)")

@@ -121,8 +121,11 @@ pkv_status pkv_kv_block_copy(void *k_cache, void *v_cache, pkv_dtype dt, const i
 /*
  * Bytes of split-K workspace pkv_paged_decode_attention needs for these sizes and
  * num_splits on the current device (0 when the call runs in one pass).  The split
- * count chosen for num_splits == 0 depends on the device's SM count.
+ * count chosen for num_splits == 0 depends on the device's SM count.  The workspace
+ * starts with PKV_DECODE_COUNTER_BYTES of arrival counters, then the chunk partials.
  */
+#define PKV_DECODE_COUNTER_BYTES (256u << 10)
+
 size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS, int num_splits);
 
 /*
@@ -147,8 +150,13 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS
  *   num_splits   0: chosen by the library; 1: one pass; k > 1: at most k chunks per
  *                sequence (chunk = ceil(MBS / k) blocks)
  *   workspace    device scratch of at least pkv_decode_workspace_bytes(...) bytes
- *                (may be NULL when that is 0); its contents need no initialisation
- *                and are overwritten.  Calls that share a workspace must not overlap.
+ *                (may be NULL when that is 0).  Zero it once after allocating it:
+ *                its first PKV_DECODE_COUNTER_BYTES hold arrival counters that must
+ *                be zero when a call starts, and every call that completes leaves
+ *                them zero again (the rest is overwritten), so one zeroed workspace
+ *                serves any sequence of calls and shapes.  After a call that raised
+ *                PKV_DEVERR_TIMEOUT, zero it again.  Calls that share a workspace
+ *                must not overlap.
  *   Requires Hq % Hkv == 0, B >= 0, d >= 1, bs >= 1, MBS >= 1.
  *   bf16 caches with d in {64, 128, 256}, bs in {16, 32}, 16-byte aligned caches use
  *   the tensor-core path; other shapes use a CUDA-core path with the same results.
@@ -180,7 +188,9 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
  *     device current; make that first call before any stream capture.
  *   - Every call shares the one array, which keeps the last call's contents.  Calls
  *     that overlap on the GPU (other streams, other host threads) race on it: the
- *     caller must order them.  Nothing in the array has to start at zero.
+ *     caller must order them.  The array is zero when the library loads; its first
+ *     PKV_DECODE_COUNTER_BYTES are arrival counters that every completed call leaves
+ *     at zero, and the rest need not start at zero.
  *   - No call allocates or frees device memory.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -183,9 +183,7 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS
     if (check_decode_sizes(B, Hq, Hkv, d, bs, MBS) != PKV_OK || num_splits < 0) return 0;
     DeviceState *st = nullptr;
     if (device_state(&st) != PKV_OK) return 0;
-    // the plan's split count does not depend on the element type or NB
-    return plan_decode(B, Hq, Hkv, d, bs, MBS, 1, PKV_BF16, num_splits, st->sm_count, true)
-        .workspace_bytes;
+    return decode_workspace_upper_bound(B, Hq, Hkv, d, bs, MBS, num_splits, st->sm_count);
 }
 
 pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, const void *k_cache,

@@ -5,24 +5,26 @@
 //   tokens, gathered through block_table[b] (limoncc.com "大语言模型研究15——注意力机制
 //   优化之KV缓存" §3.1, §3.3; plumephp.com "KV Cache 优化与注意力机制加速" §4.2-§4.3).
 // The softmax is taken online, block by block, keeping a running max m and running sum
-// l (plumephp.com §2.2, online_softmax_update), and each chunk of blocks yields the
-// log-sum-exp statistic m + log l (§2.3) by which chunk partials merge (split-K).
+// l (plumephp.com §2.2, online_softmax_update); any stretch of blocks yields the
+// log-sum-exp statistic m + log l (§2.3) by which partial results merge (split-K).
 //
-// Tensor-core path (bf16 cache, d in {64,128,256}, bs in {16,32}):
-//   * one CTA per (sequence, KV head, group of up to 8 query heads, chunk of blocks);
-//     its warps take the chunk's blocks round-robin, each warp with a private ring of
-//     shared-memory stages filled by TMA (one K and one V tile of bs x d per block,
-//     128-byte swizzled, completion on an mbarrier with a bounded wait);
-//   * the m query heads of a GQA group share every K/V tile read from HBM: scores are
-//     one m16n8k16 bf16 MMA tile per 8 tokens whose 16 rows are the group's heads
-//     twice -- rows 0-7 the bf16 "hi" part of q, rows 8-15 the bf16 "lo" remainder --
-//     so q (fp32) enters the tensor core to ~2^-16 relative and hi+lo rows sum in fp32;
-//     the softmax weights P are split the same way for P.V, whose output rows 0-7 and
-//     8-15 again sum to one fp32 result;
-//   * per-warp running (m, l, O) merge across warps in shared memory at the end.
-// CUDA-core path: any d <= 256, fp32 or bf16 cache; one warp per (sequence, head, chunk).
-// With more than one chunk per sequence both paths write (o, lse) partials to the
-// caller's workspace and a merge kernel combines them by log-sum-exp.
+// Tensor-core page math (bf16 cache, d in {64,128,256}, bs in {16,32}), shared by two
+// kernels.  One warp consumes one block page (bs tokens x d of K, then of V) that TMA
+// brought into a 128-byte-swizzled shared-memory stage.  The m query heads of a GQA group
+// share every K/V tile read from HBM: scores are m16n8k16 bf16 MMAs whose 16 A rows are
+// the group's (up to 8) heads twice -- rows 0-7 the bf16 rounding of q ("hi"), rows
+// 8-15 the bf16 rounding of the remainder q - hi ("lo") -- so the fp32 query enters the
+// tensor core to about 2^-16 relative and the two rows of a head, held by the same
+// thread, add in fp32.  The softmax weights P are split the same way for P.V.
+//
+// decode_chunked_kernel: one CTA per (sequence, KV-head group, chunk of blocks), whose
+//   warps take the chunk's blocks round-robin, each warp with a private TMA ring.  Chunks
+//   of a unit write normalised partials; the last chunk to finish (an arrival counter, no
+//   waiting) merges them by log-sum-exp.  Many short-lived CTAs let the hardware scheduler
+//   balance SMs whose memory paths differ in speed (an equal static split of the pages
+//   over persistent warps measured a 137-209 us spread of per-warp finish times).
+// CUDA-core path (fp32 caches, other head sizes): one warp per (sequence, head, chunk),
+//   chunks merged by decode_merge_kernel.
 #include <algorithm>
 #include <atomic>
 #include <math.h>
@@ -40,17 +42,18 @@ constexpr unsigned kFull = 0xffffffffu;
 struct DecodeKParams {
     float *out;
     float *lse;
-    float *ws_o;     // [B*Hq][splits][d]
-    float *ws_lse;   // [B*Hq][splits], log2 domain
+    float *ws_o;         // partial outputs (layout per kernel, see plan_decode)
+    float *ws_lse;       // partial log-sum-exp, base 2
+    unsigned *counters;  // arrival counters, one per (sequence, KV head, head tile) unit
     const float *q;
     const int32_t *block_table;
     const int32_t *context_lens;
     unsigned *err;
     int B, Hq, Hkv, m, MBS, NB;
-    int head_tiles;   // ceil(m / 8): CTAs per KV head along grid.y
-    int chunk_pages;
-    int splits;
-    float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
+    int head_tiles;   // ceil(m / 8): head groups per KV head
+    int chunk_pages;  // blocks per chunk
+    int splits;       // chunks per sequence at most (partial slots per sequence)
+    float scale_log2; // scale * log2(e): scores are kept in the base-2 domain
 };
 
 // Sequence length after validation; an invalid length counts as empty.
@@ -63,51 +66,199 @@ __device__ __forceinline__ int checked_len(const DecodeKParams &p, int b, int bs
     return len;
 }
 
-// =============================================================== tensor-core path
+// ============================================================ tensor-core page math
 
-template <int D, int BS, int NW, int ST>
-struct MmaCfg {
-    static constexpr int kPageBytes = BS * D * 2;             // one K (or V) tile of a block
-    static constexpr int kStageBytes = 2 * kPageBytes;        // K tile then V tile
-    static constexpr int kStagesBytes = NW * ST * kStageBytes;
-    static constexpr int kMergeBytes = NW * (16 + 8 * D) * 4;
-    static constexpr int kSmemBytes = 1024 + kStagesBytes + NW * ST * 8;
-    static_assert(kMergeBytes <= kStagesBytes, "merge scratch reuses the stage buffers");
+template <int D, int BS>
+struct TcPage {
+    static constexpr int NT = BS / 8;    // 8-token score tiles per block
+    static constexpr int KT = BS / 16;   // 16-token k-steps of P.V per block
+    static constexpr int KS = D / 16;    // 16-wide k-steps of q.K
+    static constexpr int ONT = D / 8;    // 8-wide output tiles
+    static constexpr int PANELS = D / 64;
+    static constexpr int kPageBytes = BS * D * 2;        // one K (or V) tile of a block
+    static constexpr int kStageBytes = 2 * kPageBytes;   // K tile then V tile
     static_assert(D % 64 == 0 && BS % 16 == 0, "tile shape");
+
+    // A fragments of q (16 rows x D): row g = hi part of head head0+g, row g+8 = its lo
+    // remainder; rows of heads outside the group (g >= nheads) are zero.
+    __device__ static void load_q(uint32_t (&qa)[KS][4], const float *q_group, int nheads,
+                                  int lane) {
+        const int g = lane >> 2, t4 = lane & 3;
+        const bool row_ok = g < nheads;
+        const float *qrow = q_group + (row_ok ? g : 0) * D;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
+            if (row_ok) {
+                x0 = *reinterpret_cast<const float2 *>(qrow + kk * 16 + 2 * t4);
+                x1 = *reinterpret_cast<const float2 *>(qrow + kk * 16 + 8 + 2 * t4);
+            }
+            split_bf16x2(x0.x, x0.y, qa[kk][0], qa[kk][1]);
+            split_bf16x2(x1.x, x1.y, qa[kk][2], qa[kk][3]);
+        }
+    }
+
+    // Lane 0: copy the K and V tiles whose first row is `row` into stage `dst`.
+    __device__ static void issue(uint32_t dst, uint32_t bar, const CUtensorMap *tm_k,
+                                 const CUtensorMap *tm_v, int row) {
+        mbar_arrive_expect_tx(bar, kStageBytes);
+#pragma unroll
+        for (int pn = 0; pn < PANELS; ++pn) {
+            tma_load_2d(dst + pn * BS * 128, tm_k, pn * 64, row, bar);
+            tma_load_2d(dst + kPageBytes + pn * BS * 128, tm_v, pn * 64, row, bar);
+        }
+    }
+
+    __device__ static void reset(float (&o)[ONT][4], float &m_run, float &l_run) {
+#pragma unroll
+        for (int nt = 0; nt < ONT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        m_run = -INFINITY;
+        l_run = 0.f;
+    }
+
+    // Consume one page: `valid` (1..BS) of its tokens belong to the sequence.  Updates
+    // this lane's running max (head g), partial sum and output fragments.
+    __device__ static void page(uint8_t *stage, int valid, const uint32_t (&qa)[KS][4],
+                                float (&o)[ONT][4], float &m_run, float &l_run,
+                                float scale_log2, int lane) {
+        const int t4 = lane & 3;
+        if (valid < BS) {
+            // V rows past the end of the sequence may hold anything (NaN, Inf): zero them
+            // so that their zero weights contribute exactly zero.
+            for (int idx = lane; idx < (BS - valid) * (D / 8); idx += 32) {
+                const int r = valid + idx / (D / 8), c16 = idx % (D / 8);
+                *reinterpret_cast<uint4 *>(stage + kPageBytes + (c16 >> 3) * BS * 128 + r * 128 +
+                                           (c16 & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        const uint32_t k_s = smem_addr(stage), v_s = k_s + kPageBytes;
+
+        // scores S^T: (2 x group heads) x BS tokens, fp32 accumulate
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                const int mi = lane >> 3, r8 = lane & 7;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(k_s + swz128(BS, np * 16 + (mi >> 1) * 8 + r8, kk * 16 + (mi & 1) * 8),
+                        b0, b1, b2, b3);
+                mma_bf16_16816(s[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                mma_bf16_16816(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+            }
+        }
+
+        // online softmax (base 2) for head g: rows g (hi) + g+8 (lo) of each tile
+        float sc[NT][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tok = nt * 8 + 2 * t4 + e;
+                const float v = (s[nt][e] + s[nt][2 + e]) * scale_log2;
+                sc[nt][e] = tok < valid ? v : -INFINITY;
+                mx = fmaxf(mx, sc[nt][e]);
+            }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        const float m_new = fmaxf(m_run, mx);   // finite: every page holds a valid token
+        const float alpha = exp2f(m_run - m_new);
+        float psum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                sc[nt][e] = exp2f(sc[nt][e] - m_new);
+                psum += sc[nt][e];
+            }
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+#pragma unroll
+        for (int nt = 0; nt < ONT; ++nt) {
+            o[nt][0] *= alpha;
+            o[nt][1] *= alpha;
+            o[nt][2] *= alpha;
+            o[nt][3] *= alpha;
+        }
+
+        // O += P V with P = P_hi (rows 0-7) + P_lo (rows 8-15)
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+            uint32_t a0, a1, a2, a3;
+            split_bf16x2(sc[2 * kt][0], sc[2 * kt][1], a0, a1);
+            split_bf16x2(sc[2 * kt + 1][0], sc[2 * kt + 1][1], a2, a3);
+#pragma unroll
+            for (int np = 0; np < D / 16; ++np) {
+                const int mi = lane >> 3, r8 = lane & 7;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(v_s + swz128(BS, kt * 16 + (mi & 1) * 8 + r8, np * 16 + (mi >> 1) * 8),
+                              b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_bf16_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        __syncwarp();
+    }
 };
 
 template <int D, int BS, int NW, int ST>
+struct MmaCfg {
+    using PG = TcPage<D, BS>;
+    static constexpr int kStagesBytes = NW * ST * PG::kStageBytes;
+    static constexpr int kMergeBytes = NW * (16 + 8 * D) * 4;
+    static constexpr int kSmemBytes = 1024 + kStagesBytes + NW * ST * 8;
+    static_assert(kMergeBytes <= kStagesBytes, "merge scratch reuses the stage buffers");
+};
+
+// Shared-memory stages of a block, aligned to the 1024-byte swizzle atom.
+__device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                       ~static_cast<uintptr_t>(1023));
+}
+
+// ================================================================ chunked kernel
+
+template <int D, int BS, int NW, int ST>
 __global__ void __launch_bounds__(NW * 32)
-    decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const DecodeKParams p) {
+    decode_chunked_kernel(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const DecodeKParams p) {
+    using PG = TcPage<D, BS>;
     using Cfg = MmaCfg<D, BS, NW, ST>;
-    constexpr int NT = BS / 8;    // 8-token score tiles per block
-    constexpr int KT = BS / 16;   // 16-token k-steps of P.V per block
-    constexpr int KS = D / 16;    // 16-wide k-steps of q.K
-    constexpr int ONT = D / 8;    // 8-wide output tiles
-    constexpr int PANELS = D / 64;
+    constexpr int KS = PG::KS, ONT = PG::ONT;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *smem = aligned_smem(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kStagesBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
-    const int split = blockIdx.x;
-    const int kvh = blockIdx.y / p.head_tiles;
-    const int head0 = kvh * p.m + (blockIdx.y % p.head_tiles) * 8;
-    const int nheads = min(8, (kvh + 1) * p.m - head0);
+    // grid: x = (chunk, head tile) with the tile fastest, y = KV head, z = sequence.  The
+    // head tiles of one KV head read the same pages, so they run side by side and share
+    // them in L2; chunks of one stream come next; the KV heads of one block, whose pages
+    // sit side by side in HBM, are far apart in launch order.
+    const int tile = blockIdx.x % p.head_tiles;
+    const int split = blockIdx.x / p.head_tiles;
+    const int kvh = blockIdx.y;
     const int b = blockIdx.z;
+    const int g_unit = kvh * p.head_tiles + tile;
+    const int head0 = kvh * p.m + tile * 8;
+    const int nheads = min(8, (kvh + 1) * p.m - head0);
 
-    const int len = checked_len(p, b, BS, threadIdx.x == 0 && split == 0 && blockIdx.y == 0);
+    const int len = checked_len(p, b, BS, threadIdx.x == 0 && split == 0 && g_unit == 0);
     const int n_pages = (len + BS - 1) / BS;
     const int pg0 = split * p.chunk_pages;
     const int pg1 = min(n_pages, pg0 + p.chunk_pages);
     if (pg0 >= pg1) {
-        // Nothing to read.  With one chunk this is an empty sequence: out = 0, lse = -inf.
-        // With several, the merge kernel knows from the length that this chunk is absent.
-        if (p.splits == 1) {
+        // Nothing to read.  Chunk 0 of an empty sequence writes out = 0, lse = -inf; any
+        // other empty chunk is simply absent (the merge counts chunks from the length).
+        if (split == 0) {
             for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32)
                 p.out[(static_cast<size_t>(b) * p.Hq + head0 + idx / D) * D + idx % D] = 0.f;
             if (p.lse != nullptr && threadIdx.x < nheads)
@@ -126,23 +277,8 @@ __global__ void __launch_bounds__(NW * 32)
     }
     __syncwarp();
 
-    // q fragments (A operand, 16 rows x D): row g = hi part of head head0+g, row g+8 =
-    // its lo remainder; rows of heads outside this CTA's group are zero.
     uint32_t qa[KS][4];
-    {
-        const bool row_ok = g < nheads;
-        const float *qrow = p.q + (static_cast<size_t>(b) * p.Hq + head0 + (row_ok ? g : 0)) * D;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
-            if (row_ok) {
-                x0 = *reinterpret_cast<const float2 *>(qrow + kk * 16 + 2 * t4);
-                x1 = *reinterpret_cast<const float2 *>(qrow + kk * 16 + 8 + 2 * t4);
-            }
-            split_bf16x2(x0.x, x0.y, qa[kk][0], qa[kk][1]);
-            split_bf16x2(x1.x, x1.y, qa[kk][2], qa[kk][3]);
-        }
-    }
+    PG::load_q(qa, p.q + (static_cast<size_t>(b) * p.Hq + head0) * D, nheads, lane);
 
     // This warp's blocks: pg0 + warp + NW*k, k = 0 .. n_my-1.  Block-table entries are
     // fetched 32 at a time (one per lane) ahead of the copies that need them.
@@ -171,21 +307,14 @@ __global__ void __launch_bounds__(NW * 32)
                 row = (phys * p.Hkv + kvh) * BS;
             }
             const int st = warp * ST + k % ST;
-            const uint32_t bar = smem_addr(&bars[st]);
-            const uint32_t dst = smem_addr(smem + static_cast<size_t>(st) * Cfg::kStageBytes);
-            mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
-#pragma unroll
-            for (int pn = 0; pn < PANELS; ++pn) {
-                tma_load_2d(dst + pn * BS * 128, &tm_k, pn * 64, row, bar);
-                tma_load_2d(dst + Cfg::kPageBytes + pn * BS * 128, &tm_v, pn * 64, row, bar);
-            }
+            PG::issue(smem_addr(smem + static_cast<size_t>(st) * PG::kStageBytes),
+                      smem_addr(&bars[st]), &tm_k, &tm_v, row);
         }
     };
 
     float o[ONT][4];
-#pragma unroll
-    for (int nt = 0; nt < ONT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run, l_run;
+    PG::reset(o, m_run, l_run);
 
     int issued = min(ST, n_my);
     for (int k = 0; k < issued; ++k) issue(k);
@@ -198,92 +327,9 @@ __global__ void __launch_bounds__(NW * 32)
             if (lane == 0) raise_error(p.err, PKV_DEVERR_TIMEOUT);
             break;
         }
-        uint8_t *stage = smem + static_cast<size_t>(st) * Cfg::kStageBytes;
-        const uint32_t k_s = smem_addr(stage), v_s = k_s + Cfg::kPageBytes;
         const int pg = pg0 + warp + k * NW;
-        const int valid = min(BS, len - pg * BS);
-        if (valid < BS) {
-            // V rows past the end of the sequence may hold anything (NaN, Inf): zero them
-            // so that their zero weights contribute exactly zero.
-            for (int idx = lane; idx < (BS - valid) * (D / 8); idx += 32) {
-                const int r = valid + idx / (D / 8), c16 = idx % (D / 8);
-                *reinterpret_cast<uint4 *>(stage + Cfg::kPageBytes + (c16 >> 3) * BS * 128 +
-                                           r * 128 + (c16 & 7) * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-
-        // ---- scores S^T: (2 x group heads) x BS tokens, fp32 accumulate
-        float s[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-#pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                const int mi = lane >> 3, r8 = lane & 7;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(k_s + swz128(BS, np * 16 + (mi >> 1) * 8 + r8, kk * 16 + (mi & 1) * 8),
-                        b0, b1, b2, b3);
-                mma_bf16_16816(s[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                mma_bf16_16816(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-            }
-        }
-
-        // ---- online softmax (base 2) for head g: rows g (hi) + g+8 (lo) of each tile
-        float sc[NT][2];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int tok = nt * 8 + 2 * t4 + e;
-                const float v = (s[nt][e] + s[nt][2 + e]) * p.scale_log2;
-                sc[nt][e] = tok < valid ? v : -INFINITY;
-                mx = fmaxf(mx, sc[nt][e]);
-            }
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2f(m_run - m_new);
-        float psum = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                sc[nt][e] = exp2f(sc[nt][e] - m_new);
-                psum += sc[nt][e];
-            }
-        }
-        l_run = l_run * alpha + psum;
-        m_run = m_new;
-#pragma unroll
-        for (int nt = 0; nt < ONT; ++nt) {
-            o[nt][0] *= alpha;
-            o[nt][1] *= alpha;
-            o[nt][2] *= alpha;
-            o[nt][3] *= alpha;
-        }
-
-        // ---- O += P V with P = P_hi (rows 0-7) + P_lo (rows 8-15)
-#pragma unroll
-        for (int kt = 0; kt < KT; ++kt) {
-            uint32_t a0, a1, a2, a3;
-            split_bf16x2(sc[2 * kt][0], sc[2 * kt][1], a0, a1);
-            split_bf16x2(sc[2 * kt + 1][0], sc[2 * kt + 1][1], a2, a3);
-#pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
-                const int mi = lane >> 3, r8 = lane & 7;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(v_s + swz128(BS, kt * 16 + (mi & 1) * 8 + r8, np * 16 + (mi >> 1) * 8),
-                              b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
-            }
-        }
-        __syncwarp();
+        PG::page(smem + static_cast<size_t>(st) * PG::kStageBytes, min(BS, len - pg * BS), qa, o,
+                 m_run, l_run, p.scale_log2, lane);
         if (k + ST < n_my) {
             issue(k + ST);
             issued = k + ST + 1;
@@ -314,6 +360,10 @@ __global__ void __launch_bounds__(NW * 32)
         *reinterpret_cast<float2 *>(ow + (warp * 8 + g) * D + nt * 8 + 2 * t4) = v;
     }
     __syncthreads();
+    // A sequence with a single chunk writes its result directly; otherwise this chunk's
+    // normalised partial (o_c, lse_c in base 2) goes to the workspace.
+    const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
+    const size_t bi0 = static_cast<size_t>(b) * p.Hq + head0;
     for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32) {
         const int h = idx / D, c = idx % D;
         float M = -INFINITY;
@@ -326,14 +376,73 @@ __global__ void __launch_bounds__(NW * 32)
             L += lw[w * 8 + h] * f;
             acc += ow[(w * 8 + h) * D + c] * f;
         }
-        const size_t bi = static_cast<size_t>(b) * p.Hq + head0 + h;
-        if (p.splits == 1) {
+        const size_t bi = bi0 + h;
+        if (nc == 1) {
             p.out[bi * D + c] = acc / L;
             if (c == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
         } else {
             p.ws_o[(bi * p.splits + split) * D + c] = acc / L;
             if (c == 0) p.ws_lse[bi * p.splits + split] = M + log2f(L);
         }
+    }
+    if (nc == 1 || p.counters == nullptr) return;
+
+    // ---- the last chunk to finish merges all chunks of this (sequence, head group):
+    // partials are published (fence) before the arrival is counted; the CTA that sees
+    // the count reach nc resets the counter for the next call and reads them back.
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned *ctr = p.counters + (static_cast<size_t>(b) * p.Hkv + kvh) * p.head_tiles + tile;
+        const unsigned prev = atomicAdd(ctr, 1u);
+        s_last = prev + 1 == static_cast<unsigned>(nc);
+        if (s_last) *ctr = 0u;   // every chunk of this call has arrived
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // per-head chunk weights 2^{lse_c - M} and their sum, in shared memory (stage area)
+    float *wts = reinterpret_cast<float *>(smem);              // [8][nc]
+    float *inv_l = wts + 8 * nc;                                // [8]
+    float *lse_h = inv_l + 8;                                   // [8]
+    for (int h = warp; h < nheads; h += NW) {
+        const float *ls = p.ws_lse + (bi0 + h) * p.splits;
+        float M = -INFINITY;
+        for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(ls + c));
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, sh));
+        float L = 0.f;
+        for (int c = lane; c < nc; c += 32) {
+            const float w = exp2f(__ldcg(ls + c) - M);
+            wts[h * nc + c] = w;
+            L += w;
+        }
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(kFull, L, sh);
+        if (lane == 0) {
+            inv_l[h] = 1.f / L;
+            lse_h[h] = M + log2f(L);
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nheads * (D / 4); idx += NW * 32) {
+        const int h = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
+        const float *po = p.ws_o + (bi0 + h) * p.splits * D + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int c = 0; c < nc; ++c) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(po + static_cast<size_t>(c) * D));
+            const float w = wts[h * nc + c];
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        const float il = inv_l[h];
+        *reinterpret_cast<float4 *>(p.out + (bi0 + h) * D + c4) =
+            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        if (c4 == 0 && p.lse != nullptr) p.lse[bi0 + h] = lse_h[h] * kLn2;
     }
 }
 
@@ -361,8 +470,9 @@ __global__ void __launch_bounds__(32)
     const int pg0 = split * p.chunk_pages;
     const int pg1 = min(n_pages, pg0 + p.chunk_pages);
     const size_t bi = static_cast<size_t>(b) * p.Hq + i;
+    const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;   // chunks holding tokens
     if (pg0 >= pg1) {
-        if (p.splits == 1) {
+        if (split == 0) {   // an empty sequence: out = 0, lse = -inf
             for (int e = lane; e < d; e += 32) p.out[bi * d + e] = 0.f;
             if (lane == 0 && p.lse != nullptr) p.lse[bi] = -INFINITY;
         }
@@ -410,13 +520,13 @@ __global__ void __launch_bounds__(32)
     for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
         if (e >= d) continue;
-        if (p.splits == 1)
+        if (nc == 1)
             p.out[bi * d + e] = acc[j] / l_run;
         else
             p.ws_o[(bi * p.splits + split) * d + e] = acc[j] / l_run;
     }
     if (lane == 0) {
-        if (p.splits == 1) {
+        if (nc == 1) {
             if (p.lse != nullptr) p.lse[bi] = (m_run + log2f(l_run)) * kLn2;
         } else {
             p.ws_lse[bi * p.splits + split] = m_run + log2f(l_run);
@@ -427,7 +537,8 @@ __global__ void __launch_bounds__(32)
 // ==================================================================== LSE merge
 
 // One block per (sequence, query head): lse = log2 sum_c 2^{lse_c},
-// out = sum_c 2^{lse_c - lse} o_c over the chunks that hold tokens.
+// out = sum_c 2^{lse_c - lse} o_c over the chunks that hold tokens.  Sequences with at
+// most one chunk were written directly by the attention kernel.
 __global__ void __launch_bounds__(128)
     decode_merge_kernel(const DecodeKParams p, int d, int bs) {
     const size_t bi = blockIdx.x;
@@ -435,6 +546,7 @@ __global__ void __launch_bounds__(128)
     const int len = checked_len(p, b, bs, false);
     const int n_pages = (len + bs - 1) / bs;
     const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
+    if (nc <= 1) return;
     const float *ls = p.ws_lse + bi * p.splits;
     float M = -INFINITY;
     for (int c = 0; c < nc; ++c) M = fmaxf(M, ls[c]);
@@ -443,29 +555,35 @@ __global__ void __launch_bounds__(128)
     for (int e = threadIdx.x; e < d; e += blockDim.x) {
         float acc = 0.f;
         for (int c = 0; c < nc; ++c) acc += exp2f(ls[c] - M) * p.ws_o[(bi * p.splits + c) * d + e];
-        p.out[bi * d + e] = nc > 0 ? acc / L : 0.f;
+        p.out[bi * d + e] = acc / L;
     }
-    if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bi] = nc > 0 ? (M + log2f(L)) * kLn2 : -INFINITY;
+    if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
 }
 
 // ====================================================================== launch
 
-template <int D, int BS, int NW, int ST>
-cudaError_t launch_mma(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv,
-                       dim3 grid, cudaStream_t stream) {
-    using Cfg = MmaCfg<D, BS, NW, ST>;
-    auto kernel = decode_mma_kernel<D, BS, NW, ST>;
-    static std::atomic<unsigned long long> attr_set{0};   // one bit per device
+template <typename Kernel>
+cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<unsigned long long> &done) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    if (!(attr_set.load() & bit)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::kSmemBytes);
+    if (!(done.load() & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
-        attr_set.fetch_or(bit);
+        done.fetch_or(bit);
     }
+    return cudaSuccess;
+}
+
+template <int D, int BS, int NW, int ST>
+cudaError_t launch_tc(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv,
+                      dim3 grid, cudaStream_t stream) {
+    using Cfg = MmaCfg<D, BS, NW, ST>;
+    static std::atomic<unsigned long long> done{0};
+    auto kernel = decode_chunked_kernel<D, BS, NW, ST>;
+    cudaError_t e = set_smem_once(kernel, Cfg::kSmemBytes, done);
+    if (e != cudaSuccess) return e;
     kernel<<<grid, NW * 32, Cfg::kSmemBytes, stream>>>(tk, tv, kp);
     return cudaGetLastError();
 }
@@ -496,6 +614,40 @@ cudaError_t launch_simt(const DecodeArgs &a, const DecodeKParams &kp, dim3 grid,
     return cudaGetLastError();
 }
 
+// Chunk plan: a chunk size, the chunk count per sequence and the workspace layout --
+// arrival counters (a fixed-size region, so that a workspace zeroed once stays valid for
+// any later shape), then o partials [B*Hq][splits][d], then lse partials [B*Hq][splits].
+void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int MBS, int num_splits,
+                int sm_count) {
+    const int m = Hq / Hkv;
+    const long long units = static_cast<long long>(B) * Hkv * ((m + 7) / 8);
+    const long long max_counters = PKV_DECODE_COUNTER_BYTES / sizeof(unsigned);
+    int chunk = MBS;
+    if (num_splits == 1) {
+        chunk = MBS;
+    } else if (num_splits > 1) {
+        chunk = (MBS + num_splits - 1) / num_splits;
+    } else {
+        // enough (sequence, head-group, chunk) units for several waves of two CTAs per SM,
+        // without making chunks shorter than 16 blocks
+        const long long target = 8ll * std::max(sm_count, 1);
+        while (chunk > 16 && units * ((MBS + chunk - 1) / chunk) < target)
+            chunk = (chunk + 1) / 2;
+    }
+    chunk = std::max(chunk, 1);
+    // the grid's x holds chunks x head tiles
+    const int tiles = (m + 7) / 8;
+    chunk = std::max(chunk, static_cast<int>((static_cast<long long>(MBS) * tiles + 0x7ffffffell - 1) / 0x7ffffffell));
+    plan.chunk_pages = chunk;
+    plan.splits = (MBS + chunk - 1) / chunk;
+    plan.workspace_bytes = plan.splits > 1 ? PKV_DECODE_COUNTER_BYTES +
+                                                 static_cast<size_t>(B) * Hq * plan.splits *
+                                                     (static_cast<size_t>(d) + 1) * sizeof(float)
+                                           : 0;
+    plan.fused_merge = plan.tensor_core && plan.splits > 1 && plan.splits <= 1024 &&
+                       units <= max_counters;
+}
+
 }  // namespace
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
@@ -504,29 +656,18 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, p
     plan.tensor_core = dt == PKV_BF16 && (d == 64 || d == 128 || d == 256) &&
                        (bs == 16 || bs == 32) && caches_aligned &&
                        static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31);
-    // (sequence, KV head, group of up to 8 query heads) units; the same count for both
-    // paths, so that the workspace size depends only on the shapes
-    const int m = Hq / Hkv;
-    const long long units = static_cast<long long>(B) * Hkv * ((m + 7) / 8);
-    int chunk = MBS;
-    if (num_splits == 1) {
-        chunk = MBS;
-    } else if (num_splits > 1) {
-        chunk = (MBS + num_splits - 1) / num_splits;
-    } else {
-        // Enough (sequence, head-group, chunk) units for several waves of two CTAs per SM,
-        // without making chunks shorter than 16 blocks.
-        const long long target = 8ll * std::max(sm_count, 1);
-        while (chunk > 16 && units * ((MBS + chunk - 1) / chunk) < target)
-            chunk = (chunk + 1) / 2;
-    }
-    chunk = std::max(chunk, 1);
-    plan.chunk_pages = chunk;
-    plan.splits = (MBS + chunk - 1) / chunk;
-    plan.workspace_bytes = plan.splits > 1 ? static_cast<size_t>(B) * Hq * plan.splits *
-                                                 (static_cast<size_t>(d) + 1) * sizeof(float)
-                                           : 0;
+    chunk_plan(plan, B, Hq, Hkv, d, MBS, num_splits, sm_count);
     return plan;
+}
+
+size_t decode_workspace_upper_bound(int B, int Hq, int Hkv, int d, int bs, int MBS,
+                                    int num_splits, int sm_count) {
+    // the query knows neither the element type nor the alignment: cover both paths
+    DecodePlan tc{}, other{};
+    tc.tensor_core = true;
+    chunk_plan(tc, B, Hq, Hkv, d, MBS, num_splits, sm_count);
+    chunk_plan(other, B, Hq, Hkv, d, MBS, num_splits, sm_count);
+    return std::max(tc.workspace_bytes, other.workspace_bytes);
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
@@ -550,7 +691,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     kp.splits = plan.splits;
     kp.scale_log2 = a.scale * kLog2e;
     if (plan.splits > 1) {
-        kp.ws_o = static_cast<float *>(a.workspace);
+        uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+        kp.counters = plan.fused_merge ? reinterpret_cast<unsigned *>(ws) : nullptr;
+        kp.ws_o = reinterpret_cast<float *>(ws + PKV_DECODE_COUNTER_BYTES);
         kp.ws_lse = kp.ws_o + static_cast<size_t>(a.B) * a.Hq * plan.splits * a.d;
     }
 
@@ -564,22 +707,23 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
         if (!encode_map_bf16(&tk, a.k_cache, 2, dims, strides, box) ||
             !encode_map_bf16(&tv, a.v_cache, 2, dims, strides, box))
             return cudaErrorInvalidValue;
-        const dim3 grid(plan.splits, a.Hkv * kp.head_tiles, a.B);
+        const dim3 grid(static_cast<unsigned>(plan.splits) * kp.head_tiles, a.Hkv, a.B);
         if (a.bs == 16) {
-            if (a.d == 64) e = launch_mma<64, 16, 4, 6>(kp, tk, tv, grid, stream);
-            else if (a.d == 128) e = launch_mma<128, 16, 4, 3>(kp, tk, tv, grid, stream);
-            else e = launch_mma<256, 16, 4, 2>(kp, tk, tv, grid, stream);
+            if (a.d == 64) e = launch_tc<64, 16, 4, 6>(kp, tk, tv, grid, stream);
+            else if (a.d == 128) e = launch_tc<128, 16, 4, 3>(kp, tk, tv, grid, stream);
+            else e = launch_tc<256, 16, 4, 2>(kp, tk, tv, grid, stream);
         } else {
-            if (a.d == 64) e = launch_mma<64, 32, 4, 3>(kp, tk, tv, grid, stream);
-            else if (a.d == 128) e = launch_mma<128, 32, 4, 2>(kp, tk, tv, grid, stream);
-            else e = launch_mma<256, 32, 2, 2>(kp, tk, tv, grid, stream);
+            if (a.d == 64) e = launch_tc<64, 32, 4, 3>(kp, tk, tv, grid, stream);
+            else if (a.d == 128) e = launch_tc<128, 32, 4, 2>(kp, tk, tv, grid, stream);
+            else e = launch_tc<256, 32, 2, 2>(kp, tk, tv, grid, stream);
         }
+        if (e != cudaSuccess || plan.splits == 1 || plan.fused_merge) return e;
     } else {
         const dim3 grid(plan.splits, a.Hq, a.B);
         e = dt == PKV_F32 ? launch_simt<float>(a, kp, grid, stream)
                           : launch_simt<__nv_bfloat16>(a, kp, grid, stream);
+        if (e != cudaSuccess || plan.splits == 1) return e;
     }
-    if (e != cudaSuccess || plan.splits == 1) return e;
     decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, stream>>>(kp, a.d, a.bs);
     return cudaGetLastError();
 }

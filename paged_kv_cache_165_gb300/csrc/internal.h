@@ -36,13 +36,19 @@ cudaError_t launch_kv_block_copy(void *k_cache, void *v_cache, int elem_bytes,
 
 struct DecodePlan {
     bool tensor_core;   // bf16 TMA + mma path; otherwise the CUDA-core path
-    int splits;         // chunks per sequence (1: one pass, no workspace)
+    int splits;         // chunks per sequence at most (1: one pass, no workspace)
     int chunk_pages;    // blocks per chunk
+    bool fused_merge;   // the last chunk of each unit merges (counters in the workspace)
     size_t workspace_bytes;
 };
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
                        int num_splits, int sm_count, bool caches_aligned);
+
+// Workspace that covers every plan these shapes can take (element type and alignment
+// unknown).
+size_t decode_workspace_upper_bound(int B, int Hq, int Hkv, int d, int bs, int MBS,
+                                    int num_splits, int sm_count);
 
 struct DecodeArgs {
     float *out;

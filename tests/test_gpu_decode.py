@@ -32,7 +32,7 @@ def run_decode(q, kc, vc, table, lens, scale, num_splits=0, with_lse=True):
     out = torch.full((B, Hq, d), float("nan"), device="cuda")
     lse = torch.full((B, Hq), float("nan"), device="cuda") if with_lse else None
     ws_bytes = pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, table.shape[1], num_splits)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
     pkv.paged_decode_attention(out, dev(q), dev(kc), dev(vc), dev(table), dev(lens), scale, lse=lse,
                                num_splits=num_splits, workspace=ws)
     torch.cuda.synchronize()
@@ -113,7 +113,7 @@ def test_tiny_config_append_then_decode():
         lse = torch.empty((spec.batch, spec.q_heads), device="cuda")
         pkv.paged_decode_attention(out, dev(inp.q[0]), gk, gv, dev(inp.block_table), dev(lens),
                                    spec.scale, lse=lse, num_splits=s,
-                                   workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+                                   workspace=torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
         ref, ref_lse = oracle.paged_decode(inp.q[0], kc, vc, inp.block_table, lens, spec.scale)
         assert_attn_close(out, ref, "tiny out")
         assert_attn_close(lse, ref_lse, "tiny lse")
@@ -190,3 +190,24 @@ def test_bad_lengths_and_block_ids_raise_device_errors():
         out, _ = run_decode(q, kc, vc, bad_table, lens, 0.1, s)
         assert pkv.get_device_error() & pkv.DEVERR["block"]
         assert torch.isfinite(out).all()
+
+
+def test_one_zeroed_workspace_serves_many_calls_and_shapes():
+    """The arrival counters at the start of the workspace return to zero after every call,
+    so a workspace zeroed once stays valid across calls with different shapes and splits."""
+    ws = torch.zeros(16 << 20, dtype=torch.uint8, device="cuda")
+    cases = [([300, 17, 1000, 0, 65], 16, 2, 128, 0), ([2000, 5], 64, 8, 128, 0),
+             ([900] * 6, 8, 8, 64, 5), ([4000, 1, 33], 32, 4, 256, 0), ([300, 17, 1000, 0, 65], 16, 2, 128, 3)]
+    for k, (lens, hq, hkv, d, s) in enumerate(cases):
+        q, kc, vc, table, lens_t = random_case(500 + k, lens, hq, hkv, d, 16, torch.bfloat16)
+        assert pkv.decode_workspace_bytes(len(lens), hq, hkv, d, 16, table.shape[1], s) <= ws.numel()
+        out = torch.empty((len(lens), hq, d), device="cuda")
+        lse = torch.empty((len(lens), hq), device="cuda")
+        pkv.paged_decode_attention(out, dev(q), dev(kc), dev(vc), dev(table), dev(lens_t), 0.1, lse=lse,
+                                   num_splits=s, workspace=ws)
+        torch.cuda.synchronize()
+        ref, ref_lse = oracle.paged_decode(q, kc, vc, table, lens_t, 0.1)
+        assert_attn_close(out, ref, f"case {k}")
+        assert_attn_close(lse, ref_lse, f"case {k} lse")
+        assert int(ws[: 256 << 10].count_nonzero()) == 0     # counters back at zero
+    assert pkv.get_device_error() == 0

@@ -33,7 +33,7 @@ def _lib():
 def decode(q, gk, gv, table, lens, scale):
     B, Hq, d = q.shape
     NB, Hkv, bs, _ = gk.shape
-    ws = torch.empty(max(pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, table.shape[1], 0), 16),
+    ws = torch.zeros(max(pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, table.shape[1], 0), 16),
                      dtype=torch.uint8, device="cuda")
     out = torch.full((B, Hq, d), float("nan"), device="cuda")
     lse = torch.full((B, Hq), float("nan"), device="cuda")

@@ -75,7 +75,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(L):
         assert 0 < need <= SCRATCH_BYTES          # the split-K path, using the scratch array
     ref = []
     for c in (first, second):
-        ws = torch.empty(SCRATCH_BYTES, dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(SCRATCH_BYTES, dtype=torch.uint8, device="cuda")
         status, out, lse = _call(L, c, 0, noalloc=False, workspace=ws)
         assert status == _binding.PKV_OK
         ref.append((out, lse))
