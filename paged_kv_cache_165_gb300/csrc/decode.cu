@@ -446,6 +446,200 @@ __global__ void __launch_bounds__(NW * 32)
     }
 }
 
+// ============================================================ large-group kernel
+
+// For m > 8 query heads per KV head (MQA is m = Hq): one CTA per (sequence, KV head,
+// chunk) holds every head tile of the group.  A producer warp streams each block page of
+// the chunk once into a shared ring (TMA, "full" mbarrier per stage); one consumer warp
+// per 8-head tile reads every page from shared memory and releases the stage on an
+// "empty" mbarrier that counts the consumer warps.  Each page thus leaves L2 once per CTA
+// instead of once per head tile.
+template <int D, int BS, int ST>
+struct GroupCfg {
+    using PG = TcPage<D, BS>;
+    static constexpr int kMaxTiles = 8;   // m <= 64
+    static constexpr int kStagesBytes = ST * PG::kStageBytes;
+    static constexpr int kSmemBytes = 1024 + kStagesBytes + 2 * ST * 8;
+};
+
+template <int D, int BS, int ST>
+__global__ void __launch_bounds__((GroupCfg<D, BS, ST>::kMaxTiles + 1) * 32, 1)
+    decode_group_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const DecodeKParams p) {
+    using PG = TcPage<D, BS>;
+    using Cfg = GroupCfg<D, BS, ST>;
+    constexpr int KS = PG::KS, ONT = PG::ONT;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = aligned_smem(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::kStagesBytes);
+    uint64_t *empty = full + ST;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int tiles = p.head_tiles;          // consumer warps; warp `tiles` is the producer
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+
+    const int len = checked_len(p, b, BS, threadIdx.x == 0 && split == 0 && kvh == 0);
+    const int n_pages = (len + BS - 1) / BS;
+    const int pg0 = split * p.chunk_pages;
+    const int pg1 = min(n_pages, pg0 + p.chunk_pages);
+    const size_t bi_group = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.m;
+    if (pg0 >= pg1) {
+        if (split == 0) {   // an empty sequence: out = 0, lse = -inf for the whole group
+            for (int idx = threadIdx.x; idx < p.m * D; idx += blockDim.x) p.out[bi_group * D + idx] = 0.f;
+            if (p.lse != nullptr)
+                for (int h = threadIdx.x; h < p.m; h += blockDim.x) p.lse[bi_group + h] = -INFINITY;
+        }
+        return;
+    }
+    const int pages = pg1 - pg0;
+    __shared__ int s_issued;
+    if (threadIdx.x == 0) {
+        s_issued = 0;
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), tiles);
+        }
+        fence_barrier_init();
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+    }
+    __syncthreads();
+
+    bool ok = true;
+    if (warp == tiles) {
+        // ---- producer: page k goes to stage k % ST once the consumers released it
+        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + pg0;
+        int tcur = lane < pages ? __ldg(tbl + lane) : 0;
+        int tnext = 32 + lane < pages ? __ldg(tbl + 32 + lane) : 0;
+        int tbase = 0;
+        const int oob_row = p.NB * p.Hkv * BS;
+        for (int k = 0; k < pages; ++k) {
+            while (k >= tbase + 32) {
+                tcur = tnext;
+                tbase += 32;
+                tnext = tbase + 32 + lane < pages ? __ldg(tbl + tbase + 32 + lane) : 0;
+            }
+            const int phys = __shfl_sync(kFull, tcur, k & 31);
+            const int st = k % ST;
+            bool free_ = true;
+            if (lane == 0 && k >= ST)
+                free_ = mbar_wait_bounded(smem_addr(&empty[st]), ((k / ST) - 1) & 1);
+            if (!__shfl_sync(kFull, free_ ? 1 : 0, 0)) {
+                if (lane == 0) raise_error(p.err, PKV_DEVERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                int row = oob_row;
+                if (phys < 0 || phys >= p.NB) raise_error(p.err, PKV_DEVERR_BLOCK);
+                else row = (phys * p.Hkv + kvh) * BS;
+                PG::issue(smem_addr(smem + static_cast<size_t>(st) * PG::kStageBytes),
+                          smem_addr(&full[st]), &tm_k, &tm_v, row);
+                s_issued = k + 1;
+            }
+            __syncwarp();
+        }
+    } else {
+        // ---- consumer warp: heads head0 .. head0 + nheads - 1 of the group
+        const int head0 = warp * 8;
+        const int nheads = min(8, p.m - head0);
+        uint32_t qa[KS][4];
+        PG::load_q(qa, p.q + (bi_group + head0) * D, nheads, lane);
+        float o[ONT][4];
+        float m_run, l_run;
+        PG::reset(o, m_run, l_run);
+        int k = 0;
+        for (; k < pages; ++k) {
+            const int st = k % ST;
+            const bool arrived = mbar_wait_bounded(smem_addr(&full[st]), (k / ST) & 1);
+            if (!__all_sync(kFull, arrived)) {
+                if (lane == 0) raise_error(p.err, PKV_DEVERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const int pg = pg0 + k;
+            PG::page(smem + static_cast<size_t>(st) * PG::kStageBytes, min(BS, len - pg * BS), qa, o,
+                     m_run, l_run, p.scale_log2, lane);
+            if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+        }
+        l_run += __shfl_xor_sync(kFull, l_run, 1);
+        l_run += __shfl_xor_sync(kFull, l_run, 2);
+        const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
+        if (ok && g < nheads) {
+            const float inv_l = 1.f / l_run;
+            const size_t bi = bi_group + head0 + g;
+            float *dst = nc == 1 ? p.out + bi * D : p.ws_o + (bi * p.splits + split) * D;
+#pragma unroll
+            for (int nt = 0; nt < ONT; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * t4) =
+                    make_float2((o[nt][0] + o[nt][2]) * inv_l, (o[nt][1] + o[nt][3]) * inv_l);
+            if (t4 == 0) {
+                const float lse2 = m_run + log2f(l_run);
+                if (nc == 1) {
+                    if (p.lse != nullptr) p.lse[bi] = lse2 * kLn2;
+                } else {
+                    p.ws_lse[bi * p.splits + split] = lse2;
+                }
+            }
+        }
+    }
+    if (__syncthreads_or(!ok)) {
+        // a wait gave up: let the last copies issued land (bounded) before the block exits
+        if (threadIdx.x == 0)
+            for (int k = max(0, s_issued - ST); k < s_issued; ++k)
+                mbar_wait_bounded(smem_addr(&full[k % ST]), (k / ST) & 1);
+        return;
+    }
+    const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
+    if (nc == 1 || p.counters == nullptr) return;
+
+    // ---- the last chunk of this (sequence, KV head) to finish merges the chunks
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned *ctr = p.counters + static_cast<size_t>(b) * p.Hkv + kvh;
+        const unsigned prev = atomicAdd(ctr, 1u);
+        s_last = prev + 1 == static_cast<unsigned>(nc);
+        if (s_last) *ctr = 0u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int nw = blockDim.x >> 5;
+    for (int h = warp; h < p.m; h += nw) {
+        const size_t bi = bi_group + h;
+        const float *ls = p.ws_lse + bi * p.splits;
+        float M = -INFINITY;
+        for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(ls + c));
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, sh));
+        float L = 0.f;
+        for (int c = lane; c < nc; c += 32) L += exp2f(__ldcg(ls + c) - M);
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(kFull, L, sh);
+        const float il = 1.f / L;
+        for (int c4 = lane * 4; c4 < D; c4 += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int c = 0; c < nc; ++c) {
+                const float w = exp2f(__ldcg(ls + c) - M);
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                    p.ws_o + (bi * p.splits + c) * D + c4));
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+            }
+            *reinterpret_cast<float4 *>(p.out + bi * D + c4) =
+                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        }
+        if (lane == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
+    }
+}
+
 // ================================================================ CUDA-core path
 
 template <typename T>
@@ -536,28 +730,66 @@ __global__ void __launch_bounds__(32)
 
 // ==================================================================== LSE merge
 
-// One block per (sequence, query head): lse = log2 sum_c 2^{lse_c},
-// out = sum_c 2^{lse_c - lse} o_c over the chunks that hold tokens.  Sequences with at
-// most one chunk were written directly by the attention kernel.
-__global__ void __launch_bounds__(128)
+// One block of 128 threads per (sequence, query head): lse = log2 sum_c 2^{lse_c} and
+// out = sum_c 2^{lse_c - lse} o_c over the chunks that hold tokens.  The chunk weights
+// are computed in parallel into shared memory; each thread then sums one column over the
+// chunks with independent, coalesced loads.  Sequences with at most one chunk were
+// written directly by the attention kernel.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeMaxChunks = 4096;
+
+__global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const DecodeKParams p, int d, int bs) {
+    __shared__ float w[kMergeMaxChunks];
+    __shared__ float red[kMergeThreads / 32];
     const size_t bi = blockIdx.x;
     const int b = static_cast<int>(bi / p.Hq);
     const int len = checked_len(p, b, bs, false);
     const int n_pages = (len + bs - 1) / bs;
     const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
     if (nc <= 1) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *ls = p.ws_lse + bi * p.splits;
     float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, ls[c]);
-    float L = 0.f;
-    for (int c = 0; c < nc; ++c) L += exp2f(ls[c] - M);
-    for (int e = threadIdx.x; e < d; e += blockDim.x) {
-        float acc = 0.f;
-        for (int c = 0; c < nc; ++c) acc += exp2f(ls[c] - M) * p.ws_o[(bi * p.splits + c) * d + e];
-        p.out[bi * d + e] = acc / L;
+    for (int c = tid; c < nc; c += kMergeThreads) {
+        w[c] = ls[c];
+        M = fmaxf(M, w[c]);
     }
-    if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, sh));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int i = 1; i < kMergeThreads / 32; ++i) M = fmaxf(M, red[i]);
+    __syncthreads();
+    float L = 0.f;
+    for (int c = tid; c < nc; c += kMergeThreads) {
+        w[c] = exp2f(w[c] - M);
+        L += w[c];
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(kFull, L, sh);
+    if (lane == 0) red[warp] = L;
+    __syncthreads();
+    L = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMergeThreads / 32; ++i) L += red[i];
+    const float il = 1.f / L;
+    const float *po = p.ws_o + bi * p.splits * d;
+    for (int e = tid; e < d; e += kMergeThreads) {
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        int c = 0;
+        for (; c + 4 <= nc; c += 4) {
+            acc0 += w[c] * po[static_cast<size_t>(c) * d + e];
+            acc1 += w[c + 1] * po[static_cast<size_t>(c + 1) * d + e];
+            acc2 += w[c + 2] * po[static_cast<size_t>(c + 2) * d + e];
+            acc3 += w[c + 3] * po[static_cast<size_t>(c + 3) * d + e];
+        }
+        for (; c < nc; ++c) acc0 += w[c] * po[static_cast<size_t>(c) * d + e];
+        p.out[bi * d + e] = ((acc0 + acc1) + (acc2 + acc3)) * il;
+    }
+    if (tid == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
 }
 
 // ====================================================================== launch
@@ -588,6 +820,18 @@ cudaError_t launch_tc(const DecodeKParams &kp, const CUtensorMap &tk, const CUte
     return cudaGetLastError();
 }
 
+template <int D, int BS, int ST>
+cudaError_t launch_group(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv,
+                         dim3 grid, cudaStream_t stream) {
+    using Cfg = GroupCfg<D, BS, ST>;
+    static std::atomic<unsigned long long> done{0};
+    auto kernel = decode_group_kernel<D, BS, ST>;
+    cudaError_t e = set_smem_once(kernel, Cfg::kSmemBytes, done);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, (kp.head_tiles + 1) * 32, Cfg::kSmemBytes, stream>>>(tk, tv, kp);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_simt(const DecodeArgs &a, const DecodeKParams &kp, dim3 grid,
                         cudaStream_t stream) {
@@ -614,6 +858,9 @@ cudaError_t launch_simt(const DecodeArgs &a, const DecodeKParams &kp, dim3 grid,
     return cudaGetLastError();
 }
 
+// Units with at most this many chunks merge inside the attention kernel.
+constexpr int kFusedMergeMaxChunks = 8;
+
 // Chunk plan: a chunk size, the chunk count per sequence and the workspace layout --
 // arrival counters (a fixed-size region, so that a workspace zeroed once stays valid for
 // any later shape), then o partials [B*Hq][splits][d], then lse partials [B*Hq][splits].
@@ -634,7 +881,15 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int MBS, int nu
         while (chunk > 16 && units * ((MBS + chunk - 1) / chunk) < target)
             chunk = (chunk + 1) / 2;
     }
+    chunk = std::max(chunk, (MBS + kMergeMaxChunks - 1) / kMergeMaxChunks);   // merge capacity
     chunk = std::max(chunk, 1);
+    if (plan.group && num_splits == 0) {
+        // one CTA per (sequence, KV head, chunk) with up to 9 warps: about four waves
+        chunk = MBS;
+        const long long gunits = static_cast<long long>(B) * Hkv;
+        const long long target = 2ll * std::max(sm_count, 1);
+        while (chunk > 16 && gunits * ((MBS + chunk - 1) / chunk) < target) chunk = (chunk + 1) / 2;
+    }
     // the grid's x holds chunks x head tiles
     const int tiles = (m + 7) / 8;
     chunk = std::max(chunk, static_cast<int>((static_cast<long long>(MBS) * tiles + 0x7ffffffell - 1) / 0x7ffffffell));
@@ -644,8 +899,10 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int MBS, int nu
                                                  static_cast<size_t>(B) * Hq * plan.splits *
                                                      (static_cast<size_t>(d) + 1) * sizeof(float)
                                            : 0;
-    plan.fused_merge = plan.tensor_core && plan.splits > 1 && plan.splits <= 1024 &&
-                       units <= max_counters;
+    // The last chunk merges in place when a unit has few chunks; many chunks (long
+    // contexts, the group kernel) merge in a separate kernel, many blocks at once.
+    plan.fused_merge = plan.tensor_core && !plan.group && plan.splits > 1 &&
+                       plan.splits <= kFusedMergeMaxChunks && units <= max_counters;
 }
 
 }  // namespace
@@ -656,6 +913,8 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, p
     plan.tensor_core = dt == PKV_BF16 && (d == 64 || d == 128 || d == 256) &&
                        (bs == 16 || bs == 32) && caches_aligned &&
                        static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31);
+    const int tiles = (Hq / Hkv + 7) / 8;
+    plan.group = plan.tensor_core && tiles >= 2 && tiles <= 8;
     chunk_plan(plan, B, Hq, Hkv, d, MBS, num_splits, sm_count);
     return plan;
 }
@@ -665,6 +924,8 @@ size_t decode_workspace_upper_bound(int B, int Hq, int Hkv, int d, int bs, int M
     // the query knows neither the element type nor the alignment: cover both paths
     DecodePlan tc{}, other{};
     tc.tensor_core = true;
+    const int tiles = (Hq / Hkv + 7) / 8;
+    tc.group = tiles >= 2 && tiles <= 8;
     chunk_plan(tc, B, Hq, Hkv, d, MBS, num_splits, sm_count);
     chunk_plan(other, B, Hq, Hkv, d, MBS, num_splits, sm_count);
     return std::max(tc.workspace_bytes, other.workspace_bytes);
@@ -707,6 +968,22 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
         if (!encode_map_bf16(&tk, a.k_cache, 2, dims, strides, box) ||
             !encode_map_bf16(&tv, a.v_cache, 2, dims, strides, box))
             return cudaErrorInvalidValue;
+        if (plan.group) {
+            const dim3 ggrid(plan.splits, a.Hkv, a.B);
+            if (a.bs == 16) {
+                if (a.d == 64) e = launch_group<64, 16, 16>(kp, tk, tv, ggrid, stream);
+                else if (a.d == 128) e = launch_group<128, 16, 12>(kp, tk, tv, ggrid, stream);
+                else e = launch_group<256, 16, 6>(kp, tk, tv, ggrid, stream);
+            } else {
+                if (a.d == 64) e = launch_group<64, 32, 12>(kp, tk, tv, ggrid, stream);
+                else if (a.d == 128) e = launch_group<128, 32, 6>(kp, tk, tv, ggrid, stream);
+                else e = launch_group<256, 32, 3>(kp, tk, tv, ggrid, stream);
+            }
+            if (e != cudaSuccess || plan.splits == 1) return e;
+            decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), kMergeThreads, 0, stream>>>(
+                kp, a.d, a.bs);
+            return cudaGetLastError();
+        }
         const dim3 grid(static_cast<unsigned>(plan.splits) * kp.head_tiles, a.Hkv, a.B);
         if (a.bs == 16) {
             if (a.d == 64) e = launch_tc<64, 16, 4, 6>(kp, tk, tv, grid, stream);
@@ -724,7 +1001,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
                           : launch_simt<__nv_bfloat16>(a, kp, grid, stream);
         if (e != cudaSuccess || plan.splits == 1) return e;
     }
-    decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, stream>>>(kp, a.d, a.bs);
+    decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), kMergeThreads, 0, stream>>>(kp, a.d, a.bs);
     return cudaGetLastError();
 }
 

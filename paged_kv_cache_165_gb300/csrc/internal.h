@@ -36,6 +36,8 @@ cudaError_t launch_kv_block_copy(void *k_cache, void *v_cache, int elem_bytes,
 
 struct DecodePlan {
     bool tensor_core;   // bf16 TMA + mma path; otherwise the CUDA-core path
+    bool group;         // tensor-core path with 9..64 query heads per KV head: all head
+                        // tiles of a KV head in one CTA sharing each page
     int splits;         // chunks per sequence at most (1: one pass, no workspace)
     int chunk_pages;    // blocks per chunk
     bool fused_merge;   // the last chunk of each unit merges (counters in the workspace)
