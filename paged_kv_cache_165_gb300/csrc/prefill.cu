@@ -6,13 +6,14 @@
 // aligned so that a query at position t sees keys 0..t, §13), with query head i reading
 // KV head floor(i/m) (limoncc.com "大语言模型研究15——注意力机制优化之KV缓存" §3.3).
 //
-// Tensor-core path (bf16, d in {64, 128}): one CTA of 4 warps per (64-query tile, query
-// head, sequence).  TMA brings the Q tile once and 64-key K/V tiles through a two-stage
-// ring (128-byte swizzle, mbarrier completion with a bounded wait).  Each warp owns 16
-// query rows: S = Q K^T on m16n8k16 bf16 MMAs, an online softmax per row (running max
-// and sum, plumephp.com "KV Cache 优化与注意力机制加速" §2.2-§2.3), and O += P V with
-// P split into bf16 hi + lo parts (two MMAs) so the weights keep ~16 bits.  Only key
-// tiles at or below the diagonal are visited.
+// Tensor-core path (bf16, d in {64, 128}): 5th-generation tensor cores (tcgen05).  One
+// CTA per (query head, 128-query tile, sequence): TMA brings the Q tile once and 64-key
+// K/V tiles through a multi-stage ring (128-byte swizzle, mbarrier completion with bounded
+// waits); one thread issues S = Q K^T into tensor memory (double-buffered) and O += P V
+// into a tensor-memory accumulator; four warps own one query row per thread for the online
+// softmax (running max and sum, plumephp.com "KV Cache 优化与注意力机制加速" §2.2-§2.3) and
+// hand P back through shared memory as bf16 hi + lo parts, so the weights keep ~16 bits.
+// Only key tiles at or below the diagonal are visited.
 // CUDA-core path (fp32 or other d): one warp per (query row, head).
 #include <math.h>
 
@@ -49,219 +50,278 @@ __device__ __forceinline__ bool seq_range(const PrefillKParams &p, int b, int &s
     return true;
 }
 
-// ============================================================ tensor-core path
+// ============================================================ tcgen05 path
 
+// Tiles of the tcgen05 prefill: 128 query rows per CTA, 64-key K/V tiles.
 template <int D>
-struct PrefillCfg {
-    static constexpr int kBM = 64, kBN = 64;
-    static constexpr int kTileBytes = 64 * D * 2;
-    static constexpr int kSmemBytes = 1024 + 5 * kTileBytes + 3 * 8;   // Q + 2 x (K, V) + bars
+struct TcPrefillCfg {
+    static constexpr int kBM = 128, kBN = 64;
+    static constexpr int kStages = D == 64 ? 6 : 4;    // K/V ring depth: loads run several tiles ahead
+    static constexpr int kQBytes = kBM * D * 2;        // D/64 panels of [128 rows][128 B]
+    static constexpr int kKVBytes = kBN * D * 2;       // one K or V tile: D/64 panels of [64][128 B]
+    static constexpr int kPBytes = kBM * kBN * 2;      // P (bf16) [128][64]: one panel
+    static constexpr int kOffKV = kQBytes;             // stage s: K, then V
+    static constexpr int kOffP = kOffKV + kStages * 2 * kKVBytes;   // P_hi, then P_lo
+    static constexpr int kOffBar = kOffP + 2 * kPBytes;
+    static constexpr int kNumBars = 8 + kStages;
+    static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
+    static constexpr int kTmemCols = 256;              // S: 2 x 64 columns, then O: D columns
+    static constexpr int kSCol = 0, kOCol = 2 * kBN;
+    static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
 };
 
+// mbarrier slots: Q, S full x2, S free x2, P full, O done, then K/V full per stage
+enum : int { kBarQ = 0, kBarSFull = 1, kBarSFree = 3, kBarPFull = 5, kBarODone = 6, kBarKvFull = 8 };
+
+// Bounded wait that also gives up as soon as another thread of the block has given up.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
+                                              unsigned *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            raise_error(err, PKV_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// One CTA per (query head, 128-query tile, sequence); five warps.
+//   warp 4 (one lane): TMA loads of Q and of a two-stage K/V ring, and every tcgen05.mma:
+//     S_j = Q K_j^T into one of two tensor-memory S buffers, and O += P_j V_j (P as bf16
+//     hi + lo, two MMA chains) into the tensor-memory O accumulator.
+//   warps 0-3: one query row per thread.  Each tile: read the row of S_j from tensor
+//     memory, apply the causal mask (key <= query), update the running max and sum (online
+//     softmax), rescale the O row in tensor memory when the reference max grew by more
+//     than 2^8 (exponentials stay <= 256 otherwise, and O and l share the same reference),
+//     and write the row of P_hi and P_lo to shared memory in the 128-byte-swizzled K-major
+//     layout the MMA reads.  At the end: O / l and lse from tensor memory.
 template <int D>
-__global__ void __launch_bounds__(128)
-    prefill_mma_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const PrefillKParams p) {
-    using Cfg = PrefillCfg<D>;
-    constexpr int BN = Cfg::kBN, BM = Cfg::kBM, TB = Cfg::kTileBytes;
-    constexpr int KS = D / 16, ONT = D / 8, PANELS = D / 64;
+__global__ void __launch_bounds__(160, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const PrefillKParams p) {
+    using Cfg = TcPrefillCfg<D>;
+    constexpr int BM = Cfg::kBM, BN = Cfg::kBN, PANELS = D / 64, NS = Cfg::kStages;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *q_s = smem;                       // Q tile
-    uint8_t *kv_s = smem + TB;                 // stage s: K at kv_s + 2*s*TB, V at + TB
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 5 * TB);   // [0] Q, [1..2] K/V stages
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + Cfg::kNumBars);
+    volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
+    auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int qt = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
-    const int kvh = i / p.m;
+    const int i = blockIdx.x, b = blockIdx.z;
     int start = 0, len = 0;
-    if (!seq_range(p, b, start, len, threadIdx.x == 0 && qt == 0 && i == 0)) return;
-    const int q0 = qt * BM;
+    if (!seq_range(p, b, start, len, threadIdx.x == 0 && blockIdx.y == 0 && i == 0)) return;
+    const int nqt = (p.max_seqlen + BM - 1) / BM;
+    const int q0 = (nqt - 1 - static_cast<int>(blockIdx.y)) * BM;   // longest tiles first
     if (q0 >= len) return;
-    const int n_kt = (min(q0 + BM, len) - 1) / BN + 1;   // key tiles at or below the diagonal
+    const int kvh = i / p.m;
+    const int n_kt = (min(q0 + BM, len) - 1) / BN + 1;                 // key tiles up to the diagonal
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 3; ++s) mbar_init(smem_addr(&bars[s]), 1);
+        mbar_init(bar(kBarQ), 1);
+        for (int s2 = 0; s2 < 2; ++s2) {
+            mbar_init(bar(kBarSFull + s2), 1);
+            mbar_init(bar(kBarSFree + s2), 4);
+        }
+        for (int s2 = 0; s2 < NS; ++s2) mbar_init(bar(kBarKvFull + s2), 1);
+        mbar_init(bar(kBarPFull), 4);
+        mbar_init(bar(kBarODone), 1);
+        *abort = 0;
         fence_barrier_init();
     }
+    if (warp == 0) tmem_alloc(smem_addr(tslot), Cfg::kTmemCols);
+    tc_fence_before_sync();
     __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t sQ = smem_addr(smem);
+    auto sK = [&](int st) { return smem_addr(smem + Cfg::kOffKV + st * 2 * Cfg::kKVBytes); };
+    auto sV = [&](int st) { return sK(st) + Cfg::kKVBytes; };
+    const uint32_t sP = smem_addr(smem + Cfg::kOffP);   // P_hi; P_lo at + kPBytes
 
-    auto issue_kv = [&](int kt) {   // thread 0 only
-        const int s = kt & 1;
-        const uint32_t bar = smem_addr(&bars[1 + s]);
-        const uint32_t dk = smem_addr(kv_s + 2 * s * TB), dv = dk + TB;
-        mbar_arrive_expect_tx(bar, 2 * TB);
+    if (warp == 4) {
+        if (lane == 0) {
+            auto load_kv = [&](int j) {
+                const int st = j % NS;
+                mbar_arrive_expect_tx(bar(kBarKvFull + st), 2 * Cfg::kKVBytes);
 #pragma unroll
-        for (int pn = 0; pn < PANELS; ++pn) {
-            tma_load_3d(dk + pn * BN * 128, &tm_k, pn * 64, kvh, start + kt * BN, bar);
-            tma_load_3d(dv + pn * BN * 128, &tm_v, pn * 64, kvh, start + kt * BN, bar);
+                for (int pn = 0; pn < PANELS; ++pn) {
+                    tma_load_3d(sK(st) + pn * BN * 128, &tm_k, pn * 64, kvh, start + j * BN, bar(kBarKvFull + st));
+                    tma_load_3d(sV(st) + pn * BN * 128, &tm_v, pn * 64, kvh, start + j * BN, bar(kBarKvFull + st));
+                }
+            };
+            const uint32_t idesc_s = umma_idesc_bf16(BM, BN, 0);
+            const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
+            auto issue_s = [&](int j) {   // S[j & 1] = Q K_j^T
+                const int st = j % NS, sb = j & 1;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ad = umma_desc_sw128(sQ + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
+                    const uint64_t bd = umma_desc_sw128(sK(st) + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024);
+                    umma_bf16(tmem + Cfg::kSCol + sb * BN, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(kBarSFull + sb));
+            };
+            auto issue_pv = [&](int j) {  // O += P_hi V_j + P_lo V_j
+                const int st = j % NS;
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(sP + half * Cfg::kPBytes + kk * 32, 16, 1024);
+                        const uint64_t bd = umma_desc_sw128(sV(st) + kk * 16 * 128, BN * 128, 1024);
+                        umma_bf16(tmem + Cfg::kOCol, ad, bd, idesc_o, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                    }
+                umma_commit(bar(kBarODone));
+            };
+            mbar_arrive_expect_tx(bar(kBarQ), Cfg::kQBytes);
+#pragma unroll
+            for (int pn = 0; pn < PANELS; ++pn)
+                tma_load_3d(sQ + pn * BM * 128, &tm_q, pn * 64, i, start + q0, bar(kBarQ));
+            for (int t = 0; t < min(NS, n_kt); ++t) load_kv(t);
+            int j = 0;
+            if (wait_or_abort(bar(kBarQ), 0, abort, p.err) && wait_or_abort(bar(kBarKvFull), 0, abort, p.err)) {
+                tc_fence_after_sync();
+                issue_s(0);
+                for (; j < n_kt; ++j) {
+                    if (j + 1 < n_kt) {
+                        const int t = j + 1;
+                        if (!wait_or_abort(bar(kBarKvFull + t % NS), (t / NS) & 1, abort, p.err)) break;
+                        if (t >= 2 && !wait_or_abort(bar(kBarSFree + (t & 1)), ((t >> 1) - 1) & 1, abort, p.err)) break;
+                        tc_fence_after_sync();
+                        issue_s(t);
+                    }
+                    if (!wait_or_abort(bar(kBarPFull), j & 1, abort, p.err)) break;
+                    tc_fence_after_sync();
+                    issue_pv(j);
+                    if (j + NS < n_kt) {   // stage j % NS is free once P.V_j is done
+                        if (!wait_or_abort(bar(kBarODone), j & 1, abort, p.err)) break;
+                        load_kv(j + NS);
+                    }
+                }
+            }
+            if (*abort) {
+                // let every copy and MMA already issued finish (bounded) before teardown
+                mbar_wait_bounded(bar(kBarQ), 0);
+                for (int t = max(0, j - 1); t < min(n_kt, j + NS); ++t)
+                    mbar_wait_bounded(bar(kBarKvFull + t % NS), (t / NS) & 1);
+                if (j > 0) mbar_wait_bounded(bar(kBarODone), (j - 1) & 1);
+            }
         }
-    };
-    if (threadIdx.x == 0) {
-        const uint32_t bar = smem_addr(&bars[0]);
-        mbar_arrive_expect_tx(bar, TB);
-#pragma unroll
-        for (int pn = 0; pn < PANELS; ++pn)
-            tma_load_3d(smem_addr(q_s) + pn * BM * 128, &tm_q, pn * 64, i, start + q0, bar);
-        issue_kv(0);
-        if (n_kt > 1) issue_kv(1);
-    }
+    } else {
+        const int r = warp * 32 + lane;      // the query row this thread owns
+        const int qpos = q0 + r;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kt && ok; ++j) {
+            const int buf = j & 1;
+            ok = wait_or_abort(bar(kBarSFull + buf), (j >> 1) & 1, abort, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+            uint32_t sr[BN];
+            tmem_ld32(lane_base + Cfg::kSCol + buf * BN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(lane_base + Cfg::kSCol + buf * BN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarSFree + buf));
 
-    bool ok = __syncthreads_and(mbar_wait_bounded(smem_addr(&bars[0]), 0)) != 0;
-    uint32_t qa[KS][4];
+            // causal mask (diagonal tiles only), tile max, reference max (moved only when it
+            // grows by more than 2^8); scores stay raw and the scale enters one FMA
+            const int key0 = j * BN;
+            float sc[BN];
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-        const int mi = lane >> 3, r8 = lane & 7;
-        ldsm_x4(smem_addr(q_s) + swz128(BM, warp * 16 + (mi & 1) * 8 + r8, kk * 16 + (mi >> 1) * 8),
-                qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-    }
-
-    const int row0 = q0 + warp * 16 + g;   // this thread's rows: row0 and row0 + 8
-    float o[ONT][4];
+            for (int c = 0; c < BN; ++c) sc[c] = __uint_as_float(sr[c]);
+            if (key0 + BN - 1 > q0) {
 #pragma unroll
-    for (int nt = 0; nt < ONT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-
-    int kt = 0;
-    for (; kt < n_kt && ok; ++kt) {
-        const int s = kt & 1;
-        const bool arrived = mbar_wait_bounded(smem_addr(&bars[1 + s]), (kt >> 1) & 1);
-        if (!__syncthreads_and(arrived)) {
-            ok = false;
-            break;
-        }
-        uint8_t *k_tile = kv_s + 2 * s * TB;
-        uint8_t *v_tile = k_tile + TB;
-        const int key0 = kt * BN;
-        if (key0 + BN > len) {
-            // V rows past the sequence end hold other sequences' data or TMA's zero fill;
-            // zero them so that their zero weights contribute exactly zero.
-            const int valid = len - key0;
-            for (int idx = threadIdx.x; idx < (BN - valid) * (D / 8); idx += 128) {
-                const int r = valid + idx / (D / 8), c16 = idx % (D / 8);
-                *reinterpret_cast<uint4 *>(v_tile + (c16 >> 3) * BN * 128 + r * 128 +
-                                           (c16 & 7) * 16) = make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < BN; ++c)
+                    if (key0 + c > qpos) sc[c] = -INFINITY;
+            }
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            const float m_new = mx > m_ref + 8.f ? mx : m_ref;
+            const float alpha = ex2_approx(m_ref - m_new);
+            m_ref = m_new;
+            const float neg_m = -m_ref;
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < BN; ++c) {
+                sc[c] = ex2_approx(fmaf(sc[c], p.scale_log2, neg_m));
+                l4[c & 3] += sc[c];
+            }
+            l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+            // the previous P.V must be done: P is free and O is current
+            if (j > 0) {
+                ok = wait_or_abort(bar(kBarODone), (j - 1) & 1, abort, p.err);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (__any_sync(kFull, alpha != 1.f)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_base + Cfg::kOCol + cc * 32, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(lane_base + Cfg::kOCol + cc * 32, ov);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            // row r of P_hi and P_lo: 8 chunks of 8 keys, 128-byte swizzle
+#pragma unroll
+            for (int c16 = 0; c16 < BN / 8; ++c16) {
+                uint32_t h[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    split_bf16x2(sc[c16 * 8 + 2 * e], sc[c16 * 8 + 2 * e + 1], h[e], lo[e]);
+                const uint32_t off = r * 128 + ((c16 ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(smem + Cfg::kOffP + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(smem + Cfg::kOffP + Cfg::kPBytes + off) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
             fence_proxy_async_smem();
-            __syncthreads();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarPFull));
         }
-        const uint32_t k_a = smem_addr(k_tile), v_a = smem_addr(v_tile);
-
-        float sacc[BN / 8][4];
+        if (ok) ok = wait_or_abort(bar(kBarODone), (n_kt - 1) & 1, abort, p.err);
+        if (ok) {
+            tc_fence_after_sync();
+            const float inv_l = 1.f / l;
+            const bool row_ok = qpos < len;
+            float *dst = p.out + (static_cast<size_t>(start + qpos) * p.Hq + i) * D;
 #pragma unroll
-        for (int nt = 0; nt < BN / 8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t ov[32];
+                tmem_ld32(lane_base + Cfg::kOCol + cc * 32, ov);
+                tmem_ld_wait();
+                if (row_ok) {
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-#pragma unroll
-            for (int np = 0; np < BN / 16; ++np) {
-                const int mi = lane >> 3, r8 = lane & 7;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(k_a + swz128(BN, np * 16 + (mi >> 1) * 8 + r8, kk * 16 + (mi & 1) * 8), b0,
-                        b1, b2, b3);
-                mma_bf16_16816(sacc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                mma_bf16_16816(sacc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(dst + cc * 32 + e) =
+                            make_float4(__uint_as_float(ov[e]) * inv_l, __uint_as_float(ov[e + 1]) * inv_l,
+                                        __uint_as_float(ov[e + 2]) * inv_l, __uint_as_float(ov[e + 3]) * inv_l);
+                }
             }
+            if (row_ok && p.lse != nullptr)
+                p.lse[static_cast<size_t>(start + qpos) * p.Hq + i] = (m_ref + log2f(l)) * kLn2;
         }
-
-        // online softmax per row (base 2): rows row0 (c0, c1) and row0 + 8 (c2, c3)
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < BN / 8; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = key0 + nt * 8 + 2 * t4 + (e & 1);
-                const int row = row0 + (e >> 1) * 8;
-                const float v = sacc[nt][e] * p.scale_log2;
-                sacc[nt][e] = key <= row ? v : -INFINITY;
-                mx[e >> 1] = fmaxf(mx[e >> 1], sacc[nt][e]);
-            }
-        }
-        float alpha[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 2));
-            const float m_new = fmaxf(m_run[r], mx[r]);
-            // a row can only be fully masked in a tile after it already saw key 0
-            alpha[r] = m_new == -INFINITY ? 1.f : exp2f(m_run[r] - m_new);
-            m_run[r] = m_new;
-        }
-        float psum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < BN / 8; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float mr = m_run[e >> 1];
-                sacc[nt][e] = mr == -INFINITY ? 0.f : exp2f(sacc[nt][e] - mr);
-                psum[e >> 1] += sacc[nt][e];
-            }
-        }
-        l_run[0] = l_run[0] * alpha[0] + psum[0];
-        l_run[1] = l_run[1] * alpha[1] + psum[1];
-#pragma unroll
-        for (int nt = 0; nt < ONT; ++nt) {
-            o[nt][0] *= alpha[0];
-            o[nt][1] *= alpha[0];
-            o[nt][2] *= alpha[1];
-            o[nt][3] *= alpha[1];
-        }
-
-        // O += (P_hi + P_lo) V
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-            uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-            split_bf16x2(sacc[2 * ks][0], sacc[2 * ks][1], h0, l0);          // row g, keys 2t..
-            split_bf16x2(sacc[2 * ks][2], sacc[2 * ks][3], h1, l1);          // row g+8
-            split_bf16x2(sacc[2 * ks + 1][0], sacc[2 * ks + 1][1], h2, l2);  // row g, keys 2t+8..
-            split_bf16x2(sacc[2 * ks + 1][2], sacc[2 * ks + 1][3], h3, l3);  // row g+8
-#pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
-                const int mi = lane >> 3, r8 = lane & 7;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(v_a + swz128(BN, ks * 16 + (mi & 1) * 8 + r8, np * 16 + (mi >> 1) * 8),
-                              b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * np], h0, h1, h2, h3, b0, b1);
-                mma_bf16_16816(o[2 * np], l0, l1, l2, l3, b0, b1);
-                mma_bf16_16816(o[2 * np + 1], h0, h1, h2, h3, b2, b3);
-                mma_bf16_16816(o[2 * np + 1], l0, l1, l2, l3, b2, b3);
-            }
-        }
-        __syncthreads();   // every warp is done with this stage
-        if (threadIdx.x == 0 && kt + 2 < n_kt) issue_kv(kt + 2);
     }
-    if (!ok) {
-        if (threadIdx.x == 0) {
-            raise_error(p.err, PKV_DEVERR_TIMEOUT);
-            // let the copies still in flight land before the block exits
-            mbar_wait_bounded(smem_addr(&bars[0]), 0);
-            for (int k2 = kt; k2 < min(n_kt, kt + 2); ++k2)
-                mbar_wait_bounded(smem_addr(&bars[1 + (k2 & 1)]), (k2 >> 1) & 1);
-        }
-        return;
-    }
-
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        l_run[r] += __shfl_xor_sync(kFull, l_run[r], 1);
-        l_run[r] += __shfl_xor_sync(kFull, l_run[r], 2);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int row = row0 + r * 8;
-        if (row >= len) continue;
-        const size_t tok = static_cast<size_t>(start + row);
-        float *dst = p.out + (tok * p.Hq + i) * D;
-        const float inv = 1.f / l_run[r];
-#pragma unroll
-        for (int nt = 0; nt < ONT; ++nt)
-            *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * t4) =
-                make_float2(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
-        if (t4 == 0 && p.lse != nullptr) p.lse[tok * p.Hq + i] = (m_run[r] + log2f(l_run[r])) * kLn2;
-    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
 // ============================================================== CUDA-core path
@@ -328,9 +388,8 @@ __global__ void __launch_bounds__(32)
 }
 
 template <int D>
-cudaError_t launch_prefill_mma(const PrefillArgs &a, const PrefillKParams &kp,
-                               cudaStream_t stream) {
-    using Cfg = PrefillCfg<D>;
+cudaError_t launch_prefill_tc(const PrefillArgs &a, const PrefillKParams &kp, cudaStream_t stream) {
+    using Cfg = TcPrefillCfg<D>;
     CUtensorMap tq, tk, tv;
     const uint64_t dq[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Hq),
                             static_cast<uint64_t>(a.T)};
@@ -338,16 +397,17 @@ cudaError_t launch_prefill_mma(const PrefillArgs &a, const PrefillKParams &kp,
     const uint64_t dk[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Hkv),
                             static_cast<uint64_t>(a.T)};
     const uint64_t sk[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.Hkv) * D * 2};
-    const uint32_t box[3] = {64, 1, 64};
-    if (!encode_map_bf16(&tq, a.q, 3, dq, sq, box) || !encode_map_bf16(&tk, a.k, 3, dk, sk, box) ||
-        !encode_map_bf16(&tv, a.v, 3, dk, sk, box))
+    const uint32_t qbox[3] = {64, 1, static_cast<uint32_t>(Cfg::kBM)};
+    const uint32_t kvbox[3] = {64, 1, static_cast<uint32_t>(Cfg::kBN)};
+    if (!encode_map_bf16(&tq, a.q, 3, dq, sq, qbox) || !encode_map_bf16(&tk, a.k, 3, dk, sk, kvbox) ||
+        !encode_map_bf16(&tv, a.v, 3, dk, sk, kvbox))
         return cudaErrorInvalidValue;
-    auto kernel = prefill_mma_kernel<D>;
+    auto kernel = prefill_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const dim3 grid((a.max_seqlen + Cfg::kBM - 1) / Cfg::kBM, a.Hq, a.B);
-    kernel<<<grid, 128, Cfg::kSmemBytes, stream>>>(tq, tk, tv, kp);
+    const dim3 grid(a.Hq, (a.max_seqlen + Cfg::kBM - 1) / Cfg::kBM, a.B);
+    kernel<<<grid, 160, Cfg::kSmemBytes, stream>>>(tq, tk, tv, kp);
     return cudaGetLastError();
 }
 
@@ -402,8 +462,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, pkv_dtype dt, cudaStream_t stre
     kp.m = a.Hq / a.Hkv;
     kp.scale_log2 = a.scale * kLog2e;
     if (prefill_tensor_core_ok(dt, a.d, a.q, a.k, a.v, a.T, a.Hq, a.Hkv))
-        return a.d == 64 ? launch_prefill_mma<64>(a, kp, stream)
-                         : launch_prefill_mma<128>(a, kp, stream);
+        return a.d == 64 ? launch_prefill_tc<64>(a, kp, stream) : launch_prefill_tc<128>(a, kp, stream);
     return dt == PKV_F32 ? launch_prefill_simt<float>(a, kp, stream)
                          : launch_prefill_simt<__nv_bfloat16>(a, kp, stream);
 }
