@@ -52,26 +52,36 @@ __device__ __forceinline__ bool seq_range(const PrefillKParams &p, int b, int &s
 
 // ============================================================ tcgen05 path
 
-// Tiles of the tcgen05 prefill: 128 query rows per CTA, 64-key K/V tiles.
+// Tiles of the tcgen05 prefill: two 128-row query tiles per CTA, 64-key K/V tiles.
 template <int D>
 struct TcPrefillCfg {
-    static constexpr int kBM = 128, kBN = 64;
-    static constexpr int kStages = D == 64 ? 6 : 4;    // K/V ring depth: loads run several tiles ahead
-    static constexpr int kQBytes = kBM * D * 2;        // D/64 panels of [128 rows][128 B]
+    static constexpr int kBM = 128, kBN = 64, kGroups = 2;
+    static constexpr int kStages = D == 64 ? 6 : 3;    // K/V ring depth
+    static constexpr int kQBytes = kBM * D * 2;        // one Q tile: D/64 panels of [128][128 B]
     static constexpr int kKVBytes = kBN * D * 2;       // one K or V tile: D/64 panels of [64][128 B]
     static constexpr int kPBytes = kBM * kBN * 2;      // P (bf16) [128][64]: one panel
-    static constexpr int kOffKV = kQBytes;             // stage s: K, then V
-    static constexpr int kOffP = kOffKV + kStages * 2 * kKVBytes;   // P_hi, then P_lo
-    static constexpr int kOffBar = kOffP + 2 * kPBytes;
-    static constexpr int kNumBars = 8 + kStages;
+    static constexpr int kOffKV = kGroups * kQBytes;   // stage s: K, then V
+    static constexpr int kOffP = kOffKV + kStages * 2 * kKVBytes;   // per group: P_hi, P_lo
+    static constexpr int kOffBar = kOffP + kGroups * 2 * kPBytes;
+    static constexpr int kNumBars = 1 + 2 * kStages + kGroups * 6;
     static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
-    static constexpr int kTmemCols = 256;              // S: 2 x 64 columns, then O: D columns
+    static constexpr int kTmemCols = 512;              // per group: S 2 x 64 columns, O D columns
+    static constexpr int kGroupCols = 256;
     static constexpr int kSCol = 0, kOCol = 2 * kBN;
-    static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
+    static_assert(kOCol + D <= kGroupCols, "tensor memory budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// mbarrier slots: Q, S full x2, S free x2, P full, O done, then K/V full per stage
-enum : int { kBarQ = 0, kBarSFull = 1, kBarSFree = 3, kBarPFull = 5, kBarODone = 6, kBarKvFull = 8 };
+// mbarrier slots: Q; K/V full and K/V free per stage; per group S full x2, S free x2,
+// P full, O done
+template <int NS>
+struct PrefillBars {
+    static constexpr int kQ = 0, kKvFull = 1, kKvFree = 1 + NS, kGroup0 = 1 + 2 * NS;
+    static constexpr int s_full(int g, int b) { return kGroup0 + g * 6 + b; }
+    static constexpr int s_free(int g, int b) { return kGroup0 + g * 6 + 2 + b; }
+    static constexpr int p_full(int g) { return kGroup0 + g * 6 + 4; }
+    static constexpr int o_done(int g) { return kGroup0 + g * 6 + 5; }
+};
 
 // Bounded wait that also gives up as soon as another thread of the block has given up.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
@@ -89,22 +99,27 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return true;
 }
 
-// One CTA per (query head, 128-query tile, sequence); five warps.
-//   warp 4 (one lane): TMA loads of Q and of a two-stage K/V ring, and every tcgen05.mma:
-//     S_j = Q K_j^T into one of two tensor-memory S buffers, and O += P_j V_j (P as bf16
-//     hi + lo, two MMA chains) into the tensor-memory O accumulator.
-//   warps 0-3: one query row per thread.  Each tile: read the row of S_j from tensor
-//     memory, apply the causal mask (key <= query), update the running max and sum (online
-//     softmax), rescale the O row in tensor memory when the reference max grew by more
-//     than 2^8 (exponentials stay <= 256 otherwise, and O and l share the same reference),
-//     and write the row of P_hi and P_lo to shared memory in the 128-byte-swizzled K-major
-//     layout the MMA reads.  At the end: O / l and lse from tensor memory.
+// One CTA per (query head, pair of 128-query tiles, sequence); ten warps.
+//   warp 9 (one lane): TMA loads of both Q tiles and of a K/V ring shared by the two tiles;
+//     a stage is refilled as soon as the MMAs of its previous tile are done.
+//   warp 8 (one lane): every tcgen05.mma: per tile g and key tile j, S_g = Q_g K_j^T into one of
+//     two tensor-memory S buffers of g, and O_g += P_g V_j (P as bf16 hi + lo, two MMA
+//     chains) into g's tensor-memory accumulator.  Issue order alternates between the
+//     tiles, so the tensor core works on one tile while the other tile's rows are in the
+//     softmax.
+//   warps 4g .. 4g+3: one query row of tile g per thread.  Per key tile: read the row of
+//     S from tensor memory, apply the causal mask (key <= query) on diagonal tiles, update
+//     the running max and sum (online softmax), rescale the O row in tensor memory when
+//     the reference max grew by more than 2^8 (exponentials stay <= 256 otherwise, and O
+//     and l share the same reference), and write the row of P_hi and P_lo to shared memory
+//     in the 128-byte-swizzled K-major layout the MMA reads.  At the end: O / l and lse.
 template <int D>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(320, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillKParams p) {
     using Cfg = TcPrefillCfg<D>;
-    constexpr int BM = Cfg::kBM, BN = Cfg::kBN, PANELS = D / 64, NS = Cfg::kStages;
+    constexpr int BM = Cfg::kBM, BN = Cfg::kBN, PANELS = D / 64, NS = Cfg::kStages, G = Cfg::kGroups;
+    using Bars = PrefillBars<NS>;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -118,21 +133,32 @@ __global__ void __launch_bounds__(160, 1)
     const int i = blockIdx.x, b = blockIdx.z;
     int start = 0, len = 0;
     if (!seq_range(p, b, start, len, threadIdx.x == 0 && blockIdx.y == 0 && i == 0)) return;
-    const int nqt = (p.max_seqlen + BM - 1) / BM;
-    const int q0 = (nqt - 1 - static_cast<int>(blockIdx.y)) * BM;   // longest tiles first
+    const int npairs = (p.max_seqlen + G * BM - 1) / (G * BM);
+    const int q0 = (npairs - 1 - static_cast<int>(blockIdx.y)) * G * BM;   // longest first
     if (q0 >= len) return;
     const int kvh = i / p.m;
-    const int n_kt = (min(q0 + BM, len) - 1) / BN + 1;                 // key tiles up to the diagonal
+    int n_kt[G];   // key tiles up to the diagonal, per query tile (0: tile past the end)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const int qg = q0 + g * BM;
+        n_kt[g] = qg < len ? (min(qg + BM, len) - 1) / BN + 1 : 0;
+    }
+    const int n_all = max(n_kt[0], n_kt[1]);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(kBarQ), 1);
-        for (int s2 = 0; s2 < 2; ++s2) {
-            mbar_init(bar(kBarSFull + s2), 1);
-            mbar_init(bar(kBarSFree + s2), 4);
+        mbar_init(bar(Bars::kQ), 1);
+        for (int st = 0; st < NS; ++st) {
+            mbar_init(bar(Bars::kKvFull + st), 1);
+            mbar_init(bar(Bars::kKvFree + st), 1);
         }
-        for (int s2 = 0; s2 < NS; ++s2) mbar_init(bar(kBarKvFull + s2), 1);
-        mbar_init(bar(kBarPFull), 4);
-        mbar_init(bar(kBarODone), 1);
+        for (int g = 0; g < G; ++g) {
+            for (int sb = 0; sb < 2; ++sb) {
+                mbar_init(bar(Bars::s_full(g, sb)), 1);
+                mbar_init(bar(Bars::s_free(g, sb)), 4);
+            }
+            mbar_init(bar(Bars::p_full(g)), 4);
+            mbar_init(bar(Bars::o_done(g)), 1);
+        }
         *abort = 0;
         fence_barrier_init();
     }
@@ -141,98 +167,124 @@ __global__ void __launch_bounds__(160, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t sQ = smem_addr(smem);
+    auto sQ = [&](int g) { return smem_addr(smem + g * Cfg::kQBytes); };
     auto sK = [&](int st) { return smem_addr(smem + Cfg::kOffKV + st * 2 * Cfg::kKVBytes); };
     auto sV = [&](int st) { return sK(st) + Cfg::kKVBytes; };
-    const uint32_t sP = smem_addr(smem + Cfg::kOffP);   // P_hi; P_lo at + kPBytes
+    auto sP = [&](int g) { return smem_addr(smem + Cfg::kOffP + g * 2 * Cfg::kPBytes); };   // hi; lo after
 
-    if (warp == 4) {
+    if (warp == 2 * 4) {
         if (lane == 0) {
-            auto load_kv = [&](int j) {
-                const int st = j % NS;
-                mbar_arrive_expect_tx(bar(kBarKvFull + st), 2 * Cfg::kKVBytes);
-#pragma unroll
-                for (int pn = 0; pn < PANELS; ++pn) {
-                    tma_load_3d(sK(st) + pn * BN * 128, &tm_k, pn * 64, kvh, start + j * BN, bar(kBarKvFull + st));
-                    tma_load_3d(sV(st) + pn * BN * 128, &tm_v, pn * 64, kvh, start + j * BN, bar(kBarKvFull + st));
-                }
-            };
             const uint32_t idesc_s = umma_idesc_bf16(BM, BN, 0);
             const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
-            auto issue_s = [&](int j) {   // S[j & 1] = Q K_j^T
+            auto issue_s = [&](int g, int j) {   // S_g[j & 1] = Q_g K_j^T
                 const int st = j % NS, sb = j & 1;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = umma_desc_sw128(sQ + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
+                    const uint64_t ad = umma_desc_sw128(sQ(g) + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
                     const uint64_t bd = umma_desc_sw128(sK(st) + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024);
-                    umma_bf16(tmem + Cfg::kSCol + sb * BN, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    umma_bf16(tmem + g * Cfg::kGroupCols + Cfg::kSCol + sb * BN, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(kBarSFull + sb));
+                umma_commit(bar(Bars::s_full(g, sb)));
             };
-            auto issue_pv = [&](int j) {  // O += P_hi V_j + P_lo V_j
+            auto issue_pv = [&](int g, int j) {  // O_g += P_g,hi V_j + P_g,lo V_j
                 const int st = j % NS;
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t ad = umma_desc_sw128(sP + half * Cfg::kPBytes + kk * 32, 16, 1024);
+                        const uint64_t ad = umma_desc_sw128(sP(g) + half * Cfg::kPBytes + kk * 32, 16, 1024);
                         const uint64_t bd = umma_desc_sw128(sV(st) + kk * 16 * 128, BN * 128, 1024);
-                        umma_bf16(tmem + Cfg::kOCol, ad, bd, idesc_o, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16(tmem + g * Cfg::kGroupCols + Cfg::kOCol, ad, bd, idesc_o,
+                                  (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
                     }
-                umma_commit(bar(kBarODone));
+                umma_commit(bar(Bars::o_done(g)));
             };
-            mbar_arrive_expect_tx(bar(kBarQ), Cfg::kQBytes);
-#pragma unroll
-            for (int pn = 0; pn < PANELS; ++pn)
-                tma_load_3d(sQ + pn * BM * 128, &tm_q, pn * 64, i, start + q0, bar(kBarQ));
-            for (int t = 0; t < min(NS, n_kt); ++t) load_kv(t);
             int j = 0;
-            if (wait_or_abort(bar(kBarQ), 0, abort, p.err) && wait_or_abort(bar(kBarKvFull), 0, abort, p.err)) {
+            if (wait_or_abort(bar(Bars::kQ), 0, abort, p.err) &&
+                wait_or_abort(bar(Bars::kKvFull), 0, abort, p.err)) {
                 tc_fence_after_sync();
-                issue_s(0);
-                for (; j < n_kt; ++j) {
-                    if (j + 1 < n_kt) {
-                        const int t = j + 1;
-                        if (!wait_or_abort(bar(kBarKvFull + t % NS), (t / NS) & 1, abort, p.err)) break;
-                        if (t >= 2 && !wait_or_abort(bar(kBarSFree + (t & 1)), ((t >> 1) - 1) & 1, abort, p.err)) break;
+                for (int g = 0; g < G; ++g)
+                    if (n_kt[g] > 0) issue_s(g, 0);
+                bool alive = true;
+                for (; j < n_all && alive; ++j) {
+                    const int t = j + 1;
+                    if (t < n_all) {
+                        alive = wait_or_abort(bar(Bars::kKvFull + t % NS), (t / NS) & 1, abort, p.err);
+                        for (int g = 0; g < G && alive; ++g) {
+                            if (t >= n_kt[g]) continue;
+                            if (t >= 2)
+                                alive = wait_or_abort(bar(Bars::s_free(g, t & 1)), ((t >> 1) - 1) & 1, abort, p.err);
+                            if (!alive) break;
+                            tc_fence_after_sync();
+                            issue_s(g, t);
+                        }
+                    }
+                    for (int g = 0; g < G && alive; ++g) {
+                        if (j >= n_kt[g]) continue;
+                        alive = wait_or_abort(bar(Bars::p_full(g)), j & 1, abort, p.err);
+                        if (!alive) break;
                         tc_fence_after_sync();
-                        issue_s(t);
+                        issue_pv(g, j);
                     }
-                    if (!wait_or_abort(bar(kBarPFull), j & 1, abort, p.err)) break;
-                    tc_fence_after_sync();
-                    issue_pv(j);
-                    if (j + NS < n_kt) {   // stage j % NS is free once P.V_j is done
-                        if (!wait_or_abort(bar(kBarODone), j & 1, abort, p.err)) break;
-                        load_kv(j + NS);
-                    }
+                    if (!alive) break;
+                    umma_commit(bar(Bars::kKvFree + j % NS));   // stage j % NS is free after these MMAs
                 }
             }
-            if (*abort) {
-                // let every copy and MMA already issued finish (bounded) before teardown
-                mbar_wait_bounded(bar(kBarQ), 0);
-                for (int t = max(0, j - 1); t < min(n_kt, j + NS); ++t)
-                    mbar_wait_bounded(bar(kBarKvFull + t % NS), (t / NS) & 1);
-                if (j > 0) mbar_wait_bounded(bar(kBarODone), (j - 1) & 1);
+            if (*abort && j > 0) {
+                // let the MMAs already issued finish (bounded) before teardown
+                umma_commit(bar(Bars::kKvFree + j % NS));
+                mbar_wait_bounded(bar(Bars::kKvFree + j % NS), (j / NS) & 1);
             }
         }
+    } else if (warp == 2 * 4 + 1) {
+        if (lane == 0) {
+            // loader: both Q tiles, then K/V tile t into stage t % NS as soon as the MMAs of
+            // tile t - NS (the stage's previous tile) are done
+            mbar_arrive_expect_tx(bar(Bars::kQ), G * Cfg::kQBytes);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int pn = 0; pn < PANELS; ++pn)
+                    tma_load_3d(sQ(g) + pn * BM * 128, &tm_q, pn * 64, i, start + q0 + g * BM, bar(Bars::kQ));
+            int t = 0;
+            for (; t < n_all; ++t) {
+                if (t >= NS && !wait_or_abort(bar(Bars::kKvFree + t % NS), ((t - NS) / NS) & 1, abort, p.err))
+                    break;
+                const int st = t % NS;
+                mbar_arrive_expect_tx(bar(Bars::kKvFull + st), 2 * Cfg::kKVBytes);
+#pragma unroll
+                for (int pn = 0; pn < PANELS; ++pn) {
+                    tma_load_3d(sK(st) + pn * BN * 128, &tm_k, pn * 64, kvh, start + t * BN, bar(Bars::kKvFull + st));
+                    tma_load_3d(sV(st) + pn * BN * 128, &tm_v, pn * 64, kvh, start + t * BN, bar(Bars::kKvFull + st));
+                }
+            }
+            // before teardown, every copy issued must have landed (bounded)
+            mbar_wait_bounded(bar(Bars::kQ), 0);
+            for (int u = max(0, t - NS); u < t; ++u)
+                mbar_wait_bounded(bar(Bars::kKvFull + u % NS), (u / NS) & 1);
+        }
     } else {
-        const int r = warp * 32 + lane;      // the query row this thread owns
-        const int qpos = q0 + r;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const int g = warp >> 2;                 // query tile of this warp
+        const int r = (warp & 3) * 32 + lane;    // its row in the tile
+        const int qg0 = q0 + g * BM;
+        const int qpos = qg0 + r;
+        const int nk = n_kt[g];
+        const uint32_t lane_base = tmem + g * Cfg::kGroupCols + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        uint8_t *pbuf = smem + Cfg::kOffP + g * 2 * Cfg::kPBytes;
         float m_ref = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_kt && ok; ++j) {
-            const int buf = j & 1;
-            ok = wait_or_abort(bar(kBarSFull + buf), (j >> 1) & 1, abort, p.err);
+        bool ok = nk > 0;
+        for (int j = 0; j < nk && ok; ++j) {
+            const int sb = j & 1;
+            ok = wait_or_abort(bar(Bars::s_full(g, sb)), (j >> 1) & 1, abort, p.err);
             if (!ok) break;
             tc_fence_after_sync();
             uint32_t sr[BN];
-            tmem_ld32(lane_base + Cfg::kSCol + buf * BN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(lane_base + Cfg::kSCol + buf * BN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(lane_base + Cfg::kSCol + sb * BN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(lane_base + Cfg::kSCol + sb * BN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             tmem_ld_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSFree + buf));
+            if (lane == 0) mbar_arrive(bar(Bars::s_free(g, sb)));
 
             // causal mask (diagonal tiles only), tile max, reference max (moved only when it
             // grows by more than 2^8); scores stay raw and the scale enters one FMA
@@ -240,7 +292,7 @@ __global__ void __launch_bounds__(160, 1)
             float sc[BN];
 #pragma unroll
             for (int c = 0; c < BN; ++c) sc[c] = __uint_as_float(sr[c]);
-            if (key0 + BN - 1 > q0) {
+            if (key0 + BN - 1 > qg0) {
 #pragma unroll
                 for (int c = 0; c < BN; ++c)
                     if (key0 + c > qpos) sc[c] = -INFINITY;
@@ -260,9 +312,9 @@ __global__ void __launch_bounds__(160, 1)
                 l4[c & 3] += sc[c];
             }
             l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-            // the previous P.V must be done: P is free and O is current
+            // the previous P.V of this tile must be done: P is free and O is current
             if (j > 0) {
-                ok = wait_or_abort(bar(kBarODone), (j - 1) & 1, abort, p.err);
+                ok = wait_or_abort(bar(Bars::o_done(g)), (j - 1) & 1, abort, p.err);
                 if (!ok) break;
                 tc_fence_after_sync();
                 if (__any_sync(kFull, alpha != 1.f)) {
@@ -286,16 +338,15 @@ __global__ void __launch_bounds__(160, 1)
                 for (int e = 0; e < 4; ++e)
                     split_bf16x2(sc[c16 * 8 + 2 * e], sc[c16 * 8 + 2 * e + 1], h[e], lo[e]);
                 const uint32_t off = r * 128 + ((c16 ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(smem + Cfg::kOffP + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4 *>(smem + Cfg::kOffP + Cfg::kPBytes + off) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(pbuf + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(pbuf + Cfg::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarPFull));
+            if (lane == 0) mbar_arrive(bar(Bars::p_full(g)));
         }
-        if (ok) ok = wait_or_abort(bar(kBarODone), (n_kt - 1) & 1, abort, p.err);
+        if (ok) ok = wait_or_abort(bar(Bars::o_done(g)), (nk - 1) & 1, abort, p.err);
         if (ok) {
             tc_fence_after_sync();
             const float inv_l = 1.f / l;
@@ -406,8 +457,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, const PrefillKParams &kp, cu
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const dim3 grid(a.Hq, (a.max_seqlen + Cfg::kBM - 1) / Cfg::kBM, a.B);
-    kernel<<<grid, 160, Cfg::kSmemBytes, stream>>>(tq, tk, tv, kp);
+    const int pair = Cfg::kGroups * Cfg::kBM;
+    const dim3 grid(a.Hq, (a.max_seqlen + pair - 1) / pair, a.B);
+    kernel<<<grid, 320, Cfg::kSmemBytes, stream>>>(tq, tk, tv, kp);
     return cudaGetLastError();
 }
 
