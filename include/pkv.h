@@ -129,6 +129,16 @@ pkv_status pkv_kv_block_copy(void *k_cache, void *v_cache, pkv_dtype dt, const i
 size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS, int num_splits);
 
 /*
+ * Kernels one pkv_paged_decode_attention call with these arguments enqueues on the
+ * current device, for caches whose base addresses are 16-byte aligned: 0 for B == 0,
+ * 1 when the call runs in one pass or the last chunk of each sequence merges in place,
+ * 2 when a separate log-sum-exp merge kernel follows the split-K kernel.  Returns -1
+ * for arguments pkv_paged_decode_attention rejects.  Enqueues nothing.
+ */
+int pkv_decode_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
+                               int num_splits);
+
+/*
  * pkv_paged_decode_attention -- one new query per sequence against its cached K/V.
  *
  * For sequence b, query head i, KV head j = floor(i / m), len = context_lens[b]:

@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     PKV_BF16,
     PKV_F32,
     PkvError,
+    decode_kernel_launches,
     decode_workspace_bytes,
     get_device_error,
     header_functions,

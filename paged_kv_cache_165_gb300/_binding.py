@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
     L.pkv_kv_block_copy.restype = I
     L.pkv_decode_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     L.pkv_decode_workspace_bytes.restype = Z
+    L.pkv_decode_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I]
+    L.pkv_decode_kernel_launches.restype = I
     L.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P,
                                              Z, P]
     L.pkv_paged_decode_attention.restype = I
@@ -152,6 +154,12 @@ def kv_block_copy(k_cache, v_cache, pairs, stream=None) -> None:
 
 def decode_workspace_bytes(B, Hq, Hkv, d, bs, MBS, num_splits=0) -> int:
     return int(lib().pkv_decode_workspace_bytes(B, Hq, Hkv, d, bs, MBS, num_splits))
+
+
+def decode_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, dtype, num_splits=0) -> int:
+    """Kernels one paged_decode_attention call with these sizes enqueues (-1: rejected)."""
+    dt = _DTYPES[dtype]
+    return int(lib().pkv_decode_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits))
 
 
 def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, scale, lse=None,

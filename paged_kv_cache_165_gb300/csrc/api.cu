@@ -186,6 +186,19 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS
     return decode_workspace_upper_bound(B, Hq, Hkv, d, bs, MBS, num_splits, st->sm_count);
 }
 
+int pkv_decode_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
+                               int num_splits) {
+    int eb = 0;
+    if (!elem_size(dt, &eb) || check_decode_sizes(B, Hq, Hkv, d, bs, MBS) != PKV_OK || NB < 1 ||
+        num_splits < 0)
+        return -1;
+    if (B == 0) return 0;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != PKV_OK) return -1;
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count, true);
+    return plan.splits > 1 && !plan.fused_merge ? 2 : 1;
+}
+
 pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, const void *k_cache,
                                       const void *v_cache, pkv_dtype dt, const int32_t *block_table,
                                       const int32_t *context_lens, int B, int Hq, int Hkv, int d,

@@ -21,7 +21,8 @@ def L():
 def test_header_declares_the_boundary():
     names = set(pkv.header_functions())
     for fn in ["pkv_kv_append", "pkv_kv_block_copy", "pkv_paged_decode_attention",
-               "pkv_prefill_attention", "pkv_decode_workspace_bytes", "pkv_get_device_error",
+               "pkv_prefill_attention", "pkv_decode_workspace_bytes", "pkv_decode_kernel_launches",
+               "pkv_get_device_error",
                "pkv_status_string", "pkv_last_error", "pkv_version"]:
         assert fn in names
 
@@ -72,3 +73,12 @@ def test_host_validation_rejects_bad_arguments_before_any_launch(L):
     assert L.pkv_prefill_attention(*pre(8, 2, ctypes.c_void_p(16))) == _binding.PKV_ERR_INVALID_ARG
     # device error query needs a host pointer
     assert L.pkv_get_device_error(None, n) == _binding.PKV_ERR_INVALID_ARG
+
+
+def test_decode_kernel_launches_rejects_what_decode_rejects(L):
+    # invalid sizes and element types answer -1 before the device is queried; B == 0 is 0
+    assert L.pkv_decode_kernel_launches(4, 10, 3, 128, 16, 8, 64, 1, 0) == -1   # Hq % Hkv
+    assert L.pkv_decode_kernel_launches(4, 8, 8, 128, 16, 8, 0, 1, 0) == -1    # NB < 1
+    assert L.pkv_decode_kernel_launches(4, 8, 8, 128, 16, 8, 64, 7, 0) == -1   # element type
+    assert L.pkv_decode_kernel_launches(4, 8, 8, 128, 16, 8, 64, 1, -1) == -1  # num_splits
+    assert L.pkv_decode_kernel_launches(0, 8, 8, 128, 16, 8, 64, 1, 0) == 0

@@ -211,3 +211,39 @@ def test_one_zeroed_workspace_serves_many_calls_and_shapes():
         assert_attn_close(lse, ref_lse, f"case {k} lse")
         assert int(ws[: 256 << 10].count_nonzero()) == 0     # counters back at zero
     assert pkv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,lens,num_splits", [
+    (64, 8, [3000, 5000, 700, 8000] * 4, 0),   # tensor-core split-K, merge fused in the kernel
+    (64, 8, [300, 20], 1),                     # one pass
+    (64, 1, [40000, 9000], 0),                 # large group kernel: separate merge kernel
+    (32, 32, [2049] * 8, 0),
+])
+def test_decode_kernel_launches_counts_what_the_call_enqueues(hq, hkv, lens, num_splits):
+    prof = pytest.importorskip("torch.profiler")
+    q, kc, vc, table, clens = random_case(77, lens, hq, hkv, 128, 16, torch.bfloat16)
+    args = [dev(t) for t in (q, kc, vc, table, clens)]
+    B, NB, MBS = len(lens), kc.shape[0], table.shape[1]
+    want = pkv.decode_kernel_launches(B, hq, hkv, 128, 16, MBS, NB, torch.bfloat16, num_splits)
+    assert want in (1, 2)
+    out = torch.empty((B, hq, 128), device="cuda")
+    lse = torch.empty((B, hq), device="cuda")
+    ws = torch.zeros(max(pkv.decode_workspace_bytes(B, hq, hkv, 128, 16, MBS, num_splits), 16),
+                     dtype=torch.uint8, device="cuda")
+    call = lambda: pkv.paged_decode_attention(out, args[0], args[1], args[2], args[3], args[4],
+                                              1 / math.sqrt(128), lse=lse, num_splits=num_splits,
+                                              workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    for _ in range(2):   # the first session of a process may start recording late
+        with prof.profile(activities=[prof.ProfilerActivity.CUDA]) as p:
+            call()
+            torch.cuda.synchronize()
+    names = [e.name for e in p.events() if e.device_type == torch.autograd.DeviceType.CUDA
+             and "decode" in e.name]
+    if not names:
+        pytest.skip("the profiler recorded no kernels here")
+    assert len(names) == want, names
+    ref, ref_lse = oracle.paged_decode(q, kc, vc, table, clens, 1 / math.sqrt(128))
+    assert_attn_close(out, ref, "out")
+    assert_attn_close(lse, ref_lse, "lse")
