@@ -442,7 +442,10 @@ def bench_ours(args):
         value = total_bytes / (max_ms / 1e3) / 1e9
         kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
         achieved = (sum(step_bytes) / len(step_bytes)) / (kern_avg_ms / 1e3) / 1e9
-        src = kernel_source_hash(["decode.cu", "common.cuh"])
+        files = ["decode.cu", "decode_kparams.cuh", "common.cuh"]
+        if wl.spec.q_heads // wl.spec.kv_heads > 8:
+            files.append("decode_umma.cu")      # the tcgen05 large-group kernel
+        src = kernel_source_hash(files)
         traffic = profiled_traffic(f"decode_{args.workload}.md", src)
         res.update({
             "value": value, "unit": "GB/s", "pct_hbm_peak": 100 * value / hbm,

@@ -71,6 +71,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEVERR_CU_SEQLENS  8u   /* cu_seqlens decreasing, > T, or a sequence > max_seqlen */
 #define PKV_DEVERR_PAIR       16u   /* kv_block_copy pair outside [0, NB) (pair skipped) */
 #define PKV_DEVERR_TIMEOUT    32u   /* a bounded wait for an asynchronous copy gave up */
+#define PKV_DEVERR_LAYOUT     64u   /* a kernel found its shared memory misaligned and did nothing */
 
 /* Static description of a status code. */
 const char *pkv_status_string(pkv_status status);
@@ -130,7 +131,7 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS
 
 /*
  * Kernels one pkv_paged_decode_attention call with these arguments enqueues on the
- * current device, for caches whose base addresses are 16-byte aligned: 0 for B == 0,
+ * current device, for q and caches whose base addresses are 16-byte aligned: 0 for B == 0,
  * 1 when the call runs in one pass or the last chunk of each sequence merges in place,
  * 2 when a separate log-sum-exp merge kernel follows the split-K kernel.  Returns -1
  * for arguments pkv_paged_decode_attention rejects.  Enqueues nothing.

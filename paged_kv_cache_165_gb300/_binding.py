@@ -19,7 +19,7 @@ PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUD
 PKV_F32, PKV_BF16 = 0, 1
 
 DEVERR = {
-    "slot": 1, "block": 2, "len": 4, "cu_seqlens": 8, "pair": 16, "timeout": 32,
+    "slot": 1, "block": 2, "len": 4, "cu_seqlens": 8, "pair": 16, "timeout": 32, "layout": 64,
 }
 
 _DTYPES = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16}

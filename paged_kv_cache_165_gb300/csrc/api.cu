@@ -195,7 +195,7 @@ int pkv_decode_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, i
     if (B == 0) return 0;
     DeviceState *st = nullptr;
     if (device_state(&st) != PKV_OK) return -1;
-    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count, true);
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count, true, true);
     return plan.splits > 1 && !plan.fused_merge ? 2 : 1;
 }
 
@@ -219,7 +219,7 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
     s = device_state(&st);
     if (s != PKV_OK) return s;
     const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count,
-                                        aligned16(k_cache) && aligned16(v_cache));
+                                        aligned16(k_cache) && aligned16(v_cache), aligned16(q));
     if (plan.workspace_bytes > 0 &&
         (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
          reinterpret_cast<uintptr_t>(workspace) % 16 != 0))

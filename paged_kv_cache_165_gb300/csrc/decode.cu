@@ -30,41 +30,15 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "decode_kparams.cuh"
 #include "internal.h"
 
 namespace pkv {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = kDecLog2e;
+constexpr float kLn2 = kDecLn2;
 constexpr unsigned kFull = 0xffffffffu;
-
-struct DecodeKParams {
-    float *out;
-    float *lse;
-    float *ws_o;         // partial outputs (layout per kernel, see plan_decode)
-    float *ws_lse;       // partial log-sum-exp, base 2
-    unsigned *counters;  // arrival counters, one per (sequence, KV head, head tile) unit
-    const float *q;
-    const int32_t *block_table;
-    const int32_t *context_lens;
-    unsigned *err;
-    int B, Hq, Hkv, m, MBS, NB;
-    int head_tiles;   // ceil(m / 8): head groups per KV head
-    int chunk_pages;  // blocks per chunk
-    int splits;       // chunks per sequence at most (partial slots per sequence)
-    float scale_log2; // scale * log2(e): scores are kept in the base-2 domain
-};
-
-// Sequence length after validation; an invalid length counts as empty.
-__device__ __forceinline__ int checked_len(const DecodeKParams &p, int b, int bs, bool report) {
-    int len = __ldg(p.context_lens + b);
-    if (len < 0 || (long long)len > (long long)p.MBS * bs) {
-        if (report) raise_error(p.err, PKV_DEVERR_LEN);
-        len = 0;
-    }
-    return len;
-}
 
 // ============================================================ tensor-core page math
 
@@ -864,7 +838,7 @@ constexpr int kFusedMergeMaxChunks = 8;
 // Chunk plan: a chunk size, the chunk count per sequence and the workspace layout --
 // arrival counters (a fixed-size region, so that a workspace zeroed once stays valid for
 // any later shape), then o partials [B*Hq][splits][d], then lse partials [B*Hq][splits].
-void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int MBS, int num_splits,
+void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS, int num_splits,
                 int sm_count) {
     const int m = Hq / Hkv;
     const long long units = static_cast<long long>(B) * Hkv * ((m + 7) / 8);
@@ -883,7 +857,19 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int MBS, int nu
     }
     chunk = std::max(chunk, (MBS + kMergeMaxChunks - 1) / kMergeMaxChunks);   // merge capacity
     chunk = std::max(chunk, 1);
-    if (plan.group && num_splits == 0) {
+    if (plan.umma) {
+        // one CTA per (sequence, KV head, chunk) and SM, one wave: the start of a block
+        // (queries, first copies) and its end are paid once per SM; chunks of whole
+        // 64-key tiles
+        const int ppt = kUmmaDecodeKeys / bs;
+        if (num_splits == 0) {
+            const long long gunits = static_cast<long long>(B) * Hkv;
+            const long long per_unit = std::max(1ll, (std::max(sm_count, 1) + gunits - 1) / gunits);
+            chunk = static_cast<int>((MBS + per_unit - 1) / per_unit);
+        }
+        chunk = std::max(chunk, (MBS + kMergeMaxChunks - 1) / kMergeMaxChunks);
+        chunk = (chunk + ppt - 1) / ppt * ppt;
+    } else if (plan.group && num_splits == 0) {
         // one CTA per (sequence, KV head, chunk) with up to 9 warps: about four waves
         chunk = MBS;
         const long long gunits = static_cast<long long>(B) * Hkv;
@@ -908,27 +894,31 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int MBS, int nu
 }  // namespace
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
-                       int num_splits, int sm_count, bool caches_aligned) {
+                       int num_splits, int sm_count, bool caches_aligned, bool q_aligned) {
     DecodePlan plan{};
     plan.tensor_core = dt == PKV_BF16 && (d == 64 || d == 128 || d == 256) &&
                        (bs == 16 || bs == 32) && caches_aligned &&
                        static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31);
     const int tiles = (Hq / Hkv + 7) / 8;
     plan.group = plan.tensor_core && tiles >= 2 && tiles <= 8;
-    chunk_plan(plan, B, Hq, Hkv, d, MBS, num_splits, sm_count);
+    plan.umma = plan.group && (d == 64 || d == 128) && q_aligned;
+    chunk_plan(plan, B, Hq, Hkv, d, bs, MBS, num_splits, sm_count);
     return plan;
 }
 
 size_t decode_workspace_upper_bound(int B, int Hq, int Hkv, int d, int bs, int MBS,
                                     int num_splits, int sm_count) {
     // the query knows neither the element type nor the alignment: cover both paths
-    DecodePlan tc{}, other{};
+    DecodePlan tc{}, umma{}, other{};
     tc.tensor_core = true;
     const int tiles = (Hq / Hkv + 7) / 8;
     tc.group = tiles >= 2 && tiles <= 8;
-    chunk_plan(tc, B, Hq, Hkv, d, MBS, num_splits, sm_count);
-    chunk_plan(other, B, Hq, Hkv, d, MBS, num_splits, sm_count);
-    return std::max(tc.workspace_bytes, other.workspace_bytes);
+    umma = tc;
+    umma.umma = tc.group && (d == 64 || d == 128) && (bs == 16 || bs == 32);
+    chunk_plan(tc, B, Hq, Hkv, d, bs, MBS, num_splits, sm_count);
+    chunk_plan(umma, B, Hq, Hkv, d, bs, MBS, num_splits, sm_count);
+    chunk_plan(other, B, Hq, Hkv, d, bs, MBS, num_splits, sm_count);
+    return std::max({tc.workspace_bytes, umma.workspace_bytes, other.workspace_bytes});
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
@@ -968,6 +958,13 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
         if (!encode_map_bf16(&tk, a.k_cache, 2, dims, strides, box) ||
             !encode_map_bf16(&tv, a.v_cache, 2, dims, strides, box))
             return cudaErrorInvalidValue;
+        if (plan.umma) {
+            e = launch_decode_umma(kp, tk, tv, a.d, a.bs, dim3(plan.splits, a.Hkv, a.B), stream);
+            if (e != cudaSuccess || plan.splits == 1) return e;
+            decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), kMergeThreads, 0, stream>>>(
+                kp, a.d, a.bs);
+            return cudaGetLastError();
+        }
         if (plan.group) {
             const dim3 ggrid(plan.splits, a.Hkv, a.B);
             if (a.bs == 16) {

@@ -76,7 +76,8 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(
     const bool aligned = reinterpret_cast<uintptr_t>(k_cache) % 16 == 0 &&
                          reinterpret_cast<uintptr_t>(v_cache) % 16 == 0;
     const DecodePlan plan =
-        plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, sm_count, aligned);
+        plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, sm_count, aligned,
+                    reinterpret_cast<uintptr_t>(q) % 16 == 0);
     if (plan.workspace_bytes > PKV_NOALLOC_SCRATCH_BYTES) {
         char msg[200];
         snprintf(msg, sizeof msg,

@@ -38,14 +38,17 @@ struct DecodePlan {
     bool tensor_core;   // bf16 TMA + mma path; otherwise the CUDA-core path
     bool group;         // tensor-core path with 9..64 query heads per KV head: all head
                         // tiles of a KV head in one CTA sharing each page
+    bool umma;          // the large-group case on tcgen05 (d in {64, 128})
     int splits;         // chunks per sequence at most (1: one pass, no workspace)
     int chunk_pages;    // blocks per chunk
     bool fused_merge;   // the last chunk of each unit merges (counters in the workspace)
     size_t workspace_bytes;
 };
 
+// caches_aligned: both cache bases 16-byte aligned; q_aligned: q 16-byte aligned (the
+// tcgen05 large-group kernel copies the group's queries in one bulk copy).
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
-                       int num_splits, int sm_count, bool caches_aligned);
+                       int num_splits, int sm_count, bool caches_aligned, bool q_aligned);
 
 // Workspace that covers every plan these shapes can take (element type and alignment
 // unknown).

@@ -83,22 +83,6 @@ struct PrefillBars {
     static constexpr int o_done(int g) { return kGroup0 + g * 6 + 5; }
 };
 
-// Bounded wait that also gives up as soon as another thread of the block has given up.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
-                                              unsigned *err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            raise_error(err, PKV_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
 // One CTA per (query head, pair of 128-query tiles, sequence); ten warps.
 //   warp 9 (one lane): TMA loads of both Q tiles and of a K/V ring shared by the two tiles;
 //     a stage is refilled as soon as the MMAs of its previous tile are done.

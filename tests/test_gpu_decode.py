@@ -87,6 +87,30 @@ def test_block_sizes_and_poisoned_unwritten_slots(bs):
         check(q, kc, vc, table, lens, 0.0884, s, f"bs={bs} s={s}")
 
 
+@pytest.mark.parametrize("hq,hkv", [(9, 1), (16, 1), (48, 2), (64, 1), (128, 2)])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_large_group_path_ragged_and_poisoned(hq, hkv, d, bs):
+    # 9..64 query heads per KV head: tcgen05 tiles of 64 keys gathered page by page, the
+    # last tile of a chunk partly past the end, unwritten slots holding NaN / Inf
+    lens = RAGGED + [2000, 64, 65, 127, 129]
+    q, kc, vc, table, clens = random_case(hq * 7 + d + bs, lens, hq, hkv, d, bs, torch.bfloat16, poison=True)
+    for s in (1, 3, 0):
+        check(q, kc, vc, table, clens, 1 / math.sqrt(d), s, f"hq={hq} hkv={hkv} d={d} bs={bs} s={s}")
+
+
+def test_large_group_bad_block_id_reads_zeros():
+    q, kc, vc, table, lens = random_case(81, [200, 700], 64, 1, 128, 16, torch.bfloat16)
+    bad_table = table.clone()
+    bad_table[1, 3] = kc.shape[0] + 5
+    kz, vz = kc.clone(), vc.clone()
+    for s in (1, 0):
+        out, _ = run_decode(q, kc, vc, bad_table, lens, 0.1, s)
+        assert pkv.get_device_error() & pkv.DEVERR["block"]
+        assert torch.isfinite(out).all()
+        assert_attn_close(out[:1], oracle.paged_decode(q[:1], kz, vz, table[:1], lens[:1], 0.1)[0], "good seq")
+
+
 @pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.float32, 128), (torch.bfloat16, 96),
                                      (torch.float32, 40), (torch.bfloat16, 128)])
 @pytest.mark.parametrize("bs", [8, 16])
