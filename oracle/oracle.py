@@ -74,6 +74,11 @@ def _load():
         lib.oracle_prefill.argtypes = [P, P, P, P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
         lib.oracle_prefill.restype = ctypes.c_int
+        lib.oracle_paged_attention.argtypes = [P, P, P, P, P, ctypes.c_int, P, P, P, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_long, ctypes.c_double,
+                                               ctypes.c_long, ctypes.c_int]
+        lib.oracle_paged_attention.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -187,6 +192,41 @@ def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale: float,
                                      float(scale), int(chunk_tokens), int(nthreads))
     if rc != 0:
         raise ValueError("oracle: context length or block-table entry out of range")
+    return out, lse
+
+
+def paged_attention(q, k_cache, v_cache, block_table, context_lens, cu_q, scale: float,
+                    window: int = 0, nthreads: int = 1):
+    """Queries at the end of each cached sequence, causal, optional sliding window.
+
+    Sequence b holds context_lens[b] tokens in the cache (its queries' own K/V
+    among them) and owns query rows cu_q[b] .. cu_q[b+1]-1; its i-th of nq queries
+    sits at position p = len - nq + i and sees keys lo .. p, lo = max(0, p - window
+    + 1) for window > 0, else 0.  q [Tq][Hq][d] (fp32 values); caches
+    [NB][Hkv][bs][d]; block_table int32 [B][MBS].  Returns (out [Tq][Hq][d],
+    lse [Tq][Hq]) in float64.
+    """
+    qn = _c(to_numpy(q), np.float32)
+    kc, vc = _c(to_numpy(k_cache)), _c(to_numpy(v_cache))
+    dt = _dtype_code(kc)
+    if _dtype_code(vc) != dt:
+        raise TypeError("K and V caches differ in element type")
+    table = _c(to_numpy(block_table), np.int32)
+    lens = _c(to_numpy(context_lens), np.int32)
+    cu = _c(to_numpy(cu_q), np.int32)
+    Tq, Hq, d = qn.shape
+    NB, Hkv, bs, d2 = kc.shape
+    B = lens.shape[0]
+    if d2 != d or cu.shape[0] != B + 1 or cu[-1] != Tq:
+        raise ValueError("shape mismatch")
+    MBS = table.shape[1] if table.ndim == 2 else 0
+    out = np.zeros((Tq, Hq, d), np.float64)
+    lse = np.zeros((Tq, Hq), np.float64)
+    rc = _load().oracle_paged_attention(_ptr(out), _ptr(lse), _ptr(qn), _ptr(kc), _ptr(vc), dt,
+                                        _ptr(table), _ptr(lens), _ptr(cu), B, Hq, Hkv, d, bs, MBS,
+                                        NB, float(scale), int(window), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle: length, query count or block-table entry out of range")
     return out, lse
 
 

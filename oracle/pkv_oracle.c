@@ -208,6 +208,99 @@ int oracle_paged_decode(double *out, double *lse, const float *q, const void *k_
     return c.bad ? -1 : 0;
 }
 
+/* ------------------------------------- queries at the end of the cache */
+
+/*
+ * Several queries per sequence over the paged cache, with an optional sliding
+ * window.  Sequence b holds L = context_lens[b] tokens in the cache, the
+ * queries' own K/V among them, and owns query rows cu_q[b] .. cu_q[b+1]-1.  Its
+ * i-th query (nq = cu_q[b+1] - cu_q[b] of them) is the token at position
+ * p = L - nq + i and attends the keys lo .. p, causally aligned to the end of
+ * the cache (zwjcode.cn "KV Cache 的增量解码" §13: a query sees itself and the
+ * keys before it, not the later new tokens).  lo = 0 without a window; with
+ * window W > 0 it is max(0, p - W + 1): the most recent W positions
+ * (zwjcode.cn §10 "滑动窗口", §15; plumephp.com "KV Cache 优化与注意力机制加速"
+ * §5.2).  One query per sequence and no window is the decode of
+ * oracle_paged_decode; many queries is a prefill on top of cached context.
+ */
+typedef struct {
+    double *out, *lse;
+    const float *q;
+    const void *kc, *vc;
+    int dtype;
+    const int32_t *table, *lens, *cu_q;
+    int B, Hq, Hkv, d, bs, MBS;
+    long NB;
+    double scale;
+    long window;
+    volatile int bad;
+} multi_ctx;
+
+/* Gather tokens [t0, t1) of sequence b, KV head j into K[t1-t0][d], V[t1-t0][d]. */
+static int gather_range(const multi_ctx *c, int b, int j, long t0, long t1, double *K, double *V) {
+    for (long t = t0; t < t1; ++t) {
+        long page = t / c->bs, off = t % c->bs;
+        long phys = c->table[(size_t)b * c->MBS + page];
+        if (phys < 0 || phys >= c->NB) return -1;
+        size_t row = (((size_t)phys * c->Hkv + j) * c->bs + off) * c->d;
+        for (int e = 0; e < c->d; ++e) {
+            K[(size_t)(t - t0) * c->d + e] = elem(c->kc, c->dtype, row + e);
+            V[(size_t)(t - t0) * c->d + e] = elem(c->vc, c->dtype, row + e);
+        }
+    }
+    return 0;
+}
+
+static void multi_item(void *p, long item) {
+    multi_ctx *c = (multi_ctx *)p;
+    int b = (int)(item / c->Hkv), j = (int)(item % c->Hkv);
+    long L = c->lens[b], r0 = c->cu_q[b], nq = (long)c->cu_q[b + 1] - c->cu_q[b];
+    int m = c->Hq / c->Hkv, d = c->d;
+    if (L < 0 || L > (long)c->MBS * c->bs || nq < 0 || nq > L) { c->bad = 1; return; }
+    if (nq == 0) return;
+    long first = L - nq;   /* position of the first query */
+    long lo0 = c->window > 0 ? first - c->window + 1 : 0;
+    if (lo0 < 0) lo0 = 0;
+    long n = L - lo0;      /* every key any of the queries sees */
+    double *K = (double *)malloc(sizeof(double) * (size_t)n * d);
+    double *V = (double *)malloc(sizeof(double) * (size_t)n * d);
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    double *q = (double *)malloc(sizeof(double) * (size_t)d);
+    if (gather_range(c, b, j, lo0, L, K, V) != 0) c->bad = 1;
+    else {
+        for (long i = 0; i < nq; ++i) {
+            long pos = first + i;
+            long lo = c->window > 0 ? pos - c->window + 1 : 0;
+            if (lo < 0) lo = 0;
+            for (int h = j * m; h < (j + 1) * m; ++h) {   /* the heads with floor(h/m) == j */
+                size_t row = (size_t)(r0 + i) * c->Hq + h;
+                for (int e = 0; e < d; ++e) q[e] = (double)c->q[row * d + e];
+                double l = attend(q, K + (size_t)(lo - lo0) * d, V + (size_t)(lo - lo0) * d,
+                                  pos - lo + 1, d, c->scale, c->out + row * d, s);
+                if (c->lse) c->lse[row] = l;
+            }
+        }
+    }
+    free(K); free(V); free(s); free(q);
+}
+
+/*
+ * out [Tq][Hq][d], lse [Tq][Hq] (may be NULL) in double; q [Tq][Hq][d] fp32;
+ * cu_q int32 [B+1] (cu_q[0] = 0, cu_q[B] = Tq); window <= 0: no window.  Table
+ * entries of pages no query sees are never read.  Returns 0, or -1 for a bad
+ * length, a query count above its length, or a bad table entry that is read.
+ */
+int oracle_paged_attention(double *out, double *lse, const float *q, const void *k_cache,
+                           const void *v_cache, int dtype, const int32_t *block_table,
+                           const int32_t *context_lens, const int32_t *cu_q, int B, int Hq, int Hkv,
+                           int d, int bs, int MBS, long NB, double scale, long window, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || bs <= 0 || MBS < 0) return -1;
+    multi_ctx c = {out, lse, q, k_cache, v_cache, dtype, block_table, context_lens, cu_q,
+                   B, Hq, Hkv, d, bs, MBS, NB, scale, window, 0};
+    run_items(multi_item, &c, (long)B * Hkv, nthreads);
+    return c.bad ? -1 : 0;
+}
+
 /* ------------------------------------------------- contiguous (no paging) */
 
 /*

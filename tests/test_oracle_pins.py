@@ -388,3 +388,105 @@ def test_paged_cache_bytes_equal_the_formula():
     v = torch.empty_like(k)
     got = k.numel() * k.element_size() + v.numel() * v.element_size()
     assert got == oracle.kv_cache_bytes(1, n_seq, hkv, tokens, d, 2)
+
+
+# ---------------------------------------------- queries at the end of the cache
+# Queries sit at the last positions of their sequence and see keys up to their
+# own position (zwjcode.cn "KV Cache 的增量解码" §13); a sliding window keeps the
+# most recent W positions (zwjcode.cn §10, §15; plumephp.com §5.2).
+
+def _multi_case(seed, lens, nq, hq, hkv, d, bs, dtype):
+    q1, kc, vc, table = _random_paged(seed, lens, hq, hkv, d, bs, dtype)
+    g = gen.generator(seed + 99)
+    q = gen.randn(g, (nq * len(lens), hq, d), torch.float32)
+    cu = np.arange(len(lens) + 1, dtype=np.int32) * nq
+    return q, kc, vc, table, np.array(lens, np.int32), cu
+
+
+def _sdpa_masked(q_rows, K, V, positions, window, scale):
+    """torch fp64 SDPA with a boolean mask written from the definition."""
+    L = K.shape[0]
+    keys = torch.arange(L)[None, :]
+    pos = torch.tensor(positions)[:, None]
+    allowed = keys <= pos
+    if window > 0:
+        allowed &= keys > pos - window
+    qh = q_rows.double().permute(1, 0, 2)[None]
+    kh = K.double().permute(1, 0, 2)[None]
+    vh = V.double().permute(1, 0, 2)[None]
+    out = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=allowed[None, None],
+                                                           scale=scale, enable_gqa=True)
+    s = torch.einsum("hqd,hkd->hqk", qh[0], kh[0].repeat_interleave(qh.shape[1] // kh.shape[1], 0)) * scale
+    lse = torch.logsumexp(s.masked_fill(~allowed[None], float("-inf")), -1)
+    return out[0].permute(1, 0, 2), lse.permute(1, 0)
+
+
+@pytest.mark.parametrize("nq,window", [(1, 0), (1, 7), (1, 1), (3, 0), (3, 5), (17, 0), (17, 16), (17, 100)])
+def test_paged_attention_matches_torch_sdpa_with_explicit_mask(nq, window):
+    lens, hq, hkv, d, bs = [40, 17, 33], 8, 2, 32, 16
+    q, kc, vc, table, clens, cu = _multi_case(11 + nq + window, lens, nq, hq, hkv, d, bs, torch.bfloat16)
+    scale = 0.177
+    out, lse = oracle.paged_attention(q, kc, vc, table, clens, cu, scale, window)
+    for b, L in enumerate(lens):
+        K = _logical_kv(kc, table[b], L, bs)
+        V = _logical_kv(vc, table[b], L, bs)
+        rows = slice(cu[b], cu[b + 1])
+        ref, ref_lse = _sdpa_masked(q[rows], K, V, list(range(L - nq, L)), window, scale)
+        assert np.abs(out[rows] - ref.numpy()).max() < 1e-12
+        assert np.abs(lse[rows] - ref_lse.numpy()).max() < 1e-12
+
+
+def test_window_of_one_returns_the_own_value_row():
+    lens, nq, hq, hkv, d, bs = [21, 48], 4, 4, 1, 16, 16
+    q, kc, vc, table, clens, cu = _multi_case(5, lens, nq, hq, hkv, d, bs, torch.float32)
+    out, lse = oracle.paged_attention(q, kc, vc, table, clens, cu, 0.3, window=1)
+    for b, L in enumerate(lens):
+        K = _logical_kv(kc, table[b], L, bs).double()
+        V = _logical_kv(vc, table[b], L, bs).double()
+        for i in range(nq):
+            p, r = L - nq + i, cu[b] + i
+            assert np.array_equal(out[r], V[p, 0][None].expand(hq, d).numpy())
+            assert np.allclose(lse[r], (0.3 * q[r].double() @ K[p, 0]).numpy(), rtol=0, atol=1e-12)
+
+
+def test_window_covering_everything_and_one_query_reduce_to_decode():
+    lens, hq, hkv, d, bs = [300, 17, 1000, 65], 8, 2, 64, 16
+    q, kc, vc, table, clens, cu = _multi_case(8, lens, 1, hq, hkv, d, bs, torch.bfloat16)
+    full, full_lse = oracle.paged_attention(q, kc, vc, table, clens, cu, 0.125)
+    wide, wide_lse = oracle.paged_attention(q, kc, vc, table, clens, cu, 0.125, window=1000)
+    assert np.array_equal(full, wide) and np.array_equal(full_lse, wide_lse)
+    dec, dec_lse = oracle.paged_decode(q, kc, vc, table, clens, 0.125)
+    assert np.array_equal(full, dec) and np.array_equal(full_lse, dec_lse)
+
+
+def test_queries_at_the_end_equal_the_last_rows_of_full_causal_prefill():
+    # zwjcode.cn §07: the cached computation reproduces the full recomputation
+    L, nq, hq, hkv, d, bs = 45, 9, 4, 2, 16, 16
+    g = gen.generator(17)
+    qkv = [gen.randn(g, (L, h, d), torch.float32) for h in (hq, hkv, hkv)]
+    nb = gen.blocks_needed(L, bs) + 2
+    kc, vc = _fp32_cache(nb, hkv, bs, d), _fp32_cache(nb, hkv, bs, d)
+    table = gen.block_table_from_order(gen.permutation(g, nb), [gen.blocks_needed(L, bs)])
+    oracle.kv_append(kc, vc, qkv[1].numpy(), qkv[2].numpy(),
+                     np.array([oracle.slot_of(table[0], t, bs) for t in range(L)]))
+    full, full_lse = oracle.prefill(qkv[0], qkv[1], qkv[2], np.array([0, L], np.int32), 0.25)
+    out, lse = oracle.paged_attention(qkv[0][L - nq:], kc, vc, table, np.array([L], np.int32),
+                                      np.array([0, nq], np.int32), 0.25)
+    assert np.abs(out - full[L - nq:]).max() < 1e-12
+    assert np.abs(lse - full_lse[L - nq:]).max() < 1e-12
+
+
+def test_blocks_outside_the_window_are_never_read():
+    lens, nq, hq, hkv, d, bs, W = [200, 130], 2, 4, 2, 32, 16, 40
+    q, kc, vc, table, clens, cu = _multi_case(23, lens, nq, hq, hkv, d, bs, torch.float32)
+    ref, ref_lse = oracle.paged_attention(q, kc, vc, table, clens, cu, 0.2, window=W)
+    freed = table.clone()
+    kp, vp = kc.clone(), vc.clone()
+    for b, L in enumerate(lens):
+        first_seen = L - nq - W + 1
+        for page in range(first_seen // bs):          # whole blocks before the window
+            kp[int(table[b, page])] = float("nan")
+            vp[int(table[b, page])] = float("nan")
+            freed[b, page] = -1
+    out, lse = oracle.paged_attention(q, kp, vp, freed, clens, cu, 0.2, window=W)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse)
