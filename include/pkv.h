@@ -180,6 +180,46 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
                                       size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_paged_attention -- queries at the end of each cached sequence: several per
+ * sequence, causal, with an optional sliding window.
+ *
+ * Sequence b holds L = context_lens[b] tokens in the cache, its queries' own K/V among
+ * them (append first), and owns query rows cu_q[b] .. cu_q[b+1]-1.  Its i-th row, of
+ * nq = cu_q[b+1] - cu_q[b], is the token at position p = L - nq + i and attends the keys
+ * lo .. p: a query sees itself and the tokens before it, not the later new tokens
+ * (zwjcode.cn "KV Cache 的增量解码" §13).  lo = 0 without a window; with window W > 0,
+ * lo = max(0, p - W + 1), the most recent W positions (zwjcode.cn §10, §15;
+ * plumephp.com "KV Cache 优化与注意力机制加速" §5.2).  One query per sequence and
+ * W = 0 is pkv_paged_decode_attention; nq = k new tokens is a k-token verification
+ * step; a long nq is a prefill of new tokens on top of a cached prefix.
+ *
+ *   out, lse     fp32 [Tq][Hq][d] and [Tq][Hq] (lse may be NULL), row-major by query row
+ *   q            fp32 [Tq][Hq][d]
+ *   cu_q         int32 [B+1], non-decreasing, cu_q[0] = 0, cu_q[B] = Tq, each count
+ *                <= max_q and <= context_lens[b].  When Tq == B and max_q == 1 every
+ *                sequence has exactly one query and cu_q is not read (may be NULL).
+ *   window       0: none; W > 0: sliding window of W tokens.  Blocks before a row's
+ *                window are never read, so a caller may free them.
+ *   caches, block_table, context_lens, scale, num_splits: as pkv_paged_decode_attention
+ *   workspace    pkv_paged_attention_workspace_bytes(...) bytes, zeroed once, same
+ *                rules as pkv_paged_decode_attention.
+ * One query per sequence runs the decode kernels (tensor cores where they apply);
+ * several run a CUDA-core kernel, one warp per (query row, head, chunk).  An
+ * inconsistent cu_q or a row count above its sequence length sets
+ * PKV_DEVERR_CU_SEQLENS and those rows get out = 0, lse = -inf.  Requires
+ * Tq <= B * max_q and Tq * Hq < 2^31.
+ */
+size_t pkv_paged_attention_workspace_bytes(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs,
+                                           int MBS, int window, int num_splits);
+
+pkv_status pkv_paged_attention(float *out, float *lse, const float *q, const void *k_cache,
+                               const void *v_cache, pkv_dtype dt, const int32_t *block_table,
+                               const int32_t *context_lens, const int32_t *cu_q, int B, int Tq,
+                               int max_q, int Hq, int Hkv, int d, int bs, int MBS, int NB, float scale,
+                               int window, int num_splits, void *workspace, size_t workspace_bytes,
+                               pkv_stream_t stream);
+
+/*
  * pkv_paged_decode_attention_noalloc -- pkv_paged_decode_attention without a workspace.
  *
  * The paper has no counterpart for this entry point: it exists for callers that cannot

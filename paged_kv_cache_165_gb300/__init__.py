@@ -18,6 +18,8 @@ from ._binding import (  # noqa: F401
     kv_block_copy,
     lib,
     library_path,
+    paged_attention,
+    paged_attention_workspace_bytes,
     paged_decode_attention,
     paged_decode_attention_noalloc,
     prefill_attention,

@@ -61,6 +61,11 @@ def lib() -> ctypes.CDLL:
     L.pkv_kv_block_copy.restype = I
     L.pkv_decode_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     L.pkv_decode_workspace_bytes.restype = Z
+    L.pkv_paged_attention_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I, I]
+    L.pkv_paged_attention_workspace_bytes.restype = Z
+    L.pkv_paged_attention.argtypes = [P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, I, F, I, I, P,
+                                      Z, P]
+    L.pkv_paged_attention.restype = I
     L.pkv_decode_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I]
     L.pkv_decode_kernel_launches.restype = I
     L.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P,
@@ -189,6 +194,44 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table),
         _ptr(context_lens), B, Hq, Hkv, d, bs, MBS, NB, float(scale), int(num_splits),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def paged_attention_workspace_bytes(B, Tq, max_q, Hq, Hkv, d, bs, MBS, window=0, num_splits=0) -> int:
+    return int(lib().pkv_paged_attention_workspace_bytes(B, Tq, max_q, Hq, Hkv, d, bs, MBS, window,
+                                                         num_splits))
+
+
+def paged_attention(out, q, k_cache, v_cache, block_table, context_lens, scale, cu_q=None, max_q=1,
+                    window=0, lse=None, num_splits=0, workspace=None, stream=None) -> None:
+    """Queries at the end of each cached sequence (causal, optional sliding window).
+
+    q, out [Tq][Hq][d] fp32; cu_q int32 [B+1] (None: one query per sequence)."""
+    _cuda("k_cache", k_cache)
+    dt = _dtype(k_cache)
+    _cuda("v_cache", v_cache, k_cache.dtype)
+    _cuda("q", q, torch.float32)
+    _cuda("out", out, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    if cu_q is not None:
+        _cuda("cu_q", cu_q, torch.int32)
+    if lse is not None:
+        _cuda("lse", lse, torch.float32)
+    NB, Hkv, bs, d = k_cache.shape
+    Tq, Hq, dq = q.shape
+    B = context_lens.numel()
+    if dq != d or tuple(out.shape) != (Tq, Hq, d) or block_table.dim() != 2 or \
+            block_table.shape[0] != B or (cu_q is not None and cu_q.numel() != B + 1) or \
+            (cu_q is None and Tq != B) or (lse is not None and lse.numel() != Tq * Hq):
+        raise ValueError("paged_attention: shapes do not match")
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_attention(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table),
+        _ptr(context_lens), _ptr(cu_q), B, Tq, int(max_q), Hq, Hkv, d, bs, block_table.shape[1], NB,
+        float(scale), int(window), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_table, context_lens, scale,

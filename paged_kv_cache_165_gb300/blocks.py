@@ -14,6 +14,10 @@ This is the bookkeeping that sits above the C ABI and produces its inputs
   copied to a fresh block which the writer takes over; the old block loses one
   reference (copy-on-write; 0539edu.com "从KV cache共享到批量调度…" §3.2, §5.2: the
   count is checked before the write).
+* With a sliding window of W tokens (zwjcode.cn "KV Cache 的增量解码" §10;
+  plumephp.com §5.2) ``release_outside_window`` gives back the blocks that hold
+  only positions before the window: no later query of the sequence sees them.
+  Their table entries become -1 and are never read.
 * ``audit`` checks the invariant that every block's count equals the number of
   table entries that reference it (0539edu.com §5.2 suggests logging and checking
   every cache read/write per request).
@@ -82,19 +86,39 @@ class BlockManager:
             raise KeyError(f"sequence {child} exists")
         table = list(self.tables[parent])
         for blk in table:
-            self.refcount[blk] += 1
+            if blk >= 0:
+                self.refcount[blk] += 1
         self.tables[child] = table
         self.lengths[child] = self.lengths[parent]
 
     def free_sequence(self, seq: int) -> None:
         for blk in self.tables.pop(seq):
-            self._release(blk)
+            if blk >= 0:
+                self._release(blk)
         del self.lengths[seq]
+
+    def release_outside_window(self, seq: int, window: int) -> List[int]:
+        """Give back the blocks of ``seq`` that hold only positions before its last
+        ``window`` tokens; returns their ids.  The current query (position len - 1) sees
+        positions len - window .. len - 1, and later queries see later ones."""
+        if window <= 0:
+            return []
+        lo = self.lengths[seq] - window
+        table = self.tables[seq]
+        released = []
+        for j in range(max(0, lo) // self.block_size):   # blocks ending at or before lo
+            if table[j] >= 0:
+                self._release(table[j])
+                released.append(table[j])
+                table[j] = -1
+        return released
 
     def slot(self, seq: int, pos: int) -> int:
         """Cache slot of logical position ``pos``: table[pos // bs] * bs + pos % bs."""
-        table = self.tables[seq]
-        return table[pos // self.block_size] * self.block_size + pos % self.block_size
+        blk = self.tables[seq][pos // self.block_size]
+        if blk < 0:
+            raise KeyError(f"position {pos} of sequence {seq} lies in a released block")
+        return blk * self.block_size + pos % self.block_size
 
     def append_slot(self, seq: int) -> Tuple[int, Optional[Tuple[int, int]]]:
         """Reserve the slot of the next token of ``seq``.
@@ -152,7 +176,8 @@ class BlockManager:
         refs = [0] * self.num_blocks
         for table in self.tables.values():
             for blk in table:
-                refs[blk] += 1
+                if blk >= 0:
+                    refs[blk] += 1
         if refs != self.refcount:
             bad = [b for b in range(self.num_blocks) if refs[b] != self.refcount[b]][:8]
             raise AssertionError(f"refcount mismatch at blocks {bad}")

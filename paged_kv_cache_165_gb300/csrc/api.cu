@@ -232,6 +232,65 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_decode_attention launch");
 }
 
+size_t pkv_paged_attention_workspace_bytes(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs,
+                                           int MBS, int window, int num_splits) {
+    if (check_decode_sizes(B, Hq, Hkv, d, bs, MBS) != PKV_OK || Tq < 0 || max_q < 0 || window < 0 ||
+        num_splits < 0)
+        return 0;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != PKV_OK) return 0;
+    const int vis = visible_blocks(MBS, bs, window);
+    if (Tq == B && max_q <= 1)
+        return decode_workspace_upper_bound(B, Hq, Hkv, d, bs, vis, num_splits, st->sm_count);
+    // query rows run on the CUDA-core path (the plan of an unaligned fp32 cache)
+    return plan_decode(Tq, Hq, Hkv, d, bs, vis, 1, PKV_F32, num_splits, st->sm_count, false, false)
+        .workspace_bytes;
+}
+
+pkv_status pkv_paged_attention(float *out, float *lse, const float *q, const void *k_cache,
+                               const void *v_cache, pkv_dtype dt, const int32_t *block_table,
+                               const int32_t *context_lens, const int32_t *cu_q, int B, int Tq,
+                               int max_q, int Hq, int Hkv, int d, int bs, int MBS, int NB, float scale,
+                               int window, int num_splits, void *workspace, size_t workspace_bytes,
+                               pkv_stream_t stream) {
+    int eb = 0;
+    if (!elem_size(dt, &eb)) return fail(PKV_ERR_UNSUPPORTED, "paged_attention: element type %d", dt);
+    pkv_status s = check_decode_sizes(B, Hq, Hkv, d, bs, MBS);
+    if (s != PKV_OK) return s;
+    if (NB < 1 || num_splits < 0 || window < 0 || Tq < 0 || max_q < 0 ||
+        static_cast<long long>(Tq) > static_cast<long long>(B) * max_q ||
+        static_cast<long long>(Tq) * Hq > 0x7fffffffll)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attention: NB=%d num_splits=%d window=%d Tq=%d max_q=%d",
+                    NB, num_splits, window, Tq, max_q);
+    if (B == 0 || Tq == 0) return PKV_OK;
+    const bool one_per_seq = Tq == B && max_q == 1;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens || (!one_per_seq && !cu_q))
+        return fail(PKV_ERR_INVALID_ARG, "paged_attention: null pointer");
+    if (reinterpret_cast<uintptr_t>(q) % 8 != 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attention: q must be 8-byte aligned");
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != PKV_OK) return s;
+    const int vis = visible_blocks(MBS, bs, window);
+    const DecodePlan plan =
+        one_per_seq ? plan_decode(B, Hq, Hkv, d, bs, vis, NB, dt, num_splits, st->sm_count,
+                                  aligned16(k_cache) && aligned16(v_cache), aligned16(q))
+                    : plan_decode(Tq, Hq, Hkv, d, bs, vis, NB, dt, num_splits, st->sm_count, false, false);
+    if (plan.workspace_bytes > 0 &&
+        (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
+         reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+        return fail(PKV_ERR_WORKSPACE,
+                    "paged_attention: needs %zu bytes of 16-byte aligned workspace, got %zu",
+                    plan.workspace_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
+    DecodeArgs a{out, lse, q, k_cache, v_cache, block_table, context_lens,
+                 B, Hq, Hkv, d, bs, MBS, NB, scale, workspace, st->err};
+    a.window = window;
+    a.cu_q = one_per_seq ? nullptr : cu_q;
+    a.rows = one_per_seq ? B : Tq;
+    cudaError_t e = launch_decode(a, plan, dt, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_attention launch");
+}
+
 pkv_status pkv_prefill_attention(float *out, float *lse, const void *q, const void *k, const void *v,
                                  pkv_dtype dt, const int32_t *cu_seqlens, int B, int T,
                                  int max_seqlen, int Hq, int Hkv, int d, float scale,

@@ -90,9 +90,10 @@ struct TcPage {
         l_run = 0.f;
     }
 
-    // Consume one page: `valid` (1..BS) of its tokens belong to the sequence.  Updates
-    // this lane's running max (head g), partial sum and output fragments.
-    __device__ static void page(uint8_t *stage, int valid, const uint32_t (&qa)[KS][4],
+    // Consume one page: its tokens first .. valid-1 (0 <= first < valid <= BS) are
+    // visible.  Updates this lane's running max (head g), partial sum and output
+    // fragments.
+    __device__ static void page(uint8_t *stage, int first, int valid, const uint32_t (&qa)[KS][4],
                                 float (&o)[ONT][4], float &m_run, float &l_run,
                                 float scale_log2, int lane) {
         const int t4 = lane & 3;
@@ -135,7 +136,7 @@ struct TcPage {
             for (int e = 0; e < 2; ++e) {
                 const int tok = nt * 8 + 2 * t4 + e;
                 const float v = (s[nt][e] + s[nt][2 + e]) * scale_log2;
-                sc[nt][e] = tok < valid ? v : -INFINITY;
+                sc[nt][e] = tok < valid && tok >= first ? v : -INFINITY;
                 mx = fmaxf(mx, sc[nt][e]);
             }
         }
@@ -225,9 +226,10 @@ __global__ void __launch_bounds__(NW * 32)
     const int head0 = kvh * p.m + tile * 8;
     const int nheads = min(8, (kvh + 1) * p.m - head0);
 
-    const int len = checked_len(p, b, BS, threadIdx.x == 0 && split == 0 && g_unit == 0);
-    const int n_pages = (len + BS - 1) / BS;
-    const int pg0 = split * p.chunk_pages;
+    const SeqSpan sp = seq_span(p, b, BS, threadIdx.x == 0 && split == 0 && g_unit == 0);
+    const int len = sp.len;
+    const int n_pages = sp.npages;
+    const int pg0 = split * p.chunk_pages;   // pages relative to sp.pfirst
     const int pg1 = min(n_pages, pg0 + p.chunk_pages);
     if (pg0 >= pg1) {
         // Nothing to read.  Chunk 0 of an empty sequence writes out = 0, lse = -inf; any
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(NW * 32)
     // fetched 32 at a time (one per lane) ahead of the copies that need them.
     const int pages = pg1 - pg0;
     const int n_my = pages > warp ? (pages - warp + NW - 1) / NW : 0;
-    const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + pg0 + warp;
+    const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + sp.pfirst + pg0 + warp;
     int tcur = lane < n_my ? __ldg(tbl + static_cast<size_t>(lane) * NW) : 0;
     int tnext = 32 + lane < n_my ? __ldg(tbl + static_cast<size_t>(32 + lane) * NW) : 0;
     int tbase = 0;
@@ -301,9 +303,9 @@ __global__ void __launch_bounds__(NW * 32)
             if (lane == 0) raise_error(p.err, PKV_DEVERR_TIMEOUT);
             break;
         }
-        const int pg = pg0 + warp + k * NW;
-        PG::page(smem + static_cast<size_t>(st) * PG::kStageBytes, min(BS, len - pg * BS), qa, o,
-                 m_run, l_run, p.scale_log2, lane);
+        const int pg = sp.pfirst + pg0 + warp + k * NW;
+        PG::page(smem + static_cast<size_t>(st) * PG::kStageBytes, max(0, sp.lo - pg * BS),
+                 min(BS, len - pg * BS), qa, o, m_run, l_run, p.scale_log2, lane);
         if (k + ST < n_my) {
             issue(k + ST);
             issued = k + ST + 1;
@@ -454,9 +456,10 @@ __global__ void __launch_bounds__((GroupCfg<D, BS, ST>::kMaxTiles + 1) * 32, 1)
     const int tiles = p.head_tiles;          // consumer warps; warp `tiles` is the producer
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
 
-    const int len = checked_len(p, b, BS, threadIdx.x == 0 && split == 0 && kvh == 0);
-    const int n_pages = (len + BS - 1) / BS;
-    const int pg0 = split * p.chunk_pages;
+    const SeqSpan sp = seq_span(p, b, BS, threadIdx.x == 0 && split == 0 && kvh == 0);
+    const int len = sp.len;
+    const int n_pages = sp.npages;
+    const int pg0 = split * p.chunk_pages;   // pages relative to sp.pfirst
     const int pg1 = min(n_pages, pg0 + p.chunk_pages);
     const size_t bi_group = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.m;
     if (pg0 >= pg1) {
@@ -484,7 +487,7 @@ __global__ void __launch_bounds__((GroupCfg<D, BS, ST>::kMaxTiles + 1) * 32, 1)
     bool ok = true;
     if (warp == tiles) {
         // ---- producer: page k goes to stage k % ST once the consumers released it
-        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + pg0;
+        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + sp.pfirst + pg0;
         int tcur = lane < pages ? __ldg(tbl + lane) : 0;
         int tnext = 32 + lane < pages ? __ldg(tbl + 32 + lane) : 0;
         int tbase = 0;
@@ -533,9 +536,9 @@ __global__ void __launch_bounds__((GroupCfg<D, BS, ST>::kMaxTiles + 1) * 32, 1)
                 ok = false;
                 break;
             }
-            const int pg = pg0 + k;
-            PG::page(smem + static_cast<size_t>(st) * PG::kStageBytes, min(BS, len - pg * BS), qa, o,
-                     m_run, l_run, p.scale_log2, lane);
+            const int pg = sp.pfirst + pg0 + k;
+            PG::page(smem + static_cast<size_t>(st) * PG::kStageBytes, max(0, sp.lo - pg * BS),
+                     min(BS, len - pg * BS), qa, o, m_run, l_run, p.scale_log2, lane);
             if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
         }
         l_run += __shfl_xor_sync(kFull, l_run, 1);
@@ -625,19 +628,22 @@ __device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16 *p)
     return __bfloat162float(*p);
 }
 
-// One warp per (chunk, query head, sequence); lanes own head-dim elements lane + 32*j.
+// One warp per (query row, query head, chunk); lanes own head-dim elements lane + 32*j.
+// A row is a sequence (decode) or one of the query rows of a sequence (cu_q).
 template <typename T, int J>
 __global__ void __launch_bounds__(32)
     decode_simt_kernel(const T *__restrict__ kc, const T *__restrict__ vc, const DecodeKParams p,
                        int d, int bs) {
     const int lane = threadIdx.x;
-    const int split = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
+    const int row = blockIdx.x, i = blockIdx.y, split = blockIdx.z;
     const int kvh = i / p.m;
-    const int len = checked_len(p, b, bs, lane == 0 && split == 0 && i == 0);
-    const int n_pages = (len + bs - 1) / bs;
-    const int pg0 = split * p.chunk_pages;
-    const int pg1 = min(n_pages, pg0 + p.chunk_pages);
-    const size_t bi = static_cast<size_t>(b) * p.Hq + i;
+    const SeqSpan sp = row_span(p, row, bs, lane == 0 && split == 0 && i == 0);
+    const int b = sp.b;
+    const int len = sp.len;
+    const int n_pages = sp.npages;
+    const int pg0 = sp.pfirst + split * p.chunk_pages;   // absolute pages
+    const int pg1 = min(sp.pfirst + n_pages, pg0 + p.chunk_pages);
+    const size_t bi = static_cast<size_t>(row) * p.Hq + i;
     const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;   // chunks holding tokens
     if (pg0 >= pg1) {
         if (split == 0) {   // an empty sequence: out = 0, lse = -inf
@@ -659,7 +665,7 @@ __global__ void __launch_bounds__(32)
         const bool bad = phys < 0 || phys >= p.NB;
         if (bad && lane == 0) raise_error(p.err, PKV_DEVERR_BLOCK);
         const int valid = min(bs, len - pg * bs);
-        for (int off = 0; off < valid; ++off) {
+        for (int off = max(0, sp.lo - pg * bs); off < valid; ++off) {
             const size_t base =
                 bad ? 0 : ((static_cast<size_t>(phys) * p.Hkv + kvh) * bs + off) * d;
             float dot = 0.f;
@@ -718,8 +724,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     __shared__ float red[kMergeThreads / 32];
     const size_t bi = blockIdx.x;
     const int b = static_cast<int>(bi / p.Hq);
-    const int len = checked_len(p, b, bs, false);
-    const int n_pages = (len + bs - 1) / bs;
+    const int n_pages = row_span(p, b, bs, false).npages;
     const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
     if (nc <= 1) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -923,7 +928,9 @@ size_t decode_workspace_upper_bound(int B, int Hq, int Hkv, int d, int bs, int M
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
                           cudaStream_t stream) {
-    if (a.B == 0) return cudaSuccess;
+    const int rows = a.rows >= 0 ? a.rows : a.B;
+    if (a.B == 0 || rows == 0) return cudaSuccess;
+    if (a.cu_q != nullptr && plan.tensor_core) return cudaErrorInvalidValue;   // rows need the CUDA-core path
     DecodeKParams kp{};
     kp.out = a.out;
     kp.lse = a.lse;
@@ -941,11 +948,13 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     kp.chunk_pages = plan.chunk_pages;
     kp.splits = plan.splits;
     kp.scale_log2 = a.scale * kLog2e;
+    kp.window = a.window;
+    kp.cu_q = a.cu_q;
     if (plan.splits > 1) {
         uint8_t *ws = static_cast<uint8_t *>(a.workspace);
         kp.counters = plan.fused_merge ? reinterpret_cast<unsigned *>(ws) : nullptr;
         kp.ws_o = reinterpret_cast<float *>(ws + PKV_DECODE_COUNTER_BYTES);
-        kp.ws_lse = kp.ws_o + static_cast<size_t>(a.B) * a.Hq * plan.splits * a.d;
+        kp.ws_lse = kp.ws_o + static_cast<size_t>(rows) * a.Hq * plan.splits * a.d;
     }
 
     cudaError_t e;
@@ -993,12 +1002,12 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
         }
         if (e != cudaSuccess || plan.splits == 1 || plan.fused_merge) return e;
     } else {
-        const dim3 grid(plan.splits, a.Hq, a.B);
+        const dim3 grid(rows, a.Hq, plan.splits);
         e = dt == PKV_F32 ? launch_simt<float>(a, kp, grid, stream)
                           : launch_simt<__nv_bfloat16>(a, kp, grid, stream);
         if (e != cudaSuccess || plan.splits == 1) return e;
     }
-    decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), kMergeThreads, 0, stream>>>(kp, a.d, a.bs);
+    decode_merge_kernel<<<static_cast<unsigned>(rows * a.Hq), kMergeThreads, 0, stream>>>(kp, a.d, a.bs);
     return cudaGetLastError();
 }
 

@@ -25,6 +25,8 @@ struct DecodeKParams {
     int chunk_pages;  // blocks per chunk
     int splits;       // chunks per sequence at most (partial slots per sequence)
     float scale_log2; // scale * log2(e): scores are kept in the base-2 domain
+    int window;       // > 0: only the most recent `window` tokens are visible
+    const int32_t *cu_q;   // query rows per sequence [B+1]; nullptr: row b = sequence b
 };
 
 // Sequence length after validation; an invalid length counts as empty.
@@ -35,6 +37,52 @@ __device__ __forceinline__ int checked_len(const DecodeKParams &p, int b, int bs
         len = 0;
     }
     return len;
+}
+
+// The keys a query row sees: tokens [lo, len) of sequence b, on pages [pfirst, pfirst +
+// npages).  A row is the token at position len - 1 of its sequence (the decode query,
+// row b = sequence b), or with query rows cu_q the i-th of the nq rows of sequence b,
+// at position L - nq + i: `len` is then that position + 1 (causal, aligned to the end
+// of the cache).  With a sliding window of W tokens, lo = max(0, len - W), the most
+// recent W positions; blocks before pfirst are never read and may have been freed.
+struct SeqSpan {
+    int b, len, lo, pfirst, npages;
+};
+
+__device__ __forceinline__ SeqSpan span_of(const DecodeKParams &p, int b, int len, int bs) {
+    SeqSpan s;
+    s.b = b;
+    s.len = len;
+    s.lo = p.window > 0 ? max(0, len - p.window) : 0;
+    s.pfirst = s.lo / bs;
+    s.npages = len > 0 ? (len + bs - 1) / bs - s.pfirst : 0;
+    return s;
+}
+
+__device__ __forceinline__ SeqSpan seq_span(const DecodeKParams &p, int b, int bs, bool report) {
+    return span_of(p, b, checked_len(p, b, bs, report), bs);
+}
+
+// Query row r (cu_q != nullptr): its sequence by binary search over cu_q, its position,
+// its span.  An inconsistent cu_q or a row count above the sequence length raises
+// PKV_DEVERR_CU_SEQLENS and the row sees nothing (out = 0, lse = -inf).
+__device__ __forceinline__ SeqSpan row_span(const DecodeKParams &p, int r, int bs, bool report) {
+    if (p.cu_q == nullptr) return seq_span(p, r, bs, report);
+    int lo = 0, hi = p.B;   // find b with cu_q[b] <= r < cu_q[b+1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.cu_q + mid) <= r) lo = mid;
+        else hi = mid;
+    }
+    const int b = lo;
+    const int c0 = __ldg(p.cu_q + b), c1 = __ldg(p.cu_q + b + 1);
+    const int L = checked_len(p, b, bs, report);
+    const int nq = c1 - c0;
+    if (r < c0 || r >= c1 || nq > L) {
+        if (report) raise_error(p.err, PKV_DEVERR_CU_SEQLENS);
+        return span_of(p, b, 0, bs);
+    }
+    return span_of(p, b, L - nq + (r - c0) + 1, bs);
 }
 
 // Large-group decode on tcgen05 (decode_umma.cu): d in {64, 128}, bs in {16, 32},

@@ -100,9 +100,10 @@ __global__ void __launch_bounds__(352, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const int len = checked_len(p, b, BS, threadIdx.x == 0 && split == 0 && kvh == 0);
-    const int n_pages = (len + BS - 1) / BS;
-    const int pg0 = split * p.chunk_pages;
+    const SeqSpan sp = seq_span(p, b, BS, threadIdx.x == 0 && split == 0 && kvh == 0);
+    const int len = sp.len;
+    const int n_pages = sp.npages;
+    const int pg0 = split * p.chunk_pages;   // pages relative to sp.pfirst
     const int pg1 = min(n_pages, pg0 + p.chunk_pages);
     const size_t bi_group = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.m;
     if (pg0 >= pg1) {
@@ -115,8 +116,9 @@ __global__ void __launch_bounds__(352, 1)
     }
     const int pages = pg1 - pg0;
     const int ntiles = (pages + PPT - 1) / PPT;
-    const int tok0 = pg0 * BS;              // first token of the chunk
-    const int tok_end = min(len, pg1 * BS); // one past its last token
+    const int tok0 = (sp.pfirst + pg0) * BS;                // first token of the chunk's pages
+    const int tok_lo = max(tok0, sp.lo);                      // its first visible token
+    const int tok_end = min(len, (sp.pfirst + pg1) * BS);     // one past its last token
     const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
 
     if (threadIdx.x == 0) {
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(352, 1)
             mbar_arrive_expect_tx(bar(Cfg::kQRaw), q_bytes);
             bulk_load(sP(0), p.q + bi_group * D, q_bytes, bar(Cfg::kQRaw));
         }
-        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + pg0;
+        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + sp.pfirst + pg0;
         int tcur = lane < pages ? __ldg(tbl + lane) : -1;
         int tbase = 0;
         const int oob_row = p.NB * p.Hkv * BS;
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(352, 1)
         const int r_hi = r & ~1, r_lo = r | 1;
         // The chunk's last page may end inside the sequence's last block: its V rows past
         // the end hold whatever the slots hold (NaN, Inf) and must be zero for P.V.
-        const int tail_valid = tok_end - (pg1 - 1) * BS;          // 1..BS tokens
+        const int tail_valid = tok_end - (sp.pfirst + pg1 - 1) * BS;   // 1..BS tokens
         const int tail_tile = (pages - 1) / PPT;
         const int tail_row0 = ((pages - 1) % PPT) * BS + tail_valid;
         const int tail_rows = BS - tail_valid;
@@ -353,10 +355,12 @@ __global__ void __launch_bounds__(352, 1)
                 sc[c] = mine + __shfl_xor_sync(kFullMask, send, 1);
             }
             const int key0 = tok0 + j * BN + part * 32;
-            if (tok0 + (j + 1) * BN > tok_end) {   // the chunk's last tile: keys past the end
+            if (tok0 + (j + 1) * BN > tok_end || tok0 + j * BN < tok_lo) {
+                // the chunk's last tile (keys past the end) or a tile starting before
+                // the window
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
-                    if (key0 + c >= tok_end) sc[c] = -INFINITY;
+                    if (key0 + c >= tok_end || key0 + c < tok_lo) sc[c] = -INFINITY;
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll

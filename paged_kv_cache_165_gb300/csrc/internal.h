@@ -67,7 +67,18 @@ struct DecodeArgs {
     float scale;
     void *workspace;
     unsigned *err;
+    int window = 0;                  // > 0: sliding window of this many tokens
+    const int32_t *cu_q = nullptr;   // query rows per sequence; nullptr: one per sequence
+    int rows = -1;                   // query rows (B when cu_q is nullptr)
 };
+
+// Blocks a query row can see: all of MBS, or with a window of W tokens at most
+// ceil(W / bs) + 1 (the window may start inside a block).
+inline int visible_blocks(int MBS, int bs, int window) {
+    if (window <= 0) return MBS;
+    const long long w = (static_cast<long long>(window) + bs - 1) / bs + 1;
+    return static_cast<int>(w < MBS ? w : MBS);
+}
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
                           cudaStream_t stream);

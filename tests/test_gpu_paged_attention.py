@@ -1,0 +1,156 @@
+"""pkv_paged_attention on the GPU against the fp64 oracle: sliding-window decode on
+every decode path, several queries per sequence (verification steps, prefill on top of
+a cached prefix), ragged and empty query counts, blocks released outside the window,
+and the device errors."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_165_gb300 as pkv
+from paged_kv_cache_165_gb300 import _build
+from workloads import gen
+
+from helpers import assert_attn_close, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    _build.build()
+    pkv.lib()
+    pkv.get_device_error()
+
+
+def make_case(seed, lens, nqs, hq, hkv, d, bs, dtype, spare=3):
+    g = gen.generator(seed)
+    per_seq = [gen.blocks_needed(n, bs) for n in lens]
+    nb = sum(per_seq) + spare
+    table = gen.block_table_from_order(gen.permutation(g, nb), per_seq)
+    kc = gen.randn(g, (nb, hkv, bs, d), dtype)
+    vc = gen.randn(g, (nb, hkv, bs, d), dtype)
+    q = gen.randn(g, (sum(nqs), hq, d), torch.float32)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(nqs)]), dtype=torch.int32)
+    return q, kc, vc, table, torch.tensor(lens, dtype=torch.int32), cu
+
+
+def release_outside_window(kc, vc, table, lens, nqs, window, bs):
+    """Poison and unmap (-1) every block that lies wholly before each sequence's first
+    visible position: the kernels must never read them."""
+    kp, vp, tp = kc.clone(), vc.clone(), table.clone()
+    for b, (L, nq) in enumerate(zip(lens, nqs)):
+        lo = L - nq - window + 1
+        for page in range(max(0, lo) // bs):
+            blk = int(table[b, page])
+            kp[blk] = float("nan")
+            vp[blk] = float("nan")
+            tp[b, page] = -1
+    return kp, vp, tp
+
+
+def run(q, kc, vc, table, lens, cu, scale, window, num_splits, one_per_seq):
+    Tq, Hq, d = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    B = lens.numel()
+    max_q = int((cu[1:] - cu[:-1]).max()) if B else 0
+    out = torch.full((Tq, Hq, d), float("nan"), device="cuda")
+    lse = torch.full((Tq, Hq), float("nan"), device="cuda")
+    ws = torch.zeros(max(16, pkv.paged_attention_workspace_bytes(B, Tq, max_q, Hq, Hkv, d, bs, table.shape[1],
+                                                                   window, num_splits)),
+                     dtype=torch.uint8, device="cuda")
+    pkv.paged_attention(out, dev(q), dev(kc), dev(vc), dev(table), dev(lens), scale,
+                        cu_q=None if one_per_seq else dev(cu), max_q=max_q, window=window, lse=lse,
+                        num_splits=num_splits, workspace=ws)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+LENS = [1, 15, 16, 17, 100, 0, 257, 1000, 33]
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [
+    (8, 8, 128, torch.bfloat16),     # tensor-core decode, m = 1
+    (16, 2, 128, torch.bfloat16),    # tensor-core decode, m = 8
+    (64, 1, 128, torch.bfloat16),    # tcgen05 large-group decode
+    (32, 2, 64, torch.bfloat16),     # tcgen05 large-group decode, d = 64
+    (32, 2, 256, torch.bfloat16),    # large-group mma.sync kernel
+    (8, 2, 96, torch.bfloat16),      # CUDA-core path
+    (8, 2, 64, torch.float32),       # CUDA-core path, fp32 cache
+])
+@pytest.mark.parametrize("window", [1, 5, 16, 17, 100, 4096])
+def test_sliding_window_decode_on_every_path(hq, hkv, d, dtype, window):
+    lens = [max(n, 1) for n in LENS]
+    nqs = [1] * len(lens)
+    q, kc, vc, table, clens, cu = make_case(hq + d + window, lens, nqs, hq, hkv, d, 16, dtype)
+    ref, ref_lse = oracle.paged_attention(q, kc, vc, table, clens, cu, 1 / math.sqrt(d), window)
+    kp, vp, tp = release_outside_window(kc, vc, table, lens, nqs, window, 16)
+    for s in (1, 3, 0):
+        out, lse = run(q, kp, vp, tp, clens, cu, 1 / math.sqrt(d), window, s, one_per_seq=True)
+        assert pkv.get_device_error() == 0
+        assert_attn_close(out, ref, f"window {window} splits {s} out")
+        assert_attn_close(lse, ref_lse, f"window {window} splits {s} lse")
+
+
+def test_window_zero_equals_paged_decode():
+    lens = [300, 17, 1000, 65]
+    q, kc, vc, table, clens, cu = make_case(3, lens, [1] * 4, 64, 8, 128, 16, torch.bfloat16)
+    out, lse = run(q, kc, vc, table, clens, cu, 0.088, 0, 0, one_per_seq=True)
+    ref, ref_lse = oracle.paged_decode(q, kc, vc, table, clens, 0.088)
+    assert_attn_close(out, ref, "out")
+    assert_attn_close(lse, ref_lse, "lse")
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype,bs", [
+    (16, 2, 128, torch.bfloat16, 16), (8, 8, 64, torch.bfloat16, 32),
+    (64, 1, 128, torch.bfloat16, 16), (8, 2, 40, torch.float32, 8),
+])
+@pytest.mark.parametrize("window", [0, 7, 64])
+def test_several_queries_per_sequence(hq, hkv, d, dtype, bs, window):
+    # ragged query counts, a sequence with none, one whose queries are all its tokens
+    lens = [50, 300, 17, 9, 700, 64]
+    nqs = [4, 1, 0, 9, 33, 5]
+    q, kc, vc, table, clens, cu = make_case(hq * 3 + window, lens, nqs, hq, hkv, d, bs, dtype)
+    scale = 1 / math.sqrt(d)
+    ref, ref_lse = oracle.paged_attention(q, kc, vc, table, clens, cu, scale, window)
+    if window:
+        kc, vc, table = release_outside_window(kc, vc, table, lens, nqs, window, bs)
+    for s in (1, 2, 0):
+        out, lse = run(q, kc, vc, table, clens, cu, scale, window, s, one_per_seq=False)
+        assert pkv.get_device_error() == 0
+        assert_attn_close(out, ref, f"splits {s} out")
+        assert_attn_close(lse, ref_lse, f"splits {s} lse")
+
+
+def test_prefill_on_top_of_a_cached_prefix_equals_full_prefill():
+    # the new tokens' rows of a prefill over prefix + new tokens (zwjcode.cn §07)
+    P, N, hq, hkv, d, bs = 200, 56, 8, 2, 64, 16
+    L = P + N
+    g = gen.generator(31)
+    qkv = [gen.randn(g, (L, h, d), torch.bfloat16) for h in (hq, hkv, hkv)]
+    nb = gen.blocks_needed(L, bs) + 1
+    table = gen.block_table_from_order(gen.permutation(g, nb), [gen.blocks_needed(L, bs)])
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.tensor([oracle.slot_of(table[0], t, bs) for t in range(L)], device="cuda")
+    pkv.kv_append(qkv[1].cuda(), qkv[2].cuda(), kc, vc, slots)
+    full, full_lse = oracle.prefill(qkv[0], qkv[1], qkv[2], np.array([0, L], np.int32), 0.125)
+    q_new = qkv[0][P:].float()
+    out, lse = run(q_new, kc.cpu(), vc.cpu(), table, torch.tensor([L], dtype=torch.int32),
+                   torch.tensor([0, N], dtype=torch.int32), 0.125, 0, 0, one_per_seq=False)
+    assert_attn_close(out, full[P:], "new rows")
+    assert_attn_close(lse, full_lse[P:], "new rows lse")
+
+
+def test_query_count_above_length_raises_cu_seqlens_error():
+    lens = [5, 40]
+    q, kc, vc, table, clens, cu = make_case(9, lens, [2, 3], 8, 2, 64, 16, torch.bfloat16)
+    bad = torch.tensor([0, 2, 5], dtype=torch.int32)
+    clens_bad = torch.tensor([1, 40], dtype=torch.int32)        # 2 queries, 1 token
+    out, lse = run(q, kc, vc, table, clens_bad, bad, 0.1, 0, 1, one_per_seq=False)
+    assert pkv.get_device_error() & pkv.DEVERR["cu_seqlens"]
+    assert torch.all(out[:2] == 0) and torch.all(torch.isneginf(lse[:2]))
+    ref, _ = oracle.paged_attention(q[2:], kc, vc, table[1:], clens_bad[1:], torch.tensor([0, 3], dtype=torch.int32), 0.1)
+    assert_attn_close(out[2:], ref, "valid sequence")

@@ -116,3 +116,42 @@ def test_mix_layout_sharing_structure():
     for s in range(8):
         assert torch.equal(lay.tokens_k[s][:64], lay.tokens_k[0][:64])
     assert all(16 <= n <= 32768 for n in lay.lengths)
+
+
+def test_release_outside_window_frees_only_blocks_no_query_can_see():
+    import numpy as np
+    import oracle
+    bs, W = 16, 40
+    bm = BlockManager(40, bs, order=gen.permutation(gen.generator(4), 40))
+    bm.add_sequence(0, 100)
+    bm.add_sequence(1, 30)
+    full_table = bm.block_table([0, 1], max_blocks=12)
+    freed = bm.release_outside_window(0, W)          # first visible position 60: blocks 0..2
+    assert len(freed) == 3 and bm.num_free == 40 - 7 - 2 + 3
+    assert bm.release_outside_window(1, W) == []     # 30 tokens all inside the window
+    bm.audit()
+    table = bm.block_table([0, 1], max_blocks=12)
+    assert table[0, :3].tolist() == [-1, -1, -1] and table[0, 3:7].tolist() == full_table[0, 3:7].tolist()
+    with pytest.raises(KeyError):
+        bm.slot(0, 47)
+    # the windowed attention reads none of the released blocks
+    g = gen.generator(5)
+    kc = gen.randn(g, (40, 2, bs, 8), torch.float32)
+    vc = gen.randn(g, (40, 2, bs, 8), torch.float32)
+    q = gen.randn(g, (2, 4, 8), torch.float32)
+    lens = np.array([100, 30], np.int32)
+    cu = np.array([0, 1, 2], np.int32)
+    ref, _ = oracle.paged_attention(q, kc, vc, full_table, lens, cu, 0.3, window=W)
+    for blk in freed:
+        kc[blk] = float("nan")
+        vc[blk] = float("nan")
+    out, _ = oracle.paged_attention(q, kc, vc, table, lens, cu, 0.3, window=W)
+    assert np.array_equal(out, ref)
+    # appending moves the window; a block is released once its last position leaves it
+    for _ in range(12):
+        bm.append_slot(0)
+    assert bm.release_outside_window(0, W) == [int(full_table[0, 3])]   # 112 - 40 = 72 > 63
+    bm.free_sequence(0)
+    bm.free_sequence(1)
+    bm.audit()
+    assert bm.num_free == 40
