@@ -131,21 +131,24 @@ def dist_env():
 class DecodeWorkload:
     """Decode steps over a paged cache: append one token per sequence, then attend."""
 
-    def __init__(self, spec, lengths, cycle, label):
+    def __init__(self, spec, lengths, cycle, label, window=0):
         self.spec, self.lengths, self.cycle, self.label = spec, list(lengths), cycle, label
         self.num_splits = 0
+        self.window = window   # > 0: sliding window of this many tokens
 
-    # bytes of K and V read by one step c of the cycle (every cached token, every KV head)
+    # bytes of K and V read by one step c of the cycle (every visible cached token, every
+    # KV head)
     def kv_bytes(self, c):
         elt = 2 if self.spec.cache_dtype == torch.bfloat16 else 4
-        return sum(n + c + 1 for n in self.lengths) * self.spec.kv_heads * self.spec.head_dim * 2 * elt
+        seen = [n + c + 1 if self.window <= 0 else min(n + c + 1, self.window) for n in self.lengths]
+        return sum(seen) * self.spec.kv_heads * self.spec.head_dim * 2 * elt
 
     def describe(self):
         s = self.spec
         return {"workload": self.label, "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads,
                 "head_dim": s.head_dim, "block_size": s.block_size, "cache_dtype": "bf16",
                 "q_dtype": "fp32", "mean_cached_len": sum(self.lengths) / len(self.lengths),
-                "decode_steps_cycle": self.cycle,
+                "decode_steps_cycle": self.cycle, "window": self.window,
                 "kv_gb_per_step": self.kv_bytes(self.cycle // 2) / 1e9,
                 "l2": "inputs larger than L2: each step reads %.2f GB of K/V vs 129 MB L2"
                       % (self.kv_bytes(0) / 1e9)}
@@ -166,6 +169,12 @@ class DecodeWorkload:
             slots.append(torch.tensor(sl, dtype=torch.int64))
             clens.append(bm.context_lens(range(s.batch)))
         self.nb = nb
+        self.released_blocks = 0
+        if self.window > 0:
+            # blocks before every query's window go back to the pool (their table entries
+            # become -1): this step's queries see positions len - window .. len - 1
+            for b in range(s.batch):
+                self.released_blocks += len(bm.release_outside_window(b, self.window))
         self.table = bm.block_table(range(s.batch)).to(device)
         self.slots_h = [t.pin_memory() for t in slots]
         self.clens_h = [t.pin_memory() for t in clens]
@@ -207,16 +216,26 @@ class DecodeWorkload:
         self.copy_stream = torch.cuda.Stream(device=device)
         self.pkv = pkv
         # kv_append, then the kernels the decode call enqueues (as the library plans it)
-        self.launches_per_step = 1 + pkv.decode_kernel_launches(
-            B, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype, self.num_splits)
+        self.launches_per_step = 1 + pkv.paged_attention_kernel_launches(
+            B, B, 1, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype, self.window, self.num_splits)
+
+    def decode(self, out, q, clens, lse=None):
+        """The public decode call: pkv_paged_decode_attention, or with a sliding window
+        pkv_paged_attention (one query per sequence)."""
+        if self.window <= 0:
+            self.pkv.paged_decode_attention(out, q, self.k_cache, self.v_cache, self.table, clens,
+                                            self.spec.scale, lse=lse, num_splits=self.num_splits,
+                                            workspace=self.ws)
+        else:
+            self.pkv.paged_attention(out, q, self.k_cache, self.v_cache, self.table, clens, self.spec.scale,
+                                     window=self.window, lse=lse, num_splits=self.num_splits,
+                                     workspace=self.ws)
 
     def append(self, c):
         self.pkv.kv_append(self.k_new[c], self.v_new[c], self.k_cache, self.v_cache, self.slots[c])
 
     def attend(self, c):
-        self.pkv.paged_decode_attention(self.out, self.q[c], self.k_cache, self.v_cache, self.table,
-                                        self.clens[c], self.spec.scale, lse=self.lse,
-                                        num_splits=self.num_splits, workspace=self.ws)
+        self.decode(self.out, self.q[c], self.clens[c], lse=self.lse)
 
     def e2e_capture(self):
         """One CUDA graph per (cycle step c, buffer parity) of the public API calls a serving
@@ -242,9 +261,7 @@ class DecodeWorkload:
                         self.out_h[1 - buf].copy_(self.out_e[1 - buf], non_blocking=True)
                     q, kn, vn, sl, cl = self.views[buf]
                     self.pkv.kv_append(kn, vn, self.k_cache, self.v_cache, sl)
-                    self.pkv.paged_decode_attention(self.out_e[buf], q, self.k_cache, self.v_cache,
-                                                    self.table, cl, self.spec.scale,
-                                                    num_splits=self.num_splits, workspace=self.ws)
+                    self.decode(self.out_e[buf], q, cl)
                     join = torch.cuda.Event()
                     join.record(cp)
                     cs.wait_event(join)
@@ -280,10 +297,17 @@ class DecodeWorkload:
                                   for b, n in enumerate(inp.cached)])
             oracle.kv_append(inp.k_cache, inp.v_cache, inp.k_new[c], inp.v_new[c], slots)
             lens = torch.tensor([n + c + 1 for n in inp.cached], dtype=torch.int32)
-            oracle.paged_decode(inp.q[c], inp.k_cache, inp.v_cache, inp.block_table, lens, s.scale,
-                                nthreads=threads)
+            if self.window <= 0:
+                oracle.paged_decode(inp.q[c], inp.k_cache, inp.v_cache, inp.block_table, lens, s.scale,
+                                    nthreads=threads)
+                seen = lens
+            else:
+                cu = torch.arange(len(inp.cached) + 1, dtype=torch.int32)
+                oracle.paged_attention(inp.q[c], inp.k_cache, inp.v_cache, inp.block_table, lens, cu,
+                                       s.scale, window=self.window, nthreads=threads)
+                seen = lens.clamp(max=self.window)
             elt = 2 if s.cache_dtype == torch.bfloat16 else 4
-            return int(lens.sum()) * s.kv_heads * s.head_dim * 2 * elt
+            return int(seen.sum()) * s.kv_heads * s.head_dim * 2 * elt
         return run, threads
 
 
@@ -341,6 +365,10 @@ WORKLOADS = {
     "long_mqa": lambda: DecodeWorkload(gen.LONG_MQA, [gen.LONG_LENGTH] * 4, 1,
                                        "long-context split-K MQA decode: batch 4, 64 q / 1 kv head, d 128, "
                                        "131072 cached tokens, bs 16, bf16 KV"),
+    "swa": lambda: DecodeWorkload(gen.SWA, [gen.SWA_LENGTH] * gen.SWA.batch, 1,
+                                  "mistral-7b-shaped sliding-window decode: batch 64, 32 q / 8 kv heads, d 128, "
+                                  "16384 cached tokens, window 4096 (blocks outside released), bs 16, bf16 KV",
+                                  window=gen.SWA_WINDOW),
     "prefill": PrefillWorkload,
 }
 

@@ -139,6 +139,10 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS
 int pkv_decode_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
                                int num_splits);
 
+/* The same count for a pkv_paged_attention call with these arguments. */
+int pkv_paged_attention_kernel_launches(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs,
+                                        int MBS, int NB, pkv_dtype dt, int window, int num_splits);
+
 /*
  * pkv_paged_decode_attention -- one new query per sequence against its cached K/V.
  *

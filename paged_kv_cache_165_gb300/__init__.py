@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     lib,
     library_path,
     paged_attention,
+    paged_attention_kernel_launches,
     paged_attention_workspace_bytes,
     paged_decode_attention,
     paged_decode_attention_noalloc,

@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_attention.argtypes = [P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, I, F, I, I, P,
                                       Z, P]
     L.pkv_paged_attention.restype = I
+    L.pkv_paged_attention_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I, I, I, I]
+    L.pkv_paged_attention_kernel_launches.restype = I
     L.pkv_decode_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I]
     L.pkv_decode_kernel_launches.restype = I
     L.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P,
@@ -199,6 +201,13 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
 def paged_attention_workspace_bytes(B, Tq, max_q, Hq, Hkv, d, bs, MBS, window=0, num_splits=0) -> int:
     return int(lib().pkv_paged_attention_workspace_bytes(B, Tq, max_q, Hq, Hkv, d, bs, MBS, window,
                                                          num_splits))
+
+
+def paged_attention_kernel_launches(B, Tq, max_q, Hq, Hkv, d, bs, MBS, NB, dtype, window=0,
+                                    num_splits=0) -> int:
+    """Kernels one paged_attention call with these sizes enqueues (-1: rejected)."""
+    return int(lib().pkv_paged_attention_kernel_launches(B, Tq, max_q, Hq, Hkv, d, bs, MBS, NB,
+                                                         _DTYPES[dtype], window, num_splits))
 
 
 def paged_attention(out, q, k_cache, v_cache, block_table, context_lens, scale, cu_q=None, max_q=1,

@@ -199,6 +199,24 @@ int pkv_decode_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, i
     return plan.splits > 1 && !plan.fused_merge ? 2 : 1;
 }
 
+int pkv_paged_attention_kernel_launches(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs,
+                                        int MBS, int NB, pkv_dtype dt, int window, int num_splits) {
+    int eb = 0;
+    if (!elem_size(dt, &eb) || check_decode_sizes(B, Hq, Hkv, d, bs, MBS) != PKV_OK || NB < 1 ||
+        num_splits < 0 || window < 0 || Tq < 0 || max_q < 0 ||
+        static_cast<long long>(Tq) > static_cast<long long>(B) * max_q)
+        return -1;
+    if (B == 0 || Tq == 0) return 0;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != PKV_OK) return -1;
+    const int vis = visible_blocks(MBS, bs, window);
+    const bool one_per_seq = Tq == B && max_q == 1;
+    const DecodePlan plan =
+        one_per_seq ? plan_decode(B, Hq, Hkv, d, bs, vis, NB, dt, num_splits, st->sm_count, true, true)
+                    : plan_decode(Tq, Hq, Hkv, d, bs, vis, NB, dt, num_splits, st->sm_count, false, false);
+    return plan.splits > 1 && !plan.fused_merge ? 2 : 1;
+}
+
 pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, const void *k_cache,
                                       const void *v_cache, pkv_dtype dt, const int32_t *block_table,
                                       const int32_t *context_lens, int B, int Hq, int Hkv, int d,

@@ -21,6 +21,9 @@ Workload shapes (one layer each; block size 16 throughout):
 * ``LONG``   batch 4, 64 q / 8 kv heads (and 1 kv head: MQA), d 128, 131072
   cached tokens, plus a varlen causal prefill of 8 prompts with lengths
   uniform in [256, 4096].
+* ``SWA``    sliding-window decode shaped like Mistral-7B (the model the pages
+  name for sliding windows): batch 64, 32 q / 8 kv heads, d 128, 16384 cached
+  tokens per sequence, a window of the last 4096 tokens.
 """
 from __future__ import annotations
 
@@ -56,6 +59,7 @@ GQA_70B = DecodeSpec("llama2_70b_gqa", 2, 64, 64, 8, 128, torch.bfloat16, steps=
 MIX = DecodeSpec("mix_prefix_share", 3, 256, 32, 8, 128, torch.bfloat16)
 LONG_GQA = DecodeSpec("long_gqa", 4, 4, 64, 8, 128, torch.bfloat16)
 LONG_MQA = DecodeSpec("long_mqa", 4, 4, 64, 1, 128, torch.bfloat16)
+SWA = DecodeSpec("mistral_7b_swa", 5, 64, 32, 8, 128, torch.bfloat16)
 
 TINY_LENGTHS = (17, 40)
 MHA_7B_LENGTH = 2048
@@ -64,6 +68,7 @@ MIX_MEDIAN, MIX_SIGMA, MIX_CLIP = 1024, 1.0, (16, 32768)
 MIX_PREFIX_TOKENS, MIX_PREFIX_SEQS = 4096, 64
 LONG_LENGTH = 131072
 PREFILL_PROMPTS, PREFILL_RANGE = 8, (256, 4096)
+SWA_LENGTH, SWA_WINDOW = 16384, 4096
 
 
 def generator(seed: int) -> torch.Generator:
