@@ -39,7 +39,7 @@ _SRC = os.path.join(_HERE, "pkv_oracle.c")
 _LIB_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_LIB_DIR, "libpkv_oracle.so")
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -103,7 +103,9 @@ def _dtype_code(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"cache element type must be float32 or bf16 bits (uint16), got {a.dtype}")
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"cache element type must be float32, bf16 bits (uint16) or float64, got {a.dtype}")
 
 
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
@@ -154,6 +156,85 @@ def kv_block_copy(k_cache, v_cache, pairs) -> None:
     for src, dst in to_numpy(pairs).reshape(-1, 2).tolist():
         kc[dst] = kc[src]
         vc[dst] = vc[src]
+
+
+# ------------------------------------------------------------- FP8 (E4M3) cache
+# The pages leave the low-bit format open: zwjcode.cn "KV Cache 的增量解码" §14 (low-bit
+# K/V lowers memory and bandwidth; its error reaches every later query, so it must be
+# validated) and plumephp.com "KV Cache 优化与注意力机制加速" §2.5 (FP8 attention on
+# FP8 tensor cores).  The reading taken here: the OCP FP8 E4M3 format (1 sign, 4
+# exponent bits with bias 7, 3 mantissa bits; no infinities, S.1111.111 is NaN; the
+# largest finite value is 448) with one fp32 scale per cached row (token slot x KV
+# head): scale = amax(row) / 448, code = E4M3(x / scale) rounded to nearest, ties to
+# even, saturating at +-448; the cached value is code * scale.  A row of zeros stores
+# scale 0 and codes 0.  Both divisions are fp32 operations.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 value of each E4M3 byte (NaN for S.1111.111)."""
+    c = np.asarray(codes, np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 0xF) & (m == 0x7), np.nan, val)
+    return sign * val
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 bytes of float32 values: nearest representable, ties to even, saturating."""
+    x = np.asarray(x, np.float32).astype(np.float64)
+    a = np.abs(x)
+    # binade of a: 2^e <= a < 2^(e+1); normals from 2^-6, below them the spacing 2^-9
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = np.clip(ex - 1, -6, 8)
+    quantum = np.exp2(e - 3.0)
+    r = np.minimum(np.rint(a / quantum) * quantum, E4M3_MAX)   # rint: half to even
+    # encode the rounded magnitude (it may have moved up one binade)
+    _, er = np.frexp(np.where(r > 0, r, 1.0))
+    er = er - 1
+    normal = (r > 0) & (er >= -6)
+    e_field = np.where(normal, er + 7, 0)
+    m_field = np.where(normal, np.rint((r / np.exp2(er) - 1.0) * 8.0), np.rint(r / 2.0 ** -9))
+    code = (e_field.astype(np.int64) << 3) | m_field.astype(np.int64)
+    code = code | np.where(np.signbit(x), 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def quantize_rows_e4m3(rows):
+    """(codes, scales) of rows [..., d] (any float type, read as float32)."""
+    x = to_f64(rows).astype(np.float32)
+    amax = np.abs(x).max(axis=-1)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    y = (x / safe[..., None]).astype(np.float32)
+    codes = np.where(scale[..., None] > 0, e4m3_encode(y), np.uint8(0)).astype(np.uint8)
+    return codes, scale
+
+
+def kv_append_fp8(k_codes, v_codes, k_scale, v_scale, k_new, v_new, slot_mapping) -> None:
+    """In place: each new row (token t, KV head h) of K and V quantised into its slot.
+
+    codes uint8 [NB][Hkv][bs][d], scales float32 [NB][Hkv][bs]; k_new/v_new [T][Hkv][d].
+    """
+    kc, vc, ks, vs = (to_numpy(a) for a in (k_codes, v_codes, k_scale, v_scale))
+    kq, kscale = quantize_rows_e4m3(k_new)
+    vq, vscale = quantize_rows_e4m3(v_new)
+    bs = kc.shape[2]
+    for t, s in enumerate(to_numpy(slot_mapping).tolist()):
+        if s < 0:
+            continue
+        kc[s // bs, :, s % bs, :] = kq[t]
+        vc[s // bs, :, s % bs, :] = vq[t]
+        ks[s // bs, :, s % bs] = kscale[t]
+        vs[s // bs, :, s % bs] = vscale[t]
+
+
+def dequantize_fp8(codes, scales) -> np.ndarray:
+    """float64 cache [NB][Hkv][bs][d]: code value * row scale, exact."""
+    return e4m3_decode(to_numpy(codes)) * to_numpy(scales).astype(np.float64)[..., None]
 
 
 def kv_cache_bytes(layers: int, batch: int, heads: int, tokens: int, head_dim: int,

@@ -24,7 +24,8 @@
  *
  * Cache layout (chosen by this library, the pages leave it open -- 0539edu.com
  * §2.2): k_cache, v_cache are [NB][Hkv][bs][d] row-major.  Element type is fp32
- * (dtype 0) or bf16 given as its raw 16-bit pattern (dtype 1).
+ * (dtype 0), bf16 given as its raw 16-bit pattern (dtype 1), or fp64 (dtype 2, for
+ * the exact values of a dequantised FP8 cache).
  */
 #include <math.h>
 #include <pthread.h>
@@ -32,11 +33,14 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
 
-/* bf16 is the upper half of an IEEE binary32: widen by appending 16 zero bits. */
+/* bf16 is the upper half of an IEEE binary32: widen by appending 16 zero bits.  fp64
+ * caches hold values that no narrower type holds exactly (a dequantised code times its
+ * fp32 scale). */
 static double elem(const void *base, int dtype, size_t i) {
     if (dtype == ORC_F32) return (double)((const float *)base)[i];
+    if (dtype == ORC_F64) return ((const double *)base)[i];
     uint32_t u = (uint32_t)((const uint16_t *)base)[i] << 16;
     float f;
     memcpy(&f, &u, sizeof f);

@@ -490,3 +490,88 @@ def test_blocks_outside_the_window_are_never_read():
             freed[b, page] = -1
     out, lse = oracle.paged_attention(q, kp, vp, freed, clens, cu, 0.2, window=W)
     assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse)
+
+
+# ------------------------------------------------------------- FP8 (E4M3) cache
+# zwjcode.cn §14 / plumephp.com §2.5 leave the low-bit format open; the oracle's reading
+# is E4M3 with one fp32 scale per cached row.  The format pins against torch's
+# float8_e4m3fn conversions; the quantisation against its own closed-form bounds.
+
+def test_e4m3_decode_matches_torch_float8():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = oracle.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    assert np.array_equal(ref[~np.isnan(ref)], got[~np.isnan(got)])
+    assert np.nanmax(got) == 448.0 and got[0x7E] == 448.0 and np.isnan(got[0x7F])
+
+
+def test_e4m3_encode_rounds_to_nearest_even_like_torch():
+    g = np.random.default_rng(0)
+    x = (g.standard_normal(100000) * np.exp2(g.integers(-14, 9, 100000))).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    vals = np.unique(np.abs(oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))))
+    ties = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)            # exactly halfway
+    x = np.concatenate([x, ties, -ties, vals.astype(np.float32), np.float32([0.0, -0.0, 1e-30, -1e-30])])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+    # saturation at the largest finite value
+    assert oracle.e4m3_encode(np.float32([448.0001, -460.0])).tolist() == [0x7E, 0xFE]
+
+
+def test_fp8_row_quantisation_bounds():
+    g = gen.generator(41)
+    rows = gen.randn(g, (6, 2, 64), torch.bfloat16)
+    rows[3, 1] = 0.0                                   # an all-zero row
+    codes, scale = oracle.quantize_rows_e4m3(rows)
+    x = oracle.to_f64(rows)
+    deq = oracle.e4m3_decode(codes) * scale.astype(np.float64)[..., None]
+    assert scale[3, 1] == 0 and not codes[3, 1].any() and not deq[3, 1].any()
+    for t in range(6):
+        for h in range(2):
+            if scale[t, h] == 0:
+                continue
+            i = np.abs(x[t, h]).argmax()
+            assert abs(oracle.e4m3_decode(codes[t, h, i])) == 448.0   # the row's amax is +-448
+            # each element within half an E4M3 spacing (relative 2^-4 for normals,
+            # absolute 2^-10 * scale for subnormals)
+            y = x[t, h] / np.float64(scale[t, h])
+            spacing = np.where(np.abs(y) >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(np.abs(y), 1e-300))) - 3),
+                               2.0 ** -9)
+            assert np.all(np.abs(deq[t, h] - x[t, h]) <= 0.5 * spacing * scale[t, h] * (1 + 1e-6))
+
+
+def test_fp8_append_writes_named_slots_only():
+    nb, hkv, bs, d = 5, 2, 16, 32
+    kc = np.full((nb, hkv, bs, d), 0xAB, np.uint8)
+    vc = kc.copy()
+    ks = np.full((nb, hkv, bs), -1.0, np.float32)
+    vs = ks.copy()
+    g = gen.generator(2)
+    kn, vn = gen.randn(g, (3, hkv, d), torch.bfloat16), gen.randn(g, (3, hkv, d), torch.bfloat16)
+    oracle.kv_append_fp8(kc, vc, ks, vs, kn, vn, np.array([17, -1, 70]))
+    kq, ksc = oracle.quantize_rows_e4m3(kn)
+    assert np.array_equal(kc[1, :, 1], kq[0]) and np.array_equal(ks[1, :, 1], ksc[0])
+    assert np.array_equal(kc[4, :, 6], kq[2])
+    touched = np.zeros((nb, bs), bool)
+    touched[1, 1] = touched[4, 6] = True
+    assert np.all(kc.transpose(0, 2, 1, 3)[~touched] == 0xAB) and np.all(ks.transpose(0, 2, 1)[~touched] == -1)
+
+
+def test_fp8_attention_is_attention_over_the_dequantised_cache():
+    lens, hq, hkv, d, bs = [50, 17, 200], 8, 2, 32, 16
+    q, kc, vc, table = _random_paged(61, lens, hq, hkv, d, bs, torch.float32)
+    kq, ks = oracle.quantize_rows_e4m3(kc)
+    vq, vs = oracle.quantize_rows_e4m3(vc)
+    kd, vd = oracle.dequantize_fp8(kq, ks), oracle.dequantize_fp8(vq, vs)
+    cu = np.arange(len(lens) + 1, dtype=np.int32)
+    out, lse = oracle.paged_attention(q, kd, vd, table, np.array(lens, np.int32), cu, 0.2)
+    for b, L in enumerate(lens):
+        K = _logical_kv(torch.from_numpy(kd), table[b], L, bs)
+        V = _logical_kv(torch.from_numpy(vd), table[b], L, bs)
+        ref, ref_lse = _sdpa_masked(q[b:b + 1], K, V, [L - 1], 0, 0.2)
+        assert np.abs(out[b] - ref[0].numpy()).max() < 1e-12
+        assert np.abs(lse[b] - ref_lse[0].numpy()).max() < 1e-12
+    # the quantisation error itself is what the pages warn about: visible, bounded
+    exact, _ = oracle.paged_attention(q, kc, vc, table, np.array(lens, np.int32), cu, 0.2)
+    assert 1e-4 < np.abs(out - exact).max() < 0.2
