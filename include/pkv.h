@@ -62,7 +62,11 @@ typedef enum {
     PKV_ERR_CUDA = 4          /* a CUDA runtime call or kernel launch failed */
 } pkv_status;
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+/* Element types of caches and inputs.  PKV_FP8_E4M3 is a one-byte E4M3 code (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; no infinities, S.1111.111 is NaN, largest
+ * finite 448): kv_append and kv_block_copy move such codes as bytes, and the _fp8 entry
+ * points read them with their per-row scales. */
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 
 /* Bits of the device error word. */
 #define PKV_DEVERR_SLOT        1u   /* slot_mapping entry >= NB * bs (write skipped) */
@@ -222,6 +226,42 @@ pkv_status pkv_paged_attention(float *out, float *lse, const float *q, const voi
                                int max_q, int Hq, int Hkv, int d, int bs, int MBS, int NB, float scale,
                                int window, int num_splits, void *workspace, size_t workspace_bytes,
                                pkv_stream_t stream);
+
+/*
+ * FP8 KV cache.  The pages leave the low-bit format open (zwjcode.cn "KV Cache 的增量解码"
+ * §14: low-bit K/V lowers memory and bandwidth, and its error reaches every later query;
+ * plumephp.com "KV Cache 优化与注意力机制加速" §2.5: FP8 attention).  This library stores
+ * E4M3 codes [NB][Hkv][bs][d] (uint8) with one fp32 scale per row (token slot x KV head)
+ * in k_scale / v_scale [NB][Hkv][bs]; the cached value is code * scale.  Blocks move with
+ * pkv_kv_block_copy: the codes with dt = PKV_FP8_E4M3, the scales as an fp32 "cache" with
+ * d = 1.
+ *
+ * pkv_kv_append_fp8 -- quantise and scatter new rows.  For each token t with
+ * slot_mapping[t] >= 0 and each KV head h, the rows k_new[t][h][:], v_new[t][h][:]
+ * (element type new_dt: PKV_BF16 or PKV_F32) are written as
+ *   scale = amax(row) / 448,  code_e = E4M3(x_e / scale)  (fp32 divisions; round to
+ *   nearest, ties to even, saturating at +-448), a row of zeros as scale 0 and codes 0,
+ * into row (slot / bs, h, slot % bs).  Slot errors as pkv_kv_append.
+ */
+pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, pkv_dtype new_dt, uint8_t *k_codes,
+                             uint8_t *v_codes, float *k_scale, float *v_scale, const int64_t *slot_mapping,
+                             int T, int Hkv, int d, int bs, int NB, pkv_stream_t stream);
+
+/*
+ * pkv_paged_decode_attention_fp8 -- pkv_paged_attention with one query per sequence over
+ * an FP8 cache: the attention of the cached values code * scale, exactly as if they had
+ * been stored in a wider type (scores scale * k_scale[t] * (q . codes_t); weights times
+ * v_scale[t] against the codes).  window: 0 or a sliding window of that many tokens.
+ * Workspace: pkv_decode_workspace_bytes(B, Hq, Hkv, d, bs, MBS, num_splits) bytes, same
+ * rules.  d = 128, bs in {16, 32}, up to 8 query heads per KV head and 16-byte aligned
+ * codes and scales use tensor cores; other shapes a CUDA-core path with the same results.
+ */
+pkv_status pkv_paged_decode_attention_fp8(float *out, float *lse, const float *q, const uint8_t *k_codes,
+                                          const uint8_t *v_codes, const float *k_scale, const float *v_scale,
+                                          const int32_t *block_table, const int32_t *context_lens, int B,
+                                          int Hq, int Hkv, int d, int bs, int MBS, int NB, float scale,
+                                          int window, int num_splits, void *workspace,
+                                          size_t workspace_bytes, pkv_stream_t stream);
 
 /*
  * pkv_paged_decode_attention_noalloc -- pkv_paged_decode_attention without a workspace.

@@ -9,12 +9,14 @@ from ._binding import (  # noqa: F401
     DEVERR,
     PKV_BF16,
     PKV_F32,
+    PKV_FP8_E4M3,
     PkvError,
     decode_kernel_launches,
     decode_workspace_bytes,
     get_device_error,
     header_functions,
     kv_append,
+    kv_append_fp8,
     kv_block_copy,
     lib,
     library_path,
@@ -22,6 +24,7 @@ from ._binding import (  # noqa: F401
     paged_attention_kernel_launches,
     paged_attention_workspace_bytes,
     paged_decode_attention,
+    paged_decode_attention_fp8,
     paged_decode_attention_noalloc,
     prefill_attention,
 )

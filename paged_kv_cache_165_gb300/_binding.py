@@ -16,13 +16,13 @@ import torch
 from . import _build
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
-PKV_F32, PKV_BF16 = 0, 1
+PKV_F32, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 
 DEVERR = {
     "slot": 1, "block": 2, "len": 4, "cu_seqlens": 8, "pair": 16, "timeout": 32, "layout": 64,
 }
 
-_DTYPES = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16}
+_DTYPES = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3}
 
 
 class PkvError(RuntimeError):
@@ -68,6 +68,11 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_attention.restype = I
     L.pkv_paged_attention_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I, I, I, I]
     L.pkv_paged_attention_kernel_launches.restype = I
+    L.pkv_kv_append_fp8.argtypes = [P, P, I, P, P, P, P, P, I, I, I, I, I, P]
+    L.pkv_kv_append_fp8.restype = I
+    L.pkv_paged_decode_attention_fp8.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I,
+                                                 P, Z, P]
+    L.pkv_paged_decode_attention_fp8.restype = I
     L.pkv_decode_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I]
     L.pkv_decode_kernel_launches.restype = I
     L.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P,
@@ -125,7 +130,7 @@ def _cuda(name, t, dtype=None):
 
 def _dtype(t) -> int:
     if t.dtype not in _DTYPES:
-        raise TypeError(f"unsupported element type {t.dtype} (fp32 or bf16)")
+        raise TypeError(f"unsupported element type {t.dtype} (fp32, bf16 or uint8 E4M3 codes)")
     return _DTYPES[t.dtype]
 
 
@@ -145,6 +150,57 @@ def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None
         raise ValueError("kv_append: shapes do not match [T][Hkv][d] / [T]")
     _check(lib().pkv_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), dt,
                                _ptr(slot_mapping), T, Hkv, d, bs, NB, _stream(stream)))
+
+
+def kv_append_fp8(k_new, v_new, k_codes, v_codes, k_scale, v_scale, slot_mapping, stream=None) -> None:
+    """Quantise k_new/v_new [T][Hkv][d] (bf16 or fp32) into E4M3 codes [NB][Hkv][bs][d]
+    (uint8) and fp32 row scales [NB][Hkv][bs] at slot_mapping[t] (int64, <0 skipped)."""
+    _cuda("k_new", k_new)
+    new_dt = _dtype(k_new)
+    _cuda("v_new", v_new, k_new.dtype)
+    for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
+        _cuda(name, t, torch.uint8)
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _cuda(name, t, torch.float32)
+    _cuda("slot_mapping", slot_mapping, torch.int64)
+    NB, Hkv, bs, d = k_codes.shape
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, Hkv, d) or tuple(v_new.shape) != (T, Hkv, d) or \
+            tuple(v_codes.shape) != (NB, Hkv, bs, d) or tuple(k_scale.shape) != (NB, Hkv, bs) or \
+            tuple(v_scale.shape) != (NB, Hkv, bs) or slot_mapping.numel() != T:
+        raise ValueError("kv_append_fp8: shapes do not match")
+    _check(lib().pkv_kv_append_fp8(_ptr(k_new), _ptr(v_new), new_dt, _ptr(k_codes), _ptr(v_codes),
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), T, Hkv, d, bs, NB,
+                                   _stream(stream)))
+
+
+def paged_decode_attention_fp8(out, q, k_codes, v_codes, k_scale, v_scale, block_table, context_lens,
+                               scale, window=0, lse=None, num_splits=0, workspace=None, stream=None) -> None:
+    """Decode attention (one query per sequence) over an E4M3 cache with row scales."""
+    for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
+        _cuda(name, t, torch.uint8)
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _cuda(name, t, torch.float32)
+    _cuda("q", q, torch.float32)
+    _cuda("out", out, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    if lse is not None:
+        _cuda("lse", lse, torch.float32)
+    NB, Hkv, bs, d = k_codes.shape
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d) or block_table.dim() != 2 or \
+            block_table.shape[0] != B or context_lens.numel() != B or \
+            (lse is not None and lse.numel() != B * Hq):
+        raise ValueError("paged_decode_attention_fp8: shapes do not match")
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_decode_attention_fp8(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_table), _ptr(context_lens), B, Hq, Hkv, d, bs, block_table.shape[1], NB, float(scale),
+        int(window), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def kv_block_copy(k_cache, v_cache, pairs, stream=None) -> None:

@@ -67,15 +67,21 @@ std::once_flag g_encode_once;
 bool elem_size(pkv_dtype dt, int *bytes) {
     if (dt == PKV_F32) { *bytes = 4; return true; }
     if (dt == PKV_BF16) { *bytes = 2; return true; }
+    if (dt == PKV_FP8_E4M3) { *bytes = 1; return true; }
     return false;
 }
+
+// Attention over values of the cache's own type (FP8 needs its scales: the _fp8 entry).
+bool attention_dtype(pkv_dtype dt) { return dt == PKV_F32 || dt == PKV_BF16; }
 
 bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
 }  // namespace
 
-bool encode_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                     const uint64_t *strides_bytes, const uint32_t *box) {
+namespace {
+
+bool encode_map(CUtensorMapDataType type, CUtensorMap *map, const void *base, int rank,
+                const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box) {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -94,12 +100,23 @@ bool encode_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_
         estride[r] = 1;
         if (r + 1 < rank) gstride[r] = strides_bytes[r];
     }
-    const CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
-                                  const_cast<void *>(base), gdim, gstride, bdim, estride,
-                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUresult res = g_encode(map, type, rank, const_cast<void *>(base), gdim, gstride, bdim,
+                                  estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool encode_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                     const uint64_t *strides_bytes, const uint32_t *box) {
+    return encode_map(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, base, rank, dims, strides_bytes, box);
+}
+
+bool encode_map_u8(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                   const uint64_t *strides_bytes, const uint32_t *box) {
+    return encode_map(CU_TENSOR_MAP_DATA_TYPE_UINT8, map, base, rank, dims, strides_bytes, box);
 }
 
 pkv_status current_device_info(int *sm_count, unsigned **err) {
@@ -223,7 +240,8 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
                                       int bs, int MBS, int NB, float scale, int num_splits,
                                       void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
     int eb = 0;
-    if (!elem_size(dt, &eb)) return fail(PKV_ERR_UNSUPPORTED, "paged_decode_attention: element type %d", dt);
+    if (!elem_size(dt, &eb) || !attention_dtype(dt))
+        return fail(PKV_ERR_UNSUPPORTED, "paged_decode_attention: element type %d", dt);
     pkv_status s = check_decode_sizes(B, Hq, Hkv, d, bs, MBS);
     if (s != PKV_OK) return s;
     if (NB < 1 || num_splits < 0)
@@ -272,7 +290,8 @@ pkv_status pkv_paged_attention(float *out, float *lse, const float *q, const voi
                                int window, int num_splits, void *workspace, size_t workspace_bytes,
                                pkv_stream_t stream) {
     int eb = 0;
-    if (!elem_size(dt, &eb)) return fail(PKV_ERR_UNSUPPORTED, "paged_attention: element type %d", dt);
+    if (!elem_size(dt, &eb) || !attention_dtype(dt))
+        return fail(PKV_ERR_UNSUPPORTED, "paged_attention: element type %d", dt);
     pkv_status s = check_decode_sizes(B, Hq, Hkv, d, bs, MBS);
     if (s != PKV_OK) return s;
     if (NB < 1 || num_splits < 0 || window < 0 || Tq < 0 || max_q < 0 ||
@@ -309,13 +328,68 @@ pkv_status pkv_paged_attention(float *out, float *lse, const float *q, const voi
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_attention launch");
 }
 
+pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, pkv_dtype new_dt, uint8_t *k_codes,
+                             uint8_t *v_codes, float *k_scale, float *v_scale, const int64_t *slot_mapping,
+                             int T, int Hkv, int d, int bs, int NB, pkv_stream_t stream) {
+    if (!attention_dtype(new_dt)) return fail(PKV_ERR_UNSUPPORTED, "kv_append_fp8: input type %d", new_dt);
+    if (T < 0 || Hkv < 1 || d < 1 || d > 256 || bs < 1 || NB < 1)
+        return fail(PKV_ERR_INVALID_ARG, "kv_append_fp8: T=%d Hkv=%d d=%d bs=%d NB=%d", T, Hkv, d, bs, NB);
+    if (T == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_codes || !v_codes || !k_scale || !v_scale || !slot_mapping)
+        return fail(PKV_ERR_INVALID_ARG, "kv_append_fp8: null pointer");
+    DeviceState *st = nullptr;
+    pkv_status s = device_state(&st);
+    if (s != PKV_OK) return s;
+    const cudaError_t e = launch_kv_append_fp8(k_new, v_new, new_dt, k_codes, v_codes, k_scale, v_scale,
+                                               slot_mapping, T, Hkv, d, bs, NB, st->err, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_append_fp8 launch");
+}
+
+pkv_status pkv_paged_decode_attention_fp8(float *out, float *lse, const float *q, const uint8_t *k_codes,
+                                          const uint8_t *v_codes, const float *k_scale, const float *v_scale,
+                                          const int32_t *block_table, const int32_t *context_lens, int B,
+                                          int Hq, int Hkv, int d, int bs, int MBS, int NB, float scale,
+                                          int window, int num_splits, void *workspace,
+                                          size_t workspace_bytes, pkv_stream_t stream) {
+    pkv_status s = check_decode_sizes(B, Hq, Hkv, d, bs, MBS);
+    if (s != PKV_OK) return s;
+    if (NB < 1 || num_splits < 0 || window < 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attention_fp8: NB=%d num_splits=%d window=%d", NB,
+                    num_splits, window);
+    if (B == 0) return PKV_OK;
+    if (!out || !q || !k_codes || !v_codes || !k_scale || !v_scale || !block_table || !context_lens)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attention_fp8: null pointer");
+    if (reinterpret_cast<uintptr_t>(q) % 8 != 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_decode_attention_fp8: q must be 8-byte aligned");
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != PKV_OK) return s;
+    const bool aligned = aligned16(k_codes) && aligned16(v_codes) && aligned16(k_scale) && aligned16(v_scale);
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, visible_blocks(MBS, bs, window), NB, PKV_FP8_E4M3,
+                                        num_splits, st->sm_count, aligned, aligned16(q));
+    if (plan.workspace_bytes > 0 &&
+        (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
+         reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+        return fail(PKV_ERR_WORKSPACE,
+                    "paged_decode_attention_fp8: needs %zu bytes of 16-byte aligned workspace, got %zu",
+                    plan.workspace_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
+    DecodeArgs a{out, lse, q, k_codes, v_codes, block_table, context_lens,
+                 B, Hq, Hkv, d, bs, MBS, NB, scale, workspace, st->err};
+    a.window = window;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    cudaError_t e = launch_decode(a, plan, PKV_FP8_E4M3, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_decode_attention_fp8 launch");
+}
+
 pkv_status pkv_prefill_attention(float *out, float *lse, const void *q, const void *k, const void *v,
                                  pkv_dtype dt, const int32_t *cu_seqlens, int B, int T,
                                  int max_seqlen, int Hq, int Hkv, int d, float scale,
                                  void *k_cache, void *v_cache, const int64_t *slot_mapping, int bs,
                                  int NB, pkv_stream_t stream) {
     int eb = 0;
-    if (!elem_size(dt, &eb)) return fail(PKV_ERR_UNSUPPORTED, "prefill_attention: element type %d", dt);
+    if (!elem_size(dt, &eb) || !attention_dtype(dt))
+        return fail(PKV_ERR_UNSUPPORTED, "prefill_attention: element type %d", dt);
     if (B < 0 || B > 65535 || T < 0 || max_seqlen < 0 || Hq < 1 || Hq > 65535 || Hkv < 1 ||
         Hq % Hkv != 0 || d < 1 || d > 256)
         return fail(PKV_ERR_INVALID_ARG,

@@ -11,8 +11,16 @@
 // Both are pure byte copies, so they move the widest unit (16, 8, 4 or 2 bytes) that
 // divides the row (or block) size and the pointers, in a grid-stride loop sized to
 // the SM count.  Both are HBM-bound and tiny next to the attention read.
+// kv_append_fp8: the same scatter into an FP8 (E4M3) cache with one fp32 scale per row
+//   (token slot x KV head): scale = amax(row) / 448, code = E4M3(x / scale) rounded to
+//   nearest even and saturated (both divisions in fp32); a row of zeros stores scale 0
+//   and codes 0.  The low-bit cache is the trade-off of zwjcode.cn "KV Cache 的增量解码"
+//   §14.  One warp per row.
 #include <algorithm>
 #include <initializer_list>
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -67,6 +75,59 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Rows r = (t * Hkv + h) * 2 + {0: K, 1: V}, one warp each; lanes own elements lane + 32*j.
+template <typename T, int J>
+__global__ void __launch_bounds__(256)
+    kv_append_fp8_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new, uint8_t *__restrict__ kc,
+                         uint8_t *__restrict__ vc, float *__restrict__ ks, float *__restrict__ vs,
+                         const int64_t *__restrict__ slots, int T_, int Hkv, int d, int bs, long long n_slots,
+                         unsigned *err) {
+    const int lane = threadIdx.x & 31;
+    const long long rows = static_cast<long long>(T_) * Hkv * 2;
+    for (long long r = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; r < rows;
+         r += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+        const bool is_v = r & 1;
+        const long long th = r >> 1;                     // t * Hkv + h
+        const int h = static_cast<int>(th % Hkv);
+        const int t = static_cast<int>(th / Hkv);
+        const long long slot = __ldg(slots + t);
+        if (slot < 0) continue;                          // padding token
+        if (slot >= n_slots) {
+            if (h == 0 && !is_v && lane == 0) raise_error(err, PKV_DEVERR_SLOT);
+            continue;
+        }
+        const T *src = (is_v ? v_new : k_new) + th * d;
+        float x[J];
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int e = lane + 32 * j;
+            x[j] = e < d ? to_f32(src[e]) : 0.f;
+            amax = fmaxf(amax, fabsf(x[j]));
+        }
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+        const float scale = amax / 448.f;
+        const long long row = ((slot / bs) * Hkv + h) * bs + slot % bs;
+        uint8_t *dst = (is_v ? vc : kc) + row * d;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int e = lane + 32 * j;
+            if (e < d)
+                dst[e] = amax > 0.f ? static_cast<uint8_t>(__nv_cvt_float_to_fp8(x[j] / scale, __NV_SATFINITE, __NV_E4M3))
+                                    : uint8_t{0};
+        }
+        if (lane == 0) (is_v ? vs : ks)[row] = scale;
+    }
+}
+
 int unit_bytes(size_t row_bytes, std::initializer_list<const void *> ptrs) {
     for (int u : {16, 8, 4, 2}) {
         bool ok = row_bytes % u == 0;
@@ -108,6 +169,41 @@ cudaError_t launch_kv_append(const void *k_new, const void *v_new, void *k_cache
         default: PKV_APPEND(uint8_t); break;
     }
 #undef PKV_APPEND
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append_fp8(const void *k_new, const void *v_new, pkv_dtype new_dt, uint8_t *k_codes,
+                                 uint8_t *v_codes, float *k_scale, float *v_scale,
+                                 const int64_t *slot_mapping, int T, int Hkv, int d, int bs, int NB,
+                                 unsigned *err, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const long long rows = static_cast<long long>(T) * Hkv * 2;
+    const int grid = static_cast<int>(std::min<long long>((rows + 7) / 8, 8ll * sm_count_current()));
+    const long long n_slots = static_cast<long long>(NB) * bs;
+    const int J = (d + 31) / 32;
+#define PKV_FP8(TT, JJ)                                                                              \
+    kv_append_fp8_kernel<TT, JJ><<<grid, 256, 0, stream>>>(                                         \
+        static_cast<const TT *>(k_new), static_cast<const TT *>(v_new), k_codes, v_codes, k_scale, \
+        v_scale, slot_mapping, T, Hkv, d, bs, n_slots, err)
+#define PKV_FP8_J(TT)                   \
+    switch (J) {                        \
+        case 1: PKV_FP8(TT, 1); break;  \
+        case 2: PKV_FP8(TT, 2); break;  \
+        case 3: PKV_FP8(TT, 3); break;  \
+        case 4: PKV_FP8(TT, 4); break;  \
+        case 5: PKV_FP8(TT, 5); break;  \
+        case 6: PKV_FP8(TT, 6); break;  \
+        case 7: PKV_FP8(TT, 7); break;  \
+        case 8: PKV_FP8(TT, 8); break;  \
+        default: return cudaErrorInvalidValue; \
+    }
+    if (new_dt == PKV_BF16) {
+        PKV_FP8_J(__nv_bfloat16)
+    } else {
+        PKV_FP8_J(float)
+    }
+#undef PKV_FP8_J
+#undef PKV_FP8
     return cudaGetLastError();
 }
 

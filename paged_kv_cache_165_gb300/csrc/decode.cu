@@ -27,9 +27,11 @@
 //   chunks merged by decode_merge_kernel.
 #include <algorithm>
 #include <atomic>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "common.cuh"
+#include "decode_epilogue.cuh"
 #include "decode_kparams.cuh"
 #include "internal.h"
 
@@ -336,90 +338,8 @@ __global__ void __launch_bounds__(NW * 32)
         *reinterpret_cast<float2 *>(ow + (warp * 8 + g) * D + nt * 8 + 2 * t4) = v;
     }
     __syncthreads();
-    // A sequence with a single chunk writes its result directly; otherwise this chunk's
-    // normalised partial (o_c, lse_c in base 2) goes to the workspace.
-    const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
-    const size_t bi0 = static_cast<size_t>(b) * p.Hq + head0;
-    for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32) {
-        const int h = idx / D, c = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, mw[w * 8 + h]);
-        float L = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float f = exp2f(mw[w * 8 + h] - M);
-            L += lw[w * 8 + h] * f;
-            acc += ow[(w * 8 + h) * D + c] * f;
-        }
-        const size_t bi = bi0 + h;
-        if (nc == 1) {
-            p.out[bi * D + c] = acc / L;
-            if (c == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
-        } else {
-            p.ws_o[(bi * p.splits + split) * D + c] = acc / L;
-            if (c == 0) p.ws_lse[bi * p.splits + split] = M + log2f(L);
-        }
-    }
-    if (nc == 1 || p.counters == nullptr) return;
-
-    // ---- the last chunk to finish merges all chunks of this (sequence, head group):
-    // partials are published (fence) before the arrival is counted; the CTA that sees
-    // the count reach nc resets the counter for the next call and reads them back.
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned *ctr = p.counters + (static_cast<size_t>(b) * p.Hkv + kvh) * p.head_tiles + tile;
-        const unsigned prev = atomicAdd(ctr, 1u);
-        s_last = prev + 1 == static_cast<unsigned>(nc);
-        if (s_last) *ctr = 0u;   // every chunk of this call has arrived
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    // per-head chunk weights 2^{lse_c - M} and their sum, in shared memory (stage area)
-    float *wts = reinterpret_cast<float *>(smem);              // [8][nc]
-    float *inv_l = wts + 8 * nc;                                // [8]
-    float *lse_h = inv_l + 8;                                   // [8]
-    for (int h = warp; h < nheads; h += NW) {
-        const float *ls = p.ws_lse + (bi0 + h) * p.splits;
-        float M = -INFINITY;
-        for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(ls + c));
-#pragma unroll
-        for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, sh));
-        float L = 0.f;
-        for (int c = lane; c < nc; c += 32) {
-            const float w = exp2f(__ldcg(ls + c) - M);
-            wts[h * nc + c] = w;
-            L += w;
-        }
-#pragma unroll
-        for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(kFull, L, sh);
-        if (lane == 0) {
-            inv_l[h] = 1.f / L;
-            lse_h[h] = M + log2f(L);
-        }
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < nheads * (D / 4); idx += NW * 32) {
-        const int h = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
-        const float *po = p.ws_o + (bi0 + h) * p.splits * D + c4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int c = 0; c < nc; ++c) {
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(po + static_cast<size_t>(c) * D));
-            const float w = wts[h * nc + c];
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-        }
-        const float il = inv_l[h];
-        *reinterpret_cast<float4 *>(p.out + (bi0 + h) * D + c4) =
-            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
-        if (c4 == 0 && p.lse != nullptr) p.lse[bi0 + h] = lse_h[h] * kLn2;
-    }
+    finish_chunk<D, NW>(smem, p, b, kvh, tile, head0, nheads, split,
+                        (n_pages + p.chunk_pages - 1) / p.chunk_pages);
 }
 
 // ============================================================ large-group kernel
@@ -627,6 +547,11 @@ template <>
 __device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16 *p) {
     return __bfloat162float(*p);
 }
+// an E4M3 code (its row scale is applied by the caller)
+template <>
+__device__ __forceinline__ float load_f32<uint8_t>(const uint8_t *p) {
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw(*p, __NV_E4M3)));
+}
 
 // One warp per (query row, query head, chunk); lanes own head-dim elements lane + 32*j.
 // A row is a sequence (decode) or one of the query rows of a sequence (cu_q).
@@ -666,8 +591,8 @@ __global__ void __launch_bounds__(32)
         if (bad && lane == 0) raise_error(p.err, PKV_DEVERR_BLOCK);
         const int valid = min(bs, len - pg * bs);
         for (int off = max(0, sp.lo - pg * bs); off < valid; ++off) {
-            const size_t base =
-                bad ? 0 : ((static_cast<size_t>(phys) * p.Hkv + kvh) * bs + off) * d;
+            const size_t srow = bad ? 0 : (static_cast<size_t>(phys) * p.Hkv + kvh) * bs + off;
+            const size_t base = srow * d;
             float dot = 0.f;
 #pragma unroll
             for (int j = 0; j < J; ++j) {
@@ -676,16 +601,18 @@ __global__ void __launch_bounds__(32)
             }
 #pragma unroll
             for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(kFull, dot, sh);
+            if (p.k_scale != nullptr && !bad) dot *= __ldg(p.k_scale + srow);   // FP8 rows
             const float s = dot * p.scale_log2;
             const float m_new = fmaxf(m_run, s);
             const float alpha = exp2f(m_run - m_new);
             const float w = exp2f(s - m_new);
             l_run = l_run * alpha + w;
+            const float wv = p.v_scale != nullptr && !bad ? w * __ldg(p.v_scale + srow) : w;
 #pragma unroll
             for (int j = 0; j < J; ++j) {
                 const int e = lane + 32 * j;
                 const float v = (e < d && !bad) ? load_f32(vc + base + e) : 0.f;
-                acc[j] = acc[j] * alpha + w * v;
+                acc[j] = acc[j] * alpha + wv * v;
             }
             m_run = m_new;
         }
@@ -901,10 +828,17 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
                        int num_splits, int sm_count, bool caches_aligned, bool q_aligned) {
     DecodePlan plan{};
+    const int tiles = (Hq / Hkv + 7) / 8;
+    if (dt == PKV_FP8_E4M3) {
+        // E4M3 codes: the tensor-core kernel takes d = 128 and one head tile per KV head
+        plan.tensor_core = d == 128 && (bs == 16 || bs == 32) && tiles == 1 && caches_aligned &&
+                           static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31);
+        chunk_plan(plan, B, Hq, Hkv, d, bs, MBS, num_splits, sm_count);
+        return plan;
+    }
     plan.tensor_core = dt == PKV_BF16 && (d == 64 || d == 128 || d == 256) &&
                        (bs == 16 || bs == 32) && caches_aligned &&
                        static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31);
-    const int tiles = (Hq / Hkv + 7) / 8;
     plan.group = plan.tensor_core && tiles >= 2 && tiles <= 8;
     plan.umma = plan.group && (d == 64 || d == 128) && q_aligned;
     chunk_plan(plan, B, Hq, Hkv, d, bs, MBS, num_splits, sm_count);
@@ -950,6 +884,8 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     kp.scale_log2 = a.scale * kLog2e;
     kp.window = a.window;
     kp.cu_q = a.cu_q;
+    kp.k_scale = a.k_scale;
+    kp.v_scale = a.v_scale;
     if (plan.splits > 1) {
         uint8_t *ws = static_cast<uint8_t *>(a.workspace);
         kp.counters = plan.fused_merge ? reinterpret_cast<unsigned *>(ws) : nullptr;
@@ -958,7 +894,18 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     }
 
     cudaError_t e;
-    if (plan.tensor_core) {
+    if (dt == PKV_FP8_E4M3 && plan.tensor_core) {
+        CUtensorMap tk, tv;
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.d), static_cast<uint64_t>(a.NB) * a.Hkv * a.bs};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.d)};
+        const uint32_t box[2] = {128, static_cast<uint32_t>(a.bs)};
+        if (!encode_map_u8(&tk, a.k_cache, 2, dims, strides, box) ||
+            !encode_map_u8(&tv, a.v_cache, 2, dims, strides, box))
+            return cudaErrorInvalidValue;
+        e = launch_decode_fp8(kp, tk, tv, a.bs, dim3(static_cast<unsigned>(plan.splits) * kp.head_tiles, a.Hkv, a.B),
+                              stream);
+        if (e != cudaSuccess || plan.splits == 1 || plan.fused_merge) return e;
+    } else if (plan.tensor_core) {
         CUtensorMap tk, tv;
         const uint64_t dims[2] = {static_cast<uint64_t>(a.d),
                                   static_cast<uint64_t>(a.NB) * a.Hkv * a.bs};
@@ -1003,8 +950,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
         if (e != cudaSuccess || plan.splits == 1 || plan.fused_merge) return e;
     } else {
         const dim3 grid(rows, a.Hq, plan.splits);
-        e = dt == PKV_F32 ? launch_simt<float>(a, kp, grid, stream)
-                          : launch_simt<__nv_bfloat16>(a, kp, grid, stream);
+        e = dt == PKV_F32    ? launch_simt<float>(a, kp, grid, stream)
+            : dt == PKV_BF16 ? launch_simt<__nv_bfloat16>(a, kp, grid, stream)
+                             : launch_simt<uint8_t>(a, kp, grid, stream);
         if (e != cudaSuccess || plan.splits == 1) return e;
     }
     decode_merge_kernel<<<static_cast<unsigned>(rows * a.Hq), kMergeThreads, 0, stream>>>(kp, a.d, a.bs);

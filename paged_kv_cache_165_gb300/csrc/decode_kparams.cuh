@@ -27,6 +27,7 @@ struct DecodeKParams {
     float scale_log2; // scale * log2(e): scores are kept in the base-2 domain
     int window;       // > 0: only the most recent `window` tokens are visible
     const int32_t *cu_q;   // query rows per sequence [B+1]; nullptr: row b = sequence b
+    const float *k_scale, *v_scale;   // FP8 caches: fp32 scale per row [NB][Hkv][bs]
 };
 
 // Sequence length after validation; an invalid length counts as empty.
@@ -91,5 +92,10 @@ constexpr int kUmmaDecodeKeys = 64;
 
 cudaError_t launch_decode_umma(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv,
                                int d, int bs, dim3 grid, cudaStream_t stream);
+
+// FP8 (E4M3) decode (decode_fp8.cu): d = 128, bs in {16, 32}, up to 8 query heads per KV
+// head; grid (chunks x head tiles, Hkv, B).  tk / tv are uint8 maps with {128, bs} boxes.
+cudaError_t launch_decode_fp8(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int bs,
+                              dim3 grid, cudaStream_t stream);
 
 }  // namespace pkv

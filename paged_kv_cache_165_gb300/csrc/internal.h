@@ -16,6 +16,9 @@ namespace pkv {
 // innermost (contiguous) dimension; strides are the byte strides of dims 1.. .
 bool encode_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                      const uint64_t *strides_bytes, const uint32_t *box);
+// The same for a byte array (FP8 codes).
+bool encode_map_u8(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                   const uint64_t *strides_bytes, const uint32_t *box);
 
 // Per-device state of the current device (SM count, device error word), set up on
 // first use; and recording of the calling thread's pkv_last_error() message.
@@ -27,6 +30,12 @@ pkv_status record_error(pkv_status status, const char *message);
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                              int elem_bytes, const int64_t *slot_mapping, int T, int Hkv, int d,
                              int bs, int NB, unsigned *err, cudaStream_t stream);
+
+// FP8 append: new rows (dt PKV_BF16 or PKV_F32) quantised to E4M3 codes + fp32 row scales.
+cudaError_t launch_kv_append_fp8(const void *k_new, const void *v_new, pkv_dtype new_dt, uint8_t *k_codes,
+                                 uint8_t *v_codes, float *k_scale, float *v_scale,
+                                 const int64_t *slot_mapping, int T, int Hkv, int d, int bs, int NB,
+                                 unsigned *err, cudaStream_t stream);
 
 cudaError_t launch_kv_block_copy(void *k_cache, void *v_cache, int elem_bytes,
                                  const int32_t *pairs, int n, int Hkv, int d, int bs, int NB,
@@ -68,6 +77,8 @@ struct DecodeArgs {
     void *workspace;
     unsigned *err;
     int window = 0;                  // > 0: sliding window of this many tokens
+    const float *k_scale = nullptr;  // FP8 caches: per-row scales [NB][Hkv][bs]
+    const float *v_scale = nullptr;
     const int32_t *cu_q = nullptr;   // query rows per sequence; nullptr: one per sequence
     int rows = -1;                   // query rows (B when cu_q is nullptr)
 };

@@ -23,7 +23,8 @@ def test_header_declares_the_boundary():
     for fn in ["pkv_kv_append", "pkv_kv_block_copy", "pkv_paged_decode_attention",
                "pkv_prefill_attention", "pkv_decode_workspace_bytes", "pkv_decode_kernel_launches",
                "pkv_paged_attention", "pkv_paged_attention_workspace_bytes",
-               "pkv_paged_attention_kernel_launches",
+               "pkv_paged_attention_kernel_launches", "pkv_kv_append_fp8",
+               "pkv_paged_decode_attention_fp8",
                "pkv_get_device_error",
                "pkv_status_string", "pkv_last_error", "pkv_version"]:
         assert fn in names
