@@ -131,22 +131,25 @@ def dist_env():
 class DecodeWorkload:
     """Decode steps over a paged cache: append one token per sequence, then attend."""
 
-    def __init__(self, spec, lengths, cycle, label, window=0):
+    def __init__(self, spec, lengths, cycle, label, window=0, fp8=False):
         self.spec, self.lengths, self.cycle, self.label = spec, list(lengths), cycle, label
         self.num_splits = 0
         self.window = window   # > 0: sliding window of this many tokens
+        self.fp8 = fp8         # E4M3 codes + one fp32 scale per cached row
 
     # bytes of K and V read by one step c of the cycle (every visible cached token, every
-    # KV head)
+    # KV head; FP8: the code bytes and the row's 4-byte scale)
     def kv_bytes(self, c):
-        elt = 2 if self.spec.cache_dtype == torch.bfloat16 else 4
+        row = self.spec.head_dim + 4 if self.fp8 else \
+            self.spec.head_dim * (2 if self.spec.cache_dtype == torch.bfloat16 else 4)
         seen = [n + c + 1 if self.window <= 0 else min(n + c + 1, self.window) for n in self.lengths]
-        return sum(seen) * self.spec.kv_heads * self.spec.head_dim * 2 * elt
+        return sum(seen) * self.spec.kv_heads * 2 * row
 
     def describe(self):
         s = self.spec
         return {"workload": self.label, "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads,
-                "head_dim": s.head_dim, "block_size": s.block_size, "cache_dtype": "bf16",
+                "head_dim": s.head_dim, "block_size": s.block_size,
+                "cache_dtype": "e4m3 codes + fp32 row scales" if self.fp8 else "bf16",
                 "q_dtype": "fp32", "mean_cached_len": sum(self.lengths) / len(self.lengths),
                 "decode_steps_cycle": self.cycle, "window": self.window,
                 "kv_gb_per_step": self.kv_bytes(self.cycle // 2) / 1e9,
@@ -185,10 +188,22 @@ class DecodeWorkload:
         shape = (nb, s.kv_heads, bs, s.head_dim)
         self.k_cache = torch.randn(shape, generator=cg, device=device, dtype=torch.float32).to(s.cache_dtype)
         self.v_cache = torch.randn(shape, generator=cg, device=device, dtype=torch.float32).to(s.cache_dtype)
+        if self.fp8:
+            # the same values quantised through the public append (all slots at once)
+            rows = (nb * bs, s.kv_heads, s.head_dim)
+            kq = torch.empty(shape, dtype=torch.uint8, device=device)
+            vq = torch.empty_like(kq)
+            self.k_scale = torch.empty(shape[:3], device=device)
+            self.v_scale = torch.empty_like(self.k_scale)
+            all_slots = torch.arange(nb * bs, device=device, dtype=torch.int64)
+            pkv.kv_append_fp8(self.k_cache.transpose(1, 2).reshape(rows).contiguous(),
+                              self.v_cache.transpose(1, 2).reshape(rows).contiguous(),
+                              kq, vq, self.k_scale, self.v_scale, all_slots)
+            self.k_cache, self.v_cache = kq, vq
         B, Hq, Hkv, d = s.batch, s.q_heads, s.kv_heads, s.head_dim
         self.q = torch.randn((self.cycle, B, Hq, d), generator=cg, device=device)
-        self.k_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(s.cache_dtype)
-        self.v_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(s.cache_dtype)
+        self.k_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(torch.bfloat16 if self.fp8 else s.cache_dtype)
+        self.v_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(torch.bfloat16 if self.fp8 else s.cache_dtype)
         self.out = torch.empty((B, Hq, d), device=device)
         self.lse = torch.empty((B, Hq), device=device)
         ws = pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, self.table.shape[1], self.num_splits)
@@ -217,12 +232,18 @@ class DecodeWorkload:
         self.pkv = pkv
         # kv_append, then the kernels the decode call enqueues (as the library plans it)
         self.launches_per_step = 1 + pkv.paged_attention_kernel_launches(
-            B, B, 1, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype, self.window, self.num_splits)
+            B, B, 1, Hq, Hkv, d, bs, self.table.shape[1], nb, torch.uint8 if self.fp8 else s.cache_dtype,
+            self.window, self.num_splits)
 
     def decode(self, out, q, clens, lse=None):
-        """The public decode call: pkv_paged_decode_attention, or with a sliding window
-        pkv_paged_attention (one query per sequence)."""
-        if self.window <= 0:
+        """The public decode call: pkv_paged_decode_attention, with a sliding window
+        pkv_paged_attention (one query per sequence), or on an FP8 cache
+        pkv_paged_decode_attention_fp8."""
+        if self.fp8:
+            self.pkv.paged_decode_attention_fp8(out, q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                                                self.table, clens, self.spec.scale, window=self.window, lse=lse,
+                                                num_splits=self.num_splits, workspace=self.ws)
+        elif self.window <= 0:
             self.pkv.paged_decode_attention(out, q, self.k_cache, self.v_cache, self.table, clens,
                                             self.spec.scale, lse=lse, num_splits=self.num_splits,
                                             workspace=self.ws)
@@ -232,7 +253,13 @@ class DecodeWorkload:
                                      workspace=self.ws)
 
     def append(self, c):
-        self.pkv.kv_append(self.k_new[c], self.v_new[c], self.k_cache, self.v_cache, self.slots[c])
+        self.cache_append(self.k_new[c], self.v_new[c], self.slots[c])
+
+    def cache_append(self, k_new, v_new, slots):
+        if self.fp8:
+            self.pkv.kv_append_fp8(k_new, v_new, self.k_cache, self.v_cache, self.k_scale, self.v_scale, slots)
+        else:
+            self.pkv.kv_append(k_new, v_new, self.k_cache, self.v_cache, slots)
 
     def attend(self, c):
         self.decode(self.out, self.q[c], self.clens[c], lse=self.lse)
@@ -260,7 +287,7 @@ class DecodeWorkload:
                         self.stage_d[1 - buf].copy_(self.stage_h[(c + 1) % self.cycle], non_blocking=True)
                         self.out_h[1 - buf].copy_(self.out_e[1 - buf], non_blocking=True)
                     q, kn, vn, sl, cl = self.views[buf]
-                    self.pkv.kv_append(kn, vn, self.k_cache, self.v_cache, sl)
+                    self.cache_append(kn, vn, sl)
                     self.decode(self.out_e[buf], q, cl)
                     join = torch.cuda.Event()
                     join.record(cp)
@@ -291,23 +318,30 @@ class DecodeWorkload:
         inp = gen.decode_inputs(sub, self.lengths[:n_seq], steps=steps)
         bs = s.block_size
         threads = os.cpu_count() or 1
+        if self.fp8:
+            kq, ks = oracle.quantize_rows_e4m3(inp.k_cache)
+            vq, vs = oracle.quantize_rows_e4m3(inp.v_cache)
 
         def run(c):
             slots = torch.tensor([oracle.slot_of(inp.block_table[b], n + c, bs)
                                   for b, n in enumerate(inp.cached)])
-            oracle.kv_append(inp.k_cache, inp.v_cache, inp.k_new[c], inp.v_new[c], slots)
             lens = torch.tensor([n + c + 1 for n in inp.cached], dtype=torch.int32)
+            if self.fp8:
+                oracle.kv_append_fp8(kq, vq, ks, vs, inp.k_new[c], inp.v_new[c], slots)
+                kc, vc = oracle.dequantize_fp8(kq, ks), oracle.dequantize_fp8(vq, vs)
+            else:
+                oracle.kv_append(inp.k_cache, inp.v_cache, inp.k_new[c], inp.v_new[c], slots)
+                kc, vc = inp.k_cache, inp.v_cache
             if self.window <= 0:
-                oracle.paged_decode(inp.q[c], inp.k_cache, inp.v_cache, inp.block_table, lens, s.scale,
-                                    nthreads=threads)
+                oracle.paged_decode(inp.q[c], kc, vc, inp.block_table, lens, s.scale, nthreads=threads)
                 seen = lens
             else:
                 cu = torch.arange(len(inp.cached) + 1, dtype=torch.int32)
-                oracle.paged_attention(inp.q[c], inp.k_cache, inp.v_cache, inp.block_table, lens, cu,
-                                       s.scale, window=self.window, nthreads=threads)
+                oracle.paged_attention(inp.q[c], kc, vc, inp.block_table, lens, cu, s.scale,
+                                       window=self.window, nthreads=threads)
                 seen = lens.clamp(max=self.window)
-            elt = 2 if s.cache_dtype == torch.bfloat16 else 4
-            return int(seen.sum()) * s.kv_heads * s.head_dim * 2 * elt
+            row = s.head_dim + 4 if self.fp8 else s.head_dim * (2 if s.cache_dtype == torch.bfloat16 else 4)
+            return int(seen.sum()) * s.kv_heads * 2 * row
         return run, threads
 
 
@@ -365,6 +399,10 @@ WORKLOADS = {
     "long_mqa": lambda: DecodeWorkload(gen.LONG_MQA, [gen.LONG_LENGTH] * 4, 1,
                                        "long-context split-K MQA decode: batch 4, 64 q / 1 kv head, d 128, "
                                        "131072 cached tokens, bs 16, bf16 KV"),
+    "gqa70b_fp8": lambda: DecodeWorkload(gen.GQA_70B, gen.gqa_70b_lengths(), 32,
+                                         "llama2-70b-shaped GQA decode on an FP8 cache (E4M3 codes, fp32 scale "
+                                         "per row): batch 64, 64 q / 8 kv heads, d 128, lengths U[512,8192], "
+                                         "32-step append+attend cycle, bs 16", fp8=True),
     "swa": lambda: DecodeWorkload(gen.SWA, [gen.SWA_LENGTH] * gen.SWA.batch, 1,
                                   "mistral-7b-shaped sliding-window decode: batch 64, 32 q / 8 kv heads, d 128, "
                                   "16384 cached tokens, window 4096 (blocks outside released), bs 16, bf16 KV",
@@ -470,8 +508,10 @@ def bench_ours(args):
         value = total_bytes / (max_ms / 1e3) / 1e9
         kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
         achieved = (sum(step_bytes) / len(step_bytes)) / (kern_avg_ms / 1e3) / 1e9
-        files = ["decode.cu", "decode_kparams.cuh", "common.cuh"]
-        if wl.spec.q_heads // wl.spec.kv_heads > 8:
+        files = ["decode.cu", "decode_kparams.cuh", "decode_epilogue.cuh", "common.cuh"]
+        if wl.fp8:
+            files.append("decode_fp8.cu")
+        elif wl.spec.q_heads // wl.spec.kv_heads > 8:
             files.append("decode_umma.cu")      # the tcgen05 large-group kernel
         src = kernel_source_hash(files)
         traffic = profiled_traffic(f"decode_{args.workload}.md", src)

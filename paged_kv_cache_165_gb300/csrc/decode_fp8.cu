@@ -12,7 +12,8 @@
 //
 // decode_fp8_kernel (d = 128, bs 16 or 32, up to 8 query heads per KV head): the block
 // layout of decode_chunked_kernel -- one CTA per (sequence, KV head, chunk of blocks),
-// four warps taking the chunk's blocks in turn, each with a private TMA ring; a stage
+// four warps taking the chunk's blocks in turn, each with a private TMA ring (up to four
+// blocks per SM: the MMA chains are short and need the warps to hide their latency); a stage
 // holds a block's K and V codes (128-byte rows, 128-byte swizzle) and its two rows of
 // scales.  Per block and warp, with m16n8k16 f16 MMAs:
 //   scores S^T (16 rows: the heads' hi and lo query parts; 8 keys per tile): the
@@ -22,7 +23,6 @@
 //   output O^T = V^T P^T: V^T is the A operand (16 dimensions x 16 keys), read as four
 //     16-byte rows per lane and paired across keys with byte permutes; P^T is the B
 //     operand, which is exactly the softmax weights the lane already holds for its head.
-#include <cuda_fp8.h>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -35,11 +35,14 @@ namespace {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 
-// Two E4M3 codes (low byte first) to an f16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-    const __half2_raw r =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+// Four E4M3 codes (byte i = code i) to two f16x2: lo = codes 0, 1; hi = codes 2, 3 (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four));
 }
 
 // x ~= hi + lo with hi = rn_f16(x), lo = rn_f16(x - hi); the low half holds x0.
@@ -77,7 +80,7 @@ struct Fp8Cfg {
 };
 
 template <int BS, int ST>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 4)
     decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const DecodeKParams p) {
     using Cfg = Fp8Cfg<BS, ST>;
@@ -210,10 +213,12 @@ __global__ void __launch_bounds__(128)
             __syncwarp();
         }
 
-        // ---- scores of head g (rows g: hi, g+8: lo) for keys 8*nt + 2*t4 + {0, 1}
+        // ---- scores of head g (rows g: hi, g+8: lo) for keys 8*nt + 2*t4 + {0, 1}; the
+        // k-steps of a tile accumulate in two halves (independent MMA chains)
         float s[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+            float s2[4] = {0.f, 0.f, 0.f, 0.f};
             s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
             const int row = nt * 8 + g;
             const uint8_t *krow = kpage + row * 128;
@@ -221,9 +226,15 @@ __global__ void __launch_bounds__(128)
             const uint4 c1 = *reinterpret_cast<const uint4 *>(krow + (((2 * t4 + 1) ^ (row & 7)) << 4));
             const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_f16_16816(s[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], e4m3x2_to_f16x2(w[kk]),
-                              e4m3x2_to_f16x2(w[kk] >> 16));
+            for (int kk = 0; kk < 8; kk += 2) {
+                uint32_t b0, b1, b2, b3;
+                e4m3x4_to_f16x2x2(w[kk], b0, b1);
+                e4m3x4_to_f16x2x2(w[kk + 1], b2, b3);
+                mma_f16_16816(s[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                mma_f16_16816(s2, qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2], qa[kk + 1][3], b2, b3);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[nt][e] += s2[e];
         }
 
         // ---- online softmax (base 2) of head g
@@ -257,15 +268,18 @@ __global__ void __launch_bounds__(128)
         }
         l_run = l_run * alpha + psum;
         m_run = m_new;
-        // rescale O^T: its heads are 2*t4 and 2*t4+1, whose states live in lanes 8*t4 + x
-        const float alpha_a = __shfl_sync(kFullMask, alpha, 8 * t4);
-        const float alpha_b = __shfl_sync(kFullMask, alpha, 8 * t4 + 4);
+        // rescale O^T when a running max moved: its heads are 2*t4 and 2*t4+1, whose
+        // states live in lanes 8*t4 + x
+        if (__any_sync(kFullMask, alpha != 1.f)) {
+            const float alpha_a = __shfl_sync(kFullMask, alpha, 8 * t4);
+            const float alpha_b = __shfl_sync(kFullMask, alpha, 8 * t4 + 4);
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            oT[mt][0] *= alpha_a;
-            oT[mt][1] *= alpha_b;
-            oT[mt][2] *= alpha_a;
-            oT[mt][3] *= alpha_b;
+            for (int mt = 0; mt < 8; ++mt) {
+                oT[mt][0] *= alpha_a;
+                oT[mt][1] *= alpha_b;
+                oT[mt][2] *= alpha_a;
+                oT[mt][3] *= alpha_b;
+            }
         }
 
         // ---- O^T += V^T P^T, 16 keys per step
@@ -287,10 +301,9 @@ __global__ void __launch_bounds__(128)
                 // bytes 2*mt and 2*mt+1 of each row: dimensions 16g + 2mt (+1)
                 const int wi = mt >> 1, bi = 2 * (mt & 1);
                 const uint32_t sel = bi | ((4 + bi) << 4) | ((bi + 1) << 8) | ((5 + bi) << 12);
-                const uint32_t x01 = __byte_perm(w0[wi], w1[wi], sel);
-                const uint32_t x23 = __byte_perm(w2[wi], w3[wi], sel);
-                const uint32_t a0 = e4m3x2_to_f16x2(x01), a1 = e4m3x2_to_f16x2(x01 >> 16);
-                const uint32_t a2 = e4m3x2_to_f16x2(x23), a3 = e4m3x2_to_f16x2(x23 >> 16);
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(__byte_perm(w0[wi], w1[wi], sel), a0, a1);
+                e4m3x4_to_f16x2x2(__byte_perm(w2[wi], w3[wi], sel), a2, a3);
                 mma_f16_16816(oT[mt], a0, a1, a2, a3, bh0, bh1);
                 mma_f16_16816(oT[mt], a0, a1, a2, a3, bl0, bl1);
             }
@@ -345,7 +358,8 @@ cudaError_t launch_fp8(const DecodeKParams &kp, const CUtensorMap &tk, const CUt
 
 cudaError_t launch_decode_fp8(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int bs,
                               dim3 grid, cudaStream_t stream) {
-    return bs == 16 ? launch_fp8<16, 6>(kp, tk, tv, grid, stream) : launch_fp8<32, 3>(kp, tk, tv, grid, stream);
+    // 12 KB (bs 16) or 16 KB (bs 32) of copies in flight per warp; four (three) blocks per SM
+    return bs == 16 ? launch_fp8<16, 3>(kp, tk, tv, grid, stream) : launch_fp8<32, 2>(kp, tk, tv, grid, stream);
 }
 
 }  // namespace pkv
