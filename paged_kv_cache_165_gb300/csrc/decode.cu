@@ -157,12 +157,14 @@ struct TcPage {
         }
         l_run = l_run * alpha + psum;
         m_run = m_new;
+        if (__any_sync(kFull, alpha != 1.f)) {   // only when a running max moved
 #pragma unroll
-        for (int nt = 0; nt < ONT; ++nt) {
-            o[nt][0] *= alpha;
-            o[nt][1] *= alpha;
-            o[nt][2] *= alpha;
-            o[nt][3] *= alpha;
+            for (int nt = 0; nt < ONT; ++nt) {
+                o[nt][0] *= alpha;
+                o[nt][1] *= alpha;
+                o[nt][2] *= alpha;
+                o[nt][3] *= alpha;
+            }
         }
 
         // O += P V with P = P_hi (rows 0-7) + P_lo (rows 8-15)
