@@ -131,18 +131,21 @@ def dist_env():
 class DecodeWorkload:
     """Decode steps over a paged cache: append one token per sequence, then attend."""
 
-    def __init__(self, spec, lengths, cycle, label, window=0, fp8=False):
+    def __init__(self, spec, lengths, cycle, label, window=0, fp8=False, qlen=1):
         self.spec, self.lengths, self.cycle, self.label = spec, list(lengths), cycle, label
         self.num_splits = 0
         self.window = window   # > 0: sliding window of this many tokens
         self.fp8 = fp8         # E4M3 codes + one fp32 scale per cached row
+        self.qlen = qlen       # new tokens per sequence per step, all verified at once
 
     # bytes of K and V read by one step c of the cycle (every visible cached token, every
     # KV head; FP8: the code bytes and the row's 4-byte scale)
     def kv_bytes(self, c):
         row = self.spec.head_dim + 4 if self.fp8 else \
             self.spec.head_dim * (2 if self.spec.cache_dtype == torch.bfloat16 else 4)
-        seen = [n + c + 1 if self.window <= 0 else min(n + c + 1, self.window) for n in self.lengths]
+        q = self.qlen
+        seen = [n + q * (c + 1) if self.window <= 0 else min(n + q * (c + 1), self.window + q - 1)
+                for n in self.lengths]
         return sum(seen) * self.spec.kv_heads * 2 * row
 
     def describe(self):
@@ -151,7 +154,7 @@ class DecodeWorkload:
                 "head_dim": s.head_dim, "block_size": s.block_size,
                 "cache_dtype": "e4m3 codes + fp32 row scales" if self.fp8 else "bf16",
                 "q_dtype": "fp32", "mean_cached_len": sum(self.lengths) / len(self.lengths),
-                "decode_steps_cycle": self.cycle, "window": self.window,
+                "decode_steps_cycle": self.cycle, "window": self.window, "new_tokens_per_step": self.qlen,
                 "kv_gb_per_step": self.kv_bytes(self.cycle // 2) / 1e9,
                 "l2": "inputs larger than L2: each step reads %.2f GB of K/V vs 129 MB L2"
                       % (self.kv_bytes(0) / 1e9)}
@@ -161,15 +164,18 @@ class DecodeWorkload:
         s = self.spec
         bs = s.block_size
         g = gen.generator(s.seed)
-        nb = sum(gen.blocks_needed(n + self.cycle, bs) for n in self.lengths)
+        nb = sum(gen.blocks_needed(n + self.cycle * self.qlen, bs) for n in self.lengths)
         bm = pkv.BlockManager(nb, bs, order=gen.permutation(g, nb))
         for b, n in enumerate(self.lengths):
             bm.add_sequence(b, n)
         slots, clens = [], []
         for c in range(self.cycle):
-            sl, copies = bm.append_step(range(s.batch))
-            assert not copies
-            slots.append(torch.tensor(sl, dtype=torch.int64))
+            step = []
+            for _ in range(self.qlen):   # token-major within a sequence: rows b*qlen + i
+                sl, copies = bm.append_step(range(s.batch))
+                assert not copies
+                step.append(sl)
+            slots.append(torch.tensor(step, dtype=torch.int64).t().reshape(-1))
             clens.append(bm.context_lens(range(s.batch)))
         self.nb = nb
         self.released_blocks = 0
@@ -201,12 +207,17 @@ class DecodeWorkload:
                               kq, vq, self.k_scale, self.v_scale, all_slots)
             self.k_cache, self.v_cache = kq, vq
         B, Hq, Hkv, d = s.batch, s.q_heads, s.kv_heads, s.head_dim
-        self.q = torch.randn((self.cycle, B, Hq, d), generator=cg, device=device)
-        self.k_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(torch.bfloat16 if self.fp8 else s.cache_dtype)
-        self.v_new = torch.randn((self.cycle, B, Hkv, d), generator=cg, device=device).to(torch.bfloat16 if self.fp8 else s.cache_dtype)
-        self.out = torch.empty((B, Hq, d), device=device)
-        self.lse = torch.empty((B, Hq), device=device)
-        ws = pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, self.table.shape[1], self.num_splits)
+        R = B * self.qlen                # query rows per step
+        new_dt = torch.bfloat16 if self.fp8 else s.cache_dtype
+        self.q = torch.randn((self.cycle, R, Hq, d), generator=cg, device=device)
+        self.k_new = torch.randn((self.cycle, R, Hkv, d), generator=cg, device=device).to(new_dt)
+        self.v_new = torch.randn((self.cycle, R, Hkv, d), generator=cg, device=device).to(new_dt)
+        self.out = torch.empty((R, Hq, d), device=device)
+        self.lse = torch.empty((R, Hq), device=device)
+        self.cu_q = torch.arange(B + 1, dtype=torch.int32, device=device) * self.qlen
+        ws = pkv.paged_attention_workspace_bytes(B, R, self.qlen, Hq, Hkv, d, bs, self.table.shape[1],
+                                                 self.window, self.num_splits)
+        ws = max(ws, pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, self.table.shape[1], self.num_splits))
         self.ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)   # zeroed once
         self.splits = 1 if ws == 0 else None
         # end-to-end arm: each step's inputs (q, new K/V rows, slot mapping, context lengths)
@@ -226,13 +237,13 @@ class DecodeWorkload:
         self.stage_d = [torch.empty(offs[-1], dtype=torch.uint8, device=device) for _ in range(2)]
         self.views = [[sd[o:o + n].view(t.dtype).view(t.shape[1:]) for t, o, n in zip(parts, offs, sizes)]
                       for sd in self.stage_d]
-        self.out_e = [torch.empty((B, Hq, d), device=device) for _ in range(2)]
-        self.out_h = [torch.empty((B, Hq, d)).pin_memory() for _ in range(2)]
+        self.out_e = [torch.empty((R, Hq, d), device=device) for _ in range(2)]
+        self.out_h = [torch.empty((R, Hq, d)).pin_memory() for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(device=device)
         self.pkv = pkv
         # kv_append, then the kernels the decode call enqueues (as the library plans it)
         self.launches_per_step = 1 + pkv.paged_attention_kernel_launches(
-            B, B, 1, Hq, Hkv, d, bs, self.table.shape[1], nb, torch.uint8 if self.fp8 else s.cache_dtype,
+            B, R, self.qlen, Hq, Hkv, d, bs, self.table.shape[1], nb, torch.uint8 if self.fp8 else s.cache_dtype,
             self.window, self.num_splits)
 
     def decode(self, out, q, clens, lse=None):
@@ -243,6 +254,10 @@ class DecodeWorkload:
             self.pkv.paged_decode_attention_fp8(out, q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                                                 self.table, clens, self.spec.scale, window=self.window, lse=lse,
                                                 num_splits=self.num_splits, workspace=self.ws)
+        elif self.qlen > 1:
+            self.pkv.paged_attention(out, q, self.k_cache, self.v_cache, self.table, clens, self.spec.scale,
+                                     cu_q=self.cu_q, max_q=self.qlen, window=self.window, lse=lse,
+                                     num_splits=self.num_splits, workspace=self.ws)
         elif self.window <= 0:
             self.pkv.paged_decode_attention(out, q, self.k_cache, self.v_cache, self.table, clens,
                                             self.spec.scale, lse=lse, num_splits=self.num_splits,
@@ -313,6 +328,7 @@ class DecodeWorkload:
     def oracle_sample(self, n_seq, steps=1):
         import oracle
         s = self.spec
+        steps = max(steps, self.qlen)
         sub = gen.DecodeSpec(s.name + "_sample", s.seed + 77, n_seq, s.q_heads, s.kv_heads, s.head_dim,
                              s.cache_dtype, s.block_size, steps)
         inp = gen.decode_inputs(sub, self.lengths[:n_seq], steps=steps)
@@ -321,6 +337,23 @@ class DecodeWorkload:
         if self.fp8:
             kq, ks = oracle.quantize_rows_e4m3(inp.k_cache)
             vq, vs = oracle.quantize_rows_e4m3(inp.v_cache)
+
+        def run_verify(c):
+            # qlen new tokens per sequence appended, then attended causally at once
+            q = self.qlen
+            for i in range(q):
+                slots = torch.tensor([oracle.slot_of(inp.block_table[b], n + i, bs)
+                                      for b, n in enumerate(inp.cached)])
+                oracle.kv_append(inp.k_cache, inp.v_cache, inp.k_new[i], inp.v_new[i], slots)
+            lens = torch.tensor([n + q for n in inp.cached], dtype=torch.int32)
+            rows = torch.stack([inp.q[i] for i in range(q)], 1).reshape(-1, s.q_heads, s.head_dim)
+            cu = torch.arange(len(inp.cached) + 1, dtype=torch.int32) * q
+            oracle.paged_attention(rows, inp.k_cache, inp.v_cache, inp.block_table, lens, cu, s.scale,
+                                   window=self.window, nthreads=threads)
+            return int(lens.sum()) * s.kv_heads * s.head_dim * 2 * (2 if s.cache_dtype == torch.bfloat16 else 4)
+
+        if self.qlen > 1:
+            return run_verify, threads
 
         def run(c):
             slots = torch.tensor([oracle.slot_of(inp.block_table[b], n + c, bs)
@@ -403,6 +436,10 @@ WORKLOADS = {
                                          "llama2-70b-shaped GQA decode on an FP8 cache (E4M3 codes, fp32 scale "
                                          "per row): batch 64, 64 q / 8 kv heads, d 128, lengths U[512,8192], "
                                          "32-step append+attend cycle, bs 16", fp8=True),
+    "verify4": lambda: DecodeWorkload(gen.GQA_70B, gen.gqa_70b_lengths(), 1,
+                                      "llama2-70b-shaped GQA verification step: batch 64, 64 q / 8 kv heads, "
+                                      "d 128, lengths U[512,8192], 4 new tokens per sequence appended and "
+                                      "attended causally, bs 16, bf16 KV", qlen=4),
     "swa": lambda: DecodeWorkload(gen.SWA, [gen.SWA_LENGTH] * gen.SWA.batch, 1,
                                   "mistral-7b-shaped sliding-window decode: batch 64, 32 q / 8 kv heads, d 128, "
                                   "16384 cached tokens, window 4096 (blocks outside released), bs 16, bf16 KV",
@@ -517,7 +554,7 @@ def bench_ours(args):
         traffic = profiled_traffic(f"decode_{args.workload}.md", src)
         res.update({
             "value": value, "unit": "GB/s", "pct_hbm_peak": 100 * value / hbm,
-            "tokens_per_s_per_layer": wl.spec.batch * world / (ms_per_step / 1e3),
+            "tokens_per_s_per_layer": wl.spec.batch * wl.qlen * world / (ms_per_step / 1e3),
             "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (split-K partials + LSE merge)",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"

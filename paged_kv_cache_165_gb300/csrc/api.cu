@@ -4,6 +4,7 @@
 // maps CUDA failures to PKV_ERR_CUDA, and records a message for pkv_last_error().
 // Per-device state is limited to the SM count and the address of the device error
 // word (a static __device__ variable: nothing is allocated).
+#include <algorithm>
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
@@ -226,11 +227,14 @@ int pkv_paged_attention_kernel_launches(int B, int Tq, int max_q, int Hq, int Hk
     if (B == 0 || Tq == 0) return 0;
     DeviceState *st = nullptr;
     if (device_state(&st) != PKV_OK) return -1;
-    const int vis = visible_blocks(MBS, bs, window);
     const bool one_per_seq = Tq == B && max_q == 1;
     const DecodePlan plan =
-        one_per_seq ? plan_decode(B, Hq, Hkv, d, bs, vis, NB, dt, num_splits, st->sm_count, true, true)
-                    : plan_decode(Tq, Hq, Hkv, d, bs, vis, NB, dt, num_splits, st->sm_count, false, false);
+        one_per_seq
+            ? plan_decode(B, Hq, Hkv, d, bs, visible_blocks(MBS, bs, window), NB, dt, num_splits, st->sm_count,
+                          true, true)
+            : plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs,
+                                  visible_blocks(MBS, bs, window > 0 ? window + max_q - 1 : 0), NB, dt,
+                                  num_splits, st->sm_count, true, true);
     return plan.splits > 1 && !plan.fused_merge ? 2 : 1;
 }
 
@@ -275,12 +279,15 @@ size_t pkv_paged_attention_workspace_bytes(int B, int Tq, int max_q, int Hq, int
         return 0;
     DeviceState *st = nullptr;
     if (device_state(&st) != PKV_OK) return 0;
-    const int vis = visible_blocks(MBS, bs, window);
     if (Tq == B && max_q <= 1)
-        return decode_workspace_upper_bound(B, Hq, Hkv, d, bs, vis, num_splits, st->sm_count);
-    // query rows run on the CUDA-core path (the plan of an unaligned fp32 cache)
-    return plan_decode(Tq, Hq, Hkv, d, bs, vis, 1, PKV_F32, num_splits, st->sm_count, false, false)
-        .workspace_bytes;
+        return decode_workspace_upper_bound(B, Hq, Hkv, d, bs, visible_blocks(MBS, bs, window), num_splits,
+                                            st->sm_count);
+    // query rows: cover the tcgen05 and the CUDA-core plans
+    const int vis = visible_blocks(MBS, bs, window > 0 ? window + max_q - 1 : 0);
+    return std::max(plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs, vis, 1, PKV_BF16, num_splits,
+                                        st->sm_count, true, true).workspace_bytes,
+                    plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs, vis, 1, PKV_F32, num_splits,
+                                        st->sm_count, false, false).workspace_bytes);
 }
 
 pkv_status pkv_paged_attention(float *out, float *lse, const float *q, const void *k_cache,
@@ -308,11 +315,14 @@ pkv_status pkv_paged_attention(float *out, float *lse, const float *q, const voi
     DeviceState *st = nullptr;
     s = device_state(&st);
     if (s != PKV_OK) return s;
-    const int vis = visible_blocks(MBS, bs, window);
+    const bool caches_aligned = aligned16(k_cache) && aligned16(v_cache);
     const DecodePlan plan =
-        one_per_seq ? plan_decode(B, Hq, Hkv, d, bs, vis, NB, dt, num_splits, st->sm_count,
-                                  aligned16(k_cache) && aligned16(v_cache), aligned16(q))
-                    : plan_decode(Tq, Hq, Hkv, d, bs, vis, NB, dt, num_splits, st->sm_count, false, false);
+        one_per_seq
+            ? plan_decode(B, Hq, Hkv, d, bs, visible_blocks(MBS, bs, window), NB, dt, num_splits, st->sm_count,
+                          caches_aligned, aligned16(q))
+            : plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs,
+                                  visible_blocks(MBS, bs, window > 0 ? window + max_q - 1 : 0), NB, dt,
+                                  num_splits, st->sm_count, caches_aligned, aligned16(q));
     if (plan.workspace_bytes > 0 &&
         (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
          reinterpret_cast<uintptr_t>(workspace) % 16 != 0))

@@ -567,16 +567,22 @@ __global__ void __launch_bounds__(32)
     const SeqSpan sp = row_span(p, row, bs, lane == 0 && split == 0 && i == 0);
     const int b = sp.b;
     const int len = sp.len;
-    const int n_pages = sp.npages;
-    const int pg0 = sp.pfirst + split * p.chunk_pages;   // absolute pages
-    const int pg1 = min(sp.pfirst + n_pages, pg0 + p.chunk_pages);
+    const int nc = (sp.cnpages + p.chunk_pages - 1) / p.chunk_pages;   // the sequence's chunks
+    const int c0 = sp.cpfirst + split * p.chunk_pages;                  // this chunk's pages
+    const int c1 = min(sp.cpfirst + sp.cnpages, c0 + p.chunk_pages);
+    const int pg0 = max(c0, sp.pfirst);                                 // ... that this row sees
+    const int pg1 = min(c1, sp.pfirst + sp.npages);
     const size_t bi = static_cast<size_t>(row) * p.Hq + i;
-    const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;   // chunks holding tokens
-    if (pg0 >= pg1) {
+    if (c0 >= c1) {
         if (split == 0) {   // an empty sequence: out = 0, lse = -inf
             for (int e = lane; e < d; e += 32) p.out[bi * d + e] = 0.f;
             if (lane == 0 && p.lse != nullptr) p.lse[bi] = -INFINITY;
         }
+        return;
+    }
+    if (pg0 >= pg1) {   // the chunk holds none of this row's keys: an empty partial
+        for (int e = lane; e < d; e += 32) p.ws_o[(bi * p.splits + split) * d + e] = 0.f;
+        if (lane == 0) p.ws_lse[bi * p.splits + split] = -INFINITY;
         return;
     }
     float qv[J], acc[J];
@@ -653,7 +659,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     __shared__ float red[kMergeThreads / 32];
     const size_t bi = blockIdx.x;
     const int b = static_cast<int>(bi / p.Hq);
-    const int n_pages = row_span(p, b, bs, false).npages;
+    const int n_pages = row_span(p, b, bs, false).cnpages;
     const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
     if (nc <= 1) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -773,7 +779,8 @@ constexpr int kFusedMergeMaxChunks = 8;
 // arrival counters (a fixed-size region, so that a workspace zeroed once stays valid for
 // any later shape), then o partials [B*Hq][splits][d], then lse partials [B*Hq][splits].
 void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS, int num_splits,
-                int sm_count) {
+                int sm_count, int rows = -1) {
+    if (rows < 0) rows = B;   // query rows (partials are per row and head)
     const int m = Hq / Hkv;
     const long long units = static_cast<long long>(B) * Hkv * ((m + 7) / 8);
     const long long max_counters = PKV_DECODE_COUNTER_BYTES / sizeof(unsigned);
@@ -797,7 +804,7 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
         // 64-key tiles
         const int ppt = kUmmaDecodeKeys / bs;
         if (num_splits == 0) {
-            const long long gunits = static_cast<long long>(B) * Hkv;
+            const long long gunits = static_cast<long long>(B) * Hkv * plan.qtiles;
             const long long per_unit = std::max(1ll, (std::max(sm_count, 1) + gunits - 1) / gunits);
             chunk = static_cast<int>((MBS + per_unit - 1) / per_unit);
         }
@@ -816,7 +823,7 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
     plan.chunk_pages = chunk;
     plan.splits = (MBS + chunk - 1) / chunk;
     plan.workspace_bytes = plan.splits > 1 ? PKV_DECODE_COUNTER_BYTES +
-                                                 static_cast<size_t>(B) * Hq * plan.splits *
+                                                 static_cast<size_t>(rows) * Hq * plan.splits *
                                                      (static_cast<size_t>(d) + 1) * sizeof(float)
                                            : 0;
     // The last chunk merges in place when a unit has few chunks; many chunks (long
@@ -847,6 +854,24 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, p
     return plan;
 }
 
+DecodePlan plan_attention_rows(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs, int MBS, int NB,
+                               pkv_dtype dt, int num_splits, int sm_count, bool caches_aligned,
+                               bool q_aligned) {
+    DecodePlan plan{};
+    const int m = Hq / Hkv;
+    plan.umma = dt == PKV_BF16 && (d == 64 || d == 128) && (bs == 16 || bs == 32) && caches_aligned &&
+                q_aligned && m <= 64 && static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31);
+    if (plan.umma) {
+        plan.q_per_tile = 64 / m;
+        plan.qtiles = (max_q + plan.q_per_tile - 1) / plan.q_per_tile;
+        plan.umma = static_cast<long long>(B) * plan.qtiles <= 65535;
+    }
+    if (!plan.umma) plan.q_per_tile = plan.qtiles = 1;
+    plan.tensor_core = plan.group = plan.umma;
+    chunk_plan(plan, B, Hq, Hkv, d, bs, MBS, num_splits, sm_count, Tq);
+    return plan;
+}
+
 size_t decode_workspace_upper_bound(int B, int Hq, int Hkv, int d, int bs, int MBS,
                                     int num_splits, int sm_count) {
     // the query knows neither the element type nor the alignment: cover both paths
@@ -866,7 +891,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
                           cudaStream_t stream) {
     const int rows = a.rows >= 0 ? a.rows : a.B;
     if (a.B == 0 || rows == 0) return cudaSuccess;
-    if (a.cu_q != nullptr && plan.tensor_core) return cudaErrorInvalidValue;   // rows need the CUDA-core path
+    if (a.cu_q != nullptr && plan.tensor_core && !plan.umma) return cudaErrorInvalidValue;
     DecodeKParams kp{};
     kp.out = a.out;
     kp.lse = a.lse;
@@ -888,6 +913,8 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     kp.cu_q = a.cu_q;
     kp.k_scale = a.k_scale;
     kp.v_scale = a.v_scale;
+    kp.q_per_tile = plan.q_per_tile;
+    kp.qtiles = plan.qtiles;
     if (plan.splits > 1) {
         uint8_t *ws = static_cast<uint8_t *>(a.workspace);
         kp.counters = plan.fused_merge ? reinterpret_cast<unsigned *>(ws) : nullptr;
@@ -917,9 +944,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
             !encode_map_bf16(&tv, a.v_cache, 2, dims, strides, box))
             return cudaErrorInvalidValue;
         if (plan.umma) {
-            e = launch_decode_umma(kp, tk, tv, a.d, a.bs, dim3(plan.splits, a.Hkv, a.B), stream);
+            e = launch_decode_umma(kp, tk, tv, a.d, a.bs, dim3(plan.splits, a.Hkv, a.B * plan.qtiles), stream);
             if (e != cudaSuccess || plan.splits == 1) return e;
-            decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), kMergeThreads, 0, stream>>>(
+            decode_merge_kernel<<<static_cast<unsigned>(rows * a.Hq), kMergeThreads, 0, stream>>>(
                 kp, a.d, a.bs);
             return cudaGetLastError();
         }

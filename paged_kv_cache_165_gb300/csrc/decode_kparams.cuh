@@ -28,6 +28,8 @@ struct DecodeKParams {
     int window;       // > 0: only the most recent `window` tokens are visible
     const int32_t *cu_q;   // query rows per sequence [B+1]; nullptr: row b = sequence b
     const float *k_scale, *v_scale;   // FP8 caches: fp32 scale per row [NB][Hkv][bs]
+    int q_per_tile;   // tcgen05 kernel: query rows of a sequence per block (1 for decode)
+    int qtiles;       // tcgen05 kernel: query tiles per sequence (grid z = B * qtiles)
 };
 
 // Sequence length after validation; an invalid length counts as empty.
@@ -46,8 +48,12 @@ __device__ __forceinline__ int checked_len(const DecodeKParams &p, int b, int bs
 // at position L - nq + i: `len` is then that position + 1 (causal, aligned to the end
 // of the cache).  With a sliding window of W tokens, lo = max(0, len - W), the most
 // recent W positions; blocks before pfirst are never read and may have been freed.
+// Chunks of a sequence cover the pages [cpfirst, cpfirst + cnpages) that any of its query
+// rows sees (the same boundaries for every row, so that chunk partials line up); a row
+// whose own keys miss a chunk writes an empty partial there.
 struct SeqSpan {
     int b, len, lo, pfirst, npages;
+    int cpfirst, cnpages;
 };
 
 __device__ __forceinline__ SeqSpan span_of(const DecodeKParams &p, int b, int len, int bs) {
@@ -57,6 +63,8 @@ __device__ __forceinline__ SeqSpan span_of(const DecodeKParams &p, int b, int le
     s.lo = p.window > 0 ? max(0, len - p.window) : 0;
     s.pfirst = s.lo / bs;
     s.npages = len > 0 ? (len + bs - 1) / bs - s.pfirst : 0;
+    s.cpfirst = s.pfirst;
+    s.cnpages = s.npages;
     return s;
 }
 
@@ -83,7 +91,12 @@ __device__ __forceinline__ SeqSpan row_span(const DecodeKParams &p, int r, int b
         if (report) raise_error(p.err, PKV_DEVERR_CU_SEQLENS);
         return span_of(p, b, 0, bs);
     }
-    return span_of(p, b, L - nq + (r - c0) + 1, bs);
+    SeqSpan s = span_of(p, b, L - nq + (r - c0) + 1, bs);
+    // the sequence's chunk range: from the first row's window start to the last key
+    const SeqSpan first = span_of(p, b, L - nq + 1, bs);
+    s.cpfirst = first.pfirst;
+    s.cnpages = (L + bs - 1) / bs - first.pfirst;
+    return s;
 }
 
 // Large-group decode on tcgen05 (decode_umma.cu): d in {64, 128}, bs in {16, 32},

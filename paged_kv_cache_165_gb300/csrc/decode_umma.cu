@@ -99,27 +99,59 @@ __global__ void __launch_bounds__(352, 1)
     auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const SeqSpan sp = seq_span(p, b, BS, threadIdx.x == 0 && split == 0 && kvh == 0);
-    const int len = sp.len;
-    const int n_pages = sp.npages;
-    const int pg0 = split * p.chunk_pages;   // pages relative to sp.pfirst
-    const int pg1 = min(n_pages, pg0 + p.chunk_pages);
-    const size_t bi_group = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.m;
-    if (pg0 >= pg1) {
-        if (split == 0) {   // an empty sequence: out = 0, lse = -inf for the whole group
-            for (int idx = threadIdx.x; idx < p.m * D; idx += blockDim.x) p.out[bi_group * D + idx] = 0.f;
+    const int split = blockIdx.x, kvh = blockIdx.y;
+    const int b = blockIdx.z / p.qtiles, qt = blockIdx.z % p.qtiles;
+    const bool report = threadIdx.x == 0 && split == 0 && kvh == 0 && qt == 0;
+    // the sequence's query rows c0 .. c0+nq-1 (decode: row b) sit at positions L-nq ..
+    // L-1; this block takes rows q0 .. q0+nqt-1 of them, slot = (row - q0) * m + head
+    const int L = checked_len(p, b, BS, report);
+    int c0 = b, nq = 1;
+    bool rows_ok = true;
+    if (p.cu_q != nullptr) {
+        c0 = __ldg(p.cu_q + b);
+        nq = __ldg(p.cu_q + b + 1) - c0;
+        if (nq < 0 || nq > L) {
+            if (report) raise_error(p.err, PKV_DEVERR_CU_SEQLENS);
+            rows_ok = false;
+        }
+    }
+    const int q0 = qt * p.q_per_tile;
+    const int nqt = max(0, min(p.q_per_tile, nq - q0));
+    const int slots = nqt * p.m;   // 1..64 query rows x heads
+    const int P0 = L - nq + q0;    // position of the tile's first query
+    // keys the whole sequence's rows see (chunk boundaries) and this tile's rows see
+    const int lo_seq = p.window > 0 ? max(0, L - nq + 1 - p.window) : 0;
+    const int cpfirst = lo_seq / BS, cnpages = L > 0 ? (L + BS - 1) / BS - cpfirst : 0;
+    const int nc = (cnpages + p.chunk_pages - 1) / p.chunk_pages;
+    const int lo_tile = p.window > 0 ? max(0, P0 + 1 - p.window) : 0;    // first query's window
+    const int lo_last = p.window > 0 ? max(0, P0 + nqt - p.window) : 0;   // last query's window
+    const int hi_tile = P0 + nqt;                                         // one past the last query
+    const int cp0 = cpfirst + split * p.chunk_pages;                      // this chunk's pages
+    const int cp1 = min(cpfirst + cnpages, cp0 + p.chunk_pages);
+    const int apg0 = max(cp0, lo_tile / BS);                              // ... that the tile sees
+    const int apg1 = min(cp1, (hi_tile + BS - 1) / BS);
+    auto row_of = [&](int slot) { return static_cast<size_t>(c0 + q0 + slot / p.m) * p.Hq + kvh * p.m + slot % p.m; };
+    if (nqt <= 0) return;
+    if (!rows_ok || cp0 >= cp1) {
+        if (split == 0) {   // an empty sequence or inconsistent rows: out = 0, lse = -inf
+            for (int idx = threadIdx.x; idx < slots * D; idx += blockDim.x) p.out[row_of(idx / D) * D + idx % D] = 0.f;
             if (p.lse != nullptr)
-                for (int h = threadIdx.x; h < p.m; h += blockDim.x) p.lse[bi_group + h] = -INFINITY;
+                for (int sl = threadIdx.x; sl < slots; sl += blockDim.x) p.lse[row_of(sl)] = -INFINITY;
         }
         return;
     }
-    const int pages = pg1 - pg0;
+    if (apg0 >= apg1) {     // none of the tile's keys in this chunk: empty partials
+        for (int idx = threadIdx.x; idx < slots * D; idx += blockDim.x)
+            p.ws_o[(row_of(idx / D) * p.splits + split) * D + idx % D] = 0.f;
+        for (int sl = threadIdx.x; sl < slots; sl += blockDim.x) p.ws_lse[row_of(sl) * p.splits + split] = -INFINITY;
+        return;
+    }
+    const int len = L;
+    const int pfirst = apg0, pages = apg1 - apg0;
     const int ntiles = (pages + PPT - 1) / PPT;
-    const int tok0 = (sp.pfirst + pg0) * BS;                // first token of the chunk's pages
-    const int tok_lo = max(tok0, sp.lo);                      // its first visible token
-    const int tok_end = min(len, (sp.pfirst + pg1) * BS);     // one past its last token
-    const int nc = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
+    const int tok0 = pfirst * BS;                        // first token of the pages read
+    const int tok_lo = max(tok0, lo_tile);               // first key any row sees
+    const int tok_end = min(hi_tile, apg1 * BS);         // one past the last key any row sees
 
     if (threadIdx.x == 0) {
         mbar_init(bar(Cfg::kQRaw), 1);
@@ -158,18 +190,20 @@ __global__ void __launch_bounds__(352, 1)
 
     if (warp >= 9) {
         // ---- TMA loaders: warp 9 the raw queries and the K tiles, warp 10 the V tiles.
-        // Tile t (pages pg0 + t*PPT ...) goes to stage t % N of its ring once the stage's
+        // Tile t (pages pfirst + t*PPT ...) goes to stage t % N of its ring once the stage's
         // previous tile is consumed (K: by S_{t-NK}; V: by P_{t-NV} V).
         const bool is_k = warp == 9;
         const int N = is_k ? NK : NV;
         const int full0 = is_k ? Cfg::kKFull : Cfg::kVFull, free0 = is_k ? Cfg::kKFree : Cfg::kVFree;
         const CUtensorMap *map = is_k ? &tm_k : &tm_v;
         if (is_k && lane == 0) {
-            const uint32_t q_bytes = static_cast<uint32_t>(p.m) * D * 4;
-            mbar_arrive_expect_tx(bar(Cfg::kQRaw), q_bytes);
-            bulk_load(sP(0), p.q + bi_group * D, q_bytes, bar(Cfg::kQRaw));
+            // the m heads of one query row are contiguous: one copy per row of the tile
+            const uint32_t row_bytes = static_cast<uint32_t>(p.m) * D * 4;
+            mbar_arrive_expect_tx(bar(Cfg::kQRaw), row_bytes * nqt);
+            for (int qi = 0; qi < nqt; ++qi)
+                bulk_load(sP(0) + qi * row_bytes, p.q + row_of(qi * p.m) * D, row_bytes, bar(Cfg::kQRaw));
         }
-        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + sp.pfirst + pg0;
+        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + pfirst;
         int tcur = lane < pages ? __ldg(tbl + lane) : -1;
         int tbase = 0;
         const int oob_row = p.NB * p.Hkv * BS;
@@ -275,23 +309,27 @@ __global__ void __launch_bounds__(352, 1)
         // ---- softmax group g: thread r owns row r of the tile (TMEM lane r)
         const int g = warp >> 2;
         const int r = threadIdx.x & 127;
-        const int h = r >> 1, part = r & 1;
-        const bool head_ok = h < p.m;
+        const int slot = r >> 1, part = r & 1;
+        const bool slot_ok = slot < slots;
+        // this row's query position and visible keys [lo_r, hi_r)
+        const int pos_r = P0 + (slot_ok ? slot / p.m : 0);
+        const int lo_r = p.window > 0 ? max(0, pos_r + 1 - p.window) : 0;
+        const int hi_r = min(pos_r + 1, apg1 * BS);
         const uint32_t lane_base = tmem + g * Cfg::kGroupCols + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int njj = (ntiles - g + 1) / 2;   // tiles of this group
         bool ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kQRaw), 0, abort, p.err));
 
-        // Q rows from the raw queries: group g writes panels g, g+2, ...; row 2h = rn(q_h),
-        // row 2h+1 = rn(q_h - rn(q_h)), 128-byte swizzle.  Reads are rotated by h so that
-        // the rows read by a quarter warp fall in distinct banks.
+        // Q rows from the raw queries: group g writes panels g, g+2, ...; row 2s = rn(q_s),
+        // row 2s+1 = rn(q_s - rn(q_s)) for slot s, 128-byte swizzle.  Reads are rotated by
+        // s so that the rows read by a quarter warp fall in distinct banks.
         if (ok) {
-            const float *qraw = reinterpret_cast<const float *>(smem + Cfg::kOffP) + (head_ok ? h : 0) * D;
+            const float *qraw = reinterpret_cast<const float *>(smem + Cfg::kOffP) + (slot_ok ? slot : 0) * D;
             for (int pn = g; pn < PANELS; pn += 2) {
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
-                    const int cc = (c8 + h) & 7;
+                    const int cc = (c8 + slot) & 7;
                     float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-                    if (head_ok) {
+                    if (slot_ok) {
                         x0 = *reinterpret_cast<const float4 *>(qraw + pn * 64 + cc * 8);
                         x1 = *reinterpret_cast<const float4 *>(qraw + pn * 64 + cc * 8 + 4);
                     }
@@ -317,7 +355,7 @@ __global__ void __launch_bounds__(352, 1)
         const int r_hi = r & ~1, r_lo = r | 1;
         // The chunk's last page may end inside the sequence's last block: its V rows past
         // the end hold whatever the slots hold (NaN, Inf) and must be zero for P.V.
-        const int tail_valid = tok_end - (sp.pfirst + pg1 - 1) * BS;   // 1..BS tokens
+        const int tail_valid = tok_end - (apg1 - 1) * BS;   // 1..BS tokens
         const int tail_tile = (pages - 1) / PPT;
         const int tail_row0 = ((pages - 1) % PPT) * BS + tail_valid;
         const int tail_rows = BS - tail_valid;
@@ -355,22 +393,23 @@ __global__ void __launch_bounds__(352, 1)
                 sc[c] = mine + __shfl_xor_sync(kFullMask, send, 1);
             }
             const int key0 = tok0 + j * BN + part * 32;
-            if (tok0 + (j + 1) * BN > tok_end || tok0 + j * BN < tok_lo) {
-                // the chunk's last tile (keys past the end) or a tile starting before
-                // the window
+            if (tok0 + j * BN < lo_r || tok0 + (j + 1) * BN > hi_r) {
+                // keys outside this row's [lo_r, hi_r): before its window, after its own
+                // position (causal), or past the end of the chunk
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
-                    if (key0 + c >= tok_end || key0 + c < tok_lo) sc[c] = -INFINITY;
+                    if (key0 + c < lo_r || key0 + c >= hi_r) sc[c] = -INFINITY;
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
             float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1)) * p.scale_log2;
+            // a row that has seen no key yet keeps m = -inf and weight 0
             const float m_new = mx > m_ref + 8.f ? mx : m_ref;
-            const float alpha = ex2_approx(m_ref - m_new);
+            const float alpha = m_new == m_ref ? 1.f : ex2_approx(m_ref - m_new);
             m_ref = m_new;
-            const float neg_m = -m_ref;
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
             float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -425,10 +464,12 @@ __global__ void __launch_bounds__(352, 1)
         const int o = 1 - g;
         const bool good = ok && xch[(o * 3 + 2) * BM + r] != 0.f;   // warp-uniform
         const float m_o = xch[(o * 3 + 0) * BM + r], l_o = xch[(o * 3 + 1) * BM + r];
-        const float M = fmaxf(m_ref, m_o);                 // finite: group 0 has a tile
-        const float f = ex2_approx(m_ref - M), f_o = ex2_approx(m_o - M);
+        // M = -inf: the row sees no key of this chunk (an empty partial)
+        const float M = fmaxf(m_ref, m_o);
+        const bool empty = M == -INFINITY;
+        const float f = empty ? 0.f : ex2_approx(m_ref - M), f_o = empty ? 0.f : ex2_approx(m_o - M);
         const float L = f * l_pair + f_o * l_o;
-        const float scale = f / L;
+        const float scale = empty ? 0.f : f / L;
         float *stage = reinterpret_cast<float *>(smem + Cfg::kOffK) + r * Cfg::kStageRow;
         const int njj1 = ntiles / 2;
         if (g == 1 && good && njj1 > 0) {
@@ -449,10 +490,10 @@ __global__ void __launch_bounds__(352, 1)
         named_barrier(1, 256);
         if (g == 0 && good) {
             tc_fence_after_sync();
-            const size_t bi = bi_group + h;
+            const size_t bi = row_of(slot_ok ? slot : 0);
             float *dst = nc == 1 ? p.out + bi * D : p.ws_o + (bi * p.splits + split) * D;
-            // O[2h] + O[2h+1] over both groups; lane 2h writes the first half of the
-            // columns, 2h+1 the second
+            // O[2s] + O[2s+1] over both groups; lane 2s writes the first half of the
+            // columns, 2s+1 the second
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t ov[32];
@@ -470,15 +511,15 @@ __global__ void __launch_bounds__(352, 1)
                 }
 #pragma unroll
                 for (int e = 0; e < 32; ++e) sum[e] += __shfl_xor_sync(kFullMask, sum[e], 1);
-                if (head_ok && (cc < D / 64) == (part == 0)) {
+                if (slot_ok && (cc < D / 64) == (part == 0)) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4 *>(dst + cc * 32 + e) =
                             make_float4(sum[e], sum[e + 1], sum[e + 2], sum[e + 3]);
                 }
             }
-            if (head_ok && part == 0) {
-                const float lse2 = M + log2f(L);
+            if (slot_ok && part == 0) {
+                const float lse2 = empty ? -INFINITY : M + log2f(L);
                 if (nc == 1) {
                     if (p.lse != nullptr) p.lse[bi] = lse2 * kDecLn2;
                 } else {
