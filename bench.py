@@ -548,8 +548,8 @@ def bench_ours(args):
         files = ["decode.cu", "decode_kparams.cuh", "decode_epilogue.cuh", "common.cuh"]
         if wl.fp8:
             files.append("decode_fp8.cu")
-        elif wl.spec.q_heads // wl.spec.kv_heads > 8:
-            files.append("decode_umma.cu")      # the tcgen05 large-group kernel
+        elif wl.spec.q_heads // wl.spec.kv_heads > 8 or wl.qlen > 1:
+            files.append("decode_umma.cu")      # the tcgen05 kernel (large groups, query rows)
         src = kernel_source_hash(files)
         traffic = profiled_traffic(f"decode_{args.workload}.md", src)
         res.update({
