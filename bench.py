@@ -126,6 +126,22 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time: each rank contributes its own and all receive the max."""
+    if not torch.distributed.is_available() or not torch.distributed.is_initialized() or \
+            torch.distributed.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Units all ranks processed (independent replicas: weak scaling) per second of the
+    slowest rank."""
+    return units_per_rank * world / (max_ms / 1e3)
+
+
 # ------------------------------------------------------------------ workloads
 
 class DecodeWorkload:
@@ -530,19 +546,14 @@ def bench_ours(args):
     kernel_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error during the timed region")
-    max_ms = elapsed_ms
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        max_ms = float(t.item())
+    max_ms = max_over_ranks(elapsed_ms, device)
 
     hbm, bf16, bf16_sus, peak_kind = peaks()
     ms_per_step = max_ms / args.steps
     res = {"metric": METRIC, "impl": "ours"}
     if is_decode:
         step_bytes = [wl.kv_bytes((first + k) % wl.cycle) for k in range(args.steps)]
-        total_bytes = sum(step_bytes) * world
-        value = total_bytes / (max_ms / 1e3) / 1e9
+        value = whole_job_rate(sum(step_bytes), world, max_ms) / 1e9
         kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
         achieved = (sum(step_bytes) / len(step_bytes)) / (kern_avg_ms / 1e3) / 1e9
         files = ["decode.cu", "decode_kparams.cuh", "decode_epilogue.cuh", "common.cuh"]
@@ -565,7 +576,7 @@ def bench_ours(args):
         })
     else:
         flops = wl.flops()
-        value = flops * world * args.steps / (max_ms / 1e3) / 1e12
+        value = whole_job_rate(flops * args.steps, world, max_ms) / 1e12
         kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
         achieved = flops / (kern_avg_ms / 1e3) / 1e12
         src = kernel_source_hash(["prefill.cu", "common.cuh"])
@@ -601,11 +612,7 @@ def bench_ours(args):
         wl.e2e_steps(first, args.steps)
         e_stop.record(stream)
         torch.cuda.synchronize()
-        e_ms = e_start.elapsed_time(e_stop)
-        if world > 1:
-            t = torch.tensor([e_ms], device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_start.elapsed_time(e_stop), device)
         # the last step's output, as it reached host memory, equals the same step run eagerly
         last_c, last_buf = (first + args.steps - 1) % wl.cycle, (args.steps - 1) % 2
         wl.append(last_c)
@@ -613,7 +620,7 @@ def bench_ours(args):
         if not torch.equal(wl.out_h[last_buf], wl.out.cpu()):
             raise RuntimeError("end-to-end output differs from the eager step")
         h2d, d2h = wl.e2e_bytes()
-        res["e2e"] = {"value": sum(step_bytes) * world / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+        res["e2e"] = {"value": whole_job_rate(sum(step_bytes), world, e_ms) / 1e9, "unit": "GB/s",
                       "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h,
                       "path": "public API calls (kv_append, paged_decode_attention) replayed as one "
