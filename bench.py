@@ -153,6 +153,7 @@ class DecodeWorkload:
         self.window = window   # > 0: sliding window of this many tokens
         self.fp8 = fp8         # E4M3 codes + one fp32 scale per cached row
         self.qlen = qlen       # new tokens per sequence per step, all verified at once
+        self.copies = None     # copy-on-write block pairs run before each step's appends
 
     # bytes of K and V read by one step c of the cycle (every visible cached token, every
     # KV head; FP8: the code bytes and the row's 4-byte scale)
@@ -193,6 +194,11 @@ class DecodeWorkload:
                 step.append(sl)
             slots.append(torch.tensor(step, dtype=torch.int64).t().reshape(-1))
             clens.append(bm.context_lens(range(s.batch)))
+        self._finish_setup(device, pkv, bm, nb, slots, clens)
+
+    def _finish_setup(self, device, pkv, bm, nb, slots, clens):
+        s = self.spec
+        bs = s.block_size
         self.nb = nb
         self.released_blocks = 0
         if self.window > 0:
@@ -287,6 +293,8 @@ class DecodeWorkload:
         self.cache_append(self.k_new[c], self.v_new[c], self.slots[c])
 
     def cache_append(self, k_new, v_new, slots):
+        if self.copies is not None:   # copy-on-write of shared blocks before the writes
+            self.pkv.kv_block_copy(self.k_cache, self.v_cache, self.copies)
         if self.fp8:
             self.pkv.kv_append_fp8(k_new, v_new, self.k_cache, self.v_cache, self.k_scale, self.v_scale, slots)
         else:
@@ -394,6 +402,67 @@ class DecodeWorkload:
         return run, threads
 
 
+class MixWorkload(DecodeWorkload):
+    """Continuous-batching mix: 256 sequences with lognormal lengths; sequences 0..63 share
+    one 4096-token prefix and form 32 fork pairs that share their whole history, so the
+    step's appends first copy each pair's shared partial last block (copy-on-write)."""
+
+    def __init__(self):
+        super().__init__(gen.MIX, gen.mix_lengths(), 1,
+                         "continuous-batching mix: batch 256, 32 q / 8 kv heads, d 128, lognormal lengths "
+                         "(median 1024, sigma 1, [16, 32768]); 64 sequences share a 4096-token prefix as "
+                         "32 fork pairs, copy-on-write before the appends, bs 16, bf16 KV")
+
+    def kv_bytes(self, c):
+        # logical bytes: every sequence's tokens, shared or not (after this step's append)
+        return sum(n + 1 for n in self.lengths) * self.spec.kv_heads * self.spec.head_dim * 2 * 2
+
+    def setup(self, device):
+        import paged_kv_cache_165_gb300 as pkv
+        s = self.spec
+        bs, B = s.block_size, s.batch
+        P, S = gen.MIX_PREFIX_TOKENS, gen.MIX_PREFIX_SEQS
+        unique = P + sum(n - (P if b < S else 0) for b, n in enumerate(self.lengths)
+                         if not (b < S and b % 2 == 1))
+        nb = gen.blocks_needed(unique, bs) + 2 * B + 64
+        bm = pkv.BlockManager(nb, bs, order=gen.permutation(gen.generator(s.seed), nb))
+        root = B                                    # the shared prefix, outside the batch
+        bm.add_sequence(root, P)
+        for b, n in enumerate(self.lengths):
+            if b < S and b % 2 == 1:
+                bm.fork(b - 1, b)                   # the pair shares its whole history
+                continue
+            if b < S:
+                bm.fork(root, b)
+                start = P
+            else:
+                bm.add_sequence(b, 0)
+                start = 0
+            for _ in range(start, n):
+                bm.append_slot(b)
+        bm.free_sequence(root)
+        sl, copies = bm.append_step(range(B))
+        bm.audit()
+        # bytes of the distinct blocks read (the shared prefix and pair histories once)
+        used = {}
+        for b in range(B):
+            n = bm.lengths[b]
+            for j, blk in enumerate(bm.tables[b]):
+                used[blk] = max(used.get(blk, 0), min(bs, n - j * bs))
+        self.unique_bytes = sum(used.values()) * s.kv_heads * s.head_dim * 2 * 2
+        self.n_copies = len(copies)
+        self._finish_setup(device, pkv, bm, nb, [torch.tensor(sl, dtype=torch.int64)],
+                           [bm.context_lens(range(B))])
+        self.copies = torch.tensor(copies, dtype=torch.int32, device=device)
+        self.launches_per_step += 1                 # kv_block_copy
+
+    def describe(self):
+        d = super().describe()
+        d.update({"cow_copies_per_step": getattr(self, "n_copies", None),
+                  "unique_gb_per_step": getattr(self, "unique_bytes", 0) / 1e9})
+        return d
+
+
 class PrefillWorkload:
     """Varlen causal prefill of 8 prompts (lengths uniform in [256, 4096]) writing the cache."""
 
@@ -456,6 +525,7 @@ WORKLOADS = {
                                       "llama2-70b-shaped GQA verification step: batch 64, 64 q / 8 kv heads, "
                                       "d 128, lengths U[512,8192], 4 new tokens per sequence appended and "
                                       "attended causally, bs 16, bf16 KV", qlen=4),
+    "mix": MixWorkload,
     "swa": lambda: DecodeWorkload(gen.SWA, [gen.SWA_LENGTH] * gen.SWA.batch, 1,
                                   "mistral-7b-shaped sliding-window decode: batch 64, 32 q / 8 kv heads, d 128, "
                                   "16384 cached tokens, window 4096 (blocks outside released), bs 16, bf16 KV",
@@ -566,6 +636,8 @@ def bench_ours(args):
         res.update({
             "value": value, "unit": "GB/s", "pct_hbm_peak": 100 * value / hbm,
             "tokens_per_s_per_layer": wl.spec.batch * wl.qlen * world / (ms_per_step / 1e3),
+            **({"unique_gb_per_s": whole_job_rate(wl.unique_bytes * args.steps, world, max_ms) / 1e9}
+               if hasattr(wl, "unique_bytes") else {}),
             "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (split-K partials + LSE merge)",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"

@@ -209,6 +209,16 @@ class MixLayout:
     v_new: torch.Tensor
 
 
+def mix_lengths(spec: DecodeSpec = MIX, prefix_tokens: int = MIX_PREFIX_TOKENS,
+                prefix_seqs: int = MIX_PREFIX_SEQS) -> List[int]:
+    """The lengths mix_layout draws (its generator's first draws), without the tokens."""
+    lengths = lognormal_lengths(generator(spec.seed), spec.batch, MIX_MEDIAN, MIX_SIGMA, *MIX_CLIP)
+    prefix_seqs = min(prefix_seqs, spec.batch - (spec.batch % 2))
+    for k in range(0, prefix_seqs, 2):
+        lengths[k] = lengths[k + 1] = min(prefix_tokens + lengths[k], MIX_CLIP[1])
+    return lengths
+
+
 def mix_layout(spec: DecodeSpec = MIX, batch: int | None = None,
                prefix_tokens: int = MIX_PREFIX_TOKENS, prefix_seqs: int = MIX_PREFIX_SEQS,
                median: float = MIX_MEDIAN, clip=MIX_CLIP) -> MixLayout:
