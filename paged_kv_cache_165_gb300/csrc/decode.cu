@@ -645,18 +645,21 @@ __global__ void __launch_bounds__(32)
 
 // ==================================================================== LSE merge
 
-// One block of 128 threads per (sequence, query head): lse = log2 sum_c 2^{lse_c} and
+// One block of 256 threads per (sequence, query head): lse = log2 sum_c 2^{lse_c} and
 // out = sum_c 2^{lse_c - lse} o_c over the chunks that hold tokens.  The chunk weights
-// are computed in parallel into shared memory; each thread then sums one column over the
-// chunks with independent, coalesced loads.  Sequences with at most one chunk were
-// written directly by the attention kernel.
-constexpr int kMergeThreads = 128;
+// are computed in parallel into shared memory.  The threads then form G groups of d/4
+// (d/1 when d is not a multiple of 4) threads; group k sums chunks k, k+G, ... of its
+// columns, so each thread has nc/G independent row loads in flight rather than a chain
+// of nc/4, and the G partial sums are added through shared memory.  Sequences with at
+// most one chunk were written directly by the attention kernel.
+constexpr int kMergeThreads = 256;
 constexpr int kMergeMaxChunks = 4096;
 
 __global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const DecodeKParams p, int d, int bs) {
     __shared__ float w[kMergeMaxChunks];
     __shared__ float red[kMergeThreads / 32];
+    __shared__ __align__(16) float part[4 * kMergeThreads];   // G x d partial sums, G * d <= 1024
     const size_t bi = blockIdx.x;
     const int b = static_cast<int>(bi / p.Hq);
     const int n_pages = row_span(p, b, bs, false).cnpages;
@@ -691,17 +694,44 @@ __global__ void __launch_bounds__(kMergeThreads)
     for (int i = 0; i < kMergeThreads / 32; ++i) L += red[i];
     const float il = 1.f / L;
     const float *po = p.ws_o + bi * p.splits * d;
-    for (int e = tid; e < d; e += kMergeThreads) {
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-        int c = 0;
-        for (; c + 4 <= nc; c += 4) {
-            acc0 += w[c] * po[static_cast<size_t>(c) * d + e];
-            acc1 += w[c + 1] * po[static_cast<size_t>(c + 1) * d + e];
-            acc2 += w[c + 2] * po[static_cast<size_t>(c + 2) * d + e];
-            acc3 += w[c + 3] * po[static_cast<size_t>(c + 3) * d + e];
+    const bool vec = d % 4 == 0 && (reinterpret_cast<uintptr_t>(p.ws_o) & 15) == 0;
+    const int width = vec ? d / 4 : d;          // threads per group (d <= 256)
+    const int G = kMergeThreads / width;        // groups
+    const int grp = tid / width, col = tid % width;
+    if (grp < G) {
+        if (vec) {
+            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+            int c = grp;
+            for (; c + G < nc; c += 2 * G) {
+                const float4 x = *reinterpret_cast<const float4 *>(po + static_cast<size_t>(c) * d + 4 * col);
+                const float4 y = *reinterpret_cast<const float4 *>(po + static_cast<size_t>(c + G) * d + 4 * col);
+                const float wx = w[c], wy = w[c + G];
+                a0.x += wx * x.x; a0.y += wx * x.y; a0.z += wx * x.z; a0.w += wx * x.w;
+                a1.x += wy * y.x; a1.y += wy * y.y; a1.z += wy * y.z; a1.w += wy * y.w;
+            }
+            if (c < nc) {
+                const float4 x = *reinterpret_cast<const float4 *>(po + static_cast<size_t>(c) * d + 4 * col);
+                const float wx = w[c];
+                a0.x += wx * x.x; a0.y += wx * x.y; a0.z += wx * x.z; a0.w += wx * x.w;
+            }
+            *reinterpret_cast<float4 *>(part + grp * d + 4 * col) =
+                make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+        } else {
+            float a0 = 0.f, a1 = 0.f;
+            int c = grp;
+            for (; c + G < nc; c += 2 * G) {
+                a0 += w[c] * po[static_cast<size_t>(c) * d + col];
+                a1 += w[c + G] * po[static_cast<size_t>(c + G) * d + col];
+            }
+            if (c < nc) a0 += w[c] * po[static_cast<size_t>(c) * d + col];
+            part[grp * d + col] = a0 + a1;
         }
-        for (; c < nc; ++c) acc0 += w[c] * po[static_cast<size_t>(c) * d + e];
-        p.out[bi * d + e] = ((acc0 + acc1) + (acc2 + acc3)) * il;
+    }
+    __syncthreads();
+    for (int e = tid; e < d; e += kMergeThreads) {
+        float acc = 0.f;
+        for (int k = 0; k < G; ++k) acc += part[k * d + e];
+        p.out[bi * d + e] = acc * il;
     }
     if (tid == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
 }
@@ -801,7 +831,7 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
     if (plan.umma) {
         // one CTA per (sequence, KV head, chunk) and SM, one wave: the start of a block
         // (queries, first copies) and its end are paid once per SM; chunks of whole
-        // 64-key tiles
+        // 128-key tiles
         const int ppt = kUmmaDecodeKeys / bs;
         if (num_splits == 0) {
             const long long gunits = static_cast<long long>(B) * Hkv * plan.qtiles;

@@ -101,7 +101,7 @@ __device__ __forceinline__ SeqSpan row_span(const DecodeKParams &p, int r, int b
 
 // Large-group decode on tcgen05 (decode_umma.cu): d in {64, 128}, bs in {16, 32},
 // grid (chunks, Hkv, B).  Key tiles hold this many tokens.
-constexpr int kUmmaDecodeKeys = 64;
+constexpr int kUmmaDecodeKeys = 128;
 
 cudaError_t launch_decode_umma(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv,
                                int d, int bs, dim3 grid, cudaStream_t stream);

@@ -8,32 +8,35 @@
 // with the online softmax of plumephp.com §2.2-§2.3 and log-sum-exp partials per chunk.
 //
 // With m heads sharing every K/V page the page math is a real contraction: S = Q K^T
-// with M = 2m rows.  One CTA per (sequence, KV head, chunk of blocks) and SM, 11 warps:
-//   warps 9 and 10 (TMA): warp 9 first the group's fp32 queries (one bulk copy), then the
-//     K pages of each 64-key tile into a ring of shared stages; warp 10 the V pages into a
-//     second ring (one {64, bs} box per page and 64-column panel, 128-byte swizzle, one
-//     lane per page).  A K stage is free once its scores are computed, a V stage once its
-//     P.V is, so K runs ahead of V by the two tiles in softmax.  A page past the chunk
-//     is placed outside the cache, where TMA fills zeros.
-//   warp 8 (one lane issues): S_j = Q K_j^T (M = 128, N = 64) into tensor memory, and
-//     O += P_j V_j (M = 128, N = d) into a tensor-memory O.
-//   warps 0-3 and 4-7: two softmax groups taking the tiles in turn (tile j goes to group
-//     j % 2), each with its own S buffers, P buffer, O and online-softmax state, so one
-//     group's exponentials overlap the other's hand-offs with the tensor core.  Thread r
-//     of a group owns row r of the 128-row tile.  Row 2h holds the bf16 rounding of head
-//     h's fp32 query ("hi"), row 2h+1 the bf16 rounding of the remainder ("lo"), so
-//     s = S[2h] + S[2h+1] carries q to about 2^-16 relative.  The two rows sit in lanes
-//     2h and 2h+1 of one warp: each lane takes half of the tile's 64 keys, receives the
-//     partner row's values for its half by one shuffle per key, and runs the online
-//     softmax for its half (the running max is shared by one more shuffle).  The weights
-//     P go back to shared memory as hi (row 2h) and lo (row 2h+1) bf16 parts, so
-//     O[2h] + O[2h+1] = sum_t P_t V_t to about 2^-16 relative as well.  O rows are
-//     rescaled in tensor memory only when the running max grew by more than 2^8.
-// At the end the two groups' (max, sum, O) merge by log-sum-exp inside the CTA; a chunk
-// then writes a normalised partial and its base-2 log-sum-exp into the workspace, merged
-// by the merge kernel of decode.cu.  Every wait is bounded and shares an abort flag: on a
-// timeout the block drains the copies and MMAs it issued, frees tensor memory and returns
-// with PKV_DEVERR_TIMEOUT.
+// with M = 2m rows.  One CTA per (sequence, KV head, chunk of blocks) and SM, 11 warps,
+// key tiles of 128 tokens:
+//   warps 9 and 10 (TMA): the K and the V pages of each tile into two rings of tile
+//     slots (one {64, bs} box per page and 64-column panel, 128-byte swizzle, one box per
+//     lane: copies issued by different threads proceed in parallel, one thread's copies
+//     largely one after another).  A K slot is free once its scores are computed, a V
+//     slot once its P.V is.  A page past the chunk is placed outside the cache, where TMA
+//     fills zeros.
+//   warp 8 (one lane issues): S_j = Q K_j^T (M = 128, N = 128) into one of two tensor-
+//     memory S buffers, and O += P_j V_j (N = d) into a tensor-memory O.  Q and P are the
+//     A operands and live in tensor memory; K and V are read from shared memory.  The
+//     issue order is P_j V_j, then S_{j+2} into the buffer S_j leaves (P_j being written
+//     means S_j has been read), so the tensor core works on the next scores while the
+//     softmax runs.
+//   warps 0-7 (softmax): row r of the 128-row tile is tensor-memory lane r, shared by
+//     warps w and w+4 (w = r / 32); warp half h = w / 4 takes keys 64h .. 64h+63 of each
+//     tile.  Row 2s holds the bf16 rounding of query slot s ("hi"), row 2s+1 the bf16
+//     rounding of the remainder ("lo"), so s = S[2s] + S[2s+1] carries q to about 2^-16
+//     relative.  The two rows sit in lanes 2s and 2s+1 of a warp: each lane takes half of
+//     its warp's 64 keys and receives the partner row's values for them by one shuffle per
+//     key; the row maximum is shared by a shuffle and, between the two warps, through
+//     shared memory.  The weights go back to tensor memory as hi (row 2s) and lo (row 2s+1)
+//     bf16 parts, so O[2s] + O[2s+1] = sum_t P_t V_t to about 2^-16 relative as well.  O
+//     rows are rescaled in tensor memory only when the running maximum grew by more than
+//     2^8.
+// A chunk writes a normalised partial and its base-2 log-sum-exp into the workspace,
+// merged by the merge kernel of decode.cu (or, for a single chunk, the output).  Every wait
+// is bounded and shares an abort flag: on a timeout the block drains the copies and MMAs
+// it issued, frees tensor memory and returns with PKV_DEVERR_TIMEOUT.
 #include <math.h>
 
 #include "common.cuh"
@@ -45,49 +48,39 @@ namespace {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <int D, int BS, int NK, int NV>
+template <int D, int BS, int NKT, int NVT>
 struct UmmaDecodeCfg {
-    static constexpr int kBM = 128, kBN = kUmmaDecodeKeys, kPPT = kBN / BS;   // pages per tile
+    static constexpr int kBM = 128, kTK = kUmmaDecodeKeys, kPPT = kTK / BS;   // pages per tile
     static constexpr int PANELS = D / 64;
-    static constexpr int kQBytes = kBM * D * 2;     // Q hi/lo rows: D/64 panels of [128][128 B]
-    static constexpr int kKVBytes = kBN * D * 2;    // one K or V tile: D/64 panels of [64][128 B]
-    static constexpr int kPBytes = kBM * kBN * 2;   // P hi/lo rows [128][64] bf16: one panel
-    static constexpr int kOffK = kQBytes;           // K ring, NK stages
-    static constexpr int kOffV = kOffK + NK * kKVBytes;        // V ring, NV stages
-    static constexpr int kOffP = kOffV + NV * kKVBytes;        // P of group g; first the raw fp32 q
-    static constexpr int kOffBar = kOffP + 2 * kPBytes;
-    // barriers: raw q; Q; K full / free per K stage; V full / free per V stage; per group:
-    // S full x2, S free x2, P full, O done
-    static constexpr int kQRaw = 0, kQ = 1, kKFull = 2, kKFree = 2 + NK, kVFull = 2 + 2 * NK,
-                         kVFree = 2 + 2 * NK + NV, kGroup0 = 2 + 2 * NK + 2 * NV;
-    static constexpr int kDrain = kGroup0 + 12;   // completes once every MMA issued is done
-    static constexpr int kNumBars = kGroup0 + 13;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;     // TMEM slot, abort flag
-    static constexpr int kOffXch = (kOffMisc + 16 + 15) / 16 * 16;   // [group][m, l, ok][128]
-    static constexpr int kSmemBytes = 1024 + kOffXch + 2 * 3 * kBM * 4;
-    static constexpr int kTmemCols = 512;           // per group: S 2 x 64 columns, O D columns
-    static constexpr int kGroupCols = 256;
-    static constexpr int kSCol = 0, kOCol = 2 * kBN;
-    static constexpr int kStageRow = D + 4;         // fp32 row stride of the O staging area
+    static constexpr int kSlotBytes = kTK * D * 2;   // one K or V tile: D/64 panels of [128][128 B]
+    static constexpr int kOffK = 0;                  // K ring, NKT tile slots
+    static constexpr int kOffV = kOffK + NKT * kSlotBytes;    // V ring, NVT tile slots
+    static constexpr int kOffBar = kOffV + NVT * kSlotBytes;
+    // barriers: Q built; K full / free per slot; V full / free per slot; S full x2; P full;
+    // O done (after each P.V); all MMAs done; drain
+    static constexpr int kQ = 0, kKFull = 1, kKFree = 1 + NKT, kVFull = 1 + 2 * NKT, kVFree = 1 + 2 * NKT + NVT,
+                         kSFull = 1 + 2 * NKT + 2 * NVT, kPFull = kSFull + 2, kODone = kPFull + 1,
+                         kDone = kODone + 1, kDrain = kDone + 1, kNumBars = kDrain + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;          // TMEM slot, abort flag
+    static constexpr int kOffXch = (kOffMisc + 16 + 15) / 16 * 16;   // [warp half][value, ok][128]
+    static constexpr int kSmemBytes = 1024 + kOffXch + 4 * kBM * 4;
+    // tensor memory: two S buffers, O, P, Q
+    static constexpr int kTmemCols = 512;
+    static constexpr int kSCol = 0, kOCol = 2 * kTK, kPCol = kOCol + D, kQCol = kPCol + kTK / 2;
     static constexpr int kThreads = 352;
-    static constexpr int s_full(int g, int b) { return kGroup0 + g * 6 + b; }
-    static constexpr int s_free(int g, int b) { return kGroup0 + g * 6 + 2 + b; }
-    static constexpr int p_full(int g) { return kGroup0 + g * 6 + 4; }
-    static constexpr int o_done(int g) { return kGroup0 + g * 6 + 5; }
     static_assert(D == 64 || D == 128, "head size");
     static_assert(BS == 16 || BS == 32, "block size");
-    static_assert(kOCol + D <= kGroupCols, "tensor memory budget");
-    static_assert(64 * D * 4 <= 2 * kPBytes, "raw queries fit the P buffers");
-    static_assert(kBM * kStageRow * 4 <= NK * kKVBytes, "O staging fits the K ring");
+    static_assert(kQCol + D / 2 <= kTmemCols, "tensor memory budget");
+    static_assert(kPPT * PANELS <= 32 && 32 % kPPT == 0, "one box per loader lane; tiles within 32 pages");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int D, int BS, int NK, int NV>
+template <int D, int BS, int NKT, int NVT>
 __global__ void __launch_bounds__(352, 1)
     decode_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const DecodeKParams p) {
-    using Cfg = UmmaDecodeCfg<D, BS, NK, NV>;
-    constexpr int BM = Cfg::kBM, BN = Cfg::kBN, PPT = Cfg::kPPT, PANELS = Cfg::PANELS;
+    using Cfg = UmmaDecodeCfg<D, BS, NKT, NVT>;
+    constexpr int BM = Cfg::kBM, TK = Cfg::kTK, PPT = Cfg::kPPT, PANELS = Cfg::PANELS;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -124,7 +117,6 @@ __global__ void __launch_bounds__(352, 1)
     const int cpfirst = lo_seq / BS, cnpages = L > 0 ? (L + BS - 1) / BS - cpfirst : 0;
     const int nc = (cnpages + p.chunk_pages - 1) / p.chunk_pages;
     const int lo_tile = p.window > 0 ? max(0, P0 + 1 - p.window) : 0;    // first query's window
-    const int lo_last = p.window > 0 ? max(0, P0 + nqt - p.window) : 0;   // last query's window
     const int hi_tile = P0 + nqt;                                         // one past the last query
     const int cp0 = cpfirst + split * p.chunk_pages;                      // this chunk's pages
     const int cp1 = min(cpfirst + cnpages, cp0 + p.chunk_pages);
@@ -146,33 +138,27 @@ __global__ void __launch_bounds__(352, 1)
         for (int sl = threadIdx.x; sl < slots; sl += blockDim.x) p.ws_lse[row_of(sl) * p.splits + split] = -INFINITY;
         return;
     }
-    const int len = L;
     const int pfirst = apg0, pages = apg1 - apg0;
     const int ntiles = (pages + PPT - 1) / PPT;
     const int tok0 = pfirst * BS;                        // first token of the pages read
-    const int tok_lo = max(tok0, lo_tile);               // first key any row sees
     const int tok_end = min(hi_tile, apg1 * BS);         // one past the last key any row sees
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(Cfg::kQRaw), 1);
         mbar_init(bar(Cfg::kQ), 8);
+        for (int s = 0; s < NKT; ++s) {
+            mbar_init(bar(Cfg::kKFull + s), 1);
+            mbar_init(bar(Cfg::kKFree + s), 1);
+        }
+        for (int s = 0; s < NVT; ++s) {
+            mbar_init(bar(Cfg::kVFull + s), 1);
+            mbar_init(bar(Cfg::kVFree + s), 1);
+        }
+        mbar_init(bar(Cfg::kSFull), 1);
+        mbar_init(bar(Cfg::kSFull + 1), 1);
+        mbar_init(bar(Cfg::kPFull), 8);
+        mbar_init(bar(Cfg::kODone), 1);
+        mbar_init(bar(Cfg::kDone), 1);
         mbar_init(bar(Cfg::kDrain), 1);
-        for (int st = 0; st < NK; ++st) {
-            mbar_init(bar(Cfg::kKFull + st), 1);
-            mbar_init(bar(Cfg::kKFree + st), 1);
-        }
-        for (int st = 0; st < NV; ++st) {
-            mbar_init(bar(Cfg::kVFull + st), 1);
-            mbar_init(bar(Cfg::kVFree + st), 1);
-        }
-        for (int g = 0; g < 2; ++g) {
-            for (int sb = 0; sb < 2; ++sb) {
-                mbar_init(bar(Cfg::s_full(g, sb)), 1);
-                mbar_init(bar(Cfg::s_free(g, sb)), 4);
-            }
-            mbar_init(bar(Cfg::p_full(g)), 4);
-            mbar_init(bar(Cfg::o_done(g)), 1);
-        }
         *abort = 0;
         fence_barrier_init();
         tma_prefetch_map(&tm_k);
@@ -183,122 +169,104 @@ __global__ void __launch_bounds__(352, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t sQ = smem_addr(smem);
-    auto sK = [&](int st) { return smem_addr(smem + Cfg::kOffK + st * Cfg::kKVBytes); };
-    auto sV = [&](int st) { return smem_addr(smem + Cfg::kOffV + st * Cfg::kKVBytes); };
-    auto sP = [&](int g) { return smem_addr(smem + Cfg::kOffP + g * Cfg::kPBytes); };
+    auto sK = [&](int s) { return smem_addr(smem + Cfg::kOffK + s * Cfg::kSlotBytes); };
+    auto sV = [&](int s) { return smem_addr(smem + Cfg::kOffV + s * Cfg::kSlotBytes); };
 
     if (warp >= 9) {
-        // ---- TMA loaders: warp 9 the raw queries and the K tiles, warp 10 the V tiles.
-        // Tile t (pages pfirst + t*PPT ...) goes to stage t % N of its ring once the stage's
-        // previous tile is consumed (K: by S_{t-NK}; V: by P_{t-NV} V).
+        // ---- TMA loaders: warp 9 the K tiles, warp 10 the V tiles.  Tile t goes to slot
+        // t % N of its ring once the slot's previous tile is consumed (K: by S_{t-N}; V: by
+        // P_{t-N} V).  Lane i < PPT * PANELS copies panel i % PANELS of page i / PANELS.
         const bool is_k = warp == 9;
-        const int N = is_k ? NK : NV;
+        const int N = is_k ? NKT : NVT;
         const int full0 = is_k ? Cfg::kKFull : Cfg::kVFull, free0 = is_k ? Cfg::kKFree : Cfg::kVFree;
         const CUtensorMap *map = is_k ? &tm_k : &tm_v;
-        if (is_k && lane == 0) {
-            // the m heads of one query row are contiguous: one copy per row of the tile
-            const uint32_t row_bytes = static_cast<uint32_t>(p.m) * D * 4;
-            mbar_arrive_expect_tx(bar(Cfg::kQRaw), row_bytes * nqt);
-            for (int qi = 0; qi < nqt; ++qi)
-                bulk_load(sP(0) + qi * row_bytes, p.q + row_of(qi * p.m) * D, row_bytes, bar(Cfg::kQRaw));
-        }
         const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + pfirst;
         int tcur = lane < pages ? __ldg(tbl + lane) : -1;
         int tbase = 0;
         const int oob_row = p.NB * p.Hkv * BS;
+        const int pg = lane / PANELS, pn = lane % PANELS;
         int t = 0;
         for (; t < ntiles; ++t) {
             bool fr = true;
             if (lane == 0 && t >= N)
                 fr = wait_or_abort(bar(free0 + t % N), ((t - N) / N) & 1, abort, p.err);
             if (!__shfl_sync(kFullMask, fr ? 1 : 0, 0)) break;
-            const int st = t % N;
+            const int s = t % N;
             if (t * PPT >= tbase + 32) {   // a tile never straddles 32 pages (32 % PPT == 0)
                 tbase += 32;
                 tcur = tbase + lane < pages ? __ldg(tbl + tbase + lane) : -1;
             }
-            // lane i < PPT issues the copies of the tile's page i
-            const int k = t * PPT + lane;
+            const int k = t * PPT + pg;
             const int phys = __shfl_sync(kFullMask, tcur, k & 31);
-            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + st), Cfg::kKVBytes);
+            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), Cfg::kSlotBytes);
             __syncwarp();
-            if (lane < PPT) {
+            if (lane < PPT * PANELS) {
                 int row = oob_row;
                 if (k < pages) {
                     if (phys < 0 || phys >= p.NB) {
-                        if (is_k) raise_error(p.err, PKV_DEVERR_BLOCK);
+                        if (is_k && pn == 0) raise_error(p.err, PKV_DEVERR_BLOCK);
                     } else {
                         row = (phys * p.Hkv + kvh) * BS;
                     }
                 }
-                const uint32_t dst = (is_k ? sK(st) : sV(st)) + lane * BS * 128;
-#pragma unroll
-                for (int pn = 0; pn < PANELS; ++pn) tma_load_2d(dst + pn * BN * 128, map, pn * 64, row, bar(full0 + st));
+                const uint32_t dst = (is_k ? sK(s) : sV(s)) + pn * TK * 128 + pg * BS * 128;
+                tma_load_2d(dst, map, pn * 64, row, bar(full0 + s));
             }
         }
         // before teardown every copy issued must have landed (bounded)
-        if (lane == 0) {
-            if (is_k) mbar_wait_bounded(bar(Cfg::kQRaw), 0);
+        if (lane == 0)
             for (int u = max(0, t - N); u < t; ++u) mbar_wait_bounded(bar(full0 + u % N), (u / N) & 1);
-        }
     } else if (warp == 8) {
-        // ---- MMA issue.  Tile j belongs to group j % 2 (its (j/2)-th tile); S_{j+2} goes
-        // out before P_j V_j, so the next tile of a group is scored while it is in softmax.
+        // ---- MMA issue (one lane).  S_0, S_1; then per tile j: P_j V_j, and S_{j+2} into the
+        // S buffer that S_j leaves.
         if (lane == 0) {
-            const uint32_t idesc_s = umma_idesc_bf16(BM, BN, 0);
+            const uint32_t idesc_s = umma_idesc_bf16(BM, TK, 0);
             const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
-            auto issue_s = [&](int j) {
-                const int st = j % NK, g = j & 1, sb = (j >> 1) & 1;
+            auto issue_s = [&](int t) {
+                const int s = t % NKT;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = umma_desc_sw128(sQ + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
-                    const uint64_t bd = umma_desc_sw128(sK(st) + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024);
-                    umma_bf16(tmem + g * Cfg::kGroupCols + Cfg::kSCol + sb * BN, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    const uint64_t bd = umma_desc_sw128(sK(s) + (kk / 4) * TK * 128 + (kk % 4) * 32, 16, 1024);
+                    umma_bf16_ts(tmem + Cfg::kSCol + (t & 1) * TK, tmem + Cfg::kQCol + kk * 8, bd, idesc_s,
+                                 kk > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(Cfg::s_full(g, sb)));
-                umma_commit(bar(Cfg::kKFree + st));
+                umma_commit(bar(Cfg::kSFull + (t & 1)));
+                umma_commit(bar(Cfg::kKFree + s));
             };
             auto issue_pv = [&](int j) {
-                const int st = j % NV, g = j & 1;
+                const int s = j % NVT;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = umma_desc_sw128(sP(g) + kk * 32, 16, 1024);
-                    const uint64_t bd = umma_desc_sw128(sV(st) + kk * 16 * 128, BN * 128, 1024);
-                    umma_bf16(tmem + g * Cfg::kGroupCols + Cfg::kOCol, ad, bd, idesc_o,
-                              (j > 1 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < TK / 16; ++kk) {
+                    const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
+                    umma_bf16_ts(tmem + Cfg::kOCol, tmem + Cfg::kPCol + kk * 8, bd, idesc_o,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(bar(Cfg::o_done(g)));
-                umma_commit(bar(Cfg::kVFree + st));
+                umma_commit(bar(Cfg::kODone));
+                umma_commit(bar(Cfg::kVFree + s));
             };
-            // Tile j belongs to group j % 2 (its (j/2)-th tile).  S_{j+2} goes out before
-            // P_j V_j, so a group's next tile is scored while the group is in softmax.
-            int j = 0;
             bool issued = false, alive = wait_or_abort(bar(Cfg::kQ), 0, abort, p.err);
             for (int t = 0; t < 2 && t < ntiles && alive; ++t) {
-                alive = wait_or_abort(bar(Cfg::kKFull + t), 0, abort, p.err);
+                alive = wait_or_abort(bar(Cfg::kKFull + t % NKT), (t / NKT) & 1, abort, p.err);
                 if (!alive) break;
                 tc_fence_after_sync();
                 issue_s(t);
                 issued = true;
             }
-            for (; j < ntiles && alive; ++j) {
-                const int g = j & 1, t = j + 2;
+            for (int j = 0; j < ntiles && alive; ++j) {
+                alive = wait_or_abort(bar(Cfg::kPFull), j & 1, abort, p.err) &&
+                        wait_or_abort(bar(Cfg::kVFull + j % NVT), (j / NVT) & 1, abort, p.err);
+                if (!alive) break;
+                tc_fence_after_sync();
+                issue_pv(j);
+                const int t = j + 2;
                 if (t < ntiles) {
-                    alive = wait_or_abort(bar(Cfg::kKFull + t % NK), (t / NK) & 1, abort, p.err);
-                    const int tt = t >> 1;   // the group's tile index of t
-                    if (alive && tt >= 2)
-                        alive = wait_or_abort(bar(Cfg::s_free(g, tt & 1)), ((tt >> 1) - 1) & 1, abort, p.err);
+                    alive = wait_or_abort(bar(Cfg::kKFull + t % NKT), (t / NKT) & 1, abort, p.err);
                     if (!alive) break;
                     tc_fence_after_sync();
                     issue_s(t);
                 }
-                alive = wait_or_abort(bar(Cfg::p_full(g)), (j >> 1) & 1, abort, p.err) &&
-                        wait_or_abort(bar(Cfg::kVFull + j % NV), (j / NV) & 1, abort, p.err);
-                if (!alive) break;
-                tc_fence_after_sync();
-                issue_pv(j);
             }
+            if (alive) umma_commit(bar(Cfg::kDone));
             if (*abort && issued) {
                 // let the MMAs already issued finish (bounded) before teardown
                 umma_commit(bar(Cfg::kDrain));
@@ -306,53 +274,44 @@ __global__ void __launch_bounds__(352, 1)
             }
         }
     } else {
-        // ---- softmax group g: thread r owns row r of the tile (TMEM lane r)
-        const int g = warp >> 2;
-        const int r = threadIdx.x & 127;
+        // ---- softmax: thread (w, lane) owns tensor-memory lane r = 32 (w % 4) + lane, keys
+        // 64h .. 64h + 63 of each tile (h = w / 4), of which lane parity `part` takes 32
+        const int h = warp >> 2;
+        const int r = ((warp & 3) << 5) | lane;
         const int slot = r >> 1, part = r & 1;
         const bool slot_ok = slot < slots;
         // this row's query position and visible keys [lo_r, hi_r)
         const int pos_r = P0 + (slot_ok ? slot / p.m : 0);
         const int lo_r = p.window > 0 ? max(0, pos_r + 1 - p.window) : 0;
         const int hi_r = min(pos_r + 1, apg1 * BS);
-        const uint32_t lane_base = tmem + g * Cfg::kGroupCols + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const int njj = (ntiles - g + 1) / 2;   // tiles of this group
-        bool ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kQRaw), 0, abort, p.err));
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4
+        float *xv = xch;                       // [half][128]: maxima, then sums
+        float *xo = xch + 2 * BM;              // [half][128]: the half is still ok
 
-        // Q rows from the raw queries: group g writes panels g, g+2, ...; row 2s = rn(q_s),
-        // row 2s+1 = rn(q_s - rn(q_s)) for slot s, 128-byte swizzle.  Reads are rotated by
-        // s so that the rows read by a quarter warp fall in distinct banks.
-        if (ok) {
-            const float *qraw = reinterpret_cast<const float *>(smem + Cfg::kOffP) + (slot_ok ? slot : 0) * D;
-            for (int pn = g; pn < PANELS; pn += 2) {
+        // Q row r in tensor memory (hi or lo part of slot r/2): warp half h writes d = D/2 h
+        // .. D/2 h + D/2 - 1, i.e. columns D/4 h .. D/4 h + D/4 - 1 (two values a column)
+        {
+            const float *qrow = p.q + row_of(slot_ok ? slot : 0) * D + h * (D / 2);
+            uint32_t w[D / 4];
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    const int cc = (c8 + slot) & 7;
-                    float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-                    if (slot_ok) {
-                        x0 = *reinterpret_cast<const float4 *>(qraw + pn * 64 + cc * 8);
-                        x1 = *reinterpret_cast<const float4 *>(qraw + pn * 64 + cc * 8 + 4);
-                    }
-                    uint32_t w[4], hi, lo;
-                    split_bf16x2(x0.x, x0.y, hi, lo);
-                    w[0] = part ? lo : hi;
-                    split_bf16x2(x0.z, x0.w, hi, lo);
-                    w[1] = part ? lo : hi;
-                    split_bf16x2(x1.x, x1.y, hi, lo);
-                    w[2] = part ? lo : hi;
-                    split_bf16x2(x1.z, x1.w, hi, lo);
-                    w[3] = part ? lo : hi;
-                    *reinterpret_cast<uint4 *>(smem + pn * BM * 128 + r * 128 + ((cc ^ (r & 7)) << 4)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
+            for (int e = 0; e < D / 8; ++e) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (slot_ok) x = __ldg(reinterpret_cast<const float4 *>(qrow + 4 * e));
+                uint32_t hi, lo;
+                split_bf16x2(x.x, x.y, hi, lo);
+                w[2 * e] = part ? lo : hi;
+                split_bf16x2(x.z, x.w, hi, lo);
+                w[2 * e + 1] = part ? lo : hi;
             }
-            fence_proxy_async_smem();
+            if constexpr (D == 128) tmem_st32(lane_base + Cfg::kQCol + h * (D / 4), w);
+            else tmem_st16(lane_base + Cfg::kQCol + h * (D / 4), w);
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Cfg::kQ));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Cfg::kQ));
 
-        uint8_t *pbuf = smem + Cfg::kOffP + g * Cfg::kPBytes;
-        const int r_hi = r & ~1, r_lo = r | 1;
         // The chunk's last page may end inside the sequence's last block: its V rows past
         // the end hold whatever the slots hold (NaN, Inf) and must be zero for P.V.
         const int tail_valid = tok_end - (apg1 - 1) * BS;   // 1..BS tokens
@@ -360,40 +319,44 @@ __global__ void __launch_bounds__(352, 1)
         const int tail_row0 = ((pages - 1) % PPT) * BS + tail_valid;
         const int tail_rows = BS - tail_valid;
         float m_ref = -INFINITY, l = 0.f;
-        for (int jj = 0; jj < njj && ok; ++jj) {
-            const int j = 2 * jj + g, sb = jj & 1;
-            ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::s_full(g, sb)), (jj >> 1) & 1, abort, p.err));
-            if (!ok) break;
-            tc_fence_after_sync();
-            uint32_t sr[BN];
-            tmem_ld32(lane_base + Cfg::kSCol + sb * BN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(lane_base + Cfg::kSCol + sb * BN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Cfg::s_free(g, sb)));
-            if (j == tail_tile && tail_rows > 0) {
-                // once the V copies of this tile have landed
-                ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kVFull + j % NV), (j / NV) & 1, abort, p.err));
-                if (!ok) break;
-                uint8_t *vt = smem + Cfg::kOffV + (j % NV) * Cfg::kKVBytes;
-                for (int idx = r; idx < tail_rows * PANELS * 8; idx += BM) {
-                    const int row = tail_row0 + idx / (PANELS * 8), rem = idx % (PANELS * 8);
-                    *reinterpret_cast<uint4 *>(vt + (rem >> 3) * BN * 128 + row * 128 + (rem & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-            }
-
-            // keys part*32 .. part*32+31 of the tile: own row plus the partner row
+        // ok is warp-uniform, and after each tile's exchange the same in both warps of a
+        // pair: a failed wait skips the remaining work but never a named barrier
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int sb = j & 1;
+            if (ok) ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kSFull + sb), (j >> 1) & 1, abort, p.err));
+            // keys 64h + 32 part .. + 31: own row plus the partner row, by one shuffle a key
             float sc[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float mine = __uint_as_float(part ? sr[32 + c] : sr[c]);
-                const float send = __uint_as_float(part ? sr[c] : sr[32 + c]);
-                sc[c] = mine + __shfl_xor_sync(kFullMask, send, 1);
+            for (int c = 0; c < 32; ++c) sc[c] = -INFINITY;
+            if (ok) {
+                tc_fence_after_sync();
+                uint32_t s0[32], s1[32];
+                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64, s0);
+                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64 + 32, s1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float mine = __uint_as_float(part ? s1[c] : s0[c]);
+                    const float send = __uint_as_float(part ? s0[c] : s1[c]);
+                    sc[c] = mine + __shfl_xor_sync(kFullMask, send, 1);
+                }
             }
-            const int key0 = tok0 + j * BN + part * 32;
-            if (tok0 + j * BN < lo_r || tok0 + (j + 1) * BN > hi_r) {
+            if (ok && j == tail_tile && tail_rows > 0) {
+                // once the V copies of this tile have landed
+                ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kVFull + j % NVT), (j / NVT) & 1, abort, p.err));
+                if (ok) {
+                    uint8_t *vt = smem + Cfg::kOffV + (j % NVT) * Cfg::kSlotBytes;
+                    for (int idx = threadIdx.x; idx < tail_rows * PANELS * 8; idx += 256) {
+                        const int row = tail_row0 + idx / (PANELS * 8), rem = idx % (PANELS * 8);
+                        *reinterpret_cast<uint4 *>(vt + (rem >> 3) * TK * 128 + row * 128 + (rem & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
+            const int key0 = tok0 + j * TK + h * 64 + part * 32;
+            if (tok0 + j * TK < lo_r || tok0 + (j + 1) * TK > hi_r) {
                 // keys outside this row's [lo_r, hi_r): before its window, after its own
                 // position (causal), or past the end of the chunk
 #pragma unroll
@@ -404,7 +367,15 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
             float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1)) * p.scale_log2;
+            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
+            // the other warp half's maximum of this row, and whether it is still ok
+            xv[h * BM + r] = mx;
+            xo[h * BM + r] = ok ? 1.f : 0.f;
+            named_barrier(pair_bar, 64);
+            mx = fmaxf(mx, xv[(1 - h) * BM + r]) * p.scale_log2;
+            ok = ok && xo[(1 - h) * BM + r] != 0.f;
+            named_barrier(pair_bar, 64);   // xch is rewritten next tile
+            if (!ok) continue;
             // a row that has seen no key yet keeps m = -inf and weight 0
             const float m_new = mx > m_ref + 8.f ? mx : m_ref;
             const float alpha = m_new == m_ref ? 1.f : ex2_approx(m_ref - m_new);
@@ -420,106 +391,78 @@ __global__ void __launch_bounds__(352, 1)
             uint32_t phi[16], plo[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) split_bf16x2(sc[2 * e], sc[2 * e + 1], phi[e], plo[e]);
-            // P.V of the group's previous tile must be done: P is free and O is current
-            if (jj > 0) {
-                ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::o_done(g)), (jj - 1) & 1, abort, p.err));
-                if (!ok) break;
+            // P_{j-1} V_{j-1} must be done: the P columns are free and O is current
+            if (j > 0) {
+                ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kODone), (j - 1) & 1, abort, p.err));
+                if (!ok) continue;
                 tc_fence_after_sync();
                 if (__any_sync(kFullMask, alpha != 1.f)) {
+                    // this warp half rescales columns D/2 h .. D/2 h + D/2 - 1 of its rows
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < D / 64; ++cc) {
                         uint32_t ov[32];
-                        tmem_ld32(lane_base + Cfg::kOCol + cc * 32, ov);
+                        tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(lane_base + Cfg::kOCol + cc * 32, ov);
+                        tmem_st32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
                     }
-                    tmem_st_wait();
                 }
             }
-            // P_hi into row 2h, P_lo into row 2h+1, keys part*32 .. part*32+31
+            // row 2s gets P_hi and row 2s+1 P_lo of keys 64h .. 64h + 63 (32 columns): each
+            // lane keeps its own part of its 32 keys and trades the other part for the
+            // partner's
+            uint32_t pw[32];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int c16 = part * 4 + q4;
-                *reinterpret_cast<uint4 *>(pbuf + r_hi * 128 + ((c16 ^ (r_hi & 7)) << 4)) =
-                    make_uint4(phi[4 * q4], phi[4 * q4 + 1], phi[4 * q4 + 2], phi[4 * q4 + 3]);
-                *reinterpret_cast<uint4 *>(pbuf + r_lo * 128 + ((c16 ^ (r_lo & 7)) << 4)) =
-                    make_uint4(plo[4 * q4], plo[4 * q4 + 1], plo[4 * q4 + 2], plo[4 * q4 + 3]);
+            for (int e = 0; e < 16; ++e) {
+                const uint32_t got = __shfl_xor_sync(kFullMask, part ? phi[e] : plo[e], 1);
+                pw[e] = part ? got : phi[e];        // keys 64h + 2e, +1 (part 0's keys)
+                pw[16 + e] = part ? plo[e] : got;   // keys 64h + 32 + 2e, +1 (part 1's keys)
             }
-            fence_proxy_async_smem();
+            tmem_st32(lane_base + Cfg::kPCol + h * 32, pw);
+            tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Cfg::p_full(g)));
+            if (lane == 0) mbar_arrive(bar(Cfg::kPFull));
         }
-        if (ok && njj > 0)
-            ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::o_done(g)), (njj - 1) & 1, abort, p.err));
+        if (ok) ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kDone), 0, abort, p.err));
 
-        // ---- merge the two groups: rows r of both groups hold the same query row
-        const float l_pair = l + __shfl_xor_sync(kFullMask, l, 1);   // the head's sum in this group
-        xch[(g * 3 + 0) * BM + r] = m_ref;
-        xch[(g * 3 + 1) * BM + r] = l_pair;
-        xch[(g * 3 + 2) * BM + r] = ok ? 1.f : 0.f;
-        named_barrier(1, 256);
-        const int o = 1 - g;
-        const bool good = ok && xch[(o * 3 + 2) * BM + r] != 0.f;   // warp-uniform
-        const float m_o = xch[(o * 3 + 0) * BM + r], l_o = xch[(o * 3 + 1) * BM + r];
-        // M = -inf: the row sees no key of this chunk (an empty partial)
-        const float M = fmaxf(m_ref, m_o);
-        const bool empty = M == -INFINITY;
-        const float f = empty ? 0.f : ex2_approx(m_ref - M), f_o = empty ? 0.f : ex2_approx(m_o - M);
-        const float L = f * l_pair + f_o * l_o;
-        const float scale = empty ? 0.f : f / L;
-        float *stage = reinterpret_cast<float *>(smem + Cfg::kOffK) + r * Cfg::kStageRow;
-        const int njj1 = ntiles / 2;
-        if (g == 1 && good && njj1 > 0) {
-            // every MMA is done (both groups saw their last O), so the K ring is free
-            tc_fence_after_sync();
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t ov[32];
-                tmem_ld32(lane_base + Cfg::kOCol + cc * 32, ov);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4 *>(stage + cc * 32 + e) =
-                        make_float4(__uint_as_float(ov[e]) * scale, __uint_as_float(ov[e + 1]) * scale,
-                                    __uint_as_float(ov[e + 2]) * scale, __uint_as_float(ov[e + 3]) * scale);
-            }
-        }
-        named_barrier(1, 256);
-        if (g == 0 && good) {
+        // ---- the row's sum over the four threads that hold it (the loop's last barrier
+        // ended every read of xch); O[2s] + O[2s+1] normalised
+        float lr = l + __shfl_xor_sync(kFullMask, l, 1);
+        xv[h * BM + r] = lr;
+        named_barrier(pair_bar, 64);
+        lr += xv[(1 - h) * BM + r];
+        // m = -inf: the row sees no key of this chunk (an empty partial)
+        const bool empty = m_ref == -INFINITY;
+        const float scale = empty ? 0.f : 1.f / lr;
+        if (ok) {
             tc_fence_after_sync();
             const size_t bi = row_of(slot_ok ? slot : 0);
             float *dst = nc == 1 ? p.out + bi * D : p.ws_o + (bi * p.splits + split) * D;
-            // O[2s] + O[2s+1] over both groups; lane 2s writes the first half of the
-            // columns, 2s+1 the second
+            // this warp half: columns D/2 h .. D/2 h + D/2 - 1, 32 at a time; lane 2s writes
+            // the first 16 of each 32, lane 2s+1 the last 16
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t ov[32];
-                tmem_ld32(lane_base + Cfg::kOCol + cc * 32, ov);
+                tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
                 tmem_ld_wait();
                 float sum[32];
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    float4 s1 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (njj1 > 0) s1 = *reinterpret_cast<const float4 *>(stage + cc * 32 + e);
-                    sum[e] = __uint_as_float(ov[e]) * scale + s1.x;
-                    sum[e + 1] = __uint_as_float(ov[e + 1]) * scale + s1.y;
-                    sum[e + 2] = __uint_as_float(ov[e + 2]) * scale + s1.z;
-                    sum[e + 3] = __uint_as_float(ov[e + 3]) * scale + s1.w;
-                }
+                for (int e = 0; e < 32; ++e) sum[e] = __uint_as_float(ov[e]) * scale;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) sum[e] += __shfl_xor_sync(kFullMask, sum[e], 1);
-                if (slot_ok && (cc < D / 64) == (part == 0)) {
+                if (slot_ok) {
+                    float *o = dst + h * (D / 2) + cc * 32 + part * 16;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(dst + cc * 32 + e) =
-                            make_float4(sum[e], sum[e + 1], sum[e + 2], sum[e + 3]);
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(o + e) =
+                            part ? make_float4(sum[16 + e], sum[17 + e], sum[18 + e], sum[19 + e])
+                                 : make_float4(sum[e], sum[e + 1], sum[e + 2], sum[e + 3]);
                 }
             }
-            if (slot_ok && part == 0) {
-                const float lse2 = empty ? -INFINITY : M + log2f(L);
+            if (slot_ok && part == 0 && h == 0) {
+                const float lse2 = empty ? -INFINITY : m_ref + log2f(lr);
                 if (nc == 1) {
                     if (p.lse != nullptr) p.lse[bi] = lse2 * kDecLn2;
                 } else {
@@ -534,11 +477,11 @@ __global__ void __launch_bounds__(352, 1)
     if (warp == 0) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
-template <int D, int BS, int NK, int NV>
+template <int D, int BS, int NKT, int NVT>
 cudaError_t launch_umma(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
                         cudaStream_t stream) {
-    using Cfg = UmmaDecodeCfg<D, BS, NK, NV>;
-    auto kernel = decode_umma_kernel<D, BS, NK, NV>;
+    using Cfg = UmmaDecodeCfg<D, BS, NKT, NVT>;
+    auto kernel = decode_umma_kernel<D, BS, NKT, NVT>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tk, tv, kp);
@@ -549,10 +492,10 @@ cudaError_t launch_umma(const DecodeKParams &kp, const CUtensorMap &tk, const CU
 
 cudaError_t launch_decode_umma(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv,
                                int d, int bs, dim3 grid, cudaStream_t stream) {
-    if (d == 128) return bs == 16 ? launch_umma<128, 16, 5, 4>(kp, tk, tv, grid, stream)
-                                  : launch_umma<128, 32, 5, 4>(kp, tk, tv, grid, stream);
-    if (d == 64) return bs == 16 ? launch_umma<64, 16, 8, 8>(kp, tk, tv, grid, stream)
-                                 : launch_umma<64, 32, 8, 8>(kp, tk, tv, grid, stream);
+    if (d == 128) return bs == 16 ? launch_umma<128, 16, 3, 3>(kp, tk, tv, grid, stream)
+                                  : launch_umma<128, 32, 3, 3>(kp, tk, tv, grid, stream);
+    if (d == 64) return bs == 16 ? launch_umma<64, 16, 6, 6>(kp, tk, tv, grid, stream)
+                                 : launch_umma<64, 32, 6, 6>(kp, tk, tv, grid, stream);
     return cudaErrorInvalidValue;
 }
 
