@@ -94,6 +94,18 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return true;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// In a grid launched with programmatic stream serialization: wait until the grids it
+// depends on have completed and their memory operations are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the grid that depends on this one to be scheduled now (it still waits in
+// pdl_wait() for this grid to complete).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {

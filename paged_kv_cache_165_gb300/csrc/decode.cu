@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(NW * 32)
     uint8_t *smem = aligned_smem(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kStagesBytes);
 
+    pdl_launch_dependents();   // a merge kernel after this one waits for the whole grid
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     // grid: x = (chunk, head tile) with the tile fastest, y = KV head, z = sequence.  The
@@ -373,6 +374,7 @@ __global__ void __launch_bounds__((GroupCfg<D, BS, ST>::kMaxTiles + 1) * 32, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::kStagesBytes);
     uint64_t *empty = full + ST;
 
+    pdl_launch_dependents();   // the merge kernel after this one waits for the whole grid
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int tiles = p.head_tiles;          // consumer warps; warp `tiles` is the producer
@@ -561,6 +563,7 @@ template <typename T, int J>
 __global__ void __launch_bounds__(32)
     decode_simt_kernel(const T *__restrict__ kc, const T *__restrict__ vc, const DecodeKParams p,
                        int d, int bs) {
+    pdl_launch_dependents();   // the merge kernel after this one waits for the whole grid
     const int lane = threadIdx.x;
     const int row = blockIdx.x, i = blockIdx.y, split = blockIdx.z;
     const int kvh = i / p.m;
@@ -660,6 +663,10 @@ __global__ void __launch_bounds__(kMergeThreads)
     __shared__ float w[kMergeMaxChunks];
     __shared__ float red[kMergeThreads / 32];
     __shared__ __align__(16) float part[4 * kMergeThreads];   // G x d partial sums, G * d <= 1024
+    // Every block waits for the attention kernel before it (launched as its programmatic
+    // dependent) to complete, also one that has nothing to merge: the grid must not end
+    // before that kernel, which work queued after it relies on.
+    pdl_wait();
     const size_t bi = blockIdx.x;
     const int b = static_cast<int>(bi / p.Hq);
     const int n_pages = row_span(p, b, bs, false).cnpages;
@@ -734,6 +741,22 @@ __global__ void __launch_bounds__(kMergeThreads)
         p.out[bi * d + e] = acc * il;
     }
     if (tid == 0 && p.lse != nullptr) p.lse[bi] = (M + log2f(L)) * kLn2;
+}
+
+// The merge as a programmatic dependent of the attention kernel just launched on `stream`:
+// its blocks may be scheduled while the attention kernel drains and wait in pdl_wait().
+cudaError_t launch_merge(const DecodeKParams &kp, int d, int bs, unsigned rows_x_heads, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(rows_x_heads);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel, kp, d, bs);
 }
 
 // ====================================================================== launch
@@ -976,9 +999,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
         if (plan.umma) {
             e = launch_decode_umma(kp, tk, tv, a.d, a.bs, dim3(plan.splits, a.Hkv, a.B * plan.qtiles), stream);
             if (e != cudaSuccess || plan.splits == 1) return e;
-            decode_merge_kernel<<<static_cast<unsigned>(rows * a.Hq), kMergeThreads, 0, stream>>>(
-                kp, a.d, a.bs);
-            return cudaGetLastError();
+            return launch_merge(kp, a.d, a.bs, static_cast<unsigned>(rows * a.Hq), stream);
         }
         if (plan.group) {
             const dim3 ggrid(plan.splits, a.Hkv, a.B);
@@ -992,9 +1013,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
                 else e = launch_group<256, 32, 3>(kp, tk, tv, ggrid, stream);
             }
             if (e != cudaSuccess || plan.splits == 1) return e;
-            decode_merge_kernel<<<static_cast<unsigned>(a.B * a.Hq), kMergeThreads, 0, stream>>>(
-                kp, a.d, a.bs);
-            return cudaGetLastError();
+            return launch_merge(kp, a.d, a.bs, static_cast<unsigned>(a.B * a.Hq), stream);
         }
         const dim3 grid(static_cast<unsigned>(plan.splits) * kp.head_tiles, a.Hkv, a.B);
         if (a.bs == 16) {
@@ -1014,8 +1033,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
                              : launch_simt<uint8_t>(a, kp, grid, stream);
         if (e != cudaSuccess || plan.splits == 1) return e;
     }
-    decode_merge_kernel<<<static_cast<unsigned>(rows * a.Hq), kMergeThreads, 0, stream>>>(kp, a.d, a.bs);
-    return cudaGetLastError();
+    return launch_merge(kp, a.d, a.bs, static_cast<unsigned>(rows * a.Hq), stream);
 }
 
 }  // namespace pkv

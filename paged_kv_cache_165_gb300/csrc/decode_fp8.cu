@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(128, 4)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
 
+    pdl_launch_dependents();   // a merge kernel after this one waits for the whole grid
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int tile = blockIdx.x % p.head_tiles;

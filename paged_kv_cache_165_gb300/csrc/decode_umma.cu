@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(352, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    pdl_launch_dependents();   // the merge kernel may be scheduled; it waits for this grid
     const uint32_t tmem = *tslot;
     auto sK = [&](int s) { return smem_addr(smem + Cfg::kOffK + s * Cfg::kSlotBytes); };
     auto sV = [&](int s) { return smem_addr(smem + Cfg::kOffV + s * Cfg::kSlotBytes); };
