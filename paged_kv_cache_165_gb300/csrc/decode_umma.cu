@@ -8,7 +8,7 @@
 // with the online softmax of plumephp.com §2.2-§2.3 and log-sum-exp partials per chunk.
 //
 // With m heads sharing every K/V page the page math is a real contraction: S = Q K^T
-// with M = 2m rows.  One CTA per (sequence, KV head, chunk of blocks) and SM, 11 warps,
+// with M = 2m rows.  One CTA per (sequence, KV head, chunk of blocks) and SM, 12 warps,
 // key tiles of 128 tokens:
 //   warps 9 and 10 (TMA): the K and the V pages of each tile into two rings of tile
 //     slots (one {64, bs} box per page and 64-column panel, 128-byte swizzle, one box per
@@ -16,12 +16,12 @@
 //     largely one after another).  A K slot is free once its scores are computed, a V
 //     slot once its P.V is.  A page past the chunk is placed outside the cache, where TMA
 //     fills zeros.
-//   warp 8 (one lane issues): S_j = Q K_j^T (M = 128, N = 128) into one of two tensor-
-//     memory S buffers, and O += P_j V_j (N = d) into a tensor-memory O.  Q and P are the
-//     A operands and live in tensor memory; K and V are read from shared memory.  The
-//     issue order is P_j V_j, then S_{j+2} into the buffer S_j leaves (P_j being written
-//     means S_j has been read), so the tensor core works on the next scores while the
-//     softmax runs.
+//   warps 11 and 8 (one lane each issues): S_t = Q K_t^T (M = 128, N = 128) into one of two
+//     tensor-memory S buffers, and O += P_j V_j (N = d) into a tensor-memory O.  Q and P
+//     are the A operands and live in tensor memory; K and V are read from shared memory.
+//     S_t goes into the buffer S_{t-2} leaves once P_{t-2} is written (S_{t-2} has been
+//     read), so the tensor core computes the next scores while the softmax runs; with one
+//     issuer per kind, the waits of one overlap the MMAs of the other.
 //   warps 0-7 (softmax): row r of the 128-row tile is tensor-memory lane r, shared by
 //     warps w and w+4 (w = r / 32); warp half h = w / 4 takes keys 64h .. 64h+63 of each
 //     tile.  Row 2s holds the bf16 rounding of query slot s ("hi"), row 2s+1 the bf16
@@ -57,17 +57,17 @@ struct UmmaDecodeCfg {
     static constexpr int kOffV = kOffK + NKT * kSlotBytes;    // V ring, NVT tile slots
     static constexpr int kOffBar = kOffV + NVT * kSlotBytes;
     // barriers: Q built; K full / free per slot; V full / free per slot; S full x2; P full;
-    // O done (after each P.V); all MMAs done; drain
+    // O done (after each P.V); all MMAs done; drain x2 (one per MMA-issuing thread)
     static constexpr int kQ = 0, kKFull = 1, kKFree = 1 + NKT, kVFull = 1 + 2 * NKT, kVFree = 1 + 2 * NKT + NVT,
                          kSFull = 1 + 2 * NKT + 2 * NVT, kPFull = kSFull + 2, kODone = kPFull + 1,
-                         kDone = kODone + 1, kDrain = kDone + 1, kNumBars = kDrain + 1;
+                         kDone = kODone + 1, kDrain = kDone + 1, kNumBars = kDrain + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;          // TMEM slot, abort flag
     static constexpr int kOffXch = (kOffMisc + 16 + 15) / 16 * 16;   // [warp half][value, ok][128]
     static constexpr int kSmemBytes = 1024 + kOffXch + 4 * kBM * 4;
     // tensor memory: two S buffers, O, P, Q
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 0, kOCol = 2 * kTK, kPCol = kOCol + D, kQCol = kPCol + kTK / 2;
-    static constexpr int kThreads = 352;
+    static constexpr int kThreads = 384;
     static_assert(D == 64 || D == 128, "head size");
     static_assert(BS == 16 || BS == 32, "block size");
     static_assert(kQCol + D / 2 <= kTmemCols, "tensor memory budget");
@@ -76,7 +76,7 @@ struct UmmaDecodeCfg {
 };
 
 template <int D, int BS, int NKT, int NVT>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     decode_umma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const DecodeKParams p) {
     using Cfg = UmmaDecodeCfg<D, BS, NKT, NVT>;
@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(352, 1)
         mbar_init(bar(Cfg::kODone), 1);
         mbar_init(bar(Cfg::kDone), 1);
         mbar_init(bar(Cfg::kDrain), 1);
+        mbar_init(bar(Cfg::kDrain + 1), 1);
         *abort = 0;
         fence_barrier_init();
         tma_prefetch_map(&tm_k);
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(352, 1)
     auto sK = [&](int s) { return smem_addr(smem + Cfg::kOffK + s * Cfg::kSlotBytes); };
     auto sV = [&](int s) { return smem_addr(smem + Cfg::kOffV + s * Cfg::kSlotBytes); };
 
-    if (warp >= 9) {
+    if (warp == 9 || warp == 10) {
         // ---- TMA loaders: warp 9 the K tiles, warp 10 the V tiles.  Tile t goes to slot
         // t % N of its ring once the slot's previous tile is consumed (K: by S_{t-N}; V: by
         // P_{t-N} V).  Lane i < PPT * PANELS copies panel i % PANELS of page i / PANELS.
@@ -217,61 +218,60 @@ __global__ void __launch_bounds__(352, 1)
         // before teardown every copy issued must have landed (bounded)
         if (lane == 0)
             for (int u = max(0, t - N); u < t; ++u) mbar_wait_bounded(bar(full0 + u % N), (u / N) & 1);
-    } else if (warp == 8) {
-        // ---- MMA issue (one lane).  S_0, S_1; then per tile j: P_j V_j, and S_{j+2} into the
-        // S buffer that S_j leaves.
+    } else if (warp == 8 || warp == 11) {
+        // ---- MMA issue, one lane of each of two warps: warp 11 the scores S_t (once K_t has
+        // landed and, for t >= 2, P_{t-2} is written, i.e. S_{t-2} has been read from the
+        // buffer S_t goes to), warp 8 the products P_j V_j.  Each waits only for its own
+        // inputs, so one issuer's waits overlap the other's MMAs.  tcgen05.commit covers
+        // the committing thread's MMAs: warp 11 signals S full and K free, warp 8 O done,
+        // V free and, after the last P.V (which follows every S), all MMAs done.
         if (lane == 0) {
-            const uint32_t idesc_s = umma_idesc_bf16(BM, TK, 0);
-            const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
-            auto issue_s = [&](int t) {
-                const int s = t % NKT;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t bd = umma_desc_sw128(sK(s) + (kk / 4) * TK * 128 + (kk % 4) * 32, 16, 1024);
-                    umma_bf16_ts(tmem + Cfg::kSCol + (t & 1) * TK, tmem + Cfg::kQCol + kk * 8, bd, idesc_s,
-                                 kk > 0 ? 1u : 0u);
-                }
-                umma_commit(bar(Cfg::kSFull + (t & 1)));
-                umma_commit(bar(Cfg::kKFree + s));
-            };
-            auto issue_pv = [&](int j) {
-                const int s = j % NVT;
-#pragma unroll
-                for (int kk = 0; kk < TK / 16; ++kk) {
-                    const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
-                    umma_bf16_ts(tmem + Cfg::kOCol, tmem + Cfg::kPCol + kk * 8, bd, idesc_o,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                umma_commit(bar(Cfg::kODone));
-                umma_commit(bar(Cfg::kVFree + s));
-            };
-            bool issued = false, alive = wait_or_abort(bar(Cfg::kQ), 0, abort, p.err);
-            for (int t = 0; t < 2 && t < ntiles && alive; ++t) {
-                alive = wait_or_abort(bar(Cfg::kKFull + t % NKT), (t / NKT) & 1, abort, p.err);
-                if (!alive) break;
-                tc_fence_after_sync();
-                issue_s(t);
-                issued = true;
-            }
-            for (int j = 0; j < ntiles && alive; ++j) {
-                alive = wait_or_abort(bar(Cfg::kPFull), j & 1, abort, p.err) &&
-                        wait_or_abort(bar(Cfg::kVFull + j % NVT), (j / NVT) & 1, abort, p.err);
-                if (!alive) break;
-                tc_fence_after_sync();
-                issue_pv(j);
-                const int t = j + 2;
-                if (t < ntiles) {
-                    alive = wait_or_abort(bar(Cfg::kKFull + t % NKT), (t / NKT) & 1, abort, p.err);
+            const bool is_s = warp == 11;
+            bool issued = false, alive = true;
+            if (is_s) {
+                const uint32_t idesc_s = umma_idesc_bf16(BM, TK, 0);
+                alive = wait_or_abort(bar(Cfg::kQ), 0, abort, p.err);
+                for (int t = 0; t < ntiles && alive; ++t) {
+                    if (t >= 2) alive = wait_or_abort(bar(Cfg::kPFull), (t - 2) & 1, abort, p.err);
+                    alive = alive && wait_or_abort(bar(Cfg::kKFull + t % NKT), (t / NKT) & 1, abort, p.err);
                     if (!alive) break;
                     tc_fence_after_sync();
-                    issue_s(t);
+                    const int s = t % NKT;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t bd = umma_desc_sw128(sK(s) + (kk / 4) * TK * 128 + (kk % 4) * 32, 16, 1024);
+                        umma_bf16_ts(tmem + Cfg::kSCol + (t & 1) * TK, tmem + Cfg::kQCol + kk * 8, bd, idesc_s,
+                                     kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(Cfg::kSFull + (t & 1)));
+                    umma_commit(bar(Cfg::kKFree + s));
+                    issued = true;
                 }
+            } else {
+                const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
+                for (int j = 0; j < ntiles && alive; ++j) {
+                    alive = wait_or_abort(bar(Cfg::kPFull), j & 1, abort, p.err) &&
+                            wait_or_abort(bar(Cfg::kVFull + j % NVT), (j / NVT) & 1, abort, p.err);
+                    if (!alive) break;
+                    tc_fence_after_sync();
+                    const int s = j % NVT;
+#pragma unroll
+                    for (int kk = 0; kk < TK / 16; ++kk) {
+                        const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
+                        umma_bf16_ts(tmem + Cfg::kOCol, tmem + Cfg::kPCol + kk * 8, bd, idesc_o,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar(Cfg::kODone));
+                    umma_commit(bar(Cfg::kVFree + s));
+                    issued = true;
+                }
+                if (alive) umma_commit(bar(Cfg::kDone));
             }
-            if (alive) umma_commit(bar(Cfg::kDone));
             if (*abort && issued) {
-                // let the MMAs already issued finish (bounded) before teardown
-                umma_commit(bar(Cfg::kDrain));
-                mbar_wait_bounded(bar(Cfg::kDrain), 0);
+                // let this thread's MMAs finish (bounded) before teardown
+                const int drain = is_s ? Cfg::kDrain + 1 : Cfg::kDrain;
+                umma_commit(bar(drain));
+                mbar_wait_bounded(bar(drain), 0);
             }
         }
     } else {
