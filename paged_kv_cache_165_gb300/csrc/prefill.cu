@@ -52,294 +52,310 @@ __device__ __forceinline__ bool seq_range(const PrefillKParams &p, int b, int &s
 
 // ============================================================ tcgen05 path
 
-// Tiles of the tcgen05 prefill: two 128-row query tiles per CTA, 64-key K/V tiles.
+// Tiles of the tcgen05 prefill: one 128-row query tile per CTA, 128-key K/V tiles.
 template <int D>
 struct TcPrefillCfg {
-    static constexpr int kBM = 128, kBN = 64, kGroups = 2;
-    static constexpr int kStages = D == 64 ? 6 : 3;    // K/V ring depth
-    static constexpr int kQBytes = kBM * D * 2;        // one Q tile: D/64 panels of [128][128 B]
-    static constexpr int kKVBytes = kBN * D * 2;       // one K or V tile: D/64 panels of [64][128 B]
-    static constexpr int kPBytes = kBM * kBN * 2;      // P (bf16) [128][64]: one panel
-    static constexpr int kOffKV = kGroups * kQBytes;   // stage s: K, then V
-    static constexpr int kOffP = kOffKV + kStages * 2 * kKVBytes;   // per group: P_hi, P_lo
-    static constexpr int kOffBar = kOffP + kGroups * 2 * kPBytes;
-    static constexpr int kNumBars = 1 + 2 * kStages + kGroups * 6;
-    static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
-    static constexpr int kTmemCols = 512;              // per group: S 2 x 64 columns, O D columns
-    static constexpr int kGroupCols = 256;
-    static constexpr int kSCol = 0, kOCol = 2 * kBN;
-    static_assert(kOCol + D <= kGroupCols, "tensor memory budget");
+    static constexpr int kBM = 128, kTK = 128;
+    static constexpr int PANELS = D / 64;
+    static constexpr int NK = D == 64 ? 6 : 3, NV = D == 64 ? 5 : 2;   // K and V ring slots
+    static constexpr int kQBytes = kBM * D * 2;        // the Q tile: D/64 panels of [128][128 B]
+    static constexpr int kSlotBytes = kTK * D * 2;     // one K or V tile: D/64 panels of [128][128 B]
+    static constexpr int kOffK = kQBytes;
+    static constexpr int kOffV = kOffK + NK * kSlotBytes;
+    static constexpr int kOffBar = kOffV + NV * kSlotBytes;
+    // barriers: Q; K full / free per slot; V full / free per slot; S full x2; P full; O done;
+    // all MMAs done; drain x2 (one per MMA-issuing thread)
+    static constexpr int kQ = 0, kKFull = 1, kKFree = 1 + NK, kVFull = 1 + 2 * NK, kVFree = 1 + 2 * NK + NV,
+                         kSFull = 1 + 2 * NK + 2 * NV, kPFull = kSFull + 2, kODone = kPFull + 1,
+                         kDone = kODone + 1, kDrain = kDone + 1, kNumBars = kDrain + 2;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;          // TMEM slot, abort flag
+    // row exchange of the two warps of a row, double-buffered by tile parity:
+    // [buffer][value, ok][half][128 rows] floats
+    static constexpr int kOffXch = (kOffMisc + 16 + 15) / 16 * 16;
+    static constexpr int kSmemBytes = 1024 + kOffXch + 2 * 2 * 2 * kBM * 4;
+    // tensor memory: two S buffers, O, P_hi, P_lo
+    static constexpr int kTmemCols = 512;
+    static constexpr int kSCol = 0, kOCol = 2 * kTK, kPHiCol = kOCol + D, kPLoCol = kPHiCol + kTK / 2;
+    static constexpr int kThreads = 384;
+    static_assert(kPLoCol + kTK / 2 <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// mbarrier slots: Q; K/V full and K/V free per stage; per group S full x2, S free x2,
-// P full, O done
-template <int NS>
-struct PrefillBars {
-    static constexpr int kQ = 0, kKvFull = 1, kKvFree = 1 + NS, kGroup0 = 1 + 2 * NS;
-    static constexpr int s_full(int g, int b) { return kGroup0 + g * 6 + b; }
-    static constexpr int s_free(int g, int b) { return kGroup0 + g * 6 + 2 + b; }
-    static constexpr int p_full(int g) { return kGroup0 + g * 6 + 4; }
-    static constexpr int o_done(int g) { return kGroup0 + g * 6 + 5; }
-};
-
-// One CTA per (query head, pair of 128-query tiles, sequence); ten warps.
-//   warp 9 (one lane): TMA loads of both Q tiles and of a K/V ring shared by the two tiles;
-//     a stage is refilled as soon as the MMAs of its previous tile are done.
-//   warp 8 (one lane): every tcgen05.mma: per tile g and key tile j, S_g = Q_g K_j^T into one of
-//     two tensor-memory S buffers of g, and O_g += P_g V_j (P as bf16 hi + lo, two MMA
-//     chains) into g's tensor-memory accumulator.  Issue order alternates between the
-//     tiles, so the tensor core works on one tile while the other tile's rows are in the
-//     softmax.
-//   warps 4g .. 4g+3: one query row of tile g per thread.  Per key tile: read the row of
-//     S from tensor memory, apply the causal mask (key <= query) on diagonal tiles, update
-//     the running max and sum (online softmax), rescale the O row in tensor memory when
-//     the reference max grew by more than 2^8 (exponentials stay <= 256 otherwise, and O
-//     and l share the same reference), and write the row of P_hi and P_lo to shared memory
-//     in the 128-byte-swizzled K-major layout the MMA reads.  At the end: O / l and lse.
+// One CTA per (query head, 128-query tile, sequence), the tiles with the most key tiles
+// launched first; twelve warps:
+//   warps 9 and 10 (TMA): the Q tile once (lane 0 of warp 9), then the K and the V tiles
+//     into two rings of tile slots, one {64, 1, 16} box (16 rows of one 64-column panel) per
+//     lane, so that sixteen threads issue copies at once; a K slot is free once its scores
+//     are computed, a V slot once its P.V is.
+//   warps 11 and 8 (one lane each issues tcgen05.mma): S_j = Q K_j^T (N = 128 keys) into one
+//     of two tensor-memory S buffers, once K_j has landed and, for j >= 2, P_{j-2} has been
+//     written (S_{j-2} read); and O += P_hi V_j + P_lo V_j (N = d) with P_hi and P_lo read
+//     from tensor memory.  Each issuer waits only for its own inputs.
+//   warps 0-7 (softmax): row r of the query tile is tensor-memory lane r, shared by warps
+//     w and w+4 (w = r / 32); warp half h = w / 4 takes keys 64h .. 64h + 63 of each key tile.
+//     Per tile: read the row of S, apply the causal mask (key <= query) on the diagonal tile,
+//     share the row maximum between the two warps through shared memory, update the running
+//     maximum and sum (online softmax), rescale the O row in tensor memory when the
+//     reference maximum grew by more than 2^8 (exponentials stay <= 256 otherwise, and O and
+//     l share the reference), and write P as bf16 hi and lo parts (P = P_hi + P_lo to about
+//     2^-16 relative) into tensor memory.  At the end: O / l and the log-sum-exp.
+// Every wait is bounded and shares an abort flag: on a timeout the block drains its copies
+// and MMAs, frees tensor memory and returns with PKV_DEVERR_TIMEOUT.
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillKParams p) {
     using Cfg = TcPrefillCfg<D>;
-    constexpr int BM = Cfg::kBM, BN = Cfg::kBN, PANELS = D / 64, NS = Cfg::kStages, G = Cfg::kGroups;
-    using Bars = PrefillBars<NS>;
+    constexpr int BM = Cfg::kBM, TK = Cfg::kTK, PANELS = Cfg::PANELS, NK = Cfg::NK, NV = Cfg::NV;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + Cfg::kNumBars);
-    volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
+    float *xch = reinterpret_cast<float *>(smem + Cfg::kOffXch);
     auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blockIdx.x, b = blockIdx.z;
     int start = 0, len = 0;
     if (!seq_range(p, b, start, len, threadIdx.x == 0 && blockIdx.y == 0 && i == 0)) return;
-    const int npairs = (p.max_seqlen + G * BM - 1) / (G * BM);
-    const int q0 = (npairs - 1 - static_cast<int>(blockIdx.y)) * G * BM;   // longest first
+    const int nqt = (p.max_seqlen + BM - 1) / BM;
+    const int q0 = (nqt - 1 - static_cast<int>(blockIdx.y)) * BM;   // longest first
     if (q0 >= len) return;
     const int kvh = i / p.m;
-    int n_kt[G];   // key tiles up to the diagonal, per query tile (0: tile past the end)
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const int qg = q0 + g * BM;
-        n_kt[g] = qg < len ? (min(qg + BM, len) - 1) / BN + 1 : 0;
-    }
-    const int n_all = max(n_kt[0], n_kt[1]);
+    const int ntiles = (min(q0 + BM, len) - 1) / TK + 1;   // key tiles up to the diagonal
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(Bars::kQ), 1);
-        for (int st = 0; st < NS; ++st) {
-            mbar_init(bar(Bars::kKvFull + st), 1);
-            mbar_init(bar(Bars::kKvFree + st), 1);
+        mbar_init(bar(Cfg::kQ), 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(bar(Cfg::kKFull + s), 1);
+            mbar_init(bar(Cfg::kKFree + s), 1);
         }
-        for (int g = 0; g < G; ++g) {
-            for (int sb = 0; sb < 2; ++sb) {
-                mbar_init(bar(Bars::s_full(g, sb)), 1);
-                mbar_init(bar(Bars::s_free(g, sb)), 4);
-            }
-            mbar_init(bar(Bars::p_full(g)), 4);
-            mbar_init(bar(Bars::o_done(g)), 1);
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(bar(Cfg::kVFull + s), 1);
+            mbar_init(bar(Cfg::kVFree + s), 1);
         }
+        mbar_init(bar(Cfg::kSFull), 1);
+        mbar_init(bar(Cfg::kSFull + 1), 1);
+        mbar_init(bar(Cfg::kPFull), 8);
+        mbar_init(bar(Cfg::kODone), 1);
+        mbar_init(bar(Cfg::kDone), 1);
+        mbar_init(bar(Cfg::kDrain), 1);
+        mbar_init(bar(Cfg::kDrain + 1), 1);
         *abort = 0;
         fence_barrier_init();
+        tma_prefetch_map(&tm_q);
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
     }
     if (warp == 0) tmem_alloc(smem_addr(tslot), Cfg::kTmemCols);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tslot;
-    auto sQ = [&](int g) { return smem_addr(smem + g * Cfg::kQBytes); };
-    auto sK = [&](int st) { return smem_addr(smem + Cfg::kOffKV + st * 2 * Cfg::kKVBytes); };
-    auto sV = [&](int st) { return sK(st) + Cfg::kKVBytes; };
-    auto sP = [&](int g) { return smem_addr(smem + Cfg::kOffP + g * 2 * Cfg::kPBytes); };   // hi; lo after
+    const uint32_t sQ = smem_addr(smem);
+    auto sK = [&](int s) { return smem_addr(smem + Cfg::kOffK + s * Cfg::kSlotBytes); };
+    auto sV = [&](int s) { return smem_addr(smem + Cfg::kOffV + s * Cfg::kSlotBytes); };
 
-    if (warp == 2 * 4) {
-        if (lane == 0) {
-            const uint32_t idesc_s = umma_idesc_bf16(BM, BN, 0);
-            const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
-            auto issue_s = [&](int g, int j) {   // S_g[j & 1] = Q_g K_j^T
-                const int st = j % NS, sb = j & 1;
+    if (warp == 9 || warp == 10) {
+        // ---- TMA loaders: warp 9 the Q tile and the K tiles, warp 10 the V tiles.  Tile t
+        // (keys t*128 ..) goes to slot t % N once the slot's previous tile is consumed.  Lane
+        // l < 8 * PANELS copies rows 16 (l / PANELS) .. + 15 of panel l % PANELS.
+        const bool is_k = warp == 9;
+        const int N = is_k ? NK : NV;
+        const int full0 = is_k ? Cfg::kKFull : Cfg::kVFull, free0 = is_k ? Cfg::kKFree : Cfg::kVFree;
+        const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+        if (is_k && lane == 0) {
+            mbar_arrive_expect_tx(bar(Cfg::kQ), Cfg::kQBytes);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = umma_desc_sw128(sQ(g) + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
-                    const uint64_t bd = umma_desc_sw128(sK(st) + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024);
-                    umma_bf16(tmem + g * Cfg::kGroupCols + Cfg::kSCol + sb * BN, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(bar(Bars::s_full(g, sb)));
-            };
-            auto issue_pv = [&](int g, int j) {  // O_g += P_g,hi V_j + P_g,lo V_j
-                const int st = j % NS;
-#pragma unroll
-                for (int half = 0; half < 2; ++half)
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t ad = umma_desc_sw128(sP(g) + half * Cfg::kPBytes + kk * 32, 16, 1024);
-                        const uint64_t bd = umma_desc_sw128(sV(st) + kk * 16 * 128, BN * 128, 1024);
-                        umma_bf16(tmem + g * Cfg::kGroupCols + Cfg::kOCol, ad, bd, idesc_o,
-                                  (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
-                    }
-                umma_commit(bar(Bars::o_done(g)));
-            };
-            int j = 0;
-            if (wait_or_abort(bar(Bars::kQ), 0, abort, p.err) &&
-                wait_or_abort(bar(Bars::kKvFull), 0, abort, p.err)) {
-                tc_fence_after_sync();
-                for (int g = 0; g < G; ++g)
-                    if (n_kt[g] > 0) issue_s(g, 0);
-                bool alive = true;
-                for (; j < n_all && alive; ++j) {
-                    const int t = j + 1;
-                    if (t < n_all) {
-                        alive = wait_or_abort(bar(Bars::kKvFull + t % NS), (t / NS) & 1, abort, p.err);
-                        for (int g = 0; g < G && alive; ++g) {
-                            if (t >= n_kt[g]) continue;
-                            if (t >= 2)
-                                alive = wait_or_abort(bar(Bars::s_free(g, t & 1)), ((t >> 1) - 1) & 1, abort, p.err);
-                            if (!alive) break;
-                            tc_fence_after_sync();
-                            issue_s(g, t);
-                        }
-                    }
-                    for (int g = 0; g < G && alive; ++g) {
-                        if (j >= n_kt[g]) continue;
-                        alive = wait_or_abort(bar(Bars::p_full(g)), j & 1, abort, p.err);
-                        if (!alive) break;
-                        tc_fence_after_sync();
-                        issue_pv(g, j);
-                    }
-                    if (!alive) break;
-                    umma_commit(bar(Bars::kKvFree + j % NS));   // stage j % NS is free after these MMAs
-                }
-            }
-            if (*abort && j > 0) {
-                // let the MMAs already issued finish (bounded) before teardown
-                umma_commit(bar(Bars::kKvFree + j % NS));
-                mbar_wait_bounded(bar(Bars::kKvFree + j % NS), (j / NS) & 1);
+            for (int pn = 0; pn < PANELS; ++pn)
+                tma_load_3d(sQ + pn * BM * 128, &tm_q, pn * 64, i, start + q0, bar(Cfg::kQ));
+        }
+        const int chunk = lane / PANELS, pn = lane % PANELS;
+        int t = 0;
+        for (; t < ntiles; ++t) {
+            bool fr = true;
+            if (lane == 0 && t >= N) fr = wait_or_abort(bar(free0 + t % N), ((t - N) / N) & 1, abort, p.err);
+            if (!__shfl_sync(kFull, fr ? 1 : 0, 0)) break;
+            const int s = t % N;
+            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), Cfg::kSlotBytes);
+            __syncwarp();
+            if (lane < 8 * PANELS) {
+                const uint32_t dst = (is_k ? sK(s) : sV(s)) + pn * TK * 128 + chunk * 16 * 128;
+                tma_load_3d(dst, map, pn * 64, kvh, start + t * TK + chunk * 16, bar(full0 + s));
             }
         }
-    } else if (warp == 2 * 4 + 1) {
+        // before teardown every copy issued must have landed (bounded)
         if (lane == 0) {
-            // loader: both Q tiles, then K/V tile t into stage t % NS as soon as the MMAs of
-            // tile t - NS (the stage's previous tile) are done
-            mbar_arrive_expect_tx(bar(Bars::kQ), G * Cfg::kQBytes);
+            if (is_k) mbar_wait_bounded(bar(Cfg::kQ), 0);
+            for (int u = max(0, t - N); u < t; ++u) mbar_wait_bounded(bar(full0 + u % N), (u / N) & 1);
+        }
+    } else if (warp == 8 || warp == 11) {
+        // ---- MMA issue, one lane each: warp 11 the scores, warp 8 the products with V.
+        // tcgen05.commit covers the committing thread's MMAs: warp 11 signals S full and K
+        // free, warp 8 O done, V free and, after the last P.V (which follows every S), all
+        // MMAs done.
+        if (lane == 0) {
+            const bool is_s = warp == 11;
+            bool issued = false, alive = true;
+            if (is_s) {
+                const uint32_t idesc_s = umma_idesc_bf16(BM, TK, 0);
+                alive = wait_or_abort(bar(Cfg::kQ), 0, abort, p.err);
+                for (int t = 0; t < ntiles && alive; ++t) {
+                    if (t >= 2) alive = wait_or_abort(bar(Cfg::kPFull), (t - 2) & 1, abort, p.err);
+                    alive = alive && wait_or_abort(bar(Cfg::kKFull + t % NK), (t / NK) & 1, abort, p.err);
+                    if (!alive) break;
+                    tc_fence_after_sync();
+                    const int s = t % NK;
 #pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int pn = 0; pn < PANELS; ++pn)
-                    tma_load_3d(sQ(g) + pn * BM * 128, &tm_q, pn * 64, i, start + q0 + g * BM, bar(Bars::kQ));
-            int t = 0;
-            for (; t < n_all; ++t) {
-                if (t >= NS && !wait_or_abort(bar(Bars::kKvFree + t % NS), ((t - NS) / NS) & 1, abort, p.err))
-                    break;
-                const int st = t % NS;
-                mbar_arrive_expect_tx(bar(Bars::kKvFull + st), 2 * Cfg::kKVBytes);
-#pragma unroll
-                for (int pn = 0; pn < PANELS; ++pn) {
-                    tma_load_3d(sK(st) + pn * BN * 128, &tm_k, pn * 64, kvh, start + t * BN, bar(Bars::kKvFull + st));
-                    tma_load_3d(sV(st) + pn * BN * 128, &tm_v, pn * 64, kvh, start + t * BN, bar(Bars::kKvFull + st));
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(sQ + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
+                        const uint64_t bd = umma_desc_sw128(sK(s) + (kk / 4) * TK * 128 + (kk % 4) * 32, 16, 1024);
+                        umma_bf16(tmem + Cfg::kSCol + (t & 1) * TK, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(Cfg::kSFull + (t & 1)));
+                    umma_commit(bar(Cfg::kKFree + s));
+                    issued = true;
                 }
+            } else {
+                const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
+                for (int j = 0; j < ntiles && alive; ++j) {
+                    alive = wait_or_abort(bar(Cfg::kPFull), j & 1, abort, p.err) &&
+                            wait_or_abort(bar(Cfg::kVFull + j % NV), (j / NV) & 1, abort, p.err);
+                    if (!alive) break;
+                    tc_fence_after_sync();
+                    const int s = j % NV;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+#pragma unroll
+                        for (int kk = 0; kk < TK / 16; ++kk) {
+                            const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
+                            umma_bf16_ts(tmem + Cfg::kOCol, tmem + (half ? Cfg::kPLoCol : Cfg::kPHiCol) + kk * 8, bd,
+                                         idesc_o, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    umma_commit(bar(Cfg::kODone));
+                    umma_commit(bar(Cfg::kVFree + s));
+                    issued = true;
+                }
+                if (alive) umma_commit(bar(Cfg::kDone));
             }
-            // before teardown, every copy issued must have landed (bounded)
-            mbar_wait_bounded(bar(Bars::kQ), 0);
-            for (int u = max(0, t - NS); u < t; ++u)
-                mbar_wait_bounded(bar(Bars::kKvFull + u % NS), (u / NS) & 1);
+            if (*abort && issued) {
+                // let this thread's MMAs finish (bounded) before teardown
+                const int drain = is_s ? Cfg::kDrain + 1 : Cfg::kDrain;
+                umma_commit(bar(drain));
+                mbar_wait_bounded(bar(drain), 0);
+            }
         }
     } else {
-        const int g = warp >> 2;                 // query tile of this warp
-        const int r = (warp & 3) * 32 + lane;    // its row in the tile
-        const int qg0 = q0 + g * BM;
-        const int qpos = qg0 + r;
-        const int nk = n_kt[g];
-        const uint32_t lane_base = tmem + g * Cfg::kGroupCols + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        uint8_t *pbuf = smem + Cfg::kOffP + g * 2 * Cfg::kPBytes;
+        // ---- softmax: thread (w, lane) owns query row r = 32 (w % 4) + lane (tensor-memory
+        // lane r) and keys 64h .. 64h + 63 of each key tile (h = w / 4)
+        const int h = warp >> 2;
+        const int r = ((warp & 3) << 5) | lane;
+        const int qpos = q0 + r;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4
+        auto xs = [&](int buf, int kind, int hh) { return xch + ((buf * 2 + kind) * 2 + hh) * BM + r; };
         float m_ref = -INFINITY, l = 0.f;
-        bool ok = nk > 0;
-        for (int j = 0; j < nk && ok; ++j) {
+        // ok is warp-uniform, and after each tile's exchange the same in both warps of a
+        // row: a failed wait skips the remaining work but never a named barrier
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
             const int sb = j & 1;
-            ok = wait_or_abort(bar(Bars::s_full(g, sb)), (j >> 1) & 1, abort, p.err);
-            if (!ok) break;
-            tc_fence_after_sync();
-            uint32_t sr[BN];
-            tmem_ld32(lane_base + Cfg::kSCol + sb * BN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(lane_base + Cfg::kSCol + sb * BN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Bars::s_free(g, sb)));
-
-            // causal mask (diagonal tiles only), tile max, reference max (moved only when it
-            // grows by more than 2^8); scores stay raw and the scale enters one FMA
-            const int key0 = j * BN;
-            float sc[BN];
+            if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kSFull + sb), (j >> 1) & 1, abort, p.err));
+            float sc[64];
+            if (ok) {
+                tc_fence_after_sync();
+                uint32_t s0[32], s1[32];
+                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64, s0);
+                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64 + 32, s1);
+                tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < BN; ++c) sc[c] = __uint_as_float(sr[c]);
-            if (key0 + BN - 1 > qg0) {
+                for (int c = 0; c < 32; ++c) {
+                    sc[c] = __uint_as_float(s0[c]);
+                    sc[32 + c] = __uint_as_float(s1[c]);
+                }
+            } else {
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
+                for (int c = 0; c < 64; ++c) sc[c] = -INFINITY;
+            }
+            // causal mask on the diagonal tile: key <= query
+            const int key0 = j * TK + h * 64;
+            if (key0 + 63 > q0) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
                     if (key0 + c > qpos) sc[c] = -INFINITY;
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            for (int c = 0; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
+            float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            // the other half's maximum of this row, and whether it is still ok; the exchange
+            // buffer alternates with the tile, so one barrier a tile suffices
+            *xs(sb, 0, h) = mx;
+            *xs(sb, 1, h) = ok ? 1.f : 0.f;
+            named_barrier(pair_bar, 64);
+            mx = fmaxf(mx, *xs(sb, 0, 1 - h)) * p.scale_log2;
+            ok = ok && *xs(sb, 1, 1 - h) != 0.f;
+            if (!ok) continue;
+            // key 0 is always visible, so the row maximum is finite from the first tile on
             const float m_new = mx > m_ref + 8.f ? mx : m_ref;
             const float alpha = ex2_approx(m_ref - m_new);
             m_ref = m_new;
             const float neg_m = -m_ref;
             float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
+            for (int c = 0; c < 64; ++c) {
                 sc[c] = ex2_approx(fmaf(sc[c], p.scale_log2, neg_m));
                 l4[c & 3] += sc[c];
             }
             l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-            // the previous P.V of this tile must be done: P is free and O is current
+            uint32_t phi[32], plo[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) split_bf16x2(sc[2 * e], sc[2 * e + 1], phi[e], plo[e]);
+            // P_{j-1} V_{j-1} must be done: the P columns are free and O is current
             if (j > 0) {
-                ok = wait_or_abort(bar(Bars::o_done(g)), (j - 1) & 1, abort, p.err);
-                if (!ok) break;
+                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kODone), (j - 1) & 1, abort, p.err));
+                if (!ok) continue;
                 tc_fence_after_sync();
                 if (__any_sync(kFull, alpha != 1.f)) {
+                    // this half rescales columns D/2 h .. D/2 h + D/2 - 1 of its rows
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < D / 64; ++cc) {
                         uint32_t ov[32];
-                        tmem_ld32(lane_base + Cfg::kOCol + cc * 32, ov);
+                        tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(lane_base + Cfg::kOCol + cc * 32, ov);
+                        tmem_st32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
                     }
-                    tmem_st_wait();
                 }
             }
-            // row r of P_hi and P_lo: 8 chunks of 8 keys, 128-byte swizzle
-#pragma unroll
-            for (int c16 = 0; c16 < BN / 8; ++c16) {
-                uint32_t h[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    split_bf16x2(sc[c16 * 8 + 2 * e], sc[c16 * 8 + 2 * e + 1], h[e], lo[e]);
-                const uint32_t off = r * 128 + ((c16 ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(pbuf + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4 *>(pbuf + Cfg::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-            fence_proxy_async_smem();
+            tmem_st32(lane_base + Cfg::kPHiCol + h * 32, phi);
+            tmem_st32(lane_base + Cfg::kPLoCol + h * 32, plo);
+            tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Bars::p_full(g)));
+            if (lane == 0) mbar_arrive(bar(Cfg::kPFull));
         }
-        if (ok) ok = wait_or_abort(bar(Bars::o_done(g)), (nk - 1) & 1, abort, p.err);
+        if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kDone), 0, abort, p.err));
+
+        // ---- the row's sum over its two threads, through the exchange buffer the last tile
+        // did not use; O / l and the log-sum-exp
+        const int fb = ntiles & 1;
+        *xs(fb, 0, h) = l;
+        named_barrier(pair_bar, 64);
+        const float lr = l + *xs(fb, 0, 1 - h);
         if (ok) {
             tc_fence_after_sync();
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / lr;
             const bool row_ok = qpos < len;
-            float *dst = p.out + (static_cast<size_t>(start + qpos) * p.Hq + i) * D;
+            float *dst = p.out + (static_cast<size_t>(start + qpos) * p.Hq + i) * D + h * (D / 2);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t ov[32];
-                tmem_ld32(lane_base + Cfg::kOCol + cc * 32, ov);
+                tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
                 tmem_ld_wait();
                 if (row_ok) {
 #pragma unroll
@@ -349,8 +365,8 @@ __global__ void __launch_bounds__(320, 1)
                                         __uint_as_float(ov[e + 2]) * inv_l, __uint_as_float(ov[e + 3]) * inv_l);
                 }
             }
-            if (row_ok && p.lse != nullptr)
-                p.lse[static_cast<size_t>(start + qpos) * p.Hq + i] = (m_ref + log2f(l)) * kLn2;
+            if (row_ok && h == 0 && p.lse != nullptr)
+                p.lse[static_cast<size_t>(start + qpos) * p.Hq + i] = (m_ref + log2f(lr)) * kLn2;
         }
     }
     tc_fence_before_sync();
@@ -433,7 +449,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, const PrefillKParams &kp, cu
                             static_cast<uint64_t>(a.T)};
     const uint64_t sk[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.Hkv) * D * 2};
     const uint32_t qbox[3] = {64, 1, static_cast<uint32_t>(Cfg::kBM)};
-    const uint32_t kvbox[3] = {64, 1, static_cast<uint32_t>(Cfg::kBN)};
+    const uint32_t kvbox[3] = {64, 1, 16};   // 16 rows of one panel: one box per loader lane
     if (!encode_map_bf16(&tq, a.q, 3, dq, sq, qbox) || !encode_map_bf16(&tk, a.k, 3, dk, sk, kvbox) ||
         !encode_map_bf16(&tv, a.v, 3, dk, sk, kvbox))
         return cudaErrorInvalidValue;
@@ -441,9 +457,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, const PrefillKParams &kp, cu
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int pair = Cfg::kGroups * Cfg::kBM;
-    const dim3 grid(a.Hq, (a.max_seqlen + pair - 1) / pair, a.B);
-    kernel<<<grid, 320, Cfg::kSmemBytes, stream>>>(tq, tk, tv, kp);
+    const dim3 grid(a.Hq, (a.max_seqlen + Cfg::kBM - 1) / Cfg::kBM, a.B);
+    kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, kp);
     return cudaGetLastError();
 }
 
