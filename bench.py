@@ -165,6 +165,23 @@ class DecodeWorkload:
                 for n in self.lengths]
         return sum(seen) * self.spec.kv_heads * 2 * row
 
+    # attention flops of step c (4 Hq d per visible (query, key) pair: scores and P.V)
+    def attn_flops(self, c):
+        q, s = self.qlen, self.spec
+        pairs = sum(q * (n + q * c) + q * (q + 1) // 2 for n in self.lengths) if self.window <= 0 else None
+        return None if pairs is None else 4 * s.q_heads * s.head_dim * pairs
+
+    def sample_flops(self, n_seq):
+        """Attention flops of one step of the oracle sample (its first n_seq sequences)."""
+        q, s = self.qlen, self.spec
+        return 4 * s.q_heads * s.head_dim * sum(q * n + q * (q + 1) // 2 for n in self.lengths[:n_seq])
+
+    def tensor_bound(self, hbm_gbs, bf16_tflops):
+        """Many query rows per sequence put the step above the bf16 / HBM ridge: it is then
+        measured in attention TFLOP/s against the tensor roofline."""
+        f = self.attn_flops(0) if self.qlen > 1 else None
+        return bool(f) and f / self.kv_bytes(0) > bf16_tflops * 1e3 / hbm_gbs
+
     def describe(self):
         s = self.spec
         return {"workload": self.label, "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads,
@@ -525,6 +542,11 @@ WORKLOADS = {
                                       "llama2-70b-shaped GQA verification step: batch 64, 64 q / 8 kv heads, "
                                       "d 128, lengths U[512,8192], 4 new tokens per sequence appended and "
                                       "attended causally, bs 16, bf16 KV", qlen=4),
+    "prefix_chunk": lambda: DecodeWorkload(gen.PREFIX_CHUNK, [gen.PREFIX_LENGTH] * gen.PREFIX_CHUNK.batch, 1,
+                                           "chunked prefill on a cached prefix: batch 8, 4096 cached tokens each, "
+                                           "512 new tokens per sequence appended and attended causally (bottom-"
+                                           "right), 64 q / 8 kv heads, d 128, bs 16, bf16 KV, fp32 q",
+                                           qlen=gen.PREFIX_CHUNK_LEN),
     "mix": MixWorkload,
     "swa": lambda: DecodeWorkload(gen.SWA, [gen.SWA_LENGTH] * gen.SWA.batch, 1,
                                   "mistral-7b-shaped sliding-window decode: batch 64, 32 q / 8 kv heads, d 128, "
@@ -636,6 +658,9 @@ def bench_ours(args):
         res.update({
             "value": value, "unit": "GB/s", "pct_hbm_peak": 100 * value / hbm,
             "tokens_per_s_per_layer": wl.spec.batch * wl.qlen * world / (ms_per_step / 1e3),
+            **({"attention_tflops": world * sum(wl.attn_flops((first + k) % wl.cycle) for k in range(args.steps))
+                / (max_ms / 1e3) / 1e12}
+               if wl.qlen > 1 and wl.window <= 0 else {}),
             **({"unique_gb_per_s": whole_job_rate(wl.unique_bytes * args.steps, world, max_ms) / 1e9}
                if hasattr(wl, "unique_bytes") else {}),
             "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (split-K partials + LSE merge)",
@@ -646,6 +671,24 @@ def bench_ours(args):
                          "avg_launch_ms": kern_avg_ms,
                          "traffic": traffic, "kernel_source_sha256_16": src},
         })
+        step_flops = [wl.attn_flops((first + k) % wl.cycle) for k in range(args.steps)] \
+            if wl.qlen > 1 and wl.window <= 0 else None
+        if step_flops and wl.tensor_bound(hbm, bf16):
+            # many query rows per sequence (chunked prefill on a cached prefix): the work is
+            # above the bf16 / HBM ridge, so the metric is attention TFLOP/s against the
+            # tensor roofline; the cache-read rate stays as a key of its own
+            flops = sum(step_flops) / len(step_flops)
+            ach = flops / (kern_avg_ms / 1e3) / 1e12
+            res.update({
+                "metric": "chunked prefill on a cached prefix: attention TFLOP/s (4*Hq*d per visible query-key pair)",
+                "value": res["attention_tflops"], "unit": "TFLOP/s", "kv_read_gb_per_s": value,
+                "roofline": {"bound": "tensor", "kernel": "paged_attention (query rows over the cache)",
+                             "achieved": ach, "peak": bf16, "unit": "TFLOP/s", "frac": ach / bf16,
+                             "peak_source": "measured bf16_tflops (burst)" if peak_kind == "measured"
+                             else "fallback 1.9 PFLOP/s",
+                             "algorithmic_flops_per_launch": flops, "avg_launch_ms": kern_avg_ms,
+                             "traffic": traffic, "kernel_source_sha256_16": src},
+            })
     else:
         flops = wl.flops()
         value = whole_job_rate(flops * args.steps, world, max_ms) / 1e12
@@ -692,7 +735,9 @@ def bench_ours(args):
         if not torch.equal(wl.out_h[last_buf], wl.out.cpu()):
             raise RuntimeError("end-to-end output differs from the eager step")
         h2d, d2h = wl.e2e_bytes()
-        res["e2e"] = {"value": whole_job_rate(sum(step_bytes), world, e_ms) / 1e9, "unit": "GB/s",
+        tb = res["unit"] == "TFLOP/s"   # the tensor-bound query-row workload: the same metric
+        res["e2e"] = {"value": whole_job_rate(sum(step_flops) if tb else sum(step_bytes), world, e_ms)
+                      / (1e12 if tb else 1e9), "unit": res["unit"],
                       "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h,
                       "path": "public API calls (kv_append, paged_decode_attention) replayed as one "
@@ -702,13 +747,16 @@ def bench_ours(args):
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
     if world == 1 and rank == 0 and not args.no_cpu_baseline and is_decode:
-        run, threads = wl.oracle_sample(min(args.cpu_seqs, wl.spec.batch))
+        tb = wl.tensor_bound(hbm, bf16)
+        n_seq = 1 if tb else min(args.cpu_seqs, wl.spec.batch)   # ~10-30 s of CPU work
+        run, threads = wl.oracle_sample(n_seq)
         t0 = time.perf_counter()
         nbytes = run(0)
         dt = time.perf_counter() - t0
-        res["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads,
+        res["cpu_baseline"] = {"value": wl.sample_flops(n_seq) / dt / 1e12 if tb else nbytes / dt / 1e9,
+                               "unit": "TFLOP/s" if tb else "GB/s", "cores": threads,
                                "kind": "oracle",
-                               "sample": f"one append+attend step of {min(args.cpu_seqs, wl.spec.batch)} of the {wl.spec.batch} "
+                               "sample": f"one append+attend step of {n_seq} of the {wl.spec.batch} "
                                          f"sequences (same lengths and shapes, own seeded draws), "
                                          f"fp64 C oracle, {threads} threads, {dt:.2f} s"}
     if world > 1:
@@ -728,7 +776,10 @@ def bench_reference(args):
     if not isinstance(wl, DecodeWorkload):
         print(json.dumps({"impl": "reference", "unavailable": "reference arm covers the decode workloads"}))
         return
-    run, threads = wl.oracle_sample(args.ref_seqs, steps=wl.cycle)
+    hbm, bf16, _, _ = peaks()
+    tb = wl.tensor_bound(hbm, bf16)
+    n_seq = 1 if tb else args.ref_seqs
+    run, threads = wl.oracle_sample(n_seq, steps=wl.cycle)
     for k in range(args.warmup):
         run(k % wl.cycle)
     t0 = time.perf_counter()
@@ -736,16 +787,19 @@ def bench_reference(args):
     for k in range(args.steps):
         nbytes += run((args.warmup + k) % wl.cycle)
     dt = time.perf_counter() - t0
-    value = nbytes / dt / 1e9
-    sample = (f"each step: one append+attend step of {args.ref_seqs} of the {wl.spec.batch} sequences "
+    value = wl.sample_flops(n_seq) * args.steps / dt / 1e12 if tb else nbytes / dt / 1e9
+    unit = "TFLOP/s" if tb else "GB/s"
+    metric = ("chunked prefill on a cached prefix: attention TFLOP/s (4*Hq*d per visible query-key pair)"
+              if tb else METRIC)
+    sample = (f"each step: one append+attend step of {n_seq} of the {wl.spec.batch} sequences "
               f"(same lengths and shapes, own seeded draws), fp64 C oracle, {threads} threads")
     print(json.dumps({
-        "metric": METRIC, "impl": "reference", "value": value, "unit": "GB/s", "n_gpus": world,
+        "metric": metric, "impl": "reference", "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": wl.describe(),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
 

@@ -154,3 +154,25 @@ def test_query_count_above_length_raises_cu_seqlens_error():
     assert torch.all(out[:2] == 0) and torch.all(torch.isneginf(lse[:2]))
     ref, _ = oracle.paged_attention(q[2:], kc, vc, table[1:], clens_bad[1:], torch.tensor([0, 3], dtype=torch.int32), 0.1)
     assert_attn_close(out[2:], ref, "valid sequence")
+
+
+def test_prefix_chunk_prefill_at_full_size_on_sampled_rows():
+    # the benched shape: 8 sequences with 4096 cached tokens each append a 512-token chunk
+    # and attend it causally (bottom-right), 64 q / 8 kv heads, d 128, in the launch
+    # configuration the bench uses (automatic splits); sampled rows are checked one by one
+    # against the oracle, a row at position p being a single query over the first p+1 tokens
+    P, N, B, hq, hkv, d, bs = 4096, 512, 8, 64, 8, 128, 16
+    lens, nqs = [P + N] * B, [N] * B
+    q, kc, vc, table, clens, cu = make_case(61, lens, nqs, hq, hkv, d, bs, torch.bfloat16, spare=1)
+    scale = 1 / math.sqrt(d)
+    out, lse = run(q, kc, vc, table, clens, cu, scale, 0, 0, one_per_seq=False)
+    assert pkv.get_device_error() == 0
+    for b in (0, 5, 7):
+        for i in (0, 1, 127, 128, 300, N - 1):
+            row = b * N + i
+            pos = P + i
+            ref, ref_lse = oracle.paged_attention(q[row:row + 1], kc, vc, table[b:b + 1],
+                                                  torch.tensor([pos + 1], dtype=torch.int32),
+                                                  torch.tensor([0, 1], dtype=torch.int32), scale)
+            assert_attn_close(out[row:row + 1], ref, f"seq {b} row {i} out")
+            assert_attn_close(lse[row:row + 1], ref_lse, f"seq {b} row {i} lse")

@@ -60,6 +60,9 @@ MIX = DecodeSpec("mix_prefix_share", 3, 256, 32, 8, 128, torch.bfloat16)
 LONG_GQA = DecodeSpec("long_gqa", 4, 4, 64, 8, 128, torch.bfloat16)
 LONG_MQA = DecodeSpec("long_mqa", 4, 4, 64, 1, 128, torch.bfloat16)
 SWA = DecodeSpec("mistral_7b_swa", 5, 64, 32, 8, 128, torch.bfloat16)
+# chunked prefill on top of a cached prefix (prefix-cache hit): 8 sequences with 4096
+# cached tokens each append and attend a chunk of 512 new tokens, causal within the chunk
+PREFIX_CHUNK = DecodeSpec("prefix_chunk_prefill", 6, 8, 64, 8, 128, torch.bfloat16)
 
 TINY_LENGTHS = (17, 40)
 MHA_7B_LENGTH = 2048
@@ -69,6 +72,7 @@ MIX_PREFIX_TOKENS, MIX_PREFIX_SEQS = 4096, 64
 LONG_LENGTH = 131072
 PREFILL_PROMPTS, PREFILL_RANGE = 8, (256, 4096)
 SWA_LENGTH, SWA_WINDOW = 16384, 4096
+PREFIX_LENGTH, PREFIX_CHUNK_LEN = 4096, 512
 
 
 def generator(seed: int) -> torch.Generator:
