@@ -183,18 +183,15 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
 // Split two fp32 values into bf16 pairs hi + lo with x ~= hi + lo to about 2^-16
-// relative: hi = rn(x), lo = rn(x - hi).  The low 16 bits hold the first value.
+// relative: hi = rn(x), lo = rn(x - hi).  The low 16 bits hold the first value.  Written
+// out as one packed conversion, the two bf16 halves of hi widened back to fp32 by bit
+// operations (a bf16 is the top half of an fp32), two exact subtractions and a second
+// packed conversion.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const __nv_bfloat162 l =
-        __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
-    hi = bf16x2_bits(h);
-    lo = bf16x2_bits(l);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(x1), "f"(x0));
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(x1 - h1), "f"(x0 - h0));
 }
 
 // 2^x by the SFU's approximate base-2 exponential (flushes subnormals; 2^-inf = 0).
