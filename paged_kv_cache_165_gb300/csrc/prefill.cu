@@ -81,8 +81,8 @@ struct TcPrefillCfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// One CTA per (query head, 128-query tile, sequence), the tiles with the most key tiles
-// launched first; twelve warps:
+// One CTA per (query head, sequence, 128-query tile), the tiles with the most key tiles
+// launched first across all sequences; twelve warps:
 //   warps 9 and 10 (TMA): the Q tile once (lane 0 of warp 9), then the K and the V tiles
 //     into two rings of tile slots, one {64, 1, 16} box (16 rows of one 64-column panel) per
 //     lane, so that sixteen threads issue copies at once; a K slot is free once its scores
@@ -118,11 +118,13 @@ __global__ void __launch_bounds__(384, 1)
     auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = blockIdx.x, b = blockIdx.z;
+    const int i = blockIdx.x, b = blockIdx.y;
     int start = 0, len = 0;
-    if (!seq_range(p, b, start, len, threadIdx.x == 0 && blockIdx.y == 0 && i == 0)) return;
+    if (!seq_range(p, b, start, len, threadIdx.x == 0 && blockIdx.z == 0 && i == 0)) return;
     const int nqt = (p.max_seqlen + BM - 1) / BM;
-    const int q0 = (nqt - 1 - static_cast<int>(blockIdx.y)) * BM;   // longest first
+    // grid z ranks the query tiles by start, largest first, across all sequences: a tile
+    // at q0 has q0 / 128 + 1 key tiles, so the launch order is longest first globally
+    const int q0 = (nqt - 1 - static_cast<int>(blockIdx.z)) * BM;
     if (q0 >= len) return;
     const int kvh = i / p.m;
     const int ntiles = (min(q0 + BM, len) - 1) / TK + 1;   // key tiles up to the diagonal
@@ -457,7 +459,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, const PrefillKParams &kp, cu
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const dim3 grid(a.Hq, (a.max_seqlen + Cfg::kBM - 1) / Cfg::kBM, a.B);
+    const dim3 grid(a.Hq, a.B, (a.max_seqlen + Cfg::kBM - 1) / Cfg::kBM);
     kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, kp);
     return cudaGetLastError();
 }
@@ -512,7 +514,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, pkv_dtype dt, cudaStream_t stre
     kp.Hkv = a.Hkv;
     kp.m = a.Hq / a.Hkv;
     kp.scale_log2 = a.scale * kLog2e;
-    if (prefill_tensor_core_ok(dt, a.d, a.q, a.k, a.v, a.T, a.Hq, a.Hkv))
+    // the tcgen05 grid's z counts 128-query tiles (at most 65535 of them)
+    if (prefill_tensor_core_ok(dt, a.d, a.q, a.k, a.v, a.T, a.Hq, a.Hkv) &&
+        static_cast<long long>(a.max_seqlen) <= 65535ll * 128)
         return a.d == 64 ? launch_prefill_tc<64>(a, kp, stream) : launch_prefill_tc<128>(a, kp, stream);
     return dt == PKV_F32 ? launch_prefill_simt<float>(a, kp, stream)
                          : launch_prefill_simt<__nv_bfloat16>(a, kp, stream);
