@@ -99,6 +99,20 @@ def test_large_group_path_ragged_and_poisoned(hq, hkv, d, bs):
         check(q, kc, vc, table, clens, 1 / math.sqrt(d), s, f"hq={hq} hkv={hkv} d={d} bs={bs} s={s}")
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(64, 1, 128), (32, 2, 64)])
+def test_large_group_running_max_jumps(hq, hkv, d):
+    # scale 1 and keys growing with their position: the row maximum moves by far more than
+    # 2^8 between key tiles, so the lazy rescale of O runs on most tiles
+    lens = [700, 2000, 129]
+    q, kc, vc, table, clens = random_case(hq + d, lens, hq, hkv, d, 16, torch.bfloat16)
+    for b, n in enumerate(lens):
+        for pos in range(n):
+            s = oracle.slot_of(table[b], pos, 16)
+            kc[s // 16, :, s % 16] = (kc[s // 16, :, s % 16].float() * (1 + pos / 200)).to(torch.bfloat16)
+    for s in (1, 0):
+        check(q, kc, vc, table, clens, 1.0, s, f"max jumps hq={hq} d={d} s={s}")
+
+
 def test_large_group_bad_block_id_reads_zeros():
     q, kc, vc, table, lens = random_case(81, [200, 700], 64, 1, 128, 16, torch.bfloat16)
     bad_table = table.clone()

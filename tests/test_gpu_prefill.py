@@ -51,6 +51,20 @@ def test_tensor_core_prefill_ragged(hq, hkv, d):
     assert_attn_close(lse, ref_lse, "prefill lse")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_core_prefill_running_max_jumps(d):
+    # scale 1 and keys growing along each prompt: the row maximum moves by far more than
+    # 2^8 from one key tile to the next, so the lazy rescale of O runs on most tiles
+    p = gen.prefill_inputs([300, 513, 1000, 129], 8, 2, d, torch.bfloat16, seed=d + 5)
+    pos = torch.cat([torch.arange(n, dtype=torch.float32) for n in p.lengths])
+    p.k.copy_((p.k.float() * (1 + pos / 96)[:, None, None]).to(torch.bfloat16))
+    out, lse = run_prefill(p, 1.0)
+    assert pkv.get_device_error() == 0
+    ref, ref_lse = oracle.prefill(p.q, p.k, p.v, p.cu_seqlens, 1.0, nthreads=8)
+    assert_attn_close(out, ref, f"prefill max jumps d={d}")
+    assert_attn_close(lse, ref_lse, "prefill max jumps lse")
+
+
 @pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.float32, 32), (torch.bfloat16, 96)])
 def test_cuda_core_prefill(dtype, d):
     p = gen.prefill_inputs([3, 0, 17, 40], 8, 2, d, dtype, seed=d)
