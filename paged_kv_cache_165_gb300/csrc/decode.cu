@@ -1018,7 +1018,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
         const dim3 grid(static_cast<unsigned>(plan.splits) * kp.head_tiles, a.Hkv, a.B);
         if (a.bs == 16) {
             if (a.d == 64) e = launch_tc<64, 16, 4, 6>(kp, tk, tv, grid, stream);
-            else if (a.d == 128) e = launch_tc<128, 16, 4, 3>(kp, tk, tv, grid, stream);
+            else if (a.d == 128) e = launch_tc<128, 16, 4, 2>(kp, tk, tv, grid, stream);
             else e = launch_tc<256, 16, 4, 2>(kp, tk, tv, grid, stream);
         } else {
             if (a.d == 64) e = launch_tc<64, 32, 4, 3>(kp, tk, tv, grid, stream);
