@@ -520,6 +520,50 @@ class PrefillWorkload:
                                    1 / math.sqrt(self.d), k_cache=self.kc, v_cache=self.vc,
                                    slot_mapping=self.slots)
 
+    # ---- end to end: the step's inputs (q, k, v, slot mapping, cu_seqlens) copied in from
+    # one pinned host buffer, the public call, the fp32 output copied back to pinned memory
+    def e2e_setup(self):
+        parts = [self.p.q, self.p.k, self.p.v, self.slots.cpu(), self.p.cu_seqlens]
+        sizes = [t.numel() * t.element_size() for t in parts]
+        offs = [0]
+        for n in sizes:
+            offs.append((offs[-1] + n + 255) // 256 * 256)
+        self.stage_h = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
+        for t, o, n in zip(parts, offs, sizes):
+            self.stage_h[o:o + n] = t.contiguous().view(-1).view(torch.uint8)
+        self.stage_d = torch.empty(offs[-1], dtype=torch.uint8, device=self.q.device)
+        self.views = [self.stage_d[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts, offs, sizes)]
+        self.out_h = torch.empty(tuple(self.out.shape)).pin_memory()
+
+    def e2e_step(self):
+        q, k, v, slots, cu = self.views
+        self.stage_d.copy_(self.stage_h, non_blocking=True)
+        self.pkv.prefill_attention(self.out, q, k, v, cu, max(self.lengths), 1 / math.sqrt(self.d),
+                                   k_cache=self.kc, v_cache=self.vc, slot_mapping=slots)
+        self.out_h.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.stage_h.numel(), self.out_h.numel() * 4
+
+    # ---- CPU oracle on a bounded sample: the shortest prompts, about 300 GFLOP (seconds of fp64)
+    def oracle_sample(self):
+        import oracle
+        order = sorted(range(len(self.lengths)), key=lambda i: self.lengths[i])
+        pick, fl = [], 0
+        for i in order:
+            pick.append(i)
+            fl += self.lengths[i] * (self.lengths[i] + 1) // 2 * self.hq * 4 * self.d
+            if fl >= 3e11:
+                break
+        lens = [self.lengths[i] for i in pick]
+        p = gen.prefill_inputs(lens, self.hq, self.hkv, self.d, torch.bfloat16, seed=44)
+        threads = os.cpu_count() or 1
+
+        def run():
+            oracle.prefill(p.q, p.k, p.v, p.cu_seqlens, 1 / math.sqrt(self.d), nthreads=threads)
+            return fl
+        return run, threads, lens
+
 
 WORKLOADS = {
     "gqa70b": lambda: DecodeWorkload(gen.GQA_70B, gen.gqa_70b_lengths(), 32,
@@ -745,7 +789,42 @@ def bench_ours(args):
                               "memory and step k-1's output copied out on a second stream while "
                               "step k computes"}
 
+    else:
+        wl.e2e_setup()
+        for _ in range(2):
+            wl.e2e_step()
+        torch.cuda.synchronize()
+        e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        for _ in range(args.steps):
+            wl.e2e_step()
+        e_stop.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e_start.elapsed_time(e_stop), device)
+        # the output, as it reached host memory, equals the same step run on device inputs
+        wl.step(0)
+        if not torch.equal(wl.out_h, wl.out.cpu()):
+            raise RuntimeError("end-to-end output differs from the eager step")
+        h2d, d2h = wl.e2e_bytes()
+        res["e2e"] = {"value": whole_job_rate(wl.flops() * args.steps, world, e_ms) / 1e12, "unit": "TFLOP/s",
+                      "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "path": "public API call (prefill_attention writing the cache) on inputs copied in "
+                              "from one pinned host buffer, the fp32 output copied back to pinned host "
+                              "memory, one step after another"}
+
     # ---- CPU oracle baseline (rank 0, one GPU only)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and not is_decode:
+        run, threads, lens = wl.oracle_sample()
+        t0 = time.perf_counter()
+        fl = run()
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                               "sample": f"causal prefill of the {len(lens)} shortest prompts (lengths {lens}, "
+                                         f"same shapes, own seeded draws), fp64 C oracle, {threads} threads, "
+                                         f"{dt:.2f} s"}
     if world == 1 and rank == 0 and not args.no_cpu_baseline and is_decode:
         tb = wl.tensor_bound(hbm, bf16)
         n_seq = 1 if tb else min(args.cpu_seqs, wl.spec.batch)   # ~10-30 s of CPU work
