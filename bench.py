@@ -57,10 +57,15 @@ def peaks():
 
 
 def kernel_source_hash(files):
+    """Identity of the kernels' code: the sources with comments, trailing blanks and empty
+    lines removed, so that a comment edit keeps a profile summary valid."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "paged_kv_cache_165_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_165_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
 
 

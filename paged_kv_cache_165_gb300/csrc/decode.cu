@@ -18,7 +18,8 @@
 // thread, add in fp32.  The softmax weights P are split the same way for P.V.
 //
 // decode_chunked_kernel: one CTA per (sequence, KV-head group, chunk of blocks), whose
-//   warps take the chunk's blocks round-robin, each warp with a private TMA ring.  Chunks
+//   warps take the chunk's blocks round-robin, each warp with a private TMA ring (d 128,
+//   bs 16: two stages, three CTAs per SM, so one CTA starting a chunk overlaps two streaming).  Chunks
 //   of a unit write normalised partials; the last chunk to finish (an arrival counter, no
 //   waiting) merges them by log-sum-exp.  Many short-lived CTAs let the hardware scheduler
 //   balance SMs whose memory paths differ in speed (an equal static split of the pages
@@ -843,7 +844,7 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
     } else if (num_splits > 1) {
         chunk = (MBS + num_splits - 1) / num_splits;
     } else {
-        // enough (sequence, head-group, chunk) units for several waves of two CTAs per SM,
+        // enough (sequence, head-group, chunk) units for several waves of the CTAs an SM holds,
         // without making chunks shorter than 16 blocks
         const long long target = 8ll * std::max(sm_count, 1);
         while (chunk > 16 && units * ((MBS + chunk - 1) / chunk) < target)

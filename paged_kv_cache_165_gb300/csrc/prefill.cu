@@ -7,12 +7,13 @@
 // KV head floor(i/m) (limoncc.com "大语言模型研究15——注意力机制优化之KV缓存" §3.3).
 //
 // Tensor-core path (bf16, d in {64, 128}): 5th-generation tensor cores (tcgen05).  One
-// CTA per (query head, 128-query tile, sequence): TMA brings the Q tile once and 64-key
-// K/V tiles through a multi-stage ring (128-byte swizzle, mbarrier completion with bounded
-// waits); one thread issues S = Q K^T into tensor memory (double-buffered) and O += P V
-// into a tensor-memory accumulator; four warps own one query row per thread for the online
-// softmax (running max and sum, plumephp.com "KV Cache 优化与注意力机制加速" §2.2-§2.3) and
-// hand P back through shared memory as bf16 hi + lo parts, so the weights keep ~16 bits.
+// CTA per (query head, sequence, 128-query tile): TMA brings the Q tile once and 128-key
+// K/V tiles through two rings (128-byte swizzle, mbarrier completion with bounded waits);
+// one thread issues S = Q K^T into tensor memory (double-buffered), another O += P V into
+// a tensor-memory accumulator with P read from tensor memory; eight warps, two per query
+// row, run the online softmax (running max and sum, plumephp.com "KV Cache 优化与注意力
+// 机制加速" §2.2-§2.3) and write P back into tensor memory as bf16 hi + lo parts, so the
+// weights keep ~16 bits (details at prefill_tc_kernel).
 // Only key tiles at or below the diagonal are visited.
 // CUDA-core path (fp32 or other d): one warp per (query row, head).
 #include <math.h>
