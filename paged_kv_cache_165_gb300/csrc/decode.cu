@@ -1023,7 +1023,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
             else e = launch_tc<256, 16, 4, 2>(kp, tk, tv, grid, stream);
         } else {
             if (a.d == 64) e = launch_tc<64, 32, 4, 3>(kp, tk, tv, grid, stream);
-            else if (a.d == 128) e = launch_tc<128, 32, 4, 2>(kp, tk, tv, grid, stream);
+            else if (a.d == 128) e = launch_tc<128, 32, 2, 2>(kp, tk, tv, grid, stream);
             else e = launch_tc<256, 32, 2, 2>(kp, tk, tv, grid, stream);
         }
         if (e != cudaSuccess || plan.splits == 1 || plan.fused_merge) return e;
