@@ -849,6 +849,14 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
         const long long target = 8ll * std::max(sm_count, 1);
         while (chunk > 16 && units * ((MBS + chunk - 1) / chunk) < target)
             chunk = (chunk + 1) / 2;
+        // and no chunk longer than 8192 tokens (equal chunks): a long sequence among short
+        // ones then spreads over several blocks instead of running alone at the end of the
+        // launch (a ragged batch with one chunk per sequence ran 1.4x slower)
+        const int cap = std::max(16, 8192 / bs);
+        if (chunk > cap) {
+            const int parts = (MBS + cap - 1) / cap;
+            chunk = (MBS + parts - 1) / parts;
+        }
     }
     chunk = std::max(chunk, (MBS + kMergeMaxChunks - 1) / kMergeMaxChunks);   // merge capacity
     chunk = std::max(chunk, 1);

@@ -135,6 +135,18 @@ def test_cuda_core_path(dtype, d, bs):
         check(q, kc, vc, table, lens, 1 / math.sqrt(d), s, f"{dtype} d={d} bs={bs} s={s}")
 
 
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.bfloat16, 256),
+                                     (torch.float32, 40), (torch.float32, 1), (torch.float32, 3)])
+def test_separate_merge_of_many_chunks(dtype, d):
+    # more chunks than the decode kernel merges in place: the LSE merge kernel folds them in
+    # groups (one full pass of 4 x groups chunks, a ragged rest, groups with no chunk), and
+    # for head dims that are not a multiple of 4 one thread per column
+    lens = [5000, 1, 1700, 333, 4096]
+    q, kc, vc, table, lens_t = random_case(900 + d, lens, 8, 2, d, 16, dtype, poison=True)
+    for s in (9, 37, 300):
+        check(q, kc, vc, table, lens_t, 1 / math.sqrt(d), s, f"{dtype} d={d} s={s}")
+
+
 def test_tiny_config_append_then_decode():
     """Tiny workload: batch 2, 8 q / 2 kv heads, d 64, lengths {17, 40} + 1 appended, fp32."""
     inp = gen.tiny_inputs()
