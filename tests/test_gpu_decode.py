@@ -135,6 +135,20 @@ def test_cuda_core_path(dtype, d, bs):
         check(q, kc, vc, table, lens, 1 / math.sqrt(d), s, f"{dtype} d={d} bs={bs} s={s}")
 
 
+def test_long_sequence_in_a_ragged_batch_splits_into_capped_chunks():
+    # 160 sequences x 8 KV heads are units enough for one chunk per sequence, but one
+    # sequence holds 10000 tokens: automatic chunks hold at most 8192 tokens, so it splits
+    # into two chunks (313 and 312 of its 625 blocks), merged in place
+    lens = [10000] + [50 + 7 * i for i in range(159)]
+    B, hq, hkv, d, bs = len(lens), 8, 8, 128, 16
+    q, kc, vc, table, lens_t = random_case(4242, lens, hq, hkv, d, bs, torch.bfloat16, spare=2)
+    MBS = table.shape[1]
+    assert MBS == 625
+    counter_bytes = 256 << 10
+    assert pkv.decode_workspace_bytes(B, hq, hkv, d, bs, MBS, 0) == counter_bytes + B * hq * 2 * (d + 1) * 4
+    check(q, kc, vc, table, lens_t, 1 / math.sqrt(d), 0, "capped chunks")
+
+
 @pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.bfloat16, 256),
                                      (torch.float32, 40), (torch.float32, 1), (torch.float32, 3)])
 def test_separate_merge_of_many_chunks(dtype, d):
