@@ -51,6 +51,19 @@ def test_tensor_core_prefill_ragged(hq, hkv, d):
     assert_attn_close(lse, ref_lse, "prefill lse")
 
 
+@pytest.mark.parametrize("nseq", [31, 40])
+def test_tensor_core_prefill_one_long_prompt_among_short_ones(nseq):
+    # one 3000-token prompt (24 query tiles) among 30 or 39 short ones: most (prompt,
+    # query tile) blocks of the grid are past their prompt's end and return at once
+    lens = ([3000] + [17 * (k % 5) + 1 for k in range(39)] + [0])[:nseq]
+    p = gen.prefill_inputs(lens, 4, 1, 64, torch.bfloat16, seed=nseq)
+    out, lse = run_prefill(p, 0.125)
+    assert pkv.get_device_error() == 0
+    ref, ref_lse = oracle.prefill(p.q, p.k, p.v, p.cu_seqlens, 0.125, nthreads=8)
+    assert_attn_close(out, ref, f"prefill {nseq} prompts")
+    assert_attn_close(lse, ref_lse, f"prefill {nseq} prompts lse")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_tensor_core_prefill_running_max_jumps(d):
     # scale 1 and keys growing along each prompt: the row maximum moves by far more than
