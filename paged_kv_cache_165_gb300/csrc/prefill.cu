@@ -80,6 +80,7 @@ struct TcPrefillCfg {
     static constexpr int kThreads = 384;
     static_assert(kPLoCol + kTK / 2 <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(8 * 32 * (D / 2 + 4) * 4 <= NK * kSlotBytes, "the output staging fits the K ring");
 };
 
 // One CTA per (query head, sequence, 128-query tile), the tiles with the most key tiles
@@ -353,22 +354,35 @@ __global__ void __launch_bounds__(384, 1)
         if (ok) {
             tc_fence_after_sync();
             const float inv_l = 1.f / lr;
-            const bool row_ok = qpos < len;
-            float *dst = p.out + (static_cast<size_t>(start + qpos) * p.Hq + i) * D + h * (D / 2);
+            // O / l of the warp's 32 rows x D/2 columns, staged in the K ring (every MMA has
+            // completed, so it is free) so that each store writes whole row segments rather
+            // than one 16-byte piece of 32 rows; the pitch spreads the rows over the banks
+            constexpr int HW = D / 2, PITCH = HW + 4;
+            float *stage = reinterpret_cast<float *>(smem + Cfg::kOffK) + warp * 32 * PITCH;
+            fence_proxy_async_smem();
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t ov[32];
-                tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
+                tmem_ld32(lane_base + Cfg::kOCol + h * HW + cc * 32, ov);
                 tmem_ld_wait();
-                if (row_ok) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(dst + cc * 32 + e) =
-                            make_float4(__uint_as_float(ov[e]) * inv_l, __uint_as_float(ov[e + 1]) * inv_l,
-                                        __uint_as_float(ov[e + 2]) * inv_l, __uint_as_float(ov[e + 3]) * inv_l);
-                }
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(stage + lane * PITCH + cc * 32 + e) =
+                        make_float4(__uint_as_float(ov[e]) * inv_l, __uint_as_float(ov[e + 1]) * inv_l,
+                                    __uint_as_float(ov[e + 2]) * inv_l, __uint_as_float(ov[e + 3]) * inv_l);
             }
-            if (row_ok && h == 0 && p.lse != nullptr)
+            __syncwarp();
+            const int row0 = q0 + ((warp & 3) << 5);
+            const int nrows = min(32, len - row0);   // rows of the warp inside the sequence
+            for (int rr = 0; rr < nrows; ++rr) {
+                float *dst = p.out + (static_cast<size_t>(start + row0 + rr) * p.Hq + i) * D + h * HW;
+                if constexpr (HW == 64)
+                    *reinterpret_cast<float2 *>(dst + 2 * lane) =
+                        *reinterpret_cast<const float2 *>(stage + rr * PITCH + 2 * lane);
+                else
+                    dst[lane] = stage[rr * PITCH + lane];
+            }
+            if (qpos < len && h == 0 && p.lse != nullptr)
                 p.lse[static_cast<size_t>(start + qpos) * p.Hq + i] = (m_ref + log2f(lr)) * kLn2;
         }
     }
@@ -516,7 +530,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, pkv_dtype dt, cudaStream_t stre
     kp.m = a.Hq / a.Hkv;
     kp.scale_log2 = a.scale * kLog2e;
     // the tcgen05 grid's z counts 128-query tiles (at most 65535 of them)
+    // the tcgen05 kernel writes out in 8-byte pieces
     if (prefill_tensor_core_ok(dt, a.d, a.q, a.k, a.v, a.T, a.Hq, a.Hkv) &&
+        reinterpret_cast<uintptr_t>(a.out) % 8 == 0 &&
         static_cast<long long>(a.max_seqlen) <= 65535ll * 128)
         return a.d == 64 ? launch_prefill_tc<64>(a, kp, stream) : launch_prefill_tc<128>(a, kp, stream);
     return dt == PKV_F32 ? launch_prefill_simt<float>(a, kp, stream)
