@@ -977,6 +977,12 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     kp.v_scale = a.v_scale;
     kp.q_per_tile = plan.q_per_tile;
     kp.qtiles = plan.qtiles;
+    // the tcgen05 kernel with one query tile per sequence (decode, verification): each block
+    // takes a whole chunk for a long time, so start the long sequences first (a block ranks
+    // up to 256 lengths at its start; a 4-token verification step on ragged lengths: 4.7%
+    // faster).  With many query tiles per sequence the blocks are fine-grained already and
+    // the ranking cost 1%.
+    kp.longest_first = plan.umma && plan.qtiles == 1 && a.B <= 256 ? 1 : 0;
     if (plan.splits > 1) {
         uint8_t *ws = static_cast<uint8_t *>(a.workspace);
         kp.counters = plan.fused_merge ? reinterpret_cast<unsigned *>(ws) : nullptr;

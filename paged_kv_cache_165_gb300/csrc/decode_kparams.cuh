@@ -30,6 +30,7 @@ struct DecodeKParams {
     const float *k_scale, *v_scale;   // FP8 caches: fp32 scale per row [NB][Hkv][bs]
     int q_per_tile;   // tcgen05 kernel: query rows of a sequence per block (1 for decode)
     int qtiles;       // tcgen05 kernel: query tiles per sequence (grid z = B * qtiles)
+    int longest_first;   // tcgen05 kernel: grid z ranks the sequences by length, longest first
 };
 
 // Sequence length after validation; an invalid length counts as empty.

@@ -93,7 +93,29 @@ __global__ void __launch_bounds__(384, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, kvh = blockIdx.y;
-    const int b = blockIdx.z / p.qtiles, qt = blockIdx.z % p.qtiles;
+    const int qt = blockIdx.z % p.qtiles;
+    int b = blockIdx.z / p.qtiles;
+    if (p.longest_first) {
+        // grid z ranks the sequences by length, longest first (ties: lower index first), so
+        // that with lengths that differ the long blocks start first and the short ones fill
+        // the end of the launch; the K ring is free scratch until the first copies
+        int *len_s = reinterpret_cast<int *>(smem + Cfg::kOffK);
+        for (int x = threadIdx.x; x < p.B; x += blockDim.x) len_s[x] = checked_len(p, x, BS, false);
+        __syncthreads();
+        for (int x = threadIdx.x; x < p.B; x += blockDim.x) {
+            const int lx = len_s[x];
+            int rank = 0;
+            for (int y = 0; y < p.B; ++y) {
+                const int ly = len_s[y];
+                rank += (ly > lx || (ly == lx && y < x)) ? 1 : 0;
+            }
+            if (rank == b) len_s[p.B] = x;   // ranks are a permutation: exactly one x
+        }
+        __syncthreads();
+        b = len_s[p.B];
+        fence_proxy_async_smem();   // the copies that will land here come after these reads
+        __syncthreads();
+    }
     const bool report = threadIdx.x == 0 && split == 0 && kvh == 0 && qt == 0;
     // the sequence's query rows c0 .. c0+nq-1 (decode: row b) sit at positions L-nq ..
     // L-1; this block takes rows q0 .. q0+nqt-1 of them, slot = (row - q0) * m + head
