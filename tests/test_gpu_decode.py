@@ -113,6 +113,17 @@ def test_large_group_running_max_jumps(hq, hkv, d):
         check(q, kc, vc, table, clens, 1.0, s, f"max jumps hq={hq} d={d} s={s}")
 
 
+@pytest.mark.parametrize("nseq", [200, 300])
+def test_large_group_ragged_batch_in_both_launch_orders(nseq):
+    # the tcgen05 kernel takes sequences longest first when there are at most 256 of them
+    # (each block ranks the lengths) and in index order beyond; both against the oracle
+    g = gen.generator(nseq)
+    lens = [int(x) for x in torch.randint(1, 400, (nseq,), generator=g)]
+    lens[7], lens[nseq - 3] = 1500, 0
+    q, kc, vc, table, clens = random_case(nseq + 11, lens, 16, 1, 64, 16, torch.bfloat16)
+    check(q, kc, vc, table, clens, 0.125, 0, f"{nseq} sequences")
+
+
 def test_large_group_bad_block_id_reads_zeros():
     q, kc, vc, table, lens = random_case(81, [200, 700], 64, 1, 128, 16, torch.bfloat16)
     bad_table = table.clone()
