@@ -4,8 +4,10 @@ Default workload: Llama-2-70B-shaped GQA decode, one layer -- batch 64, 64 query
 8 KV heads (m = 8), head_dim 128, cached lengths uniform in [512, 8192], bf16
 K/V, block size 16, shuffled physical blocks, a cycle of 32 consecutive decode
 steps that each append one token per sequence.  One bench step = one decode step
-of the whole path: kv_append of the 64 new tokens, then paged_decode_attention
-(split-K partials + log-sum-exp merge) for all 64 x 64 heads.
+of the whole path through pkv_decode_step: the 64 new tokens appended to the cache
+and the attention (split-K partials + log-sum-exp merge) for all 64 x 64 heads, in
+one launch (the block that reads a sequence's last page writes its new token
+first).  Workloads the library cannot fuse call kv_append, then the attention.
 
 Metric: KV-cache bytes read per second (logical bytes: every cached token's K and
 V of every KV head, 2 bytes each), with tokens/s per layer beside it.  Other
@@ -285,10 +287,17 @@ class DecodeWorkload:
         self.out_h = [torch.empty((R, Hq, d)).pin_memory() for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(device=device)
         self.pkv = pkv
-        # kv_append, then the kernels the decode call enqueues (as the library plans it)
-        self.launches_per_step = 1 + pkv.paged_attention_kernel_launches(
-            B, R, self.qlen, Hq, Hkv, d, bs, self.table.shape[1], nb, torch.uint8 if self.fp8 else s.cache_dtype,
-            self.window, self.num_splits)
+        # a plain decode step (one new token per sequence, no window, bf16/fp32 cache) goes
+        # through pkv_decode_step, which appends inside the attention launch where the plan
+        # allows; otherwise kv_append, then the kernels the attention call enqueues
+        self.step_call = not self.fp8 and self.qlen == 1 and self.window <= 0
+        if self.step_call:
+            self.launches_per_step = pkv.decode_step_kernel_launches(
+                B, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype, self.num_splits)
+        else:
+            self.launches_per_step = 1 + pkv.paged_attention_kernel_launches(
+                B, R, self.qlen, Hq, Hkv, d, bs, self.table.shape[1], nb,
+                torch.uint8 if self.fp8 else s.cache_dtype, self.window, self.num_splits)
 
     def decode(self, out, q, clens, lse=None):
         """The public decode call: pkv_paged_decode_attention, with a sliding window
@@ -315,19 +324,31 @@ class DecodeWorkload:
         self.cache_append(self.k_new[c], self.v_new[c], self.slots[c])
 
     def cache_append(self, k_new, v_new, slots):
+        """Copy-on-write of shared blocks, then the appends (which a decode step does itself)."""
         if self.copies is not None:   # copy-on-write of shared blocks before the writes
             self.pkv.kv_block_copy(self.k_cache, self.v_cache, self.copies)
+        if self.step_call:
+            return
         if self.fp8:
             self.pkv.kv_append_fp8(k_new, v_new, self.k_cache, self.v_cache, self.k_scale, self.v_scale, slots)
         else:
             self.pkv.kv_append(k_new, v_new, self.k_cache, self.v_cache, slots)
 
+    def attend_call(self, out, q, k_new, v_new, slots, clens, lse=None):
+        """The attention (with the step's appends, for a decode step) through the public API."""
+        if self.step_call:
+            self.pkv.decode_step(out, q, k_new, v_new, slots, self.k_cache, self.v_cache, self.table, clens,
+                                 self.spec.scale, lse=lse, num_splits=self.num_splits, workspace=self.ws)
+        else:
+            self.decode(out, q, clens, lse=lse)
+
     def attend(self, c):
-        self.decode(self.out, self.q[c], self.clens[c], lse=self.lse)
+        self.attend_call(self.out, self.q[c], self.k_new[c], self.v_new[c], self.slots[c], self.clens[c],
+                         lse=self.lse)
 
     def e2e_capture(self):
         """One CUDA graph per (cycle step c, buffer parity) of the public API calls a serving
-        loop makes per step: compute of step k (kv_append + paged_decode_attention on the
+        loop makes per step: compute of step k (decode_step, or kv_append + the attention, on the
         inputs in staging buffer k % 2) alongside, on a copy stream, the host->device copy of
         step k+1's inputs from pinned host memory into the other buffer and the
         device->host copy of step k-1's output.  Replaying them keeps the host out of the
@@ -349,7 +370,7 @@ class DecodeWorkload:
                         self.out_h[1 - buf].copy_(self.out_e[1 - buf], non_blocking=True)
                     q, kn, vn, sl, cl = self.views[buf]
                     self.cache_append(kn, vn, sl)
-                    self.decode(self.out_e[buf], q, cl)
+                    self.attend_call(self.out_e[buf], q, kn, vn, sl, cl)
                     join = torch.cuda.Event()
                     join.record(cp)
                     cs.wait_event(join)
@@ -797,7 +818,7 @@ def bench_ours(args):
                       / (1e12 if tb else 1e9), "unit": res["unit"],
                       "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h,
-                      "path": "public API calls (kv_append, paged_decode_attention) replayed as one "
+                      "path": "public API calls (decode_step, or kv_append then the attention) replayed as one "
                               "CUDA graph per step; step k+1's inputs copied in from pinned host "
                               "memory and step k-1's output copied out on a second stream while "
                               "step k computes"}

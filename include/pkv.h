@@ -188,6 +188,39 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
                                       size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_decode_step -- one decode step: the new token of each sequence is appended to the
+ * cache, then attended with the rest of the sequence.
+ *
+ * The same results as pkv_kv_append(k_new, v_new, ..., slot_mapping, T = B) followed by
+ * pkv_paged_decode_attention(...) on the same arguments (the new K/V are written into the
+ * cache once, zwjcode.cn "KV Cache 的增量解码" §04, §10; the attention as in
+ * pkv_paged_decode_attention).  Where the plan allows it (bf16 caches on the tensor-core
+ * path with at most 8 query heads per KV head, 16-byte aligned k_new and v_new) the
+ * append runs inside the attention launch: the block that reads a sequence's last page
+ * writes the new rows there first, so the step is one launch instead of two.
+ *
+ *   k_new, v_new  [B][Hkv][d], element type dt: the new token of sequence b is row b
+ *   slot_mapping  int64 [B]: its slot, which must be that of position
+ *                 context_lens[b] - 1 (block_table[b][(len-1)/bs] * bs + (len-1) % bs);
+ *                 < 0: sequence b has no new token this step.  Its block must belong to
+ *                 sequence b alone (copy-on-write before the step when it is shared).
+ *                 When the append runs inside the attention launch, a slot other than the
+ *                 last position's (or any slot for an empty sequence) sets
+ *                 PKV_DEVERR_SLOT and is not written; otherwise kv_append's rules apply.
+ *   the other arguments as pkv_paged_decode_attention (k_cache, v_cache are written).
+ */
+pkv_status pkv_decode_step(float *out, float *lse, const float *q, const void *k_new, const void *v_new,
+                           const int64_t *slot_mapping, void *k_cache, void *v_cache, pkv_dtype dt,
+                           const int32_t *block_table, const int32_t *context_lens, int B, int Hq,
+                           int Hkv, int d, int bs, int MBS, int NB, float scale, int num_splits,
+                           void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Kernels one pkv_decode_step call with these sizes enqueues (16-byte aligned new rows and
+ * caches assumed), or -1 when the call would be rejected; 0 for B == 0. */
+int pkv_decode_step_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
+                                    int num_splits);
+
+/*
  * pkv_paged_attention -- queries at the end of each cached sequence: several per
  * sequence, causal, with an optional sliding window.
  *

@@ -12,6 +12,8 @@ from ._binding import (  # noqa: F401
     PKV_FP8_E4M3,
     PkvError,
     decode_kernel_launches,
+    decode_step,
+    decode_step_kernel_launches,
     decode_workspace_bytes,
     get_device_error,
     header_functions,

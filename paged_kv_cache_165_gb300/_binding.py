@@ -78,6 +78,10 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P,
                                              Z, P]
     L.pkv_paged_decode_attention.restype = I
+    L.pkv_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, Z, P]
+    L.pkv_decode_step.restype = I
+    L.pkv_decode_step_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I]
+    L.pkv_decode_step_kernel_launches.restype = I
     L.pkv_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I,
                                                      F, I, P]
     L.pkv_paged_decode_attention_noalloc.restype = I
@@ -252,6 +256,46 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table),
         _ptr(context_lens), B, Hq, Hkv, d, bs, MBS, NB, float(scale), int(num_splits),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def decode_step(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, context_lens, scale,
+                lse=None, num_splits=0, workspace=None, stream=None) -> None:
+    """One decode step: k_new/v_new [B][Hkv][d] (row b = sequence b's new token) go to
+    slot_mapping[b] (int64, < 0: none), then out [B][Hq][d] fp32 = attention of q over the
+    cache (context_lens count the new tokens).  One launch where the library fuses them."""
+    _cuda("k_cache", k_cache)
+    dt = _dtype(k_cache)
+    _cuda("v_cache", v_cache, k_cache.dtype)
+    _cuda("k_new", k_new, k_cache.dtype)
+    _cuda("v_new", v_new, k_cache.dtype)
+    _cuda("slot_mapping", slot_mapping, torch.int64)
+    _cuda("q", q, torch.float32)
+    _cuda("out", out, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    if lse is not None:
+        _cuda("lse", lse, torch.float32)
+    NB, Hkv, bs, d = k_cache.shape
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d) or tuple(k_new.shape) != (B, Hkv, d) or \
+            tuple(v_new.shape) != (B, Hkv, d) or slot_mapping.numel() != B or block_table.dim() != 2 or \
+            block_table.shape[0] != B or context_lens.numel() != B or \
+            (lse is not None and lse.numel() != B * Hq):
+        raise ValueError("decode_step: shapes do not match")
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pkv_decode_step(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), dt, _ptr(block_table), _ptr(context_lens), B, Hq, Hkv, d, bs, block_table.shape[1],
+        NB, float(scale), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def decode_step_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, dtype, num_splits=0) -> int:
+    """Kernels one decode_step call with these sizes enqueues (-1: rejected)."""
+    return int(lib().pkv_decode_step_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, _DTYPES[dtype],
+                                                     int(num_splits)))
 
 
 def paged_attention_workspace_bytes(B, Tq, max_q, Hq, Hkv, d, bs, MBS, window=0, num_splits=0) -> int:

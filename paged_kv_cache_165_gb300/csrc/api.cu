@@ -272,6 +272,62 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_decode_attention launch");
 }
 
+pkv_status pkv_decode_step(float *out, float *lse, const float *q, const void *k_new, const void *v_new,
+                           const int64_t *slot_mapping, void *k_cache, void *v_cache, pkv_dtype dt,
+                           const int32_t *block_table, const int32_t *context_lens, int B, int Hq,
+                           int Hkv, int d, int bs, int MBS, int NB, float scale, int num_splits,
+                           void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    int eb = 0;
+    if (!elem_size(dt, &eb) || !attention_dtype(dt))
+        return fail(PKV_ERR_UNSUPPORTED, "decode_step: element type %d", dt);
+    pkv_status s = check_decode_sizes(B, Hq, Hkv, d, bs, MBS);
+    if (s != PKV_OK) return s;
+    if (NB < 1 || num_splits < 0)
+        return fail(PKV_ERR_INVALID_ARG, "decode_step: NB=%d num_splits=%d", NB, num_splits);
+    if (B == 0) return PKV_OK;
+    if (!out || !q || !k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !block_table ||
+        !context_lens)
+        return fail(PKV_ERR_INVALID_ARG, "decode_step: null pointer");
+    if (reinterpret_cast<uintptr_t>(q) % 8 != 0)
+        return fail(PKV_ERR_INVALID_ARG, "decode_step: q must be 8-byte aligned");
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != PKV_OK) return s;
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count,
+                                        aligned16(k_cache) && aligned16(v_cache), aligned16(q));
+    if (plan.workspace_bytes > 0 &&
+        (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
+         reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+        return fail(PKV_ERR_WORKSPACE, "decode_step: needs %zu bytes of 16-byte aligned workspace, got %zu",
+                    plan.workspace_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
+    DecodeArgs a{out, lse, q, k_cache, v_cache, block_table, context_lens,
+                 B, Hq, Hkv, d, bs, MBS, NB, scale, workspace, st->err};
+    cudaError_t e = cudaSuccess;
+    if (decode_fuses_append(plan, dt, Hq, Hkv, k_new, v_new)) {
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.new_slots = slot_mapping;
+    } else {
+        e = launch_kv_append(k_new, v_new, k_cache, v_cache, eb, slot_mapping, B, Hkv, d, bs, NB, st->err,
+                             stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_step append launch");
+    }
+    e = launch_decode(a, plan, dt, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "decode_step launch");
+}
+
+int pkv_decode_step_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
+                                    int num_splits) {
+    const int n = pkv_decode_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits);
+    if (n <= 0) return n;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != PKV_OK) return -1;
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count, true, true);
+    // new rows from a 16-byte aligned allocation (as tensors are)
+    static const uint4 aligned{};
+    return n + (decode_fuses_append(plan, dt, Hq, Hkv, &aligned, &aligned) ? 0 : 1);
+}
+
 size_t pkv_paged_attention_workspace_bytes(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs,
                                            int MBS, int window, int num_splits) {
     if (check_decode_sizes(B, Hq, Hkv, d, bs, MBS) != PKV_OK || Tq < 0 || max_q < 0 || window < 0 ||

@@ -241,12 +241,47 @@ __global__ void __launch_bounds__(NW * 32)
         // Nothing to read.  Chunk 0 of an empty sequence writes out = 0, lse = -inf; any
         // other empty chunk is simply absent (the merge counts chunks from the length).
         if (split == 0) {
+            // a new token for a sequence that holds none has no position: flagged, not written
+            if (p.new_slots != nullptr && threadIdx.x == 0 && len == 0 && __ldg(p.new_slots + b) >= 0)
+                raise_error(p.err, PKV_DEVERR_SLOT);
             for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32)
                 p.out[(static_cast<size_t>(b) * p.Hq + head0 + idx / D) * D + idx % D] = 0.f;
             if (p.lse != nullptr && threadIdx.x < nheads)
                 p.lse[static_cast<size_t>(b) * p.Hq + head0 + threadIdx.x] = -INFINITY;
         }
         return;
+    }
+
+    if (p.new_slots != nullptr && pg1 == n_pages) {
+        // The step's new token (the append fused into this launch): the block that reads
+        // the sequence's last page writes the token's K and V rows of its KV head there,
+        // before any copy of the page.  The slot must be that of the last position
+        // len - 1; another slot is flagged and not written.
+        if (warp == 0) {
+            const long long slot = __ldg(p.new_slots + b);
+            if (slot >= 0) {
+                const int pos = len - 1;
+                const int phys = __ldg(p.block_table + static_cast<size_t>(b) * p.MBS + pos / BS);
+                const bool ok = phys >= 0 && phys < p.NB && slot == static_cast<long long>(phys) * BS + pos % BS;
+                if (!ok) {
+                    if (lane == 0) raise_error(p.err, PKV_DEVERR_SLOT);
+                } else {
+                    const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D;
+                    const size_t dst = ((static_cast<size_t>(phys) * p.Hkv + kvh) * BS + pos % BS) * D;
+                    const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.k_new) + src);
+                    const uint4 *vn = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.v_new) + src);
+                    uint4 *kd = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.k_cache_w) + dst);
+                    uint4 *vd = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.v_cache_w) + dst);
+                    for (int u = lane; u < D / 8; u += 32) {
+                        kd[u] = __ldg(kn + u);
+                        vd[u] = __ldg(vn + u);
+                    }
+                    fence_proxy_async_global();   // the page's copies come after these writes
+                }
+            }
+        }
+        __syncthreads();
+        fence_proxy_async_global();
     }
 
     if (lane == 0) {
@@ -896,6 +931,15 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
 
 }  // namespace
 
+// The chunked bf16 kernel with one head tile per KV head (m <= 8) writes the step's new
+// tokens itself: exactly one block reads the page that holds a sequence's last position
+// for each KV head.  Its 16-byte row copies need 16-byte aligned new rows.
+bool decode_fuses_append(const DecodePlan &plan, pkv_dtype dt, int Hq, int Hkv, const void *k_new,
+                         const void *v_new) {
+    return dt == PKV_BF16 && plan.tensor_core && !plan.group && !plan.umma && Hq / Hkv <= 8 &&
+           reinterpret_cast<uintptr_t>(k_new) % 16 == 0 && reinterpret_cast<uintptr_t>(v_new) % 16 == 0;
+}
+
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
                        int num_splits, int sm_count, bool caches_aligned, bool q_aligned) {
     DecodePlan plan{};
@@ -977,6 +1021,13 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     kp.v_scale = a.v_scale;
     kp.q_per_tile = plan.q_per_tile;
     kp.qtiles = plan.qtiles;
+    if (a.new_slots != nullptr && decode_fuses_append(plan, dt, a.Hq, a.Hkv, a.k_new, a.v_new)) {
+        kp.k_new = a.k_new;
+        kp.v_new = a.v_new;
+        kp.new_slots = a.new_slots;
+        kp.k_cache_w = const_cast<void *>(a.k_cache);
+        kp.v_cache_w = const_cast<void *>(a.v_cache);
+    }
     // the tcgen05 kernel with one query tile per sequence (decode, verification): each block
     // takes a whole chunk for a long time, so start the long sequences first (a block ranks
     // up to 256 lengths at its start; a 4-token verification step on ragged lengths: 4.7%

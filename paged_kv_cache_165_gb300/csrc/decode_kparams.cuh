@@ -31,6 +31,10 @@ struct DecodeKParams {
     int q_per_tile;   // tcgen05 kernel: query rows of a sequence per block (1 for decode)
     int qtiles;       // tcgen05 kernel: query tiles per sequence (grid z = B * qtiles)
     int longest_first;   // tcgen05 kernel: grid z ranks the sequences by length, longest first
+    // the step's new tokens written inside the chunked kernel (nullptr: appended before)
+    const void *k_new, *v_new;   // [B][Hkv][d]
+    const int64_t *new_slots;    // [B]; < 0: no new token
+    void *k_cache_w, *v_cache_w; // the caches, for those writes
 };
 
 // Sequence length after validation; an invalid length counts as empty.

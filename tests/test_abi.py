@@ -24,7 +24,7 @@ def test_header_declares_the_boundary():
                "pkv_prefill_attention", "pkv_decode_workspace_bytes", "pkv_decode_kernel_launches",
                "pkv_paged_attention", "pkv_paged_attention_workspace_bytes",
                "pkv_paged_attention_kernel_launches", "pkv_kv_append_fp8",
-               "pkv_paged_decode_attention_fp8",
+               "pkv_paged_decode_attention_fp8", "pkv_decode_step", "pkv_decode_step_kernel_launches",
                "pkv_get_device_error",
                "pkv_status_string", "pkv_last_error", "pkv_version"]:
         assert fn in names
@@ -85,3 +85,19 @@ def test_decode_kernel_launches_rejects_what_decode_rejects(L):
     assert L.pkv_decode_kernel_launches(4, 8, 8, 128, 16, 8, 64, 7, 0) == -1   # element type
     assert L.pkv_decode_kernel_launches(4, 8, 8, 128, 16, 8, 64, 1, -1) == -1  # num_splits
     assert L.pkv_decode_kernel_launches(0, 8, 8, 128, 16, 8, 64, 1, 0) == 0
+
+
+def test_decode_step_rejects_bad_arguments_before_any_launch(L):
+    P = ctypes.c_void_p
+    args = dict(B=2, Hq=8, Hkv=2, d=64, bs=16, MBS=4, NB=8)
+    def call(**kw):
+        a = {**args, **kw}
+        nz = P(16)   # never dereferenced: validation fails first
+        return L.pkv_decode_step(nz, None, nz, nz, nz, nz, nz, nz, 1, nz, nz, a["B"], a["Hq"], a["Hkv"],
+                                 a["d"], a["bs"], a["MBS"], a["NB"], 0.1, 0, None, 0, None)
+    assert call(Hq=10, Hkv=3) == 1        # Hq % Hkv
+    assert call(NB=0) == 1
+    assert call(B=0) == 0                 # nothing to do
+    assert L.pkv_decode_step(P(16), None, P(16), None, P(16), P(16), P(16), P(16), 1, P(16), P(16),
+                             2, 8, 2, 64, 16, 4, 8, 0.1, 0, None, 0, None) == 1   # null k_new
+    assert L.pkv_decode_step_kernel_launches(2, 10, 3, 64, 16, 4, 8, 1, 0) == -1

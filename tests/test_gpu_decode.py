@@ -322,3 +322,104 @@ def test_decode_kernel_launches_counts_what_the_call_enqueues(hq, hkv, lens, num
     ref, ref_lse = oracle.paged_decode(q, kc, vc, table, clens, 1 / math.sqrt(128))
     assert_attn_close(out, ref, "out")
     assert_attn_close(lse, ref_lse, "lse")
+
+
+# ------------------------------------------------------------------ decode_step (append + attend)
+
+def _step_case(seed, lens, hq, hkv, d, bs, dtype):
+    """A cache with lens[b] - 1 tokens written, the new token of each sequence, its slot
+    (the last position's), and lens counting it."""
+    q, kc, vc, table, clens = random_case(seed, lens, hq, hkv, d, bs, dtype)
+    g = gen.generator(seed + 1)
+    k_new = gen.randn(g, (len(lens), hkv, d), dtype)
+    v_new = gen.randn(g, (len(lens), hkv, d), dtype)
+    slots = torch.tensor([oracle.slot_of(table[b], n - 1, bs) if n > 0 else -1 for b, n in enumerate(lens)],
+                         dtype=torch.int64)
+    return q, kc, vc, table, clens, k_new, v_new, slots
+
+
+def _run_step(q, kc, vc, table, clens, k_new, v_new, slots, scale, num_splits, fused=True):
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    out = torch.full((B, Hq, d), float("nan"), device="cuda")
+    lse = torch.full((B, Hq), float("nan"), device="cuda")
+    ws = torch.zeros(max(16, pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, table.shape[1], num_splits)),
+                     dtype=torch.uint8, device="cuda")
+    gk, gv = dev(kc), dev(vc)
+    if fused:
+        pkv.decode_step(out, dev(q), dev(k_new), dev(v_new), dev(slots), gk, gv, dev(table), dev(clens), scale,
+                        lse=lse, num_splits=num_splits, workspace=ws)
+    else:
+        pkv.kv_append(dev(k_new), dev(v_new), gk, gv, dev(slots))
+        pkv.paged_decode_attention(out, dev(q), gk, gv, dev(table), dev(clens), scale, lse=lse,
+                                   num_splits=num_splits, workspace=ws)
+    torch.cuda.synchronize()
+    return out, lse, gk.cpu(), gv.cpu()
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,dtype", [
+    (64, 8, 128, 16, torch.bfloat16),    # the chunked kernel: the append runs inside it
+    (8, 8, 64, 32, torch.bfloat16),
+    (32, 8, 256, 16, torch.bfloat16),
+    (16, 1, 128, 16, torch.bfloat16),    # tcgen05 kernel: kv_append first
+    (8, 2, 64, 16, torch.float32),       # CUDA-core path: kv_append first
+])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_decode_step_equals_append_then_decode(hq, hkv, d, bs, dtype, num_splits):
+    lens = [1, 16, 17, 700, 2049, 33, 5, 1000]
+    case = _step_case(hq + d + bs + num_splits, lens, hq, hkv, d, bs, dtype)
+    case[7][2] = -1                                   # sequence 2 has no new token this step
+    out, lse, kc, vc = _run_step(*case, 1 / math.sqrt(d), num_splits)
+    assert pkv.get_device_error() == 0
+    ref_out, ref_lse, ref_kc, ref_vc = _run_step(*case, 1 / math.sqrt(d), num_splits, fused=False)
+    assert torch.equal(kc, ref_kc) and torch.equal(vc, ref_vc)
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    q, kc0, vc0, table, clens, k_new, v_new, slots = case
+    oracle.kv_append(kc0, vc0, k_new, v_new, slots)
+    ref, ref_l = oracle.paged_decode(q, kc0, vc0, table, clens, 1 / math.sqrt(d))
+    assert_attn_close(out, ref, "decode_step out")
+    assert_attn_close(lse, ref_l, "decode_step lse")
+
+
+def test_decode_step_flags_a_slot_that_is_not_the_last_position():
+    lens = [40, 0, 300]
+    q, kc, vc, table, clens, k_new, v_new, slots = _step_case(77, lens, 16, 2, 128, 16, torch.bfloat16)
+    slots[0] = oracle.slot_of(table[0], 3, 16)        # an earlier position of sequence 0
+    slots[1] = 5                                       # an empty sequence has no position
+    out, lse, gk, gv = _run_step(q, kc, vc, table, clens, k_new, v_new, slots, 0.1, 0)
+    assert pkv.get_device_error() & pkv.DEVERR["slot"]
+    want_k, want_v = kc.clone(), vc.clone()          # only sequence 2's token is written
+    oracle.kv_append(want_k, want_v, k_new[2:], v_new[2:], slots[2:])
+    assert torch.equal(gk, want_k) and torch.equal(gv, want_v)
+
+
+def test_decode_step_with_unaligned_new_rows_appends_first():
+    lens = [100, 200]
+    q, kc, vc, table, clens, k_new, v_new, slots = _step_case(9, lens, 16, 2, 128, 16, torch.bfloat16)
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    big_k = torch.zeros(B * Hkv * d + 1, dtype=torch.bfloat16, device="cuda")
+    big_v = torch.zeros_like(big_k)
+    kn = big_k[1:].view(B, Hkv, d)                    # 2-byte aligned, not 16
+    vn = big_v[1:].view(B, Hkv, d)
+    kn.copy_(dev(k_new))
+    vn.copy_(dev(v_new))
+    out = torch.empty((B, Hq, d), device="cuda")
+    gk, gv = dev(kc), dev(vc)
+    ws = torch.zeros(max(16, pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, table.shape[1], 0)),
+                     dtype=torch.uint8, device="cuda")
+    pkv.decode_step(out, dev(q), kn, vn, dev(slots), gk, gv, dev(table), dev(clens), 0.1, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    oracle.kv_append(kc, vc, k_new, v_new, slots)
+    assert torch.equal(gk.cpu(), kc) and torch.equal(gv.cpu(), vc)
+    assert_attn_close(out, oracle.paged_decode(q, kc, vc, table, clens, 0.1)[0], "unaligned rows")
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype,fused", [(64, 8, 128, torch.bfloat16, True),
+                                                   (16, 1, 128, torch.bfloat16, False),
+                                                   (8, 2, 64, torch.float32, False)])
+def test_decode_step_kernel_launches(hq, hkv, d, dtype, fused):
+    B, bs, MBS, NB = 8, 16, 64, 600
+    n = pkv.decode_kernel_launches(B, hq, hkv, d, bs, MBS, NB, dtype, 0)
+    assert pkv.decode_step_kernel_launches(B, hq, hkv, d, bs, MBS, NB, dtype, 0) == n + (0 if fused else 1)
