@@ -287,10 +287,14 @@ class DecodeWorkload:
         self.out_h = [torch.empty((R, Hq, d)).pin_memory() for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(device=device)
         self.pkv = pkv
-        # a plain decode step (one new token per sequence, no window, bf16/fp32 cache) goes
-        # through pkv_decode_step, which appends inside the attention launch where the plan
-        # allows; otherwise kv_append, then the kernels the attention call enqueues
-        self.step_call = not self.fp8 and self.qlen == 1 and self.window <= 0
+        # a plain decode step (one new token per sequence, no window) goes through
+        # pkv_decode_step where the library appends inside the attention launch (as many
+        # launches as the attention alone); otherwise kv_append, then the attention call, so
+        # that the timed attention call is the attention's launches alone
+        self.step_call = not self.fp8 and self.qlen == 1 and self.window <= 0 and \
+            pkv.decode_step_kernel_launches(B, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype,
+                                            self.num_splits) == \
+            pkv.decode_kernel_launches(B, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype, self.num_splits)
         if self.step_call:
             self.launches_per_step = pkv.decode_step_kernel_launches(
                 B, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype, self.num_splits)
