@@ -8,6 +8,8 @@
  *   pkv_paged_decode_attention  one query per sequence against its paged cache,
  *                               GQA groups sharing each K/V tile, split-K with a
  *                               log-sum-exp merge for long contexts
+ *   pkv_decode_step             a decode step: each sequence's new token appended, then
+ *                               attended (one launch where the plan allows)
  *   pkv_prefill_attention       varlen causal attention over cu_seqlens that also
  *                               writes the cache
  *
@@ -194,10 +196,11 @@ pkv_status pkv_paged_decode_attention(float *out, float *lse, const float *q, co
  * The same results as pkv_kv_append(k_new, v_new, ..., slot_mapping, T = B) followed by
  * pkv_paged_decode_attention(...) on the same arguments (the new K/V are written into the
  * cache once, zwjcode.cn "KV Cache 的增量解码" §04, §10; the attention as in
- * pkv_paged_decode_attention).  Where the plan allows it (bf16 caches on the tensor-core
- * path with at most 8 query heads per KV head, 16-byte aligned k_new and v_new) the
- * append runs inside the attention launch: the block that reads a sequence's last page
- * writes the new rows there first, so the step is one launch instead of two.
+ * pkv_paged_decode_attention).  Where the plan allows it (bf16 caches on a tensor-core
+ * path -- the chunked kernel with at most 8 query heads per KV head, or the tcgen05
+ * kernel -- with 16-byte aligned k_new and v_new) the append runs inside the attention
+ * launch: the block that reads a sequence's last page writes the new rows there first,
+ * so the step is one launch instead of two.
  *
  *   k_new, v_new  [B][Hkv][d], element type dt: the new token of sequence b is row b
  *   slot_mapping  int64 [B]: its slot, which must be that of position

@@ -258,27 +258,8 @@ __global__ void __launch_bounds__(NW * 32)
         // before any copy of the page.  The slot must be that of the last position
         // len - 1; another slot is flagged and not written.
         if (warp == 0) {
-            const long long slot = __ldg(p.new_slots + b);
-            if (slot >= 0) {
-                const int pos = len - 1;
-                const int phys = __ldg(p.block_table + static_cast<size_t>(b) * p.MBS + pos / BS);
-                const bool ok = phys >= 0 && phys < p.NB && slot == static_cast<long long>(phys) * BS + pos % BS;
-                if (!ok) {
-                    if (lane == 0) raise_error(p.err, PKV_DEVERR_SLOT);
-                } else {
-                    const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D;
-                    const size_t dst = ((static_cast<size_t>(phys) * p.Hkv + kvh) * BS + pos % BS) * D;
-                    const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.k_new) + src);
-                    const uint4 *vn = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.v_new) + src);
-                    uint4 *kd = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.k_cache_w) + dst);
-                    uint4 *vd = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.v_cache_w) + dst);
-                    for (int u = lane; u < D / 8; u += 32) {
-                        kd[u] = __ldg(kn + u);
-                        vd[u] = __ldg(vn + u);
-                    }
-                    fence_proxy_async_global();   // the page's copies come after these writes
-                }
-            }
+            write_new_token<D, BS>(p, b, kvh, len, lane);
+            fence_proxy_async_global();   // the page's copies come after these writes
         }
         __syncthreads();
         fence_proxy_async_global();
@@ -931,13 +912,15 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
 
 }  // namespace
 
-// The chunked bf16 kernel with one head tile per KV head (m <= 8) writes the step's new
-// tokens itself: exactly one block reads the page that holds a sequence's last position
-// for each KV head.  Its 16-byte row copies need 16-byte aligned new rows.
+// The chunked bf16 kernel with one head tile per KV head (m <= 8), and the tcgen05 kernel
+// with one query tile per sequence, write the step's new tokens themselves: exactly one
+// block reads the page that holds a sequence's last position for each KV head.  The
+// 16-byte row copies need 16-byte aligned new rows.
 bool decode_fuses_append(const DecodePlan &plan, pkv_dtype dt, int Hq, int Hkv, const void *k_new,
                          const void *v_new) {
-    return dt == PKV_BF16 && plan.tensor_core && !plan.group && !plan.umma && Hq / Hkv <= 8 &&
-           reinterpret_cast<uintptr_t>(k_new) % 16 == 0 && reinterpret_cast<uintptr_t>(v_new) % 16 == 0;
+    const bool kernel_ok = (!plan.group && !plan.umma && Hq / Hkv <= 8) || (plan.umma && plan.qtiles == 1);
+    return dt == PKV_BF16 && plan.tensor_core && kernel_ok && reinterpret_cast<uintptr_t>(k_new) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(v_new) % 16 == 0;
 }
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,

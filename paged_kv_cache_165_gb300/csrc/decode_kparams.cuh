@@ -37,6 +37,33 @@ struct DecodeKParams {
     void *k_cache_w, *v_cache_w; // the caches, for those writes
 };
 
+// The step's new token, written by one warp of the block that reads sequence b's last page
+// (pkv_decode_step with the append inside the decode launch): K and V rows of KV head kvh
+// from k_new/v_new [B][Hkv][D] (bf16, 16-byte aligned) into the slot of position len - 1.
+// A slot that is not that position's is flagged and not written.  The caller fences the
+// writes for the asynchronous proxy and syncs the block before the page's TMA copies.
+template <int D, int BS>
+__device__ __forceinline__ void write_new_token(const DecodeKParams &p, int b, int kvh, int len, int lane) {
+    const long long slot = __ldg(p.new_slots + b);
+    if (slot < 0) return;                                  // no new token this step
+    const int pos = len - 1;
+    const int phys = pos >= 0 ? __ldg(p.block_table + static_cast<size_t>(b) * p.MBS + pos / BS) : -1;
+    if (phys < 0 || phys >= p.NB || slot != static_cast<long long>(phys) * BS + pos % BS) {
+        if (lane == 0) raise_error(p.err, PKV_DEVERR_SLOT);
+        return;
+    }
+    const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D;
+    const size_t dst = ((static_cast<size_t>(phys) * p.Hkv + kvh) * BS + pos % BS) * D;
+    const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.k_new) + src);
+    const uint4 *vn = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.v_new) + src);
+    uint4 *kd = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.k_cache_w) + dst);
+    uint4 *vd = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.v_cache_w) + dst);
+    for (int u = lane; u < D / 8; u += 32) {
+        kd[u] = __ldg(kn + u);
+        vd[u] = __ldg(vn + u);
+    }
+}
+
 // Sequence length after validation; an invalid length counts as empty.
 __device__ __forceinline__ int checked_len(const DecodeKParams &p, int b, int bs, bool report) {
     int len = __ldg(p.context_lens + b);

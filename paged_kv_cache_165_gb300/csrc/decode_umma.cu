@@ -147,6 +147,9 @@ __global__ void __launch_bounds__(384, 1)
     auto row_of = [&](int slot) { return static_cast<size_t>(c0 + q0 + slot / p.m) * p.Hq + kvh * p.m + slot % p.m; };
     if (nqt <= 0) return;
     if (!rows_ok || cp0 >= cp1) {
+        // a new token for a sequence that holds none has no position: flagged, not written
+        if (p.new_slots != nullptr && split == 0 && threadIdx.x == 0 && L == 0 && __ldg(p.new_slots + b) >= 0)
+            raise_error(p.err, PKV_DEVERR_SLOT);
         if (split == 0) {   // an empty sequence or inconsistent rows: out = 0, lse = -inf
             for (int idx = threadIdx.x; idx < slots * D; idx += blockDim.x) p.out[row_of(idx / D) * D + idx % D] = 0.f;
             if (p.lse != nullptr)
@@ -165,6 +168,14 @@ __global__ void __launch_bounds__(384, 1)
     const int tok0 = pfirst * BS;                        // first token of the pages read
     const int tok_end = min(hi_tile, apg1 * BS);         // one past the last key any row sees
 
+    // The step's new token (pkv_decode_step, one query per sequence): the block that reads
+    // the sequence's last page writes it there before any copy (the barrier below orders
+    // the writes before the loaders' copies)
+    const bool writes_token = p.new_slots != nullptr && cp1 == cpfirst + cnpages;
+    if (writes_token && warp == 1) {
+        write_new_token<D, BS>(p, b, kvh, L, lane);
+        fence_proxy_async_global();
+    }
     if (threadIdx.x == 0) {
         mbar_init(bar(Cfg::kQ), 8);
         for (int s = 0; s < NKT; ++s) {
@@ -197,6 +208,7 @@ __global__ void __launch_bounds__(384, 1)
     auto sV = [&](int s) { return smem_addr(smem + Cfg::kOffV + s * Cfg::kSlotBytes); };
 
     if (warp == 9 || warp == 10) {
+        if (writes_token) fence_proxy_async_global();
         // ---- TMA loaders: warp 9 the K tiles, warp 10 the V tiles.  Tile t goes to slot
         // t % N of its ring once the slot's previous tile is consumed (K: by S_{t-N}; V: by
         // P_{t-N} V).  Lane i < PPT * PANELS copies panel i % PANELS of page i / PANELS.

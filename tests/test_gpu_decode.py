@@ -361,7 +361,8 @@ def _run_step(q, kc, vc, table, clens, k_new, v_new, slots, scale, num_splits, f
     (64, 8, 128, 16, torch.bfloat16),    # the chunked kernel: the append runs inside it
     (8, 8, 64, 32, torch.bfloat16),
     (32, 8, 256, 16, torch.bfloat16),
-    (16, 1, 128, 16, torch.bfloat16),    # tcgen05 kernel: kv_append first
+    (16, 1, 128, 16, torch.bfloat16),    # the tcgen05 kernel: the append runs inside it too
+    (32, 2, 64, 32, torch.bfloat16),
     (8, 2, 64, 16, torch.float32),       # CUDA-core path: kv_append first
 ])
 @pytest.mark.parametrize("num_splits", [0, 1, 3])
@@ -381,9 +382,10 @@ def test_decode_step_equals_append_then_decode(hq, hkv, d, bs, dtype, num_splits
     assert_attn_close(lse, ref_l, "decode_step lse")
 
 
-def test_decode_step_flags_a_slot_that_is_not_the_last_position():
+@pytest.mark.parametrize("hq,hkv", [(16, 2), (16, 1)])   # chunked and tcgen05 kernels
+def test_decode_step_flags_a_slot_that_is_not_the_last_position(hq, hkv):
     lens = [40, 0, 300]
-    q, kc, vc, table, clens, k_new, v_new, slots = _step_case(77, lens, 16, 2, 128, 16, torch.bfloat16)
+    q, kc, vc, table, clens, k_new, v_new, slots = _step_case(77, lens, hq, hkv, 128, 16, torch.bfloat16)
     slots[0] = oracle.slot_of(table[0], 3, 16)        # an earlier position of sequence 0
     slots[1] = 5                                       # an empty sequence has no position
     out, lse, gk, gv = _run_step(q, kc, vc, table, clens, k_new, v_new, slots, 0.1, 0)
@@ -417,7 +419,7 @@ def test_decode_step_with_unaligned_new_rows_appends_first():
 
 
 @pytest.mark.parametrize("hq,hkv,d,dtype,fused", [(64, 8, 128, torch.bfloat16, True),
-                                                   (16, 1, 128, torch.bfloat16, False),
+                                                   (16, 1, 128, torch.bfloat16, True),
                                                    (8, 2, 64, torch.float32, False)])
 def test_decode_step_kernel_launches(hq, hkv, d, dtype, fused):
     B, bs, MBS, NB = 8, 16, 64, 600
