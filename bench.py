@@ -291,13 +291,19 @@ class DecodeWorkload:
         # pkv_decode_step where the library appends inside the attention launch (as many
         # launches as the attention alone); otherwise kv_append, then the attention call, so
         # that the timed attention call is the attention's launches alone
-        self.step_call = not self.fp8 and self.qlen == 1 and self.window <= 0 and \
-            pkv.decode_step_kernel_launches(B, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype,
-                                            self.num_splits) == \
-            pkv.decode_kernel_launches(B, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype, self.num_splits)
+        # (pkv_decode_step_fp8 on an FP8 cache, quantising the bf16 new rows)
+        mbs = self.table.shape[1]
+        if self.fp8:
+            step_launches = pkv.decode_step_fp8_kernel_launches(B, Hq, Hkv, d, bs, mbs, nb, torch.bfloat16,
+                                                                self.num_splits)
+            attn_launches = pkv.decode_kernel_launches(B, Hq, Hkv, d, bs, mbs, nb, torch.uint8, self.num_splits)
+        else:
+            step_launches = pkv.decode_step_kernel_launches(B, Hq, Hkv, d, bs, mbs, nb, s.cache_dtype,
+                                                            self.num_splits)
+            attn_launches = pkv.decode_kernel_launches(B, Hq, Hkv, d, bs, mbs, nb, s.cache_dtype, self.num_splits)
+        self.step_call = self.qlen == 1 and self.window <= 0 and step_launches == attn_launches
         if self.step_call:
-            self.launches_per_step = pkv.decode_step_kernel_launches(
-                B, Hq, Hkv, d, bs, self.table.shape[1], nb, s.cache_dtype, self.num_splits)
+            self.launches_per_step = step_launches
         else:
             self.launches_per_step = 1 + pkv.paged_attention_kernel_launches(
                 B, R, self.qlen, Hq, Hkv, d, bs, self.table.shape[1], nb,
@@ -340,7 +346,11 @@ class DecodeWorkload:
 
     def attend_call(self, out, q, k_new, v_new, slots, clens, lse=None):
         """The attention (with the step's appends, for a decode step) through the public API."""
-        if self.step_call:
+        if self.step_call and self.fp8:
+            self.pkv.decode_step_fp8(out, q, k_new, v_new, slots, self.k_cache, self.v_cache, self.k_scale,
+                                     self.v_scale, self.table, clens, self.spec.scale, lse=lse,
+                                     num_splits=self.num_splits, workspace=self.ws)
+        elif self.step_call:
             self.pkv.decode_step(out, q, k_new, v_new, slots, self.k_cache, self.v_cache, self.table, clens,
                                  self.spec.scale, lse=lse, num_splits=self.num_splits, workspace=self.ws)
         else:
@@ -727,7 +737,7 @@ def bench_ours(args):
         achieved = alg_bytes / (kern_avg_ms / 1e3) / 1e9
         files = ["decode.cu", "decode_kparams.cuh", "decode_epilogue.cuh", "common.cuh"]
         if wl.fp8:
-            files.append("decode_fp8.cu")
+            files += ["decode_fp8.cu", "fp8_codes.cuh"]
         elif wl.spec.q_heads // wl.spec.kv_heads > 8 or wl.qlen > 1:
             files.append("decode_umma.cu")      # the tcgen05 kernel (large groups, query rows)
         src = kernel_source_hash(files)

@@ -10,6 +10,7 @@
  *                               log-sum-exp merge for long contexts
  *   pkv_decode_step             a decode step: each sequence's new token appended, then
  *                               attended (one launch where the plan allows)
+ *   pkv_decode_step_fp8         the same over an FP8 (E4M3) cache, the new rows quantised
  *   pkv_prefill_attention       varlen causal attention over cu_seqlens that also
  *                               writes the cache
  *
@@ -298,6 +299,32 @@ pkv_status pkv_paged_decode_attention_fp8(float *out, float *lse, const float *q
                                           int Hq, int Hkv, int d, int bs, int MBS, int NB, float scale,
                                           int window, int num_splits, void *workspace,
                                           size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * pkv_decode_step_fp8 -- pkv_decode_step over an FP8 cache: the same results as
+ * pkv_kv_append_fp8(k_new, v_new, new_dt, ..., slot_mapping, T = B) followed by
+ * pkv_paged_decode_attention_fp8(..., window = 0, ...) on the same arguments (codes,
+ * scales, outputs and lse bit-identical).  With bf16 new rows, at most 8 query heads per
+ * KV head and 16-byte aligned codes and scales (the tensor-core path) the quantising
+ * append runs inside the attention launch, with pkv_decode_step's slot rules (the slot of
+ * position context_lens[b] - 1, or < 0; another slot, or one for an empty sequence, sets
+ * PKV_DEVERR_SLOT and is not written); otherwise kv_append_fp8 runs first, with its rules.
+ *
+ *   k_new, v_new  [B][Hkv][d], element type new_dt (PKV_BF16 or PKV_F32)
+ *   k_codes, v_codes, k_scale, v_scale  written as well as read
+ *   the other arguments as pkv_decode_step and pkv_paged_decode_attention_fp8.
+ */
+pkv_status pkv_decode_step_fp8(float *out, float *lse, const float *q, const void *k_new, const void *v_new,
+                               pkv_dtype new_dt, const int64_t *slot_mapping, uint8_t *k_codes, uint8_t *v_codes,
+                               float *k_scale, float *v_scale, const int32_t *block_table,
+                               const int32_t *context_lens, int B, int Hq, int Hkv, int d, int bs, int MBS,
+                               int NB, float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                               pkv_stream_t stream);
+
+/* Kernels one pkv_decode_step_fp8 call with these sizes enqueues (aligned codes, scales and
+ * new rows assumed), or -1 when the call would be rejected; 0 for B == 0. */
+int pkv_decode_step_fp8_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype new_dt,
+                                        int num_splits);
 
 /*
  * pkv_paged_decode_attention_noalloc -- pkv_paged_decode_attention without a workspace.

@@ -14,6 +14,8 @@ from ._binding import (  # noqa: F401
     decode_kernel_launches,
     decode_step,
     decode_step_kernel_launches,
+    decode_step_fp8,
+    decode_step_fp8_kernel_launches,
     decode_workspace_bytes,
     get_device_error,
     header_functions,

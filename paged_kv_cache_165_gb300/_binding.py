@@ -82,6 +82,10 @@ def lib() -> ctypes.CDLL:
     L.pkv_decode_step.restype = I
     L.pkv_decode_step_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I]
     L.pkv_decode_step_kernel_launches.restype = I
+    L.pkv_decode_step_fp8.argtypes = [P, P, P, P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, Z, P]
+    L.pkv_decode_step_fp8.restype = I
+    L.pkv_decode_step_fp8_kernel_launches.argtypes = [I, I, I, I, I, I, I, I, I]
+    L.pkv_decode_step_fp8_kernel_launches.restype = I
     L.pkv_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I,
                                                      F, I, P]
     L.pkv_paged_decode_attention_noalloc.restype = I
@@ -400,3 +404,46 @@ def get_device_error(stream=None) -> int:
     code = ctypes.c_int(0)
     _check(lib().pkv_get_device_error(ctypes.byref(code), _stream(stream)))
     return code.value
+
+
+def decode_step_fp8(out, q, k_new, v_new, slot_mapping, k_codes, v_codes, k_scale, v_scale, block_table,
+                    context_lens, scale, lse=None, num_splits=0, workspace=None, stream=None) -> None:
+    """decode_step over an E4M3 cache: k_new/v_new [B][Hkv][d] (bf16 or fp32) are quantised
+    into codes [NB][Hkv][bs][d] (uint8) and row scales [NB][Hkv][bs] (fp32) at
+    slot_mapping[b], then out [B][Hq][d] fp32 = attention of q over the cache."""
+    _cuda("k_new", k_new)
+    new_dt = _dtype(k_new)
+    _cuda("v_new", v_new, k_new.dtype)
+    for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
+        _cuda(name, t, torch.uint8)
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _cuda(name, t, torch.float32)
+    _cuda("slot_mapping", slot_mapping, torch.int64)
+    _cuda("q", q, torch.float32)
+    _cuda("out", out, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    if lse is not None:
+        _cuda("lse", lse, torch.float32)
+    NB, Hkv, bs, d = k_codes.shape
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d) or tuple(k_new.shape) != (B, Hkv, d) or \
+            tuple(v_new.shape) != (B, Hkv, d) or tuple(v_codes.shape) != (NB, Hkv, bs, d) or \
+            tuple(k_scale.shape) != (NB, Hkv, bs) or tuple(v_scale.shape) != (NB, Hkv, bs) or \
+            slot_mapping.numel() != B or block_table.dim() != 2 or block_table.shape[0] != B or \
+            context_lens.numel() != B or (lse is not None and lse.numel() != B * Hq):
+        raise ValueError("decode_step_fp8: shapes do not match")
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pkv_decode_step_fp8(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_new), _ptr(v_new), new_dt, _ptr(slot_mapping), _ptr(k_codes),
+        _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(context_lens), B, Hq, Hkv, d, bs,
+        block_table.shape[1], NB, float(scale), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def decode_step_fp8_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, new_dtype=torch.bfloat16, num_splits=0) -> int:
+    """Kernels one decode_step_fp8 call with these sizes enqueues (-1: rejected)."""
+    return int(lib().pkv_decode_step_fp8_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, _DTYPES[new_dtype],
+                                                         int(num_splits)))

@@ -303,7 +303,7 @@ pkv_status pkv_decode_step(float *out, float *lse, const float *q, const void *k
     DecodeArgs a{out, lse, q, k_cache, v_cache, block_table, context_lens,
                  B, Hq, Hkv, d, bs, MBS, NB, scale, workspace, st->err};
     cudaError_t e = cudaSuccess;
-    if (decode_fuses_append(plan, dt, Hq, Hkv, k_new, v_new)) {
+    if (decode_fuses_append(plan, dt, dt, Hq, Hkv, k_new, v_new)) {
         a.k_new = k_new;
         a.v_new = v_new;
         a.new_slots = slot_mapping;
@@ -325,7 +325,7 @@ int pkv_decode_step_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int M
     const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count, true, true);
     // new rows from a 16-byte aligned allocation (as tensors are)
     static const uint4 aligned{};
-    return n + (decode_fuses_append(plan, dt, Hq, Hkv, &aligned, &aligned) ? 0 : 1);
+    return n + (decode_fuses_append(plan, dt, dt, Hq, Hkv, &aligned, &aligned) ? 0 : 1);
 }
 
 size_t pkv_paged_attention_workspace_bytes(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs,
@@ -446,6 +446,65 @@ pkv_status pkv_paged_decode_attention_fp8(float *out, float *lse, const float *q
     a.v_scale = v_scale;
     cudaError_t e = launch_decode(a, plan, PKV_FP8_E4M3, stream);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_decode_attention_fp8 launch");
+}
+
+pkv_status pkv_decode_step_fp8(float *out, float *lse, const float *q, const void *k_new, const void *v_new,
+                               pkv_dtype new_dt, const int64_t *slot_mapping, uint8_t *k_codes, uint8_t *v_codes,
+                               float *k_scale, float *v_scale, const int32_t *block_table,
+                               const int32_t *context_lens, int B, int Hq, int Hkv, int d, int bs, int MBS,
+                               int NB, float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                               pkv_stream_t stream) {
+    if (!attention_dtype(new_dt)) return fail(PKV_ERR_UNSUPPORTED, "decode_step_fp8: input type %d", new_dt);
+    pkv_status s = check_decode_sizes(B, Hq, Hkv, d, bs, MBS);
+    if (s != PKV_OK) return s;
+    if (NB < 1 || num_splits < 0)
+        return fail(PKV_ERR_INVALID_ARG, "decode_step_fp8: NB=%d num_splits=%d", NB, num_splits);
+    if (B == 0) return PKV_OK;
+    if (!out || !q || !k_new || !v_new || !slot_mapping || !k_codes || !v_codes || !k_scale || !v_scale ||
+        !block_table || !context_lens)
+        return fail(PKV_ERR_INVALID_ARG, "decode_step_fp8: null pointer");
+    if (reinterpret_cast<uintptr_t>(q) % 8 != 0)
+        return fail(PKV_ERR_INVALID_ARG, "decode_step_fp8: q must be 8-byte aligned");
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != PKV_OK) return s;
+    const bool aligned = aligned16(k_codes) && aligned16(v_codes) && aligned16(k_scale) && aligned16(v_scale);
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, PKV_FP8_E4M3, num_splits, st->sm_count,
+                                        aligned, aligned16(q));
+    if (plan.workspace_bytes > 0 &&
+        (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
+         reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+        return fail(PKV_ERR_WORKSPACE, "decode_step_fp8: needs %zu bytes of 16-byte aligned workspace, got %zu",
+                    plan.workspace_bytes, workspace == nullptr ? size_t(0) : workspace_bytes);
+    DecodeArgs a{out, lse, q, k_codes, v_codes, block_table, context_lens,
+                 B, Hq, Hkv, d, bs, MBS, NB, scale, workspace, st->err};
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    cudaError_t e = cudaSuccess;
+    if (decode_fuses_append(plan, PKV_FP8_E4M3, new_dt, Hq, Hkv, k_new, v_new)) {
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.new_slots = slot_mapping;
+    } else {
+        e = launch_kv_append_fp8(k_new, v_new, new_dt, k_codes, v_codes, k_scale, v_scale, slot_mapping, B, Hkv, d,
+                                 bs, NB, st->err, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_step_fp8 append launch");
+    }
+    e = launch_decode(a, plan, PKV_FP8_E4M3, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "decode_step_fp8 launch");
+}
+
+int pkv_decode_step_fp8_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype new_dt,
+                                        int num_splits) {
+    if (!attention_dtype(new_dt)) return -1;
+    const int n = pkv_decode_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, PKV_FP8_E4M3, num_splits);
+    if (n <= 0) return n;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != PKV_OK) return -1;
+    const DecodePlan plan =
+        plan_decode(B, Hq, Hkv, d, bs, MBS, NB, PKV_FP8_E4M3, num_splits, st->sm_count, true, true);
+    static const uint4 aligned{};
+    return n + (decode_fuses_append(plan, PKV_FP8_E4M3, new_dt, Hq, Hkv, &aligned, &aligned) ? 0 : 1);
 }
 
 pkv_status pkv_prefill_attention(float *out, float *lse, const void *q, const void *k, const void *v,

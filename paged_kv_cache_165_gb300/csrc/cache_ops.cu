@@ -23,6 +23,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "fp8_codes.cuh"
 #include "internal.h"
 
 namespace pkv {
@@ -105,24 +106,19 @@ __global__ void __launch_bounds__(256)
         }
         const T *src = (is_v ? v_new : k_new) + th * d;
         float x[J];
-        float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int e = lane + 32 * j;
             x[j] = e < d ? to_f32(src[e]) : 0.f;
-            amax = fmaxf(amax, fabsf(x[j]));
         }
-#pragma unroll
-        for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
-        const float scale = amax / 448.f;
+        uint8_t code[J];
+        const float scale = e4m3_quantise_row<J>(x, code);
         const long long row = ((slot / bs) * Hkv + h) * bs + slot % bs;
         uint8_t *dst = (is_v ? vc : kc) + row * d;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int e = lane + 32 * j;
-            if (e < d)
-                dst[e] = amax > 0.f ? static_cast<uint8_t>(__nv_cvt_float_to_fp8(x[j] / scale, __NV_SATFINITE, __NV_E4M3))
-                                    : uint8_t{0};
+            if (e < d) dst[e] = code[j];
         }
         if (lane == 0) (is_v ? vs : ks)[row] = scale;
     }

@@ -915,11 +915,16 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
 // The chunked bf16 kernel with one head tile per KV head (m <= 8), and the tcgen05 kernel
 // with one query tile per sequence, write the step's new tokens themselves: exactly one
 // block reads the page that holds a sequence's last position for each KV head.  The
-// 16-byte row copies need 16-byte aligned new rows.
-bool decode_fuses_append(const DecodePlan &plan, pkv_dtype dt, int Hq, int Hkv, const void *k_new,
-                         const void *v_new) {
+// 16-byte row copies need 16-byte aligned new rows.  The FP8 kernel (m <= 8 as well)
+// quantises bf16 new rows there.
+bool decode_fuses_append(const DecodePlan &plan, pkv_dtype dt, pkv_dtype new_dt, int Hq, int Hkv,
+                         const void *k_new, const void *v_new) {
+    if (!plan.tensor_core || new_dt != PKV_BF16) return false;
+    if (dt == PKV_FP8_E4M3)
+        return Hq / Hkv <= 8 && reinterpret_cast<uintptr_t>(k_new) % 2 == 0 &&
+               reinterpret_cast<uintptr_t>(v_new) % 2 == 0;
     const bool kernel_ok = (!plan.group && !plan.umma && Hq / Hkv <= 8) || (plan.umma && plan.qtiles == 1);
-    return dt == PKV_BF16 && plan.tensor_core && kernel_ok && reinterpret_cast<uintptr_t>(k_new) % 16 == 0 &&
+    return dt == PKV_BF16 && kernel_ok && reinterpret_cast<uintptr_t>(k_new) % 16 == 0 &&
            reinterpret_cast<uintptr_t>(v_new) % 16 == 0;
 }
 
@@ -1004,12 +1009,14 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     kp.v_scale = a.v_scale;
     kp.q_per_tile = plan.q_per_tile;
     kp.qtiles = plan.qtiles;
-    if (a.new_slots != nullptr && decode_fuses_append(plan, dt, a.Hq, a.Hkv, a.k_new, a.v_new)) {
+    if (a.new_slots != nullptr && decode_fuses_append(plan, dt, PKV_BF16, a.Hq, a.Hkv, a.k_new, a.v_new)) {
         kp.k_new = a.k_new;
         kp.v_new = a.v_new;
         kp.new_slots = a.new_slots;
         kp.k_cache_w = const_cast<void *>(a.k_cache);
         kp.v_cache_w = const_cast<void *>(a.v_cache);
+        kp.k_scale_w = const_cast<float *>(a.k_scale);
+        kp.v_scale_w = const_cast<float *>(a.v_scale);
     }
     // the tcgen05 kernel with one query tile per sequence (decode, verification): each block
     // takes a whole chunk for a long time, so start the long sequences first (a block ranks

@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "decode_epilogue.cuh"
 #include "decode_kparams.cuh"
+#include "fp8_codes.cuh"
 #include "internal.h"
 
 namespace pkv {
@@ -79,6 +80,39 @@ struct Fp8Cfg {
     static_assert(kMergeBytes <= kStagesBytes, "merge scratch reuses the stage buffers");
 };
 
+// The step's new token into the FP8 cache (pkv_decode_step_fp8 with the append inside this
+// launch): warp 0 quantises and writes the K row of KV head kvh, warp 1 the V row, from
+// k_new / v_new [B][Hkv][128] (bf16) into the slot of position len - 1, with the codes and
+// the scale that kv_append_fp8 writes for the same row.  A slot that is not that
+// position's is flagged (once, by warp 0) and not written.  The caller fences the writes
+// for the asynchronous proxy and syncs the block before the page's copies.
+template <int BS>
+__device__ __forceinline__ void write_new_token_fp8(const DecodeKParams &p, int b, int kvh, int len, int warp,
+                                                    int lane) {
+    constexpr int D = 128, J = D / 32;
+    const long long slot = __ldg(p.new_slots + b);
+    if (slot < 0) return;                                  // no new token this step
+    const int pos = len - 1;
+    const int phys = pos >= 0 ? __ldg(p.block_table + static_cast<size_t>(b) * p.MBS + pos / BS) : -1;
+    if (phys < 0 || phys >= p.NB || slot != static_cast<long long>(phys) * BS + pos % BS) {
+        if (warp == 0 && lane == 0) raise_error(p.err, PKV_DEVERR_SLOT);
+        return;
+    }
+    const bool is_v = warp == 1;
+    const __nv_bfloat16 *src =
+        static_cast<const __nv_bfloat16 *>(is_v ? p.v_new : p.k_new) + (static_cast<size_t>(b) * p.Hkv + kvh) * D;
+    float x[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) x[j] = __bfloat162float(src[lane + 32 * j]);
+    uint8_t code[J];
+    const float scale = e4m3_quantise_row<J>(x, code);
+    const size_t row = (static_cast<size_t>(phys) * p.Hkv + kvh) * BS + pos % BS;
+    uint8_t *dst = static_cast<uint8_t *>(is_v ? p.v_cache_w : p.k_cache_w) + row * D;
+#pragma unroll
+    for (int j = 0; j < J; ++j) dst[lane + 32 * j] = code[j];
+    if (lane == 0) (is_v ? p.v_scale_w : p.k_scale_w)[row] = scale;
+}
+
 template <int BS, int ST>
 __global__ void __launch_bounds__(128, 4)
     decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -108,12 +142,26 @@ __global__ void __launch_bounds__(128, 4)
     const int pg1 = min(n_pages, pg0 + p.chunk_pages);
     if (pg0 >= pg1) {
         if (split == 0) {   // an empty sequence: out = 0, lse = -inf
+            // a new token for a sequence that holds none has no position: flagged, not written
+            if (p.new_slots != nullptr && threadIdx.x == 0 && len == 0 && __ldg(p.new_slots + b) >= 0)
+                raise_error(p.err, PKV_DEVERR_SLOT);
             for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32)
                 p.out[(static_cast<size_t>(b) * p.Hq + head0 + idx / D) * D + idx % D] = 0.f;
             if (p.lse != nullptr && threadIdx.x < nheads)
                 p.lse[static_cast<size_t>(b) * p.Hq + head0 + threadIdx.x] = -INFINITY;
         }
         return;
+    }
+
+    if (p.new_slots != nullptr && pg1 == n_pages) {
+        // the step's new token: the block that reads the sequence's last page writes its K
+        // and V rows there (codes and scales) before any copy of the page
+        if (warp < 2) {
+            write_new_token_fp8<BS>(p, b, kvh, len, warp, lane);
+            fence_proxy_async_global();
+        }
+        __syncthreads();
+        fence_proxy_async_global();
     }
 
     if (lane == 0) {

@@ -32,9 +32,10 @@ struct DecodeKParams {
     int qtiles;       // tcgen05 kernel: query tiles per sequence (grid z = B * qtiles)
     int longest_first;   // tcgen05 kernel: grid z ranks the sequences by length, longest first
     // the step's new tokens written inside the chunked kernel (nullptr: appended before)
-    const void *k_new, *v_new;   // [B][Hkv][d]
+    const void *k_new, *v_new;   // [B][Hkv][d] (bf16)
     const int64_t *new_slots;    // [B]; < 0: no new token
-    void *k_cache_w, *v_cache_w; // the caches, for those writes
+    void *k_cache_w, *v_cache_w; // the caches (FP8: the codes), for those writes
+    float *k_scale_w, *v_scale_w;   // FP8 caches: the row scales, for those writes
 };
 
 // The step's new token, written by one warp of the block that reads sequence b's last page

@@ -92,14 +92,15 @@ struct DecodeArgs {
     const int32_t *cu_q = nullptr;   // query rows per sequence; nullptr: one per sequence
     int rows = -1;                   // query rows (B when cu_q is nullptr)
     // the step's new tokens, appended inside the decode launch (decode_fuses_append)
-    const void *k_new = nullptr, *v_new = nullptr;   // [B][Hkv][d], cache element type
+    const void *k_new = nullptr, *v_new = nullptr;   // [B][Hkv][d], bf16
     const int64_t *new_slots = nullptr;              // [B]; < 0: no new token
 };
 
 // Whether launch_decode can write the step's new tokens (one per sequence, at its last
-// position) inside the decode launch for this plan; otherwise kv_append runs first.
-bool decode_fuses_append(const DecodePlan &plan, pkv_dtype dt, int Hq, int Hkv, const void *k_new,
-                         const void *v_new);
+// position; rows of type new_dt) inside the decode launch for this plan over a cache of
+// type dt; otherwise kv_append (kv_append_fp8) runs first.
+bool decode_fuses_append(const DecodePlan &plan, pkv_dtype dt, pkv_dtype new_dt, int Hq, int Hkv,
+                         const void *k_new, const void *v_new);
 
 // Blocks a query row can see: all of MBS, or with a window of W tokens at most
 // ceil(W / bs) + 1 (the window may start inside a block).

@@ -25,7 +25,7 @@ def test_header_declares_the_boundary():
                "pkv_paged_attention", "pkv_paged_attention_workspace_bytes",
                "pkv_paged_attention_kernel_launches", "pkv_kv_append_fp8",
                "pkv_paged_decode_attention_fp8", "pkv_decode_step", "pkv_decode_step_kernel_launches",
-               "pkv_get_device_error",
+               "pkv_decode_step_fp8", "pkv_decode_step_fp8_kernel_launches", "pkv_get_device_error",
                "pkv_status_string", "pkv_last_error", "pkv_version"]:
         assert fn in names
 
@@ -101,3 +101,17 @@ def test_decode_step_rejects_bad_arguments_before_any_launch(L):
     assert L.pkv_decode_step(P(16), None, P(16), None, P(16), P(16), P(16), P(16), 1, P(16), P(16),
                              2, 8, 2, 64, 16, 4, 8, 0.1, 0, None, 0, None) == 1   # null k_new
     assert L.pkv_decode_step_kernel_launches(2, 10, 3, 64, 16, 4, 8, 1, 0) == -1
+
+
+def test_decode_step_fp8_rejects_bad_arguments_before_any_launch(L):
+    P = ctypes.c_void_p
+    nz = P(16)   # never dereferenced: validation fails first
+    def call(new_dt=1, B=2, Hq=8, Hkv=2, NB=8, k_new=nz):
+        return L.pkv_decode_step_fp8(nz, None, nz, k_new, nz, new_dt, nz, nz, nz, nz, nz, nz, nz, B, Hq, Hkv,
+                                     128, 16, 4, NB, 0.1, 0, None, 0, None)
+    assert call(new_dt=2) == 2            # FP8 new rows: unsupported
+    assert call(Hq=10, Hkv=3) == 1        # Hq % Hkv
+    assert call(NB=0) == 1
+    assert call(k_new=None) == 1          # null pointer
+    assert call(B=0) == 0                 # nothing to do
+    assert L.pkv_decode_step_fp8_kernel_launches(2, 8, 2, 128, 16, 4, 8, 2, 0) == -1

@@ -144,3 +144,85 @@ def test_fp8_decode_bad_block_reads_zeros_and_flags():
     kd, vd = oracle.dequantize_fp8(kq, ks), oracle.dequantize_fp8(vq, vs)
     ref, _ = oracle.paged_attention(q[:1], kd, vd, table[:1], clens[:1], torch.tensor([0, 1], dtype=torch.int32), 0.1)
     assert_attn_close(out[:1], ref, "good sequence")
+
+
+def _fp8_step_case(seed, lens, hq, hkv, d, bs, new_dtype):
+    """An FP8 cache, the new token of each sequence (rows of new_dtype) and its slot (the
+    last position's); lens count the new token."""
+    q, kq, vq, ks, vs, table, clens = fp8_case(seed, lens, hq, hkv, d, bs)
+    g = gen.generator(seed + 1)
+    k_new = gen.randn(g, (len(lens), hkv, d), new_dtype)
+    v_new = gen.randn(g, (len(lens), hkv, d), new_dtype)
+    slots = torch.tensor([oracle.slot_of(table[b], n - 1, bs) if n > 0 else -1 for b, n in enumerate(lens)],
+                         dtype=torch.int64)
+    return [q, kq, vq, ks, vs, table, clens, k_new, v_new, slots]
+
+
+def _run_fp8_step(case, scale, num_splits, fused=True):
+    q, kq, vq, ks, vs, table, clens, k_new, v_new, slots = case
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = kq.shape
+    out = torch.full((B, Hq, d), float("nan"), device="cuda")
+    lse = torch.full((B, Hq), float("nan"), device="cuda")
+    ws = torch.zeros(max(16, pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, table.shape[1], num_splits)),
+                     dtype=torch.uint8, device="cuda")
+    g = [dev(t) for t in (kq, vq, ks, vs)]
+    if fused:
+        pkv.decode_step_fp8(out, dev(q), dev(k_new), dev(v_new), dev(slots), *g, dev(table), dev(clens), scale,
+                            lse=lse, num_splits=num_splits, workspace=ws)
+    else:
+        pkv.kv_append_fp8(dev(k_new), dev(v_new), *g, dev(slots))
+        pkv.paged_decode_attention_fp8(out, dev(q), *g, dev(table), dev(clens), scale, lse=lse,
+                                       num_splits=num_splits, workspace=ws)
+    torch.cuda.synchronize()
+    return out, lse, [t.cpu() for t in g]
+
+
+def _same_bits(a, b):
+    """Equal as stored bytes (the unwritten slots hold NaN scales)."""
+    return torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("hq,hkv,bs,new_dtype,fused", [
+    (64, 8, 16, torch.bfloat16, True),     # tensor cores: the append runs inside the launch
+    (8, 8, 16, torch.bfloat16, True),
+    (16, 2, 32, torch.bfloat16, True),
+    (64, 8, 16, torch.float32, False),     # fp32 new rows: kv_append_fp8 first
+    (32, 2, 16, torch.bfloat16, False),    # 16 query heads per KV head: CUDA cores, append first
+])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_fp8_decode_step_equals_append_then_decode(hq, hkv, bs, new_dtype, fused, num_splits):
+    d = 128
+    B = 8
+    assert pkv.decode_step_fp8_kernel_launches(B, hq, hkv, d, bs, 200, 600, new_dtype, num_splits) == \
+        pkv.decode_kernel_launches(B, hq, hkv, d, bs, 200, 600, torch.uint8, num_splits) + (0 if fused else 1)
+    lens = [1, 16, 17, 700, 2049, 33, 5, 1000]
+    case = _fp8_step_case(hq + bs + num_splits, lens, hq, hkv, d, bs, new_dtype)
+    case[9][2] = -1                                   # sequence 2 has no new token this step
+    scale = 1 / math.sqrt(d)
+    out, lse, caches = _run_fp8_step(case, scale, num_splits)
+    assert pkv.get_device_error() == 0
+    ref_out, ref_lse, ref_caches = _run_fp8_step(case, scale, num_splits, fused=False)
+    assert all(_same_bits(a, b) for a, b in zip(caches, ref_caches))
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    q, kq, vq, ks, vs, table, clens, k_new, v_new, slots = case
+    want = [t.clone() for t in (kq, vq, ks, vs)]     # the oracle's codes and scales
+    oracle.kv_append_fp8(*want, k_new, v_new, slots)
+    assert all(_same_bits(a, b) for a, b in zip(caches, want))
+    kd, vd = oracle.dequantize_fp8(want[0], want[2]), oracle.dequantize_fp8(want[1], want[3])
+    ref, ref_l = oracle.paged_decode(q, kd, vd, table, clens, scale)
+    assert_attn_close(out, ref, "decode_step_fp8 out")
+    assert_attn_close(lse, ref_l, "decode_step_fp8 lse")
+
+
+def test_fp8_decode_step_flags_a_slot_that_is_not_the_last_position():
+    lens = [40, 0, 300]
+    case = _fp8_step_case(78, lens, 16, 2, 128, 16, torch.bfloat16)
+    table, k_new, v_new, slots = case[5], case[7], case[8], case[9]
+    slots[0] = oracle.slot_of(table[0], 3, 16)        # an earlier position of sequence 0
+    slots[1] = 5                                       # an empty sequence has no position
+    out, lse, caches = _run_fp8_step(case, 0.1, 0)
+    assert pkv.get_device_error() & pkv.DEVERR["slot"]
+    want = [t.clone() for t in case[1:5]]              # only sequence 2's token is written
+    oracle.kv_append_fp8(*want, k_new[2:], v_new[2:], slots[2:])
+    assert all(_same_bits(a, b) for a, b in zip(caches, want))
