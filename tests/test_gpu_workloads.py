@@ -49,8 +49,23 @@ def check_sampled(out, lse, q, kc, vc, table, lens, scale, sample, what):
     assert_attn_close(lse[idx], ref_lse, what + " lse")
 
 
-def run_decode_steps(inp, steps, check_steps, sample):
-    """Append + attend for `steps` consecutive steps; oracle on `check_steps`."""
+def decode_step(q, k_new, v_new, slots, gk, gv, table, lens, scale):
+    """pkv_decode_step as the bench times it: the appends inside the attention launch
+    where the library fuses them."""
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = gk.shape
+    ws = torch.zeros(max(pkv.decode_workspace_bytes(B, Hq, Hkv, d, bs, table.shape[1], 0), 16),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.full((B, Hq, d), float("nan"), device="cuda")
+    lse = torch.full((B, Hq), float("nan"), device="cuda")
+    pkv.decode_step(out, q, k_new, v_new, slots, gk, gv, table, lens, scale, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+def run_decode_steps(inp, steps, check_steps, sample, via_step=False):
+    """Append + attend for `steps` consecutive steps (kv_append, then the decode; or one
+    pkv_decode_step per step); oracle on `check_steps`."""
     spec = inp.spec
     bs = spec.block_size
     kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
@@ -58,11 +73,16 @@ def run_decode_steps(inp, steps, check_steps, sample):
     gtable = dev(inp.block_table)
     for c in range(steps):
         slots = torch.tensor([oracle.slot_of(inp.block_table[b], n + c, bs) for b, n in enumerate(inp.cached)])
-        pkv.kv_append(dev(inp.k_new[c]), dev(inp.v_new[c]), gk, gv, dev(slots))
         oracle.kv_append(kc, vc, inp.k_new[c], inp.v_new[c], slots)
         lens = torch.tensor([n + c + 1 for n in inp.cached], dtype=torch.int32)
+        if via_step:
+            out, lse = decode_step(dev(inp.q[c]), dev(inp.k_new[c]), dev(inp.v_new[c]), dev(slots), gk, gv,
+                                   gtable, dev(lens), spec.scale)
+        else:
+            pkv.kv_append(dev(inp.k_new[c]), dev(inp.v_new[c]), gk, gv, dev(slots))
+            if c in check_steps:
+                out, lse = decode(dev(inp.q[c]), gk, gv, gtable, dev(lens), spec.scale)
         if c in check_steps:
-            out, lse = decode(dev(inp.q[c]), gk, gv, gtable, dev(lens), spec.scale)
             check_sampled(out, lse, inp.q[c], kc, vc, inp.block_table, lens, spec.scale, sample,
                           f"{spec.name} step {c}")
     assert pkv.get_device_error() == 0
@@ -75,17 +95,18 @@ def test_llama2_7b_mha_decode():
     run_decode_steps(inp, 1, {0}, sample=[0, 7, 19, 31])
 
 
-def test_llama2_70b_gqa_decode_32_steps():
+@pytest.mark.parametrize("via_step", [False, True], ids=["append_then_decode", "decode_step"])
+def test_llama2_70b_gqa_decode_32_steps(via_step):
     inp = gen.gqa_70b_inputs()
     lens = inp.cached
     sample = [int(np.argmin(lens)), int(np.argmax(lens)), 5, 33]
-    run_decode_steps(inp, 32, {0, 31}, sample)
+    run_decode_steps(inp, 32, {0, 31}, sample, via_step)
 
 
 @pytest.mark.parametrize("spec", [gen.LONG_GQA, gen.LONG_MQA], ids=["gqa", "mqa"])
 def test_long_context_split_k_decode(spec):
     inp = gen.long_inputs(spec)
-    run_decode_steps(inp, 1, {0}, sample=[0, 3])
+    run_decode_steps(inp, 1, {0}, sample=[0, 3], via_step=True)
 
 
 def test_long_context_varlen_prefill_writes_cache():
