@@ -14,7 +14,7 @@ from paged_kv_cache_165_gb300 import _build
 from workloads import gen
 
 from conftest import GOLDEN
-from helpers import ATTN_ATOL, assert_attn_close, dev
+from helpers import ATTN_ATOL, assert_attn_close, assert_bits_equal, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -173,26 +173,53 @@ def test_separate_merge_of_many_chunks(dtype, d):
 
 
 def test_tiny_config_append_then_decode():
-    """Tiny workload: batch 2, 8 q / 2 kv heads, d 64, lengths {17, 40} + 1 appended, fp32."""
+    """Tiny workload: batch 2, 8 q / 2 kv heads, d 64, lengths {17, 40} + 1 appended, fp32,
+    8 physical blocks in seeded-permutation order (5 used).  The 3 free blocks and the slots
+    past each new length hold NaN / Inf, which must stay invisible; the step runs as
+    kv_append + the attention (one pass and split-K) and as pkv_decode_step."""
     inp = gen.tiny_inputs()
     spec = inp.spec
+    bs = spec.block_size
+    assert inp.num_blocks == 8
     kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
-    slots = torch.tensor([oracle.slot_of(inp.block_table[b], n, spec.block_size)
+    used = set(inp.block_table.flatten().tolist()) - {-1}
+    for blk in set(range(inp.num_blocks)) - used:
+        kc[blk] = float("nan")
+        vc[blk] = float("nan")
+    for b, n in enumerate(inp.cached):
+        for pos in range(n + 1, gen.blocks_needed(n + 1, bs) * bs):
+            s = oracle.slot_of(inp.block_table[b], pos, bs)
+            kc[s // bs, :, s % bs] = float("nan")
+            vc[s // bs, :, s % bs] = float("inf")
+    kc0, vc0 = kc.clone(), vc.clone()
+    slots = torch.tensor([oracle.slot_of(inp.block_table[b], n, bs)
                           for b, n in enumerate(inp.cached)], dtype=torch.int64)
     gk, gv = dev(kc), dev(vc)
     pkv.kv_append(dev(inp.k_new[0]), dev(inp.v_new[0]), gk, gv, dev(slots))
     oracle.kv_append(kc, vc, inp.k_new[0], inp.v_new[0], slots)
+    assert_bits_equal(gk, kc, "tiny k_cache")
+    assert_bits_equal(gv, vc, "tiny v_cache")
     lens = torch.tensor([n + 1 for n in inp.cached], dtype=torch.int32)
-    for s in (1, 0):
-        out = torch.empty((spec.batch, spec.q_heads, spec.head_dim), device="cuda")
-        lse = torch.empty((spec.batch, spec.q_heads), device="cuda")
+    ref, ref_lse = oracle.paged_decode(inp.q[0], kc, vc, inp.block_table, lens, spec.scale)
+    assert np.isfinite(ref).all()
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    for s in (1, 0, 2):
+        out = torch.full((spec.batch, spec.q_heads, spec.head_dim), float("nan"), device="cuda")
+        lse = torch.full((spec.batch, spec.q_heads), float("nan"), device="cuda")
         pkv.paged_decode_attention(out, dev(inp.q[0]), gk, gv, dev(inp.block_table), dev(lens),
-                                   spec.scale, lse=lse, num_splits=s,
-                                   workspace=torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
-        ref, ref_lse = oracle.paged_decode(inp.q[0], kc, vc, inp.block_table, lens, spec.scale)
-        assert_attn_close(out, ref, "tiny out")
-        assert_attn_close(lse, ref_lse, "tiny lse")
-    assert torch.equal(gk.cpu(), kc) and torch.equal(gv.cpu(), vc)
+                                   spec.scale, lse=lse, num_splits=s, workspace=ws)
+        assert_attn_close(out, ref, f"tiny out, num_splits={s}")
+        assert_attn_close(lse, ref_lse, f"tiny lse, num_splits={s}")
+    # the same step through pkv_decode_step, on the cache as it was before the append
+    gk2, gv2 = dev(kc0), dev(vc0)
+    out = torch.full((spec.batch, spec.q_heads, spec.head_dim), float("nan"), device="cuda")
+    lse = torch.full((spec.batch, spec.q_heads), float("nan"), device="cuda")
+    pkv.decode_step(out, dev(inp.q[0]), dev(inp.k_new[0]), dev(inp.v_new[0]), dev(slots), gk2, gv2,
+                    dev(inp.block_table), dev(lens), spec.scale, lse=lse, workspace=ws)
+    assert_bits_equal(gk2, kc, "tiny k_cache via decode_step")
+    assert_bits_equal(gv2, vc, "tiny v_cache via decode_step")
+    assert_attn_close(out, ref, "tiny out via decode_step")
+    assert_attn_close(lse, ref_lse, "tiny lse via decode_step")
     assert pkv.get_device_error() == 0
 
 

@@ -155,3 +155,16 @@ def test_release_outside_window_frees_only_blocks_no_query_can_see():
     bm.free_sequence(1)
     bm.audit()
     assert bm.num_free == 40
+
+
+def test_tiny_workload_draws_a_pool_of_8_blocks_with_3_free():
+    """The tiny step: lengths {17, 40} plus one appended token each, over 8 physical blocks
+    handed out in the order of a seeded permutation (2 + 3 used, 3 left in the pool)."""
+    inp = gen.tiny_inputs()
+    assert inp.num_blocks == 8 and tuple(inp.k_cache.shape) == (8, 2, 16, 64)
+    order = gen.permutation(gen.generator(gen.TINY.seed), 8)
+    table = inp.block_table.tolist()
+    assert table[0][:2] == order[:2] and table[1] == order[2:5] and table[0][2] == -1
+    used = {b for row in table for b in row if b >= 0}
+    assert len(used) == 5 and used <= set(range(8))
+    assert sorted(set(range(8)) - used) == sorted(order[5:])

@@ -170,8 +170,14 @@ def decode_inputs(spec: DecodeSpec, cached: Sequence[int], spare_blocks: int = 0
     return DecodeInputs(spec, list(cached), table, nb, k_cache, v_cache, q, k_new, v_new)
 
 
+TINY_NUM_BLOCKS = 8
+
+
 def tiny_inputs() -> DecodeInputs:
-    return decode_inputs(TINY, TINY_LENGTHS)
+    """The tiny step over a pool of 8 physical blocks in seeded-permutation order: the two
+    sequences take 2 + 3 of them (room for the appended token) and 3 stay free."""
+    used = sum(blocks_needed(n + TINY.steps, TINY.block_size) for n in TINY_LENGTHS)
+    return decode_inputs(TINY, TINY_LENGTHS, spare_blocks=TINY_NUM_BLOCKS - used)
 
 
 def mha_7b_inputs() -> DecodeInputs:
