@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     paged_decode_attention_fp8,
     paged_decode_attention_noalloc,
     prefill_attention,
+    selftest_bounded_wait,
 )
 from .blocks import BlockManager, OutOfBlocks  # noqa: F401
 

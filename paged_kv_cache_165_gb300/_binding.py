@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I,
                                                      F, I, P]
     L.pkv_paged_decode_attention_noalloc.restype = I
+    L.pkv_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, I, I, P, P]
+    L.pkv_selftest_bounded_wait.restype = I
     L.pkv_prefill_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, P, P, P, I, I, P]
     L.pkv_prefill_attention.restype = I
     L.pkv_get_device_error.argtypes = [ctypes.POINTER(I), P]
@@ -397,6 +399,16 @@ def prefill_attention(out, q, k, v, cu_seqlens, max_seqlen, scale, lse=None, k_c
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k), _ptr(v), dt, _ptr(cu_seqlens), B, T,
         int(max_seqlen), Hq, Hkv, d, float(scale), _ptr(k_cache), _ptr(v_cache),
         _ptr(slot_mapping), bs, NB, _stream(stream)))
+
+
+def selftest_bounded_wait(limit_ns, blocks, hold_tmem=True, gave_up=None, stream=None) -> None:
+    """Run the kernels' bounded-wait failure path on purpose: `blocks` blocks wait on an
+    mbarrier no copy completes, give up after limit_ns and tear down (PKV_DEVERR_TIMEOUT).
+    gave_up: optional int32 device tensor of one element counting the threads that gave up."""
+    if gave_up is not None:
+        _cuda("gave_up", gave_up, torch.int32)
+    _check(lib().pkv_selftest_bounded_wait(int(limit_ns), int(blocks), 1 if hold_tmem else 0, _ptr(gave_up),
+                                           _stream(stream)))
 
 
 def get_device_error(stream=None) -> int:

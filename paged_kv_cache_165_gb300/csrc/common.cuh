@@ -85,13 +85,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 }
 
 // Bounded wait that also gives up as soon as another thread of the block has given up.
+// The first thread to give up sets *abort and PKV_DEVERR_TIMEOUT.  The attention kernels
+// wait up to kWaitLimitNs; the self-test of this path passes a short limit.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
-                                              unsigned *err) {
+                                              unsigned *err,
+                                              unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             *abort = 1;
             raise_error(err, PKV_DEVERR_TIMEOUT);
             return false;

@@ -26,6 +26,7 @@ def test_header_declares_the_boundary():
                "pkv_paged_attention_kernel_launches", "pkv_kv_append_fp8",
                "pkv_paged_decode_attention_fp8", "pkv_decode_step", "pkv_decode_step_kernel_launches",
                "pkv_decode_step_fp8", "pkv_decode_step_fp8_kernel_launches", "pkv_get_device_error",
+               "pkv_paged_decode_attention_noalloc", "pkv_selftest_bounded_wait",
                "pkv_status_string", "pkv_last_error", "pkv_version"]:
         assert fn in names
 
@@ -115,3 +116,10 @@ def test_decode_step_fp8_rejects_bad_arguments_before_any_launch(L):
     assert call(k_new=None) == 1          # null pointer
     assert call(B=0) == 0                 # nothing to do
     assert L.pkv_decode_step_fp8_kernel_launches(2, 8, 2, 128, 16, 4, 8, 2, 0) == -1
+
+
+def test_selftest_bounded_wait_rejects_limits_and_grids_out_of_range(L):
+    n = _null()
+    for limit, blocks in [(0, 1), (2_000_000_000, 1), (1_000_000, 0), (1_000_000, 1025)]:
+        assert L.pkv_selftest_bounded_wait(limit, blocks, 1, n, n) == _binding.PKV_ERR_INVALID_ARG
+        assert b"selftest_bounded_wait" in L.pkv_last_error()
