@@ -329,11 +329,11 @@ int pkv_decode_step_fp8_kernel_launches(int B, int Hq, int Hkv, int d, int bs, i
 /*
  * pkv_paged_decode_attention_noalloc -- pkv_paged_decode_attention without a workspace.
  *
- * The paper has no counterpart for this entry point: it exists for callers that cannot
- * call cudaMalloc -- a plugin or extension running inside a host application that owns
- * every byte of device memory and hands out none, or a latency-critical decode loop that
- * must not allocate or free device memory in the middle of a step because cudaFree (and
- * often cudaMalloc) synchronises the whole device.
+ * The pages this library follows (the paper) have no counterpart for this entry point:
+ * it exists for callers that cannot call cudaMalloc -- a plugin or extension running
+ * inside a host application that owns every byte of device memory and hands out none, or
+ * a latency-critical decode loop that must not allocate or free device memory in the
+ * middle of a step because cudaFree (and often cudaMalloc) synchronises the whole device.
  *
  * Arguments, layouts and results are those of pkv_paged_decode_attention, minus
  * `workspace` and `workspace_bytes`.  The split-K partials go to a scratch array built
@@ -342,13 +342,16 @@ int pkv_decode_step_fp8_kernel_launches(int B, int Hq, int Hkv, int d, int bs, i
  *   - Sizes whose partials need more than PKV_NOALLOC_SCRATCH_BYTES (the value
  *     pkv_decode_workspace_bytes returns for the same arguments) are rejected with
  *     PKV_ERR_WORKSPACE before anything is enqueued; num_splits = 1 needs no scratch.
- *   - The first call on each device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *   - The first call in each CUDA context (once per device for the runtime's primary
+ *     context) looks up the array's device address with that device current; make that
+ *     first call before any stream capture.
  *   - Every call shares the one array, which keeps the last call's contents.  Calls
  *     that overlap on the GPU (other streams, other host threads) race on it: the
- *     caller must order them.  The array is zero when the library loads; its first
- *     PKV_DECODE_COUNTER_BYTES are arrival counters that every completed call leaves
- *     at zero, and the rest need not start at zero.
+ *     caller must order them.  Its first PKV_DECODE_COUNTER_BYTES hold the arrival
+ *     counters of the split-K chunks that merge in place; a call that uses them first
+ *     clears the ones it uses (one cudaMemsetAsync on the stream, no allocation), so a
+ *     call that gave up on a wait (PKV_DEVERR_TIMEOUT) leaves nothing behind that
+ *     spoils a later call.  The rest of the array need not start at zero.
  *   - No call allocates or frees device memory.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -388,6 +391,29 @@ pkv_status pkv_prefill_attention(float *out, float *lse, const void *q, const vo
                                  int T, int max_seqlen, int Hq, int Hkv, int d, float scale,
                                  void *k_cache, void *v_cache, const int64_t *slot_mapping,
                                  int bs, int NB, pkv_stream_t stream);
+
+/*
+ * pkv_selftest_bounded_wait -- runs the kernels' failure path on purpose, for tests.
+ *
+ * Not part of the attention path, and without a counterpart on the pages: every wait of
+ * the library's kernels for an asynchronous copy or tensor-core operation is bounded
+ * (about 2 s), and a wait that runs out raises PKV_DEVERR_TIMEOUT and makes its block
+ * release what it holds and return, so that the context stays usable.  No correct call
+ * ever gets there, so this entry point launches `blocks` blocks of 128 threads that
+ * each arm an mbarrier for bytes no copy will deliver (none is issued), wait on it
+ * through the kernels' own bounded wait with a limit of `limit_ns` nanoseconds, and tear
+ * down as the attention kernels do (with `hold_tmem` != 0, holding all 512 tensor-memory
+ * columns of their SM while they wait, freed afterwards).
+ *
+ *   limit_ns  0 < limit_ns <= 1e9
+ *   blocks    1 .. 1024
+ *   gave_up   device counter (one unsigned) that every thread whose wait ran out
+ *             increments, or NULL
+ * On return of the kernel the device error word holds PKV_DEVERR_TIMEOUT
+ * (pkv_get_device_error reads and clears it).
+ */
+pkv_status pkv_selftest_bounded_wait(unsigned long long limit_ns, int blocks, int hold_tmem,
+                                     unsigned *gave_up, pkv_stream_t stream);
 
 /*
  * pkv_get_device_error -- synchronise `stream`, then read and clear the device error
