@@ -154,8 +154,9 @@ def whole_job_rate(units_per_rank: float, world: int, max_ms: float) -> float:
 class DecodeWorkload:
     """Decode steps over a paged cache: append one token per sequence, then attend."""
 
-    def __init__(self, spec, lengths, cycle, label, window=0, fp8=False, qlen=1):
+    def __init__(self, spec, lengths, cycle, label, window=0, fp8=False, qlen=1, spare_blocks=0):
         self.spec, self.lengths, self.cycle, self.label = spec, list(lengths), cycle, label
+        self.spare_blocks = spare_blocks   # physical blocks no sequence uses (free pool)
         self.num_splits = 0
         self.window = window   # > 0: sliding window of this many tokens
         self.fp8 = fp8         # E4M3 codes + one fp32 scale per cached row
@@ -193,7 +194,8 @@ class DecodeWorkload:
         s = self.spec
         return {"workload": self.label, "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads,
                 "head_dim": s.head_dim, "block_size": s.block_size,
-                "cache_dtype": "e4m3 codes + fp32 row scales" if self.fp8 else "bf16",
+                "cache_dtype": "e4m3 codes + fp32 row scales" if self.fp8 else
+                ("bf16" if s.cache_dtype == torch.bfloat16 else "fp32"),
                 "q_dtype": "fp32", "mean_cached_len": sum(self.lengths) / len(self.lengths),
                 "decode_steps_cycle": self.cycle, "window": self.window, "new_tokens_per_step": self.qlen,
                 "kv_gb_per_step": self.kv_bytes(self.cycle // 2) / 1e9,
@@ -205,7 +207,7 @@ class DecodeWorkload:
         s = self.spec
         bs = s.block_size
         g = gen.generator(s.seed)
-        nb = sum(gen.blocks_needed(n + self.cycle * self.qlen, bs) for n in self.lengths)
+        nb = sum(gen.blocks_needed(n + self.cycle * self.qlen, bs) for n in self.lengths) + self.spare_blocks
         bm = pkv.BlockManager(nb, bs, order=gen.permutation(g, nb))
         for b, n in enumerate(self.lengths):
             bm.add_sequence(b, n)
@@ -586,14 +588,14 @@ class PrefillWorkload:
         return self.stage_h.numel(), self.out_h.numel() * 4
 
     # ---- CPU oracle on a bounded sample: the shortest prompts, about 300 GFLOP (seconds of fp64)
-    def oracle_sample(self):
+    def oracle_sample(self, flops=3e11):
         import oracle
         order = sorted(range(len(self.lengths)), key=lambda i: self.lengths[i])
         pick, fl = [], 0
         for i in order:
             pick.append(i)
             fl += self.lengths[i] * (self.lengths[i] + 1) // 2 * self.hq * 4 * self.d
-            if fl >= 3e11:
+            if fl >= flops:
                 break
         lens = [self.lengths[i] for i in pick]
         p = gen.prefill_inputs(lens, self.hq, self.hkv, self.d, torch.bfloat16, seed=44)
@@ -631,6 +633,11 @@ WORKLOADS = {
                                            "512 new tokens per sequence appended and attended causally (bottom-"
                                            "right), 64 q / 8 kv heads, d 128, bs 16, bf16 KV, fp32 q",
                                            qlen=gen.PREFIX_CHUNK_LEN),
+    "tiny": lambda: DecodeWorkload(gen.TINY, list(gen.TINY_LENGTHS), 1,
+                                   "tiny decode step: batch 2, 8 q / 2 kv heads, d 64, lengths {17, 40} + 1 "
+                                   "appended, bs 16, 8 physical blocks in seeded-permutation order, fp32 q/K/V",
+                                   spare_blocks=gen.TINY_NUM_BLOCKS - sum(gen.blocks_needed(n + 1)
+                                                                          for n in gen.TINY_LENGTHS)),
     "mix": MixWorkload,
     "swa": lambda: DecodeWorkload(gen.SWA, [gen.SWA_LENGTH] * gen.SWA.batch, 1,
                                   "mistral-7b-shaped sliding-window decode: batch 64, 32 q / 8 kv heads, d 128, "
@@ -642,24 +649,14 @@ WORKLOADS = {
 
 # ------------------------------------------------------------------- our arm
 
-def bench_ours(args):
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    device = torch.device("cuda", torch.cuda.current_device())
+def measure(name, wl, args, device, world, rank, steps, warmup, soak, with_e2e=True, cpu_sample=None,
+            cpu_seconds=0.0):
+    """Set the workload up, warm it up, time exactly `steps` steps (events on the launching
+    stream, barriers and the max over ranks around them) with clocks sampled meanwhile, and
+    return the result keys of one JSON line.  cpu_sample: None for no CPU baseline, else the
+    oracle sample size (sequences for a decode workload, fp64 flops for the prefill), run
+    again and again until cpu_seconds have passed."""
     import paged_kv_cache_165_gb300 as pkv
-    from paged_kv_cache_165_gb300 import _build
-    if rank == 0 or world == 1:
-        _build.build()
-    if world > 1:
-        torch.distributed.barrier()
-    pkv.lib()
-
-    wl = WORKLOADS[args.workload]()
     if hasattr(wl, "num_splits"):
         wl.num_splits = args.num_splits
     wl.setup(device)
@@ -674,7 +671,7 @@ def bench_ours(args):
         else:
             wl.step(c)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
     if pkv.get_device_error() != 0:
@@ -683,8 +680,8 @@ def bench_ours(args):
     # soak (untimed) so that clocks settle and the sampler sees the GPU under load
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
-    t_end = time.time() + args.soak
-    i = args.warmup
+    t_end = time.time() + soak
+    i = warmup
     while time.time() < t_end:
         step(i)
         i += 1
@@ -692,17 +689,16 @@ def bench_ours(args):
             torch.cuda.synchronize()
     torch.cuda.synchronize()
 
-    # ---- timed region: exactly K steps, events on the launching stream
+    # ---- timed region: exactly `steps` steps, events on the launching stream
     first = i
-    n_ev = args.steps
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     start.record(stream)
-    for k in range(args.steps):
+    for k in range(steps):
         c = (first + k) % wl.cycle if is_decode else 0
         if is_decode:
             wl.append(c)
@@ -725,10 +721,11 @@ def bench_ours(args):
     max_ms = max_over_ranks(elapsed_ms, device)
 
     hbm, bf16, bf16_sus, peak_kind = peaks()
-    ms_per_step = max_ms / args.steps
+    ms_per_step = max_ms / steps
     res = {"metric": METRIC, "impl": "ours"}
+    step_flops = None
     if is_decode:
-        step_bytes = [wl.kv_bytes((first + k) % wl.cycle) for k in range(args.steps)]
+        step_bytes = [wl.kv_bytes((first + k) % wl.cycle) for k in range(steps)]
         value = whole_job_rate(sum(step_bytes), world, max_ms) / 1e9
         kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
         # bytes HBM has to deliver per launch: with shared blocks (a common prefix, forked
@@ -741,14 +738,14 @@ def bench_ours(args):
         elif wl.spec.q_heads // wl.spec.kv_heads > 8 or wl.qlen > 1:
             files.append("decode_umma.cu")      # the tcgen05 kernel (large groups, query rows)
         src = kernel_source_hash(files)
-        traffic = profiled_traffic(f"decode_{args.workload}.md", src)
+        traffic = profiled_traffic(f"decode_{name}.md", src)
         res.update({
             "value": value, "unit": "GB/s", "pct_hbm_peak": 100 * value / hbm,
             "tokens_per_s_per_layer": wl.spec.batch * wl.qlen * world / (ms_per_step / 1e3),
-            **({"attention_tflops": world * sum(wl.attn_flops((first + k) % wl.cycle) for k in range(args.steps))
+            **({"attention_tflops": world * sum(wl.attn_flops((first + k) % wl.cycle) for k in range(steps))
                 / (max_ms / 1e3) / 1e12}
                if wl.qlen > 1 and wl.window <= 0 else {}),
-            **({"unique_gb_per_s": whole_job_rate(wl.unique_bytes * args.steps, world, max_ms) / 1e9}
+            **({"unique_gb_per_s": whole_job_rate(wl.unique_bytes * steps, world, max_ms) / 1e9}
                if hasattr(wl, "unique_bytes") else {}),
             "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (split-K partials + LSE merge)",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
@@ -760,7 +757,7 @@ def bench_ours(args):
                          "avg_launch_ms": kern_avg_ms,
                          "traffic": traffic, "kernel_source_sha256_16": src},
         })
-        step_flops = [wl.attn_flops((first + k) % wl.cycle) for k in range(args.steps)] \
+        step_flops = [wl.attn_flops((first + k) % wl.cycle) for k in range(steps)] \
             if wl.qlen > 1 and wl.window <= 0 else None
         if step_flops and wl.tensor_bound(hbm, bf16):
             # many query rows per sequence (chunked prefill on a cached prefix): the work is
@@ -780,13 +777,14 @@ def bench_ours(args):
             })
     else:
         flops = wl.flops()
-        value = whole_job_rate(flops * args.steps, world, max_ms) / 1e12
+        value = whole_job_rate(flops * steps, world, max_ms) / 1e12
         kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
         achieved = flops / (kern_avg_ms / 1e3) / 1e12
         src = kernel_source_hash(["prefill.cu", "common.cuh"])
         res.update({
             "metric": "varlen causal prefill TFLOP/s (4*Hq*d per causal query-key pair)",
             "value": value, "unit": "TFLOP/s",
+            "prompt_tokens_per_s_per_layer": sum(wl.lengths) * world / (ms_per_step / 1e3),
             "roofline": {"bound": "tensor", "kernel": "prefill_attention (cache write + attention)",
                          "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
                          "peak_source": f"{peak_kind} bf16_tflops (burst)",
@@ -794,34 +792,35 @@ def bench_ours(args):
                          "traffic": profiled_traffic("prefill.md", src), "kernel_source_sha256_16": src},
         })
     res.update({
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "accumulate": "fp32", "data": "synthetic (seeded N(0,1), shuffled blocks)",
+        "dtype": "bf16" if not is_decode or wl.spec.cache_dtype == torch.bfloat16 else "fp32",
+        "accumulate": "fp32", "data": "synthetic (seeded N(0,1), shuffled blocks)",
         "config": dict(wl.describe(), parallelism=f"replicas x{world} (independent batches)",
-                       soak_s=args.soak, num_splits=args.num_splits),
-        "gpu_launches": wl.launches_per_step * args.steps,
+                       soak_s=soak, num_splits=args.num_splits),
+        "gpu_launches": wl.launches_per_step * steps,
         "clocks": clocks,
     })
 
     # ---- end to end through the public API with pinned host buffers
-    if is_decode:
+    if with_e2e and is_decode:
         wl.e2e_capture()
         # warm-up: the very steps the timed region replays, so that every graph it uses has
         # been launched (uploaded to the device) once; the steps are idempotent (the same
         # appends to the same slots)
-        wl.e2e_steps(first, args.steps)
+        wl.e2e_steps(first, steps)
         torch.cuda.synchronize()
         e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         e_start.record(stream)
-        wl.e2e_steps(first, args.steps)
+        wl.e2e_steps(first, steps)
         e_stop.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e_start.elapsed_time(e_stop), device)
         # the last step's output, as it reached host memory, equals the same step run eagerly
-        last_c, last_buf = (first + args.steps - 1) % wl.cycle, (args.steps - 1) % 2
+        last_c, last_buf = (first + steps - 1) % wl.cycle, (steps - 1) % 2
         wl.append(last_c)
         wl.attend(last_c)
         if not torch.equal(wl.out_h[last_buf], wl.out.cpu()):
@@ -830,14 +829,15 @@ def bench_ours(args):
         tb = res["unit"] == "TFLOP/s"   # the tensor-bound query-row workload: the same metric
         res["e2e"] = {"value": whole_job_rate(sum(step_flops) if tb else sum(step_bytes), world, e_ms)
                       / (1e12 if tb else 1e9), "unit": res["unit"],
-                      "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d,
+                      "ms_per_step": e_ms / steps, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h,
+                      "kind": "pipelined throughput: steps back to back, each step's copies overlapped "
+                              "with its neighbours' compute; not the host-to-host latency of one step",
                       "path": "public API calls (decode_step, or kv_append then the attention) replayed as one "
                               "CUDA graph per step; step k+1's inputs copied in from pinned host "
                               "memory and step k-1's output copied out on a second stream while "
                               "step k computes"}
-
-    else:
+    elif with_e2e:
         wl.e2e_setup()
         for _ in range(2):
             wl.e2e_step()
@@ -847,7 +847,7 @@ def bench_ours(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         e_start.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             wl.e2e_step()
         e_stop.record(stream)
         torch.cuda.synchronize()
@@ -857,35 +857,115 @@ def bench_ours(args):
         if not torch.equal(wl.out_h, wl.out.cpu()):
             raise RuntimeError("end-to-end output differs from the eager step")
         h2d, d2h = wl.e2e_bytes()
-        res["e2e"] = {"value": whole_job_rate(wl.flops() * args.steps, world, e_ms) / 1e12, "unit": "TFLOP/s",
-                      "ms_per_step": e_ms / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        res["e2e"] = {"value": whole_job_rate(wl.flops() * steps, world, e_ms) / 1e12, "unit": "TFLOP/s",
+                      "ms_per_step": e_ms / steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "kind": "one step after another on one stream (copy in, compute, copy out)",
                       "path": "public API call (prefill_attention writing the cache) on inputs copied in "
                               "from one pinned host buffer, the fp32 output copied back to pinned host "
                               "memory, one step after another"}
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
-    if world == 1 and rank == 0 and not args.no_cpu_baseline and not is_decode:
-        run, threads, lens = wl.oracle_sample()
+    if world == 1 and rank == 0 and cpu_sample is not None and not is_decode:
+        run, threads, lens = wl.oracle_sample(cpu_sample)
         t0 = time.perf_counter()
-        fl = run()
+        fl, reps = 0, 0
+        while reps == 0 or time.perf_counter() - t0 < cpu_seconds:
+            fl += run()
+            reps += 1
         dt = time.perf_counter() - t0
         res["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                "sample": f"causal prefill of the {len(lens)} shortest prompts (lengths {lens}, "
-                                         f"same shapes, own seeded draws), fp64 C oracle, {threads} threads, "
-                                         f"{dt:.2f} s"}
-    if world == 1 and rank == 0 and not args.no_cpu_baseline and is_decode:
+                                         f"same shapes, own seeded draws), {reps} times, fp64 C oracle, "
+                                         f"{threads} threads, {dt:.2f} s"}
+    if world == 1 and rank == 0 and cpu_sample is not None and is_decode:
         tb = wl.tensor_bound(hbm, bf16)
-        n_seq = 1 if tb else min(args.cpu_seqs, wl.spec.batch)   # ~10-30 s of CPU work
-        run, threads = wl.oracle_sample(n_seq)
+        n_seq = 1 if tb else min(cpu_sample, wl.spec.batch)
+        csteps = wl.cycle if wl.qlen == 1 else 1
+        run, threads = wl.oracle_sample(n_seq, steps=csteps)
         t0 = time.perf_counter()
-        nbytes = run(0)
+        nbytes, reps = 0, 0
+        while reps == 0 or time.perf_counter() - t0 < cpu_seconds:
+            nbytes += run(reps % csteps)   # the cycle's steps in order, then again (idempotent appends)
+            reps += 1
         dt = time.perf_counter() - t0
-        res["cpu_baseline"] = {"value": wl.sample_flops(n_seq) / dt / 1e12 if tb else nbytes / dt / 1e9,
+        res["cpu_baseline"] = {"value": wl.sample_flops(n_seq) * reps / dt / 1e12 if tb else nbytes / dt / 1e9,
                                "unit": "TFLOP/s" if tb else "GB/s", "cores": threads,
                                "kind": "oracle",
-                               "sample": f"one append+attend step of {n_seq} of the {wl.spec.batch} "
+                               "sample": f"{reps} append+attend steps of {n_seq} of the {wl.spec.batch} "
                                          f"sequences (same lengths and shapes, own seeded draws), "
                                          f"fp64 C oracle, {threads} threads, {dt:.2f} s"}
+    return res
+
+
+# The five configurations of the workload set, with the CPU-oracle sample each is timed on
+# beside it (sequences of a decode step, or fp64 flops of the shortest prompts), repeated for
+# --config-cpu-seconds.
+CONFIG_SET = [
+    ("1_tiny", "tiny", 2),   # 60 KB of K/V: the time is launch latency, not HBM
+    ("2_llama2_7b_mha", "mha7b", 8),
+    ("3_llama2_70b_gqa", "gqa70b", 16),
+    ("4_mix_prefix_share", "mix", 16),
+    ("5_long_gqa", "long_gqa", 1),
+    ("5_long_mqa", "long_mqa", 1),
+    ("5_prefill", "prefill", 5e10),
+]
+
+CONFIG_KEYS = ("workload", "value", "unit", "ms_per_step", "pct_hbm_peak", "tokens_per_s_per_layer",
+               "prompt_tokens_per_s_per_layer", "unique_gb_per_s", "gpu_launches", "cpu_baseline")
+
+
+def config_summary(res):
+    """The keys of one workload's line that the configs object carries."""
+    out = {k: res[k] for k in CONFIG_KEYS if k in res}
+    out["workload"] = res["config"]["workload"]
+    r = res["roofline"]
+    out["roofline"] = {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "avg_launch_ms")}
+    out["steps"], out["warmup"] = res["steps"], res["warmup"]
+    out["clocks"] = {k: res["clocks"].get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")} \
+        if res.get("clocks") else None
+    return out
+
+
+def bench_ours(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    import paged_kv_cache_165_gb300 as pkv
+    from paged_kv_cache_165_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pkv.lib()
+
+    cpu = None if args.no_cpu_baseline else (args.cpu_seqs if args.workload != "prefill" else 3e11)
+    res = measure(args.workload, WORKLOADS[args.workload](), args, device, world, rank, args.steps, args.warmup, args.soak,
+                  with_e2e=True, cpu_sample=cpu, cpu_seconds=args.cpu_seconds)
+    torch.cuda.empty_cache()
+
+    # ---- every configuration of the workload set at one GPU, each with its CPU-oracle
+    # baseline: the same measurement, fewer steps, no end-to-end pass
+    if world == 1 and rank == 0 and not args.no_configs and args.workload == "gqa70b":
+        configs = {}
+        for key, name, sample in CONFIG_SET:
+            if name == args.workload:
+                line = dict(res)
+            else:
+                line = measure(name, WORKLOADS[name](), args, device, 1, 0, args.config_steps, args.warmup,
+                               args.config_soak, with_e2e=False,
+                               cpu_sample=None if args.no_cpu_baseline else sample,
+                               cpu_seconds=args.config_cpu_seconds)
+                torch.cuda.empty_cache()
+            configs[key] = config_summary(line)
+            if name == "tiny":
+                configs[key]["note"] = ("correctness-size step (60 KB of K/V): its time is launch latency, "
+                                        "so its GB/s and roofline fraction say nothing about HBM")
+        res["configs"] = configs
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -945,6 +1025,14 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=8,
                     help="sequences per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration measurements of the default run")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps of each configuration")
+    ap.add_argument("--config-soak", type=float, default=0.3, help="untimed seconds before each configuration")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="the CPU-oracle baseline repeats its sample for at least this long")
+    ap.add_argument("--config-cpu-seconds", type=float, default=4.0,
+                    help="the same for each configuration of the default run")
     args = ap.parse_args()
     args.warmup_requested = args.warmup
     args.warmup = max(args.warmup, 3)     # at least three untimed warm-up steps
