@@ -908,6 +908,7 @@ void chunk_plan(DecodePlan &plan, int B, int Hq, int Hkv, int d, int bs, int MBS
     // contexts, the group kernel) merge in a separate kernel, many blocks at once.
     plan.fused_merge = plan.tensor_core && !plan.group && plan.splits > 1 &&
                        plan.splits <= kFusedMergeMaxChunks && units <= max_counters;
+    plan.counter_bytes = plan.fused_merge ? static_cast<size_t>(units) * sizeof(unsigned) : 0;
 }
 
 }  // namespace

@@ -128,13 +128,11 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(
     s = scratch_address(&scratch);   // the first call in this context looks it up
     if (s != PKV_OK) return s;
     cudaError_t e = cudaSuccess;
-    if (plan.fused_merge) {
-        // the arrival counters of the units this call merges in place, one per (sequence,
-        // KV head, head tile): cleared here, so that a call that gave up on a wait (and
-        // left its counters behind) cannot spoil this one
-        const size_t counter_bytes =
-            static_cast<size_t>(B) * Hkv * ((Hq / Hkv + 7) / 8) * sizeof(unsigned);
-        e = cudaMemsetAsync(scratch, 0, counter_bytes, stream);
+    if (plan.counter_bytes > 0) {
+        // the counters this call uses (arrivals of the chunks that merge in place, tiles
+        // taken): cleared here, so that a call that gave up on a wait (and left its
+        // counters behind) cannot spoil this one
+        e = cudaMemsetAsync(scratch, 0, plan.counter_bytes, stream);
         if (e != cudaSuccess) return record_error(PKV_ERR_CUDA, cudaGetErrorString(e));
     }
     DecodeArgs a{out, lse, q, k_cache, v_cache, block_table, context_lens,

@@ -251,7 +251,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         // before teardown every copy issued must have landed (bounded)
         if (lane == 0)
-            for (int u = max(0, t - N); u < t; ++u) mbar_wait_bounded(bar(full0 + u % N), (u / N) & 1);
+            for (int u = max(0, t - N); u < t; ++u)
+                if (!mbar_wait_bounded(bar(full0 + u % N), (u / N) & 1)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
     } else if (warp == 8 || warp == 11) {
         // ---- MMA issue, one lane of each of two warps: warp 11 the scores S_t (once K_t has
         // landed and, for t >= 2, P_{t-2} is written, i.e. S_{t-2} has been read from the
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(384, 1)
                 // let this thread's MMAs finish (bounded) before teardown
                 const int drain = is_s ? Cfg::kDrain + 1 : Cfg::kDrain;
                 umma_commit(bar(drain));
-                mbar_wait_bounded(bar(drain), 0);
+                if (!mbar_wait_bounded(bar(drain), 0)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
             }
         }
     } else {

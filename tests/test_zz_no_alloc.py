@@ -11,8 +11,8 @@ same plan and the same kernels, so their outputs must be bit-identical; both are
 also checked against the fp64 oracle.  The cases cover every kernel family: the
 chunked kernel merging in place (arrival counters in the scratch), the chunked
 kernel with the separate merge, the tcgen05 kernel (16 and 64 query heads per KV
-head), the CUDA-core kernel over an fp32 cache, and a one-pass call that needs no
-scratch.
+head; one wave of blocks and several), the CUDA-core kernel over an fp32 cache,
+and a one-pass call that needs no scratch.
 
 This file is collected last, so a run that stops at the first failure has run
 every other test before it.
@@ -93,6 +93,9 @@ CASES = [
      torch.bfloat16, 0, 2),
     ("tcgen05_m16", [1200, 1, 4000, 333], [17, 2900, 0, 640, 128], 32, 2, torch.bfloat16, 0, 2),
     ("tcgen05_mqa_m64", [9000, 20, 4100], [130, 7000], 64, 1, torch.bfloat16, 0, 2),
+    ("tcgen05_mqa_m64_5_splits", [9000, 20, 4100], [130, 7000], 64, 1, torch.bfloat16, 5, 2),
+    ("tcgen05_m16_many_blocks", _lengths(12, 50, 1, 3000), _lengths(13, 50, 1, 2000), 32, 2,
+     torch.bfloat16, 0, 2),
     ("cuda_core_f32", [300, 1, 1000, 47], [999, 12, 0, 530, 200], 8, 2, torch.float32, 3, 2),
     ("one_pass_no_scratch", [300, 1, 1000, 47], [999, 12, 0, 530], 64, 8, torch.bfloat16, 1, 1),
 ]
