@@ -233,7 +233,7 @@ int pkv_paged_attention_kernel_launches(int B, int Tq, int max_q, int Hq, int Hk
             ? plan_decode(B, Hq, Hkv, d, bs, visible_blocks(MBS, bs, window), NB, dt, num_splits, st->sm_count,
                           true, true)
             : plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs,
-                                  visible_blocks(MBS, bs, window > 0 ? window + max_q - 1 : 0), NB, dt,
+                                  visible_blocks(MBS, bs, window > 0 ? window + max_q - 1 : 0), NB, dt, window,
                                   num_splits, st->sm_count, true, true);
     return plan.splits > 1 && !plan.fused_merge ? 2 : 1;
 }
@@ -340,9 +340,9 @@ size_t pkv_paged_attention_workspace_bytes(int B, int Tq, int max_q, int Hq, int
                                             st->sm_count);
     // query rows: cover the tcgen05 and the CUDA-core plans
     const int vis = visible_blocks(MBS, bs, window > 0 ? window + max_q - 1 : 0);
-    return std::max(plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs, vis, 1, PKV_BF16, num_splits,
+    return std::max(plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs, vis, 1, PKV_BF16, window, num_splits,
                                         st->sm_count, true, true).workspace_bytes,
-                    plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs, vis, 1, PKV_F32, num_splits,
+                    plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs, vis, 1, PKV_F32, window, num_splits,
                                         st->sm_count, false, false).workspace_bytes);
 }
 
@@ -377,7 +377,7 @@ pkv_status pkv_paged_attention(float *out, float *lse, const float *q, const voi
             ? plan_decode(B, Hq, Hkv, d, bs, visible_blocks(MBS, bs, window), NB, dt, num_splits, st->sm_count,
                           caches_aligned, aligned16(q))
             : plan_attention_rows(B, Tq, max_q, Hq, Hkv, d, bs,
-                                  visible_blocks(MBS, bs, window > 0 ? window + max_q - 1 : 0), NB, dt,
+                                  visible_blocks(MBS, bs, window > 0 ? window + max_q - 1 : 0), NB, dt, window,
                                   num_splits, st->sm_count, caches_aligned, aligned16(q));
     if (plan.workspace_bytes > 0 &&
         (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||

@@ -950,10 +950,22 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, p
 }
 
 DecodePlan plan_attention_rows(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs, int MBS, int NB,
-                               pkv_dtype dt, int num_splits, int sm_count, bool caches_aligned,
+                               pkv_dtype dt, int window, int num_splits, int sm_count, bool caches_aligned,
                                bool q_aligned) {
     DecodePlan plan{};
     const int m = Hq / Hkv;
+    if (dt == PKV_BF16 && (d == 64 || d == 128) && (bs == 16 || bs == 32) && caches_aligned && q_aligned &&
+        window == 0 && max_q >= kPagedPrefillMinRows && static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31)) {
+        // a chunk of new tokens per sequence over its cached prefix: 128 query rows of one
+        // head per block over all of the sequence's keys, in one pass
+        plan.paged_prefill = plan.tensor_core = true;
+        plan.qtiles = (max_q + 127) / 128;
+        plan.splits = 1;
+        plan.chunk_pages = MBS;
+        plan.workspace_bytes = 0;
+        plan.fused_merge = false;
+        return plan;
+    }
     plan.umma = dt == PKV_BF16 && (d == 64 || d == 128) && (bs == 16 || bs == 32) && caches_aligned &&
                 q_aligned && m <= 64 && static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31);
     if (plan.umma) {
@@ -986,7 +998,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
                           cudaStream_t stream) {
     const int rows = a.rows >= 0 ? a.rows : a.B;
     if (a.B == 0 || rows == 0) return cudaSuccess;
-    if (a.cu_q != nullptr && plan.tensor_core && !plan.umma) return cudaErrorInvalidValue;
+    if (a.cu_q != nullptr && plan.tensor_core && !plan.umma && !plan.paged_prefill) return cudaErrorInvalidValue;
     DecodeKParams kp{};
     kp.out = a.out;
     kp.lse = a.lse;
@@ -1033,6 +1045,16 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     }
 
     cudaError_t e;
+    if (plan.paged_prefill) {
+        CUtensorMap tk, tv;
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.d), static_cast<uint64_t>(a.NB) * a.Hkv * a.bs};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.d) * 2};
+        const uint32_t box[2] = {64, static_cast<uint32_t>(a.bs)};
+        if (a.cu_q == nullptr || !encode_map_bf16(&tk, a.k_cache, 2, dims, strides, box) ||
+            !encode_map_bf16(&tv, a.v_cache, 2, dims, strides, box))
+            return cudaErrorInvalidValue;
+        return launch_paged_prefill(kp, tk, tv, a.d, a.bs, dim3(plan.qtiles, a.Hq, a.B), stream);
+    }
     if (dt == PKV_FP8_E4M3 && plan.tensor_core) {
         CUtensorMap tk, tv;
         const uint64_t dims[2] = {static_cast<uint64_t>(a.d), static_cast<uint64_t>(a.NB) * a.Hkv * a.bs};

@@ -139,6 +139,11 @@ constexpr int kUmmaDecodeKeys = 128;
 cudaError_t launch_decode_umma(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv,
                                int d, int bs, dim3 grid, cudaStream_t stream);
 
+// Chunked prefill over a paged cache (paged_prefill.cu): bf16 caches, d in {64, 128}, bs in
+// {16, 32}, query rows cu_q; grid (query tiles of 128 rows, Hq, B); one pass, no workspace.
+cudaError_t launch_paged_prefill(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int d,
+                                 int bs, dim3 grid, cudaStream_t stream);
+
 // FP8 (E4M3) decode (decode_fp8.cu): d = 128, bs in {16, 32}, up to 8 query heads per KV
 // head; grid (chunks x head tiles, Hkv, B).  tk / tv are uint8 maps with {128, bs} boxes.
 cudaError_t launch_decode_fp8(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int bs,

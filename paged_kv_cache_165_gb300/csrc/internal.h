@@ -55,6 +55,8 @@ struct DecodePlan {
     size_t workspace_bytes;
     int q_per_tile = 1; // tcgen05 kernel: query rows per block (several queries per sequence)
     int qtiles = 1;     // tcgen05 kernel: query tiles per sequence
+    bool paged_prefill = false;   // many query rows per sequence: the chunked-prefill kernel
+                                  // (128 rows of one head per block, all keys, no split)
 };
 
 // caches_aligned: both cache bases 16-byte aligned; q_aligned: q 16-byte aligned (the
@@ -63,11 +65,14 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, p
                        int num_splits, int sm_count, bool caches_aligned, bool q_aligned);
 
 // Several query rows per sequence (pkv_paged_attention with cu_q): Tq rows, at most max_q
-// per sequence.  bf16 caches with d in {64, 128}, bs in {16, 32}, aligned caches and q and
-// up to 64 heads per KV head use the tcgen05 kernel with tiles of floor(64 / m) query
-// rows; other shapes the CUDA-core path.  MBS: the blocks any row can see.
+// per sequence.  bf16 caches with d in {64, 128}, bs in {16, 32}, aligned caches and q:
+// without a window and with at least kPagedPrefillMinRows rows in some sequence, the
+// chunked-prefill kernel (paged_prefill.cu); otherwise, with up to 64 heads per KV head,
+// the tcgen05 kernel with tiles of floor(64 / m) query rows; other shapes the CUDA-core
+// path.  MBS: the blocks any row can see.
+constexpr int kPagedPrefillMinRows = 64;
 DecodePlan plan_attention_rows(int B, int Tq, int max_q, int Hq, int Hkv, int d, int bs, int MBS, int NB,
-                               pkv_dtype dt, int num_splits, int sm_count, bool caches_aligned,
+                               pkv_dtype dt, int window, int num_splits, int sm_count, bool caches_aligned,
                                bool q_aligned);
 
 // Workspace that covers every plan these shapes can take (element type and alignment

@@ -1,0 +1,467 @@
+// paged_prefill.cu -- chunked prefill over a paged cache: many new query rows of each
+// sequence against everything the cache holds for it (a prefix-cache hit: only the new
+// suffix is prefilled, limoncc.com "大语言模型研究15——注意力机制优化之KV缓存" §5).
+//
+// What is computed is pkv_paged_attention with query rows: the nq rows of sequence b are
+// its last nq positions, P0 .. P0 + nq - 1 with P0 = L - nq (their K/V already appended),
+// and row r sees the keys at positions 0 .. P0 + r of the sequence -- causal, aligned to
+// the end of the cache (zwjcode.cn "KV Cache 的增量解码" §13) -- read through block_table[b]
+// (plumephp.com "KV Cache 优化与注意力机制加速" §4.2-§4.3), with query head i reading KV
+// head floor(i/m) (limoncc.com §3.3) and the online softmax of plumephp.com §2.2-§2.3.
+//
+// The tile is the prefill kernel's (prefill.cu): one CTA per (128 query rows of one head,
+// head, sequence), 128-key tiles, twelve warps.  What differs:
+//   - the queries are fp32: the softmax warps split each into bf16 hi + lo parts and store
+//     them, 128-byte swizzled, as two shared-memory operand tiles; S = Q_hi K^T + Q_lo K^T
+//     (two passes over the head dimension) carries q to about 2^-16 relative.
+//   - K and V come from the paged cache: one {64, bs} TMA box per page and 64-column panel,
+//     pages found through the block table, one box per loader lane.
+//   - the causal mask is bottom-right: row r sees keys up to P0 + r, so only the last key
+//     tiles of a row tile are masked; rows past nq see nothing and are not stored.
+//   - the last page may end inside its block: its V rows past the end are zeroed in shared
+//     memory before P.V (NaN or Inf in unwritten slots stay invisible).
+// Every wait is bounded and shares an abort flag: on a timeout the block drains its copies
+// and MMAs, frees tensor memory and returns with PKV_DEVERR_TIMEOUT.
+#include <math.h>
+
+#include "common.cuh"
+#include "decode_kparams.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D, int BS>
+struct PagedPrefillCfg {
+    static constexpr int kBM = 128, kTK = 128, kPPT = kTK / BS;   // pages per key tile
+    static constexpr int PANELS = D / 64;
+    static constexpr int NK = D == 64 ? 5 : 2, NV = D == 64 ? 5 : 2;   // K and V ring slots
+    static constexpr int kQBytes = kBM * D * 2;        // one Q part: D/64 panels of [128][128 B]
+    static constexpr int kSlotBytes = kTK * D * 2;     // one K or V tile
+    static constexpr int kOffQHi = 0, kOffQLo = kQBytes;
+    static constexpr int kOffK = 2 * kQBytes;
+    static constexpr int kOffV = kOffK + NK * kSlotBytes;
+    static constexpr int kOffBar = kOffV + NV * kSlotBytes;
+    // barriers: Q written; K full / free per slot; V full / free per slot; S full x2; P full;
+    // O done; all MMAs done; drain x2 (one per MMA-issuing thread)
+    static constexpr int kQ = 0, kKFull = 1, kKFree = 1 + NK, kVFull = 1 + 2 * NK, kVFree = 1 + 2 * NK + NV,
+                         kSFull = 1 + 2 * NK + 2 * NV, kPFull = kSFull + 2, kODone = kPFull + 1,
+                         kDone = kODone + 1, kDrain = kDone + 1, kNumBars = kDrain + 2;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;          // TMEM slot, abort flag
+    // row exchange of the two warps of a row, double-buffered by tile parity:
+    // [buffer][value, ok][half][128 rows] floats
+    static constexpr int kOffXch = (kOffMisc + 16 + 15) / 16 * 16;
+    static constexpr int kSmemBytes = 1024 + kOffXch + 2 * 2 * 2 * kBM * 4;
+    // tensor memory: two S buffers, O, P_hi, P_lo
+    static constexpr int kTmemCols = 512;
+    static constexpr int kSCol = 0, kOCol = 2 * kTK, kPHiCol = kOCol + D, kPLoCol = kPHiCol + kTK / 2;
+    static constexpr int kThreads = 384;
+    static_assert(D == 64 || D == 128, "head size");
+    static_assert(BS == 16 || BS == 32, "block size");
+    static_assert(kPLoCol + kTK / 2 <= kTmemCols, "tensor memory budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kPPT * PANELS <= 32 && 32 % kPPT == 0, "one box per loader lane; tiles within 32 pages");
+    static_assert(8 * 32 * (D / 2 + 4) * 4 <= (NK + NV) * kSlotBytes, "the output staging fits the K/V rings");
+};
+
+// One CTA per (query tile, query head, sequence); twelve warps:
+//   warps 9 and 10 (TMA): the K and the V tiles into two rings, one {64, bs} box (one page,
+//     one panel) per lane; a K slot is free once its scores are computed, a V slot once
+//     its P.V is.  A page past the keys any row sees is placed outside the cache, where TMA
+//     fills zeros.
+//   warps 11 and 8 (one lane each issues): S_j = Q_hi K_j^T + Q_lo K_j^T (N = 128 keys)
+//     into one of two tensor-memory S buffers, once K_j has landed and, for j >= 2, P_{j-2}
+//     has been written; O += P_hi V_j + P_lo V_j (N = d), P read from tensor memory.
+//   warps 0-7 (softmax): first the queries -- thread (w, lane) loads row r = 32 (w % 4) +
+//     lane, columns D/2 h .. D/2 h + D/2 - 1 (h = w / 4), splits them and stores both parts;
+//     then per key tile the prefill kernel's online softmax for row r over keys 64h ..
+//     64h + 63 of the tile, with the bottom-right causal mask.
+template <int D, int BS>
+__global__ void __launch_bounds__(384, 1)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const DecodeKParams p) {
+    using Cfg = PagedPrefillCfg<D, BS>;
+    constexpr int BM = Cfg::kBM, TK = Cfg::kTK, PPT = Cfg::kPPT, PANELS = Cfg::PANELS, NK = Cfg::NK,
+                  NV = Cfg::NV;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
+    float *xch = reinterpret_cast<float *>(smem + Cfg::kOffXch);
+    auto bar = [&](int k) { return smem_addr(&bars[k]); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
+    const bool report = threadIdx.x == 0 && qt == 0 && head == 0;
+    const int L = checked_len(p, b, BS, report);
+    const int c0 = __ldg(p.cu_q + b), nq = __ldg(p.cu_q + b + 1) - c0;
+    const int r0 = qt * BM;                     // the tile's first query row
+    if (nq < 0 || nq > L) {
+        if (report) raise_error(p.err, PKV_DEVERR_CU_SEQLENS);
+        // inconsistent rows: out = 0, lse = -inf (as the other query-row kernels)
+        if (r0 == 0)
+            for (int rr = 0; rr < min(max(nq, 0), BM); ++rr) {
+                const size_t bi = static_cast<size_t>(c0 + rr) * p.Hq + head;
+                for (int e = threadIdx.x; e < D; e += blockDim.x) p.out[bi * D + e] = 0.f;
+                if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bi] = -INFINITY;
+            }
+        return;
+    }
+    if (r0 >= nq) return;
+    const int nrows = min(BM, nq - r0);         // rows of this tile
+    const int P0 = L - nq + r0;                 // position of the tile's first row
+    const int key_end = P0 + nrows;             // one past the last key any row of the tile sees
+    const int npages = (key_end + BS - 1) / BS;
+    const int ntiles = (key_end + TK - 1) / TK;
+    const int kvh = head / p.m;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(Cfg::kQ), 8);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(bar(Cfg::kKFull + s), 1);
+            mbar_init(bar(Cfg::kKFree + s), 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(bar(Cfg::kVFull + s), 1);
+            mbar_init(bar(Cfg::kVFree + s), 1);
+        }
+        mbar_init(bar(Cfg::kSFull), 1);
+        mbar_init(bar(Cfg::kSFull + 1), 1);
+        mbar_init(bar(Cfg::kPFull), 8);
+        mbar_init(bar(Cfg::kODone), 1);
+        mbar_init(bar(Cfg::kDone), 1);
+        mbar_init(bar(Cfg::kDrain), 1);
+        mbar_init(bar(Cfg::kDrain + 1), 1);
+        *abort = 0;
+        fence_barrier_init();
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+    }
+    if (warp == 0) tmem_alloc(smem_addr(tslot), Cfg::kTmemCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t sQHi = smem_addr(smem + Cfg::kOffQHi), sQLo = smem_addr(smem + Cfg::kOffQLo);
+    auto sK = [&](int s) { return smem_addr(smem + Cfg::kOffK + s * Cfg::kSlotBytes); };
+    auto sV = [&](int s) { return smem_addr(smem + Cfg::kOffV + s * Cfg::kSlotBytes); };
+
+    if (warp == 9 || warp == 10) {
+        // ---- TMA loaders: warp 9 the K tiles, warp 10 the V tiles.  Tile t goes to slot
+        // t % N once the slot's previous tile is consumed.  Lane i < PPT * PANELS copies panel
+        // i % PANELS of page i / PANELS of the tile; the block-table entries come 32 at a time.
+        const bool is_k = warp == 9;
+        const int N = is_k ? NK : NV;
+        const int full0 = is_k ? Cfg::kKFull : Cfg::kVFull, free0 = is_k ? Cfg::kKFree : Cfg::kVFree;
+        const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS;
+        int tcur = lane < npages ? __ldg(tbl + lane) : -1;
+        int tbase = 0;
+        const int oob_row = p.NB * p.Hkv * BS;
+        const int pg = lane / PANELS, pn = lane % PANELS;
+        int t = 0;
+        for (; t < ntiles; ++t) {
+            bool fr = true;
+            if (lane == 0 && t >= N) fr = wait_or_abort(bar(free0 + t % N), ((t - N) / N) & 1, abort, p.err);
+            if (!__shfl_sync(kFull, fr ? 1 : 0, 0)) break;
+            const int s = t % N;
+            if (t * PPT >= tbase + 32) {   // a tile never straddles 32 pages (32 % PPT == 0)
+                tbase += 32;
+                tcur = tbase + lane < npages ? __ldg(tbl + tbase + lane) : -1;
+            }
+            const int k = t * PPT + pg;
+            const int phys = __shfl_sync(kFull, tcur, k & 31);
+            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), Cfg::kSlotBytes);
+            __syncwarp();
+            if (lane < PPT * PANELS) {
+                int row = oob_row;
+                if (k < npages) {
+                    if (phys < 0 || phys >= p.NB) {
+                        if (is_k && pn == 0) raise_error(p.err, PKV_DEVERR_BLOCK);
+                    } else {
+                        row = (phys * p.Hkv + kvh) * BS;
+                    }
+                }
+                const uint32_t dst = (is_k ? sK(s) : sV(s)) + pn * TK * 128 + pg * BS * 128;
+                tma_load_2d(dst, map, pn * 64, row, bar(full0 + s));
+            }
+        }
+        // before teardown every copy issued must have landed (bounded)
+        if (lane == 0)
+            for (int u = max(0, t - N); u < t; ++u)
+                if (!mbar_wait_bounded(bar(full0 + u % N), (u / N) & 1)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
+    } else if (warp == 8 || warp == 11) {
+        // ---- MMA issue, one lane each: warp 11 the scores, warp 8 the products with V.
+        // tcgen05.commit covers the committing thread's MMAs: warp 11 signals S full and K
+        // free, warp 8 O done, V free and, after the last P.V (which follows every S), all
+        // MMAs done.
+        if (lane == 0) {
+            const bool is_s = warp == 11;
+            bool issued = false, alive = true;
+            if (is_s) {
+                const uint32_t idesc_s = umma_idesc_bf16(BM, TK, 0);
+                alive = wait_or_abort(bar(Cfg::kQ), 0, abort, p.err);
+                for (int t = 0; t < ntiles && alive; ++t) {
+                    if (t >= 2) alive = wait_or_abort(bar(Cfg::kPFull), (t - 2) & 1, abort, p.err);
+                    alive = alive && wait_or_abort(bar(Cfg::kKFull + t % NK), (t / NK) & 1, abort, p.err);
+                    if (!alive) break;
+                    tc_fence_after_sync();
+                    const int s = t % NK;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t ad = umma_desc_sw128((part ? sQLo : sQHi) + (kk / 4) * BM * 128 +
+                                                                    (kk % 4) * 32, 16, 1024);
+                            const uint64_t bd =
+                                umma_desc_sw128(sK(s) + (kk / 4) * TK * 128 + (kk % 4) * 32, 16, 1024);
+                            umma_bf16(tmem + Cfg::kSCol + (t & 1) * TK, ad, bd, idesc_s,
+                                      (part > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    umma_commit(bar(Cfg::kSFull + (t & 1)));
+                    umma_commit(bar(Cfg::kKFree + s));
+                    issued = true;
+                }
+            } else {
+                const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
+                for (int j = 0; j < ntiles && alive; ++j) {
+                    alive = wait_or_abort(bar(Cfg::kPFull), j & 1, abort, p.err) &&
+                            wait_or_abort(bar(Cfg::kVFull + j % NV), (j / NV) & 1, abort, p.err);
+                    if (!alive) break;
+                    tc_fence_after_sync();
+                    const int s = j % NV;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+#pragma unroll
+                        for (int kk = 0; kk < TK / 16; ++kk) {
+                            const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
+                            umma_bf16_ts(tmem + Cfg::kOCol, tmem + (half ? Cfg::kPLoCol : Cfg::kPHiCol) + kk * 8, bd,
+                                         idesc_o, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    umma_commit(bar(Cfg::kODone));
+                    umma_commit(bar(Cfg::kVFree + s));
+                    issued = true;
+                }
+                if (alive) umma_commit(bar(Cfg::kDone));
+            }
+            if (*abort && issued) {
+                // let this thread's MMAs finish (bounded) before teardown
+                const int drain = is_s ? Cfg::kDrain + 1 : Cfg::kDrain;
+                umma_commit(bar(drain));
+                if (!mbar_wait_bounded(bar(drain), 0)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
+            }
+        }
+    } else {
+        // ---- softmax: thread (w, lane) owns query row r = 32 (w % 4) + lane (tensor-memory
+        // lane r) and keys 64h .. 64h + 63 of each key tile (h = w / 4)
+        const int h = warp >> 2;
+        const int r = ((warp & 3) << 5) | lane;
+        const bool row_ok = r < nrows;
+        const int qpos = P0 + r;                  // this row's position: keys 0 .. qpos
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4
+        auto xs = [&](int buf, int kind, int hh) { return xch + ((buf * 2 + kind) * 2 + hh) * BM + r; };
+
+        // the query row's columns D/2 h .. D/2 h + D/2 - 1, split into bf16 hi and lo parts
+        // and stored as row r of the two swizzled operand tiles (zeros for rows past nq)
+        {
+            const float *qrow = p.q + (static_cast<size_t>(c0 + r0 + (row_ok ? r : 0)) * p.Hq + head) * D + h * (D / 2);
+#pragma unroll
+            for (int c8 = 0; c8 < D / 16; ++c8) {   // 8 columns (16 bytes of each part) at a time
+                float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+                if (row_ok) {
+                    x0 = __ldg(reinterpret_cast<const float4 *>(qrow + 8 * c8));
+                    x1 = __ldg(reinterpret_cast<const float4 *>(qrow + 8 * c8 + 4));
+                }
+                uint4 hi, lo;
+                split_bf16x2(x0.x, x0.y, hi.x, lo.x);
+                split_bf16x2(x0.z, x0.w, hi.y, lo.y);
+                split_bf16x2(x1.x, x1.y, hi.z, lo.z);
+                split_bf16x2(x1.z, x1.w, hi.w, lo.w);
+                const uint32_t off = swz128(BM, r, h * (D / 2) + 8 * c8);
+                *reinterpret_cast<uint4 *>(smem + Cfg::kOffQHi + off) = hi;
+                *reinterpret_cast<uint4 *>(smem + Cfg::kOffQLo + off) = lo;
+            }
+            fence_proxy_async_smem();   // the tensor core reads these through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Cfg::kQ));
+        }
+
+        // The last page may end inside its block: V rows past the last key are zeroed
+        const int tail_valid = key_end - (npages - 1) * BS;   // 1..BS tokens
+        const int tail_tile = (npages - 1) / PPT;
+        const int tail_row0 = ((npages - 1) % PPT) * BS + tail_valid;
+        const int tail_rows = BS - tail_valid;
+        float m_ref = -INFINITY, l = 0.f;
+        // ok is warp-uniform, and after each tile's exchange the same in both warps of a
+        // row: a failed wait skips the remaining work but never a named barrier
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int sb = j & 1;
+            if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kSFull + sb), (j >> 1) & 1, abort, p.err));
+            float sc[64];
+            if (ok) {
+                tc_fence_after_sync();
+                uint32_t s0[32], s1[32];
+                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64, s0);
+                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64 + 32, s1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    sc[c] = __uint_as_float(s0[c]);
+                    sc[32 + c] = __uint_as_float(s1[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) sc[c] = -INFINITY;
+            }
+            if (ok && j == tail_tile && tail_rows > 0) {
+                // once the V copies of this tile have landed
+                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kVFull + j % NV), (j / NV) & 1, abort, p.err));
+                if (ok) {
+                    uint8_t *vt = smem + Cfg::kOffV + (j % NV) * Cfg::kSlotBytes;
+                    for (int idx = threadIdx.x; idx < tail_rows * PANELS * 8; idx += 256) {
+                        const int row = tail_row0 + idx / (PANELS * 8), rem = idx % (PANELS * 8);
+                        *reinterpret_cast<uint4 *>(vt + (rem >> 3) * TK * 128 + row * 128 + (rem & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
+            // bottom-right causal mask: key <= this row's position; a row past nq sees nothing
+            const int key0 = j * TK + h * 64;
+            if (key0 + 63 > P0 || !row_ok) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (key0 + c > qpos || !row_ok) sc[c] = -INFINITY;
+            }
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
+            float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            // the other half's maximum of this row, and whether it is still ok; the exchange
+            // buffer alternates with the tile, so one barrier a tile suffices
+            *xs(sb, 0, h) = mx;
+            *xs(sb, 1, h) = ok ? 1.f : 0.f;
+            named_barrier(pair_bar, 64);
+            mx = fmaxf(mx, *xs(sb, 0, 1 - h)) * p.scale_log2;
+            ok = ok && *xs(sb, 1, 1 - h) != 0.f;
+            if (!ok) continue;
+            // a row that has seen no key yet (one past nq) keeps m = -inf and weight 0
+            const float m_new = mx > m_ref + 8.f ? mx : m_ref;
+            const float alpha = m_new == m_ref ? 1.f : ex2_approx(m_ref - m_new);
+            m_ref = m_new;
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                sc[c] = ex2_approx(fmaf(sc[c], p.scale_log2, neg_m));
+                l4[c & 3] += sc[c];
+            }
+            l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+            uint32_t phi[32], plo[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) split_bf16x2(sc[2 * e], sc[2 * e + 1], phi[e], plo[e]);
+            // P_{j-1} V_{j-1} must be done: the P columns are free and O is current
+            if (j > 0) {
+                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kODone), (j - 1) & 1, abort, p.err));
+                if (!ok) continue;
+                tc_fence_after_sync();
+                if (__any_sync(kFull, alpha != 1.f)) {
+                    // this half rescales columns D/2 h .. D/2 h + D/2 - 1 of its rows
+#pragma unroll
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
+                    }
+                }
+            }
+            tmem_st32(lane_base + Cfg::kPHiCol + h * 32, phi);
+            tmem_st32(lane_base + Cfg::kPLoCol + h * 32, plo);
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Cfg::kPFull));
+        }
+        if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kDone), 0, abort, p.err));
+
+        // ---- the row's sum over its two threads, through the exchange buffer the last tile
+        // did not use; O / l and the log-sum-exp
+        const int fb = ntiles & 1;
+        *xs(fb, 0, h) = l;
+        named_barrier(pair_bar, 64);
+        const float lr = l + *xs(fb, 0, 1 - h);
+        if (ok) {
+            tc_fence_after_sync();
+            const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+            // O / l of the warp's 32 rows x D/2 columns, staged in the K/V rings (every MMA
+            // and copy has completed, so they are free) so that each store writes whole row
+            // segments; the pitch spreads the rows over the banks
+            constexpr int HW = D / 2, PITCH = HW + 4;
+            float *stage = reinterpret_cast<float *>(smem + Cfg::kOffK) + warp * 32 * PITCH;
+            fence_proxy_async_smem();
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t ov[32];
+                tmem_ld32(lane_base + Cfg::kOCol + h * HW + cc * 32, ov);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(stage + lane * PITCH + cc * 32 + e) =
+                        make_float4(__uint_as_float(ov[e]) * inv_l, __uint_as_float(ov[e + 1]) * inv_l,
+                                    __uint_as_float(ov[e + 2]) * inv_l, __uint_as_float(ov[e + 3]) * inv_l);
+            }
+            __syncwarp();
+            const int wrow0 = (warp & 3) << 5;
+            const int wrows = min(32, nrows - wrow0);   // rows of the warp inside the tile
+            for (int rr = 0; rr < wrows; ++rr) {
+                float *dst = p.out + (static_cast<size_t>(c0 + r0 + wrow0 + rr) * p.Hq + head) * D + h * HW;
+                if constexpr (HW == 64)
+                    *reinterpret_cast<float2 *>(dst + 2 * lane) =
+                        *reinterpret_cast<const float2 *>(stage + rr * PITCH + 2 * lane);
+                else
+                    dst[lane] = stage[rr * PITCH + lane];
+            }
+            if (row_ok && h == 0 && p.lse != nullptr)
+                p.lse[static_cast<size_t>(c0 + r0 + r) * p.Hq + head] =
+                    m_ref == -INFINITY ? -INFINITY : (m_ref + log2f(lr)) * kDecLn2;
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+template <int D, int BS>
+cudaError_t launch_pp(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
+                      cudaStream_t stream) {
+    using Cfg = PagedPrefillCfg<D, BS>;
+    auto kernel = paged_prefill_kernel<D, BS>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tk, tv, kp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_paged_prefill(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int d,
+                                 int bs, dim3 grid, cudaStream_t stream) {
+    if (d == 128) return bs == 16 ? launch_pp<128, 16>(kp, tk, tv, grid, stream)
+                                  : launch_pp<128, 32>(kp, tk, tv, grid, stream);
+    if (d == 64) return bs == 16 ? launch_pp<64, 16>(kp, tk, tv, grid, stream)
+                                 : launch_pp<64, 32>(kp, tk, tv, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

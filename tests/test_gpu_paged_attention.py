@@ -3,6 +3,7 @@ every decode path, several queries per sequence (verification steps, prefill on 
 a cached prefix), ragged and empty query counts, blocks released outside the window,
 and the device errors."""
 import math
+import os
 
 import numpy as np
 import pytest
@@ -144,6 +145,83 @@ def test_prefill_on_top_of_a_cached_prefix_equals_full_prefill():
     assert_attn_close(lse, full_lse[P:], "new rows lse")
 
 
+def poison_tails(kc, vc, table, lens, bs):
+    """NaN / Inf in every slot past each sequence's length and in unused blocks."""
+    kp, vp = kc.clone(), vc.clone()
+    used = set()
+    for b, n in enumerate(lens):
+        for pos in range(n, gen.blocks_needed(n, bs) * bs):
+            s = oracle.slot_of(table[b], pos, bs)
+            kp[s // bs, :, s % bs] = float("nan")
+            vp[s // bs, :, s % bs] = float("inf")
+        used.update(int(x) for x in table[b, :gen.blocks_needed(n, bs)])
+    for blk in range(kc.shape[0]):
+        if blk not in used:
+            kp[blk] = float("nan")
+            vp[blk] = float("nan")
+    return kp, vp
+
+
+# many query rows per sequence (at least 64 in one sequence): the chunked-prefill kernel,
+# 128 rows of one head per block over all of the sequence's keys
+@pytest.mark.parametrize("hq,hkv,d,bs", [(16, 2, 128, 16), (8, 8, 64, 32), (64, 1, 128, 16), (32, 4, 64, 16),
+                                         (8, 2, 128, 32)])
+def test_chunked_prefill_kernel_ragged_rows(hq, hkv, d, bs):
+    # a prefix plus 200 new rows (two row tiles), rows that are all of a sequence's tokens
+    # (64, 129: no prefix), a single row, 300 rows over a 700-token prefix, 5 of 5
+    lens = [300, 64, 1000, 129, 1000, 5]
+    nqs = [200, 64, 1, 129, 300, 5]
+    q, kc, vc, table, clens, cu = make_case(500 + hq + d + bs, lens, nqs, hq, hkv, d, bs, torch.bfloat16)
+    kc, vc = poison_tails(kc, vc, table, lens, bs)
+    B, Tq, max_q = len(lens), sum(nqs), max(nqs)
+    assert pkv.paged_attention_kernel_launches(B, Tq, max_q, hq, hkv, d, bs, table.shape[1], kc.shape[0],
+                                               torch.bfloat16, 0, 0) == 1
+    assert pkv.paged_attention_workspace_bytes(B, Tq, max_q, hq, hkv, d, bs, table.shape[1], 0, 0) >= 0
+    scale = 1 / math.sqrt(d)
+    ref, ref_lse = oracle.paged_attention(q, kc, vc, table, clens, cu, scale)
+    assert np.isfinite(ref).all()
+    out, lse = run(q, kc, vc, table, clens, cu, scale, 0, 0, one_per_seq=False)
+    assert pkv.get_device_error() == 0
+    assert_attn_close(out, ref, "chunked prefill out")
+    assert_attn_close(lse, ref_lse, "chunked prefill lse")
+
+
+def test_chunked_prefill_kernel_equals_full_prefill_of_prefix_and_chunk():
+    # the new rows of a prefill over prefix + chunk (zwjcode.cn §07), 200 rows over 300
+    P, N, hq, hkv, d, bs = 300, 200, 8, 2, 128, 16
+    L = P + N
+    g = gen.generator(37)
+    qkv = [gen.randn(g, (L, h, d), torch.bfloat16) for h in (hq, hkv, hkv)]
+    nb = gen.blocks_needed(L, bs) + 1
+    table = gen.block_table_from_order(gen.permutation(g, nb), [gen.blocks_needed(L, bs)])
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.tensor([oracle.slot_of(table[0], t, bs) for t in range(L)], device="cuda")
+    pkv.kv_append(qkv[1].cuda(), qkv[2].cuda(), kc, vc, slots)
+    full, full_lse = oracle.prefill(qkv[0], qkv[1], qkv[2], np.array([0, L], np.int32), 1 / math.sqrt(d))
+    out, lse = run(qkv[0][P:].float(), kc.cpu(), vc.cpu(), table, torch.tensor([L], dtype=torch.int32),
+                   torch.tensor([0, N], dtype=torch.int32), 1 / math.sqrt(d), 0, 0, one_per_seq=False)
+    assert pkv.get_device_error() == 0
+    assert_attn_close(out, full[P:], "new rows")
+    assert_attn_close(lse, full_lse[P:], "new rows lse")
+
+
+def test_chunked_prefill_kernel_bad_block_id_reads_zeros():
+    lens, nqs = [400, 200], [100, 70]
+    q, kc, vc, table, clens, cu = make_case(41, lens, nqs, 16, 2, 128, 16, torch.bfloat16)
+    bad = table.clone()
+    bad[0, 3] = kc.shape[0] + 5                       # outside the cache: read as a zero page
+    kz, vz = kc.clone(), vc.clone()
+    zero = int(table[0, 3])
+    kz[zero] = 0
+    vz[zero] = 0
+    out, lse = run(q, kc, vc, bad, clens, cu, 0.09, 0, 0, one_per_seq=False)
+    assert pkv.get_device_error() & pkv.DEVERR["block"]
+    ref, ref_lse = oracle.paged_attention(q, kz, vz, table, clens, cu, 0.09)
+    assert_attn_close(out, ref, "bad block out")
+    assert_attn_close(lse, ref_lse, "bad block lse")
+
+
 def test_query_count_above_length_raises_cu_seqlens_error():
     lens = [5, 40]
     q, kc, vc, table, clens, cu = make_case(9, lens, [2, 3], 8, 2, 64, 16, torch.bfloat16)
@@ -156,23 +234,17 @@ def test_query_count_above_length_raises_cu_seqlens_error():
     assert_attn_close(out[2:], ref, "valid sequence")
 
 
-def test_prefix_chunk_prefill_at_full_size_on_sampled_rows():
+def test_prefix_chunk_prefill_at_full_size():
     # the benched shape: 8 sequences with 4096 cached tokens each append a 512-token chunk
     # and attend it causally (bottom-right), 64 q / 8 kv heads, d 128, in the launch
-    # configuration the bench uses (automatic splits); sampled rows are checked one by one
-    # against the oracle, a row at position p being a single query over the first p+1 tokens
+    # configuration the bench uses
     P, N, B, hq, hkv, d, bs = 4096, 512, 8, 64, 8, 128, 16
     lens, nqs = [P + N] * B, [N] * B
     q, kc, vc, table, clens, cu = make_case(61, lens, nqs, hq, hkv, d, bs, torch.bfloat16, spare=1)
     scale = 1 / math.sqrt(d)
     out, lse = run(q, kc, vc, table, clens, cu, scale, 0, 0, one_per_seq=False)
     assert pkv.get_device_error() == 0
-    for b in (0, 5, 7):
-        for i in (0, 1, 127, 128, 300, N - 1):
-            row = b * N + i
-            pos = P + i
-            ref, ref_lse = oracle.paged_attention(q[row:row + 1], kc, vc, table[b:b + 1],
-                                                  torch.tensor([pos + 1], dtype=torch.int32),
-                                                  torch.tensor([0, 1], dtype=torch.int32), scale)
-            assert_attn_close(out[row:row + 1], ref, f"seq {b} row {i} out")
-            assert_attn_close(lse[row:row + 1], ref_lse, f"seq {b} row {i} lse")
+    # every row of every sequence (about 0.6 TFLOP of fp64 oracle work)
+    ref, ref_lse = oracle.paged_attention(q, kc, vc, table, clens, cu, scale, nthreads=os.cpu_count() or 1)
+    assert_attn_close(out, ref, "chunk out")
+    assert_attn_close(lse, ref_lse, "chunk lse")
