@@ -735,6 +735,8 @@ def measure(name, wl, args, device, world, rank, steps, warmup, soak, with_e2e=T
         files = ["decode.cu", "decode_kparams.cuh", "decode_epilogue.cuh", "common.cuh"]
         if wl.fp8:
             files += ["decode_fp8.cu", "fp8_codes.cuh"]
+        elif wl.qlen >= 64 and wl.window <= 0:
+            files.append("paged_prefill.cu")    # the chunked-prefill kernel (many query rows)
         elif wl.spec.q_heads // wl.spec.kv_heads > 8 or wl.qlen > 1:
             files.append("decode_umma.cu")      # the tcgen05 kernel (large groups, query rows)
         src = kernel_source_hash(files)
