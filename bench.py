@@ -513,12 +513,33 @@ class MixWorkload(DecodeWorkload):
         self._finish_setup(device, pkv, bm, nb, [torch.tensor(sl, dtype=torch.int64)],
                            [bm.context_lens(range(B))])
         self.copies = torch.tensor(copies, dtype=torch.int32, device=device)
-        self.launches_per_step += 1                 # kv_block_copy
+        # the 64 rows that start with the same physical blocks: their shared prefix is read once
+        # per step (pkv_decode_step_shared_prefix), the rest of each row by the decode
+        groups = bm.shared_prefix_groups(range(B))
+        self.groups = groups.to(device)
+        self.n_groups, self.prefix_tokens = groups.n_groups, groups.max_prefix_tokens
+        mbs = self.table.shape[1]
+        ws = pkv.decode_step_shared_prefix_workspace_bytes(B, s.q_heads, s.kv_heads, s.head_dim, bs, mbs, self.groups,
+                                                           self.num_splits)
+        if ws > self.ws.numel():
+            self.ws = torch.zeros(ws, dtype=torch.uint8, device=device)
+        self.step_call = True
+        self.launches_per_step = 1 + pkv.decode_step_shared_prefix_kernel_launches(   # + kv_block_copy
+            B, s.q_heads, s.kv_heads, s.head_dim, bs, mbs, nb, s.cache_dtype, self.groups, self.num_splits)
+
+    def attend_call(self, out, q, k_new, v_new, slots, clens, lse=None):
+        """The step's appends and attention through pkv_decode_step_shared_prefix."""
+        self.pkv.decode_step_shared_prefix(out, q, k_new, v_new, slots, self.k_cache, self.v_cache, self.table,
+                                           clens, self.spec.scale, self.groups, lse=lse, num_splits=self.num_splits,
+                                           workspace=self.ws)
 
     def describe(self):
         d = super().describe()
         d.update({"cow_copies_per_step": getattr(self, "n_copies", None),
-                  "unique_gb_per_step": getattr(self, "unique_bytes", 0) / 1e9})
+                  "unique_gb_per_step": getattr(self, "unique_bytes", 0) / 1e9,
+                  "shared_prefix": {"groups": getattr(self, "n_groups", None),
+                                    "prefix_tokens": getattr(self, "prefix_tokens", None),
+                                    "call": "pkv_decode_step_shared_prefix"}})
         return d
 
 
@@ -735,6 +756,8 @@ def measure(name, wl, args, device, world, rank, steps, warmup, soak, with_e2e=T
         files = ["decode.cu", "decode_kparams.cuh", "decode_epilogue.cuh", "common.cuh"]
         if wl.fp8:
             files += ["decode_fp8.cu", "fp8_codes.cuh"]
+        elif getattr(wl, "groups", None) is not None:
+            files.append("paged_prefill.cu")    # the shared-prefix kernel and merge
         elif wl.qlen >= 64 and wl.window <= 0:
             files.append("paged_prefill.cu")    # the chunked-prefill kernel (many query rows)
         elif wl.spec.q_heads // wl.spec.kv_heads > 8 or wl.qlen > 1:

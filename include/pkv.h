@@ -79,6 +79,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 #define PKV_DEVERR_PAIR       16u   /* kv_block_copy pair outside [0, NB) (pair skipped) */
 #define PKV_DEVERR_TIMEOUT    32u   /* a bounded wait for an asynchronous copy gave up */
 #define PKV_DEVERR_LAYOUT     64u   /* a kernel found its shared memory misaligned and did nothing */
+#define PKV_DEVERR_PREFIX    128u   /* a shared-prefix group whose members' prefixes differ (length, blocks) */
 
 /* Static description of a status code. */
 const char *pkv_status_string(pkv_status status);
@@ -223,6 +224,56 @@ pkv_status pkv_decode_step(float *out, float *lse, const float *q, const void *k
  * caches assumed), or -1 when the call would be rejected; 0 for B == 0. */
 int pkv_decode_step_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
                                     int num_splits);
+
+/*
+ * pkv_decode_step_shared_prefix -- pkv_decode_step for a batch in which groups of sequences
+ * share a prefix through the same physical blocks (forks and a common prompt share their
+ * blocks by reference count: 0539edu.com "从KV cache共享到批量调度…" §3, plumephp.com
+ * "KV Cache 优化与注意力机制加速" §4.3).  The results are those of pkv_decode_step on the
+ * same arguments (caches bit-identical; outputs and lse equal to rounding): the attention
+ * over a sequence's keys is the log-sum-exp merge of the attention over its shared prefix
+ * and over the keys after it (plumephp.com §2.2-§2.3).  What changes is the work: the
+ * prefix of a group is read once, by a tensor-core kernel that attends every member's
+ * query heads to it at once, and the decode reads each sequence from the end of its prefix.
+ *
+ *   prefix_tokens  int32 [B] (device): the number of leading tokens of sequence b that are
+ *                  its group's shared prefix -- a multiple of bs, at most context_lens[b] - 1
+ *                  (the step's new token is never in it); 0 for a sequence in no group
+ *   group_start    int32 [n_groups + 1] (device): the members of group g are
+ *                  group_seqs[group_start[g] .. group_start[g+1]), group_start[0] = 0 and
+ *                  group_start[n_groups] = n_members
+ *   group_seqs     int32 [n_members] (device): sequence indices, each in at most one group;
+ *                  every member of a group has the same prefix_tokens and the same first
+ *                  prefix_tokens / bs block-table entries (otherwise PKV_DEVERR_PREFIX is set
+ *                  and that group's outputs are not to be trusted)
+ *   n_groups, n_members, max_group_size, max_prefix_tokens: host-side sizes (max_prefix_tokens
+ *                  bounds every prefix_tokens[b]); they size the grids and the workspace
+ *   workspace      at least pkv_decode_step_shared_prefix_workspace_bytes(...) bytes, 16-byte
+ *                  aligned, its first PKV_DECODE_COUNTER_BYTES zeroed once (as the decode's)
+ *   the other arguments as pkv_decode_step.
+ * The prefix path is taken for bf16 caches with d in {64, 128}, bs in {16, 32}, 16-byte aligned
+ * caches and q, and at most 8 query heads per KV head; otherwise (or with n_groups = 0) the call
+ * is exactly pkv_decode_step.
+ */
+pkv_status pkv_decode_step_shared_prefix(float *out, float *lse, const float *q, const void *k_new,
+                                         const void *v_new, const int64_t *slot_mapping, void *k_cache,
+                                         void *v_cache, pkv_dtype dt, const int32_t *block_table,
+                                         const int32_t *context_lens, const int32_t *prefix_tokens,
+                                         const int32_t *group_start, const int32_t *group_seqs, int n_groups,
+                                         int n_members, int max_group_size, int max_prefix_tokens, int B, int Hq,
+                                         int Hkv, int d, int bs, int MBS, int NB, float scale, int num_splits,
+                                         void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Workspace bytes of pkv_decode_step_shared_prefix for these sizes on the current device. */
+size_t pkv_decode_step_shared_prefix_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS, int num_splits,
+                                                     int n_groups, int n_members, int max_group_size,
+                                                     int max_prefix_tokens);
+
+/* Kernels one pkv_decode_step_shared_prefix call with these sizes enqueues (aligned pointers
+ * assumed), or -1 when the call would be rejected; 0 for B == 0. */
+int pkv_decode_step_shared_prefix_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB,
+                                                  pkv_dtype dt, int num_splits, int n_groups, int n_members,
+                                                  int max_group_size, int max_prefix_tokens);
 
 /*
  * pkv_paged_attention -- queries at the end of each cached sequence: several per

@@ -14,6 +14,9 @@ from ._binding import (  # noqa: F401
     decode_kernel_launches,
     decode_step,
     decode_step_kernel_launches,
+    decode_step_shared_prefix,
+    decode_step_shared_prefix_kernel_launches,
+    decode_step_shared_prefix_workspace_bytes,
     decode_step_fp8,
     decode_step_fp8_kernel_launches,
     decode_workspace_bytes,
@@ -33,7 +36,7 @@ from ._binding import (  # noqa: F401
     prefill_attention,
     selftest_bounded_wait,
 )
-from .blocks import BlockManager, OutOfBlocks  # noqa: F401
+from .blocks import BlockManager, OutOfBlocks, PrefixGroups  # noqa: F401
 
 
 def build(force: bool = False) -> str:

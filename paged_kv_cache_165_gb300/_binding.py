@@ -19,7 +19,7 @@ PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUD
 PKV_F32, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 
 DEVERR = {
-    "slot": 1, "block": 2, "len": 4, "cu_seqlens": 8, "pair": 16, "timeout": 32, "layout": 64,
+    "slot": 1, "block": 2, "len": 4, "cu_seqlens": 8, "pair": 16, "timeout": 32, "layout": 64, "prefix": 128,
 }
 
 _DTYPES = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3}
@@ -89,6 +89,13 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I,
                                                      F, I, P]
     L.pkv_paged_decode_attention_noalloc.restype = I
+    L.pkv_decode_step_shared_prefix.argtypes = [P, P, P, P, P, P, P, P, I, P, P, P, P, P, I, I, I, I, I, I, I, I,
+                                                I, I, I, F, I, P, Z, P]
+    L.pkv_decode_step_shared_prefix.restype = I
+    L.pkv_decode_step_shared_prefix_workspace_bytes.argtypes = [I] * 11
+    L.pkv_decode_step_shared_prefix_workspace_bytes.restype = Z
+    L.pkv_decode_step_shared_prefix_kernel_launches.argtypes = [I] * 13
+    L.pkv_decode_step_shared_prefix_kernel_launches.restype = I
     L.pkv_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, I, I, P, P]
     L.pkv_selftest_bounded_wait.restype = I
     L.pkv_prefill_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, P, P, P, I, I, P]
@@ -296,6 +303,54 @@ def decode_step(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tabl
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
         _ptr(v_cache), dt, _ptr(block_table), _ptr(context_lens), B, Hq, Hkv, d, bs, block_table.shape[1],
         NB, float(scale), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def decode_step_shared_prefix(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, context_lens,
+                              scale, groups, lse=None, num_splits=0, workspace=None, stream=None) -> None:
+    """decode_step where the batch rows of each group in ``groups`` (a PrefixGroups on the
+    device) share a prefix of physical blocks: the same results, with each group's prefix
+    read once."""
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new)):
+        _cuda(name, t, k_cache.dtype)
+    dt = _dtype(k_cache)
+    _cuda("slot_mapping", slot_mapping, torch.int64)
+    _cuda("q", q, torch.float32)
+    _cuda("out", out, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    for name in ("prefix_tokens", "group_start", "group_seqs"):
+        _cuda(name, getattr(groups, name), torch.int32)
+    if lse is not None:
+        _cuda("lse", lse, torch.float32)
+    NB, Hkv, bs, d = k_cache.shape
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d) or tuple(k_new.shape) != (B, Hkv, d) or \
+            tuple(v_new.shape) != (B, Hkv, d) or slot_mapping.numel() != B or block_table.dim() != 2 or \
+            block_table.shape[0] != B or context_lens.numel() != B or groups.prefix_tokens.numel() != B or \
+            (lse is not None and lse.numel() != B * Hq):
+        raise ValueError("decode_step_shared_prefix: shapes do not match")
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pkv_decode_step_shared_prefix(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), dt, _ptr(block_table), _ptr(context_lens), _ptr(groups.prefix_tokens),
+        _ptr(groups.group_start), _ptr(groups.group_seqs), groups.n_groups, groups.n_members,
+        groups.max_group_size, groups.max_prefix_tokens, B, Hq, Hkv, d, bs, block_table.shape[1], NB,
+        float(scale), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def decode_step_shared_prefix_workspace_bytes(B, Hq, Hkv, d, bs, MBS, groups, num_splits=0) -> int:
+    return int(lib().pkv_decode_step_shared_prefix_workspace_bytes(
+        B, Hq, Hkv, d, bs, MBS, int(num_splits), groups.n_groups, groups.n_members, groups.max_group_size,
+        groups.max_prefix_tokens))
+
+
+def decode_step_shared_prefix_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, dtype, groups, num_splits=0) -> int:
+    return int(lib().pkv_decode_step_shared_prefix_kernel_launches(
+        B, Hq, Hkv, d, bs, MBS, NB, _DTYPES[dtype], int(num_splits), groups.n_groups, groups.n_members,
+        groups.max_group_size, groups.max_prefix_tokens))
 
 
 def decode_step_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, dtype, num_splits=0) -> int:

@@ -21,13 +21,44 @@ This is the bookkeeping that sits above the C ABI and produces its inputs
 * ``audit`` checks the invariant that every block's count equals the number of
   table entries that reference it (0539edu.com §5.2 suggests logging and checking
   every cache read/write per request).
+* ``shared_prefix_groups`` finds the sequences of a batch whose leading blocks are
+  the same physical blocks (a common prompt, forks) and describes them for
+  pkv_decode_step_shared_prefix, which then reads each group's shared prefix once.
 """
 from __future__ import annotations
 
+import dataclasses
 from collections import deque
 from typing import Dict, Iterable, List, Optional, Sequence, Tuple
 
 import torch
+
+
+@dataclasses.dataclass
+class PrefixGroups:
+    """Groups of batch rows that share a prefix of whole physical blocks.
+
+    ``prefix_tokens[b]`` is the number of leading tokens of batch row b in its group's
+    shared prefix (0: no group); the members of group g are
+    ``group_seqs[group_start[g]:group_start[g+1]]`` (batch rows).  Tensors are int32.
+    """
+    prefix_tokens: torch.Tensor
+    group_start: torch.Tensor
+    group_seqs: torch.Tensor
+    max_group_size: int
+    max_prefix_tokens: int
+
+    @property
+    def n_groups(self) -> int:
+        return self.group_start.numel() - 1
+
+    @property
+    def n_members(self) -> int:
+        return self.group_seqs.numel()
+
+    def to(self, device) -> "PrefixGroups":
+        return PrefixGroups(self.prefix_tokens.to(device), self.group_start.to(device), self.group_seqs.to(device),
+                            self.max_group_size, self.max_prefix_tokens)
 
 
 class OutOfBlocks(RuntimeError):
@@ -171,6 +202,42 @@ class BlockManager:
         return torch.tensor([self.slot(seq, p) for p in positions], dtype=torch.int64)
 
     # ----------------------------------------------------------- checks
+    def shared_prefix_groups(self, seqs: Sequence[int], min_members: int = 2, min_blocks: int = 1) -> PrefixGroups:
+        """Group the batch rows whose sequences start with the same physical blocks.
+
+        Rows whose first block is the same shared block form a group; its prefix is the
+        longest run of leading table entries common to every member, cut so that it ends
+        before every member's last position (the step's new token is never in it).  Groups
+        of fewer than ``min_members`` rows or ``min_blocks`` blocks are dropped.
+        """
+        seqs = list(seqs)
+        by_first: Dict[int, List[int]] = {}
+        for row, s in enumerate(seqs):
+            t = self.tables[s]
+            if t and self.refcount[t[0]] > 1:
+                by_first.setdefault(t[0], []).append(row)
+        bs = self.block_size
+        prefix = [0] * len(seqs)
+        starts, members = [0], []
+        for rows in by_first.values():
+            if len(rows) < min_members:
+                continue
+            tabs = [self.tables[seqs[r]] for r in rows]
+            n = min(len(t) for t in tabs)
+            pages = 0
+            while pages < n and all(t[pages] == tabs[0][pages] for t in tabs):
+                pages += 1
+            pages = min(pages, min((self.lengths[seqs[r]] - 1) // bs for r in rows))
+            if pages < min_blocks:
+                continue
+            for r in rows:
+                prefix[r] = pages * bs
+            members.extend(rows)
+            starts.append(len(members))
+        sizes = [b - a for a, b in zip(starts, starts[1:])]
+        return PrefixGroups(torch.tensor(prefix, dtype=torch.int32), torch.tensor(starts, dtype=torch.int32),
+                            torch.tensor(members, dtype=torch.int32), max(sizes, default=0), max(prefix, default=0))
+
     def audit(self) -> None:
         """Every block's count equals its table references; free blocks have count 0."""
         refs = [0] * self.num_blocks

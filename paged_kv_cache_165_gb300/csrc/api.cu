@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode_kparams.cuh"
 #include "internal.h"
 
 namespace pkv {
@@ -505,6 +506,233 @@ int pkv_decode_step_fp8_kernel_launches(int B, int Hq, int Hkv, int d, int bs, i
         plan_decode(B, Hq, Hkv, d, bs, MBS, NB, PKV_FP8_E4M3, num_splits, st->sm_count, true, true);
     static const uint4 aligned{};
     return n + (decode_fuses_append(plan, PKV_FP8_E4M3, new_dt, Hq, Hkv, &aligned, &aligned) ? 0 : 1);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The shared-prefix decode step's layout: key splits of the prefix and 128-row tiles of a
+// group's (member, head) pairs for the prefix kernel, and the workspace after the decode's
+// own: prefix partials o [members][Hq][splits][d], their lse [members][Hq][splits], the
+// suffix lse [B][Hq].
+struct SharedPrefixLayout {
+    bool ok = false;   // the cascade applies (otherwise the call is a plain decode step)
+    int splits = 1, rtiles = 1;
+    size_t decode_bytes = 0, o_off = 0, lse_off = 0, suffix_off = 0, total = 0;
+};
+
+SharedPrefixLayout shared_prefix_layout(const DecodePlan &plan, pkv_dtype dt, int B, int Hq, int Hkv, int d, int bs,
+                                        int n_groups, int n_members, int max_group_size, int max_prefix_tokens,
+                                        int sm_count, bool aligned) {
+    SharedPrefixLayout L;
+    L.decode_bytes = (plan.workspace_bytes + 255) / 256 * 256;
+    L.total = plan.workspace_bytes;
+    L.ok = n_groups > 0 && n_members > 0 && max_group_size > 0 && max_prefix_tokens > 0 && dt == PKV_BF16 &&
+           (d == 64 || d == 128) && (bs == 16 || bs == 32) && aligned && plan.tensor_core && !plan.umma;
+    if (!L.ok) return L;
+    const int m = Hq / Hkv;
+    L.rtiles = static_cast<int>((static_cast<long long>(max_group_size) * m + 127) / 128);
+    const long long units = static_cast<long long>(n_groups) * Hkv * L.rtiles;
+    const int max_tiles = (max_prefix_tokens + 127) / 128;
+    // the prefix kernel runs beside the decode: about a quarter of the SMs, with whole
+    // equal key splits (each split a few thousand cycles of start-up, then 16+ key tiles)
+    const long long want = std::max<long long>(1, (sm_count / 4 + units - 1) / units);
+    const int per = static_cast<int>(std::max<long long>(1, (max_tiles + want - 1) / want));
+    L.splits = std::min((max_tiles + per - 1) / per, 256);
+    const size_t parts = static_cast<size_t>(n_members) * Hq * L.splits;
+    L.o_off = L.decode_bytes;
+    L.lse_off = L.o_off + (parts * d * sizeof(float) + 255) / 256 * 256;
+    L.suffix_off = L.lse_off + (parts * sizeof(float) + 255) / 256 * 256;
+    L.total = L.suffix_off + static_cast<size_t>(B) * Hq * sizeof(float);
+    return L;
+}
+
+// A non-blocking stream and two events per device for work that runs beside a call's
+// stream (created on first use, kept until the process exits).  The mutex keeps one call's
+// record / wait / launch / record sequence whole when several host threads call at once.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+std::mutex g_side_mutex;
+
+pkv_status side_stream(cudaStream_t *stream, cudaEvent_t *fork, cudaEvent_t *join) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideStream &s = g_side[dev];
+    if (s.stream == nullptr) {
+        e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            s = SideStream{};
+            return cuda_fail(e, "side stream");
+        }
+    }
+    *stream = s.stream;
+    *fork = s.fork;
+    *join = s.join;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_decode_step_shared_prefix_workspace_bytes(int B, int Hq, int Hkv, int d, int bs, int MBS, int num_splits,
+                                                     int n_groups, int n_members, int max_group_size,
+                                                     int max_prefix_tokens) {
+    if (check_decode_sizes(B, Hq, Hkv, d, bs, MBS) != PKV_OK || num_splits < 0 || n_groups < 0 || n_members < 0 ||
+        max_group_size < 0 || max_prefix_tokens < 0)
+        return 0;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != PKV_OK) return 0;
+    const size_t plain = decode_workspace_upper_bound(B, Hq, Hkv, d, bs, MBS, num_splits, st->sm_count);
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, 1, PKV_BF16, num_splits, st->sm_count, true, true);
+    const SharedPrefixLayout L = shared_prefix_layout(plan, PKV_BF16, B, Hq, Hkv, d, bs, n_groups, n_members,
+                                                      max_group_size, max_prefix_tokens, st->sm_count, true);
+    return std::max(plain, L.total);
+}
+
+int pkv_decode_step_shared_prefix_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB,
+                                                  pkv_dtype dt, int num_splits, int n_groups, int n_members,
+                                                  int max_group_size, int max_prefix_tokens) {
+    const int n = pkv_decode_step_kernel_launches(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits);
+    if (n <= 0 || n_groups < 0 || n_members < 0 || max_group_size < 0 || max_prefix_tokens < 0) return n;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != PKV_OK) return -1;
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count, true, true);
+    const SharedPrefixLayout L = shared_prefix_layout(plan, dt, B, Hq, Hkv, d, bs, n_groups, n_members,
+                                                      max_group_size, max_prefix_tokens, st->sm_count, true);
+    return n + (L.ok ? 2 : 0);   // the prefix kernel and the merge around the decode
+}
+
+pkv_status pkv_decode_step_shared_prefix(float *out, float *lse, const float *q, const void *k_new,
+                                         const void *v_new, const int64_t *slot_mapping, void *k_cache,
+                                         void *v_cache, pkv_dtype dt, const int32_t *block_table,
+                                         const int32_t *context_lens, const int32_t *prefix_tokens,
+                                         const int32_t *group_start, const int32_t *group_seqs, int n_groups,
+                                         int n_members, int max_group_size, int max_prefix_tokens, int B, int Hq,
+                                         int Hkv, int d, int bs, int MBS, int NB, float scale, int num_splits,
+                                         void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    int eb = 0;
+    if (!elem_size(dt, &eb) || !attention_dtype(dt))
+        return fail(PKV_ERR_UNSUPPORTED, "decode_step_shared_prefix: element type %d", dt);
+    pkv_status s = check_decode_sizes(B, Hq, Hkv, d, bs, MBS);
+    if (s != PKV_OK) return s;
+    if (NB < 1 || num_splits < 0 || n_groups < 0 || n_members < 0 || max_group_size < 0 || max_prefix_tokens < 0 ||
+        max_prefix_tokens > MBS * bs || max_group_size > n_members)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "decode_step_shared_prefix: NB=%d num_splits=%d groups=%d members=%d max_group=%d "
+                    "max_prefix=%d",
+                    NB, num_splits, n_groups, n_members, max_group_size, max_prefix_tokens);
+    if (B == 0) return PKV_OK;
+    if (!out || !q || !k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !block_table ||
+        !context_lens || (n_groups > 0 && (!prefix_tokens || !group_start || !group_seqs)))
+        return fail(PKV_ERR_INVALID_ARG, "decode_step_shared_prefix: null pointer");
+    if (reinterpret_cast<uintptr_t>(q) % 8 != 0)
+        return fail(PKV_ERR_INVALID_ARG, "decode_step_shared_prefix: q must be 8-byte aligned");
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != PKV_OK) return s;
+    const bool aligned = aligned16(k_cache) && aligned16(v_cache) && aligned16(q);
+    const DecodePlan plan = plan_decode(B, Hq, Hkv, d, bs, MBS, NB, dt, num_splits, st->sm_count,
+                                        aligned16(k_cache) && aligned16(v_cache), aligned16(q));
+    const SharedPrefixLayout L = shared_prefix_layout(plan, dt, B, Hq, Hkv, d, bs, n_groups, n_members,
+                                                      max_group_size, max_prefix_tokens, st->sm_count, aligned);
+    if (L.total > 0 && (workspace == nullptr || workspace_bytes < L.total ||
+                        reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+        return fail(PKV_ERR_WORKSPACE,
+                    "decode_step_shared_prefix: needs %zu bytes of 16-byte aligned workspace, got %zu", L.total,
+                    workspace == nullptr ? size_t(0) : workspace_bytes);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    cudaError_t e = cudaSuccess;
+    cudaEvent_t joined = nullptr;
+    std::unique_lock<std::mutex> side_lock(g_side_mutex, std::defer_lock);   // fork .. join enqueued
+    DecodeArgs a{out, lse, q, k_cache, v_cache, block_table, context_lens,
+                 B, Hq, Hkv, d, bs, MBS, NB, scale, workspace, st->err};
+    if (L.ok) {
+        // the attention of every member over its group's prefix, read once per group
+        DecodeKParams kp{};
+        kp.q = q;
+        kp.block_table = block_table;
+        kp.context_lens = context_lens;
+        kp.err = st->err;
+        kp.B = B;
+        kp.Hq = Hq;
+        kp.Hkv = Hkv;
+        kp.m = Hq / Hkv;
+        kp.MBS = MBS;
+        kp.NB = NB;
+        kp.scale_log2 = scale * 1.4426950408889634f;
+        kp.cu_q = group_start;
+        kp.group_seqs = group_seqs;
+        kp.kv_start = prefix_tokens;
+        kp.prefix_splits = L.splits;
+        kp.prefix_rtiles = L.rtiles;
+        kp.ws_o = reinterpret_cast<float *>(ws + L.o_off);
+        kp.ws_lse = reinterpret_cast<float *>(ws + L.lse_off);
+        CUtensorMap tk, tv;
+        const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(NB) * Hkv * bs};
+        const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
+        const uint32_t box[2] = {64, static_cast<uint32_t>(bs)};
+        if (!encode_map_bf16(&tk, k_cache, 2, dims, strides, box) || !encode_map_bf16(&tv, v_cache, 2, dims, strides, box))
+            return fail(PKV_ERR_CUDA, "decode_step_shared_prefix: tensor map");
+        // on the device's side stream, beside the decode (which reads other pages and writes
+        // none of the prefix kernel's); joined back to `stream` before the merge
+        cudaStream_t side = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+        s = side_stream(&side, &fork, &join);
+        if (s != PKV_OK) return s;
+        side_lock.lock();
+        e = cudaEventRecord(fork, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+        if (e == cudaSuccess) e = launch_shared_prefix(kp, tk, tv, d, bs, dim3(L.splits, Hkv, n_groups * L.rtiles), side);
+        if (e == cudaSuccess) e = cudaEventRecord(join, side);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_step_shared_prefix prefix launch");
+        joined = join;
+        // the decode reads each sequence's keys after its prefix; its lse (the caller's array,
+        // or the workspace's) feeds the merge, which rewrites the members' entries in place
+        a.kv_start = prefix_tokens;
+        a.lse = lse != nullptr ? lse : reinterpret_cast<float *>(ws + L.suffix_off);
+    }
+    if (decode_fuses_append(plan, dt, dt, Hq, Hkv, k_new, v_new)) {
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.new_slots = slot_mapping;
+    } else {
+        e = launch_kv_append(k_new, v_new, k_cache, v_cache, eb, slot_mapping, B, Hkv, d, bs, NB, st->err, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_step_shared_prefix append launch");
+    }
+    e = launch_decode(a, plan, dt, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step_shared_prefix decode launch");
+    if (L.ok) {
+        e = cudaStreamWaitEvent(stream, joined, 0);   // the prefix partials are complete
+        side_lock.unlock();
+        if (e != cudaSuccess) return cuda_fail(e, "decode_step_shared_prefix join");
+        DecodeKParams kp{};
+        kp.out = out;
+        kp.lse = lse;
+        kp.block_table = block_table;
+        kp.context_lens = context_lens;
+        kp.err = st->err;
+        kp.Hq = Hq;
+        kp.MBS = MBS;
+        kp.cu_q = group_start;
+        kp.group_seqs = group_seqs;
+        kp.kv_start = prefix_tokens;
+        kp.prefix_splits = L.splits;
+        kp.ws_o = reinterpret_cast<float *>(ws + L.o_off);
+        kp.ws_lse = reinterpret_cast<float *>(ws + L.lse_off);
+        e = launch_shared_prefix_merge(kp, a.lse, d, bs, n_groups, n_members, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_step_shared_prefix merge launch");
+    }
+    return PKV_OK;
 }
 
 pkv_status pkv_prefill_attention(float *out, float *lse, const void *q, const void *k, const void *v,

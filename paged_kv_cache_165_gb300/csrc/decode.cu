@@ -1022,6 +1022,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     kp.v_scale = a.v_scale;
     kp.q_per_tile = plan.q_per_tile;
     kp.qtiles = plan.qtiles;
+    kp.kv_start = a.kv_start;
     if (a.new_slots != nullptr && decode_fuses_append(plan, dt, PKV_BF16, a.Hq, a.Hkv, a.k_new, a.v_new)) {
         kp.k_new = a.k_new;
         kp.v_new = a.v_new;

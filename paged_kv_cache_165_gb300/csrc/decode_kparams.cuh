@@ -36,6 +36,13 @@ struct DecodeKParams {
     const int64_t *new_slots;    // [B]; < 0: no new token
     void *k_cache_w, *v_cache_w; // the caches (FP8: the codes), for those writes
     float *k_scale_w, *v_scale_w;   // FP8 caches: the row scales, for those writes
+    // shared prefixes (pkv_decode_step_shared_prefix): sequence b's first kv_start[b] tokens
+    // are its group's shared prefix, attended by the prefix kernel; the decode kernels read
+    // keys from kv_start[b] on (nullptr: from 0)
+    const int32_t *kv_start;
+    const int32_t *group_seqs;   // prefix kernel: the member sequences of each group (cu_q: offsets)
+    int prefix_splits;           // prefix kernel: key splits of a group's prefix
+    int prefix_rtiles;           // prefix kernel: 128-row tiles of (member, head) rows per group
 };
 
 // The step's new token, written by one warp of the block that reads sequence b's last page
@@ -94,6 +101,8 @@ __device__ __forceinline__ SeqSpan span_of(const DecodeKParams &p, int b, int le
     s.b = b;
     s.len = len;
     s.lo = p.window > 0 ? max(0, len - p.window) : 0;
+    // a shared prefix read elsewhere: keys from kv_start[b] on, the last token always kept
+    if (p.kv_start != nullptr && len > 0) s.lo = max(s.lo, min(__ldg(p.kv_start + b), len - 1));
     s.pfirst = s.lo / bs;
     s.npages = len > 0 ? (len + bs - 1) / bs - s.pfirst : 0;
     s.cpfirst = s.pfirst;
@@ -143,6 +152,17 @@ cudaError_t launch_decode_umma(const DecodeKParams &kp, const CUtensorMap &tk, c
 // {16, 32}, query rows cu_q; grid (query tiles of 128 rows, Hq, B); one pass, no workspace.
 cudaError_t launch_paged_prefill(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int d,
                                  int bs, dim3 grid, cudaStream_t stream);
+
+// Shared prefixes (paged_prefill.cu): the attention of every member's query heads over its
+// group's prefix, one partial per key split into ws_o / ws_lse indexed by member (cu_q:
+// group offsets, group_seqs: members, kv_start: prefix tokens); grid (prefix_splits, Hkv,
+// groups * prefix_rtiles).  Then the merge of each member's partials with its suffix result
+// (out / lse as the decode wrote them, lse in natural log in suffix_lse), one warp per
+// (member, head), in place into out (and lse when not null; suffix_lse may be lse itself).
+cudaError_t launch_shared_prefix(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int d,
+                                 int bs, dim3 grid, cudaStream_t stream);
+cudaError_t launch_shared_prefix_merge(const DecodeKParams &kp, const float *suffix_lse, int d, int bs,
+                                       int n_groups, int n_members, cudaStream_t stream);
 
 // FP8 (E4M3) decode (decode_fp8.cu): d = 128, bs in {16, 32}, up to 8 query heads per KV
 // head; grid (chunks x head tiles, Hkv, B).  tk / tv are uint8 maps with {128, bs} boxes.

@@ -100,6 +100,8 @@ struct DecodeArgs {
     // the step's new tokens, appended inside the decode launch (decode_fuses_append)
     const void *k_new = nullptr, *v_new = nullptr;   // [B][Hkv][d], bf16
     const int64_t *new_slots = nullptr;              // [B]; < 0: no new token
+    const int32_t *kv_start = nullptr;               // [B]: keys read from this token on (a shared
+                                                     // prefix attended elsewhere); nullptr: 0
 };
 
 // Whether launch_decode can write the step's new tokens (one per sequence, at its last

@@ -78,7 +78,7 @@ struct PagedPrefillCfg {
 //     lane, columns D/2 h .. D/2 h + D/2 - 1 (h = w / 4), splits them and stores both parts;
 //     then per key tile the prefill kernel's online softmax for row r over keys 64h ..
 //     64h + 63 of the tile, with the bottom-right causal mask.
-template <int D, int BS>
+template <int D, int BS, bool kShared>
 __global__ void __launch_bounds__(384, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const DecodeKParams p) {
@@ -96,29 +96,75 @@ __global__ void __launch_bounds__(384, 1)
     auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
-    const bool report = threadIdx.x == 0 && qt == 0 && head == 0;
-    const int L = checked_len(p, b, BS, report);
-    const int c0 = __ldg(p.cu_q + b), nq = __ldg(p.cu_q + b + 1) - c0;
-    const int r0 = qt * BM;                     // the tile's first query row
-    if (nq < 0 || nq > L) {
-        if (report) raise_error(p.err, PKV_DEVERR_CU_SEQLENS);
-        // inconsistent rows: out = 0, lse = -inf (as the other query-row kernels)
-        if (r0 == 0)
-            for (int rr = 0; rr < min(max(nq, 0), BM); ++rr) {
-                const size_t bi = static_cast<size_t>(c0 + rr) * p.Hq + head;
-                for (int e = threadIdx.x; e < D; e += blockDim.x) p.out[bi * D + e] = 0.f;
-                if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bi] = -INFINITY;
+    // The rows of the tile and the keys they see.
+    //   chunked prefill: rows r0 .. r0 + nrows - 1 of sequence b's nq query rows, head `head`,
+    //     row r at position P0 + r seeing keys 0 .. P0 + r (pages from block_table[b]);
+    //   shared prefix: rows rho = 128 rt .. of the group's (member, head) pairs, rho = mu m + hh
+    //     for member mu and head kvh m + hh, all seeing the group's prefix keys of this split:
+    //     key tiles kt0 .. kt0 + ntiles - 1 of the prefix (pages from the first member's row).
+    int b = 0, head = 0, kvh = 0, c0 = 0, r0 = 0, nrows = 0, P0 = 0, key_end = 0, npages = 0, ntiles = 0;
+    int kt0 = 0, gs = 0, ks = 0;
+    const int32_t *tbl_row = nullptr;
+    if constexpr (kShared) {
+        ks = blockIdx.x;
+        kvh = blockIdx.y;
+        const int g = blockIdx.z / p.prefix_rtiles, rt = blockIdx.z % p.prefix_rtiles;
+        gs = __ldg(p.cu_q + g);
+        const int nmem = __ldg(p.cu_q + g + 1) - gs;
+        r0 = rt * BM;
+        nrows = min(BM, nmem * p.m - r0);
+        if (nrows <= 0) return;
+        const int first = __ldg(p.group_seqs + gs);
+        int P = __ldg(p.kv_start + first);
+        if (P < 0 || P % BS != 0 || P > p.MBS * BS) P = 0;   // flagged by the merge
+        const int KT = (P + TK - 1) / TK;
+        const int kps = (KT + p.prefix_splits - 1) / p.prefix_splits;
+        kt0 = ks * kps;
+        ntiles = min(KT, kt0 + kps) - kt0;
+        key_end = P;
+        npages = P / BS;
+        tbl_row = p.block_table + static_cast<size_t>(first) * p.MBS;
+        if (ntiles <= 0) {   // no prefix key in this split: empty partials
+            for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
+                const int rho = r0 + idx / D;
+                const size_t slot = (static_cast<size_t>(gs + rho / p.m) * p.Hq + kvh * p.m + rho % p.m) *
+                                        p.prefix_splits + ks;
+                p.ws_o[slot * D + idx % D] = 0.f;
+                if (idx % D == 0) p.ws_lse[slot] = -INFINITY;
             }
-        return;
+            return;
+        }
+    } else {
+        const int qt = blockIdx.x;
+        head = blockIdx.y;
+        b = blockIdx.z;
+        const bool report = threadIdx.x == 0 && qt == 0 && head == 0;
+        const int L = checked_len(p, b, BS, report);
+        c0 = __ldg(p.cu_q + b);
+        const int nq = __ldg(p.cu_q + b + 1) - c0;
+        r0 = qt * BM;                     // the tile's first query row
+        if (nq < 0 || nq > L) {
+            if (report) raise_error(p.err, PKV_DEVERR_CU_SEQLENS);
+            // inconsistent rows: out = 0, lse = -inf (as the other query-row kernels)
+            if (r0 == 0)
+                for (int rr = 0; rr < min(max(nq, 0), BM); ++rr) {
+                    const size_t bi = static_cast<size_t>(c0 + rr) * p.Hq + head;
+                    for (int e = threadIdx.x; e < D; e += blockDim.x) p.out[bi * D + e] = 0.f;
+                    if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bi] = -INFINITY;
+                }
+            return;
+        }
+        if (r0 >= nq) return;
+        nrows = min(BM, nq - r0);         // rows of this tile
+        P0 = L - nq + r0;                 // position of the tile's first row
+        key_end = P0 + nrows;             // one past the last key any row of the tile sees
+        npages = (key_end + BS - 1) / BS;
+        ntiles = (key_end + TK - 1) / TK;
+        kvh = head / p.m;
+        tbl_row = p.block_table + static_cast<size_t>(b) * p.MBS;
     }
-    if (r0 >= nq) return;
-    const int nrows = min(BM, nq - r0);         // rows of this tile
-    const int P0 = L - nq + r0;                 // position of the tile's first row
-    const int key_end = P0 + nrows;             // one past the last key any row of the tile sees
-    const int npages = (key_end + BS - 1) / BS;
-    const int ntiles = (key_end + TK - 1) / TK;
-    const int kvh = head / p.m;
+    const int pbase = kt0 * PPT;                 // the first page read
+    const int npg = npages - pbase;              // pages from there to the last key
 
     if (threadIdx.x == 0) {
         mbar_init(bar(Cfg::kQ), 8);
@@ -159,8 +205,8 @@ __global__ void __launch_bounds__(384, 1)
         const int N = is_k ? NK : NV;
         const int full0 = is_k ? Cfg::kKFull : Cfg::kVFull, free0 = is_k ? Cfg::kKFree : Cfg::kVFree;
         const CUtensorMap *map = is_k ? &tm_k : &tm_v;
-        const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS;
-        int tcur = lane < npages ? __ldg(tbl + lane) : -1;
+        const int32_t *tbl = tbl_row + pbase;
+        int tcur = lane < npg ? __ldg(tbl + lane) : -1;
         int tbase = 0;
         const int oob_row = p.NB * p.Hkv * BS;
         const int pg = lane / PANELS, pn = lane % PANELS;
@@ -172,7 +218,7 @@ __global__ void __launch_bounds__(384, 1)
             const int s = t % N;
             if (t * PPT >= tbase + 32) {   // a tile never straddles 32 pages (32 % PPT == 0)
                 tbase += 32;
-                tcur = tbase + lane < npages ? __ldg(tbl + tbase + lane) : -1;
+                tcur = tbase + lane < npg ? __ldg(tbl + tbase + lane) : -1;
             }
             const int k = t * PPT + pg;
             const int phys = __shfl_sync(kFull, tcur, k & 31);
@@ -180,7 +226,7 @@ __global__ void __launch_bounds__(384, 1)
             __syncwarp();
             if (lane < PPT * PANELS) {
                 int row = oob_row;
-                if (k < npages) {
+                if (k < npg) {
                     if (phys < 0 || phys >= p.NB) {
                         if (is_k && pn == 0) raise_error(p.err, PKV_DEVERR_BLOCK);
                     } else {
@@ -262,7 +308,20 @@ __global__ void __launch_bounds__(384, 1)
         const int h = warp >> 2;
         const int r = ((warp & 3) << 5) | lane;
         const bool row_ok = r < nrows;
-        const int qpos = P0 + r;                  // this row's position: keys 0 .. qpos
+        const int qpos = P0 + r;                  // chunked prefill: this row's position, keys 0 .. qpos
+        // the (sequence, head) pair this row is: shared prefix, member mu of the group
+        auto row_seq_head = [&](int rr, int &bq, int &hq, size_t &member) {
+            if constexpr (kShared) {
+                const int rho = r0 + rr;
+                member = static_cast<size_t>(gs + rho / p.m);
+                bq = __ldg(p.group_seqs + member);
+                hq = kvh * p.m + rho % p.m;
+            } else {
+                member = 0;
+                bq = c0 + r0 + rr;   // the query row
+                hq = head;
+            }
+        };
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4
         auto xs = [&](int buf, int kind, int hh) { return xch + ((buf * 2 + kind) * 2 + hh) * BM + r; };
@@ -270,7 +329,10 @@ __global__ void __launch_bounds__(384, 1)
         // the query row's columns D/2 h .. D/2 h + D/2 - 1, split into bf16 hi and lo parts
         // and stored as row r of the two swizzled operand tiles (zeros for rows past nq)
         {
-            const float *qrow = p.q + (static_cast<size_t>(c0 + r0 + (row_ok ? r : 0)) * p.Hq + head) * D + h * (D / 2);
+            int bq, hq;
+            size_t member;
+            row_seq_head(row_ok ? r : 0, bq, hq, member);
+            const float *qrow = p.q + (static_cast<size_t>(bq) * p.Hq + hq) * D + h * (D / 2);
 #pragma unroll
             for (int c8 = 0; c8 < D / 16; ++c8) {   // 8 columns (16 bytes of each part) at a time
                 float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
@@ -293,8 +355,8 @@ __global__ void __launch_bounds__(384, 1)
         }
 
         // The last page may end inside its block: V rows past the last key are zeroed
-        const int tail_valid = key_end - (npages - 1) * BS;   // 1..BS tokens
-        const int tail_tile = (npages - 1) / PPT;
+        const int tail_valid = key_end - (npages - 1) * BS;   // 1..BS tokens (BS for a prefix)
+        const int tail_tile = (npages - 1) / PPT - kt0;
         const int tail_row0 = ((npages - 1) % PPT) * BS + tail_valid;
         const int tail_rows = BS - tail_valid;
         float m_ref = -INFINITY, l = 0.f;
@@ -333,12 +395,22 @@ __global__ void __launch_bounds__(384, 1)
                     fence_proxy_async_smem();
                 }
             }
-            // bottom-right causal mask: key <= this row's position; a row past nq sees nothing
-            const int key0 = j * TK + h * 64;
-            if (key0 + 63 > P0 || !row_ok) {
+            const int key0 = (kt0 + j) * TK + h * 64;
+            if constexpr (kShared) {
+                // every row sees every prefix key; keys past the prefix and rows past the
+                // group's pairs see nothing
+                if (key0 + 63 >= key_end || !row_ok) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (key0 + c > qpos || !row_ok) sc[c] = -INFINITY;
+                    for (int c = 0; c < 64; ++c)
+                        if (key0 + c >= key_end || !row_ok) sc[c] = -INFINITY;
+                }
+            } else {
+                // bottom-right causal mask: key <= this row's position; a row past nq sees nothing
+                if (key0 + 63 > P0 || !row_ok) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (key0 + c > qpos || !row_ok) sc[c] = -INFINITY;
+                }
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -424,16 +496,28 @@ __global__ void __launch_bounds__(384, 1)
             const int wrow0 = (warp & 3) << 5;
             const int wrows = min(32, nrows - wrow0);   // rows of the warp inside the tile
             for (int rr = 0; rr < wrows; ++rr) {
-                float *dst = p.out + (static_cast<size_t>(c0 + r0 + wrow0 + rr) * p.Hq + head) * D + h * HW;
+                int bq, hq;
+                size_t member;
+                row_seq_head(wrow0 + rr, bq, hq, member);
+                // chunked prefill: the output row; shared prefix: this split's normalised partial
+                float *dst = kShared ? p.ws_o + ((member * p.Hq + hq) * p.prefix_splits + ks) * D + h * HW
+                                     : p.out + (static_cast<size_t>(bq) * p.Hq + hq) * D + h * HW;
                 if constexpr (HW == 64)
                     *reinterpret_cast<float2 *>(dst + 2 * lane) =
                         *reinterpret_cast<const float2 *>(stage + rr * PITCH + 2 * lane);
                 else
                     dst[lane] = stage[rr * PITCH + lane];
             }
-            if (row_ok && h == 0 && p.lse != nullptr)
-                p.lse[static_cast<size_t>(c0 + r0 + r) * p.Hq + head] =
-                    m_ref == -INFINITY ? -INFINITY : (m_ref + log2f(lr)) * kDecLn2;
+            if (row_ok && h == 0) {
+                int bq, hq;
+                size_t member;
+                row_seq_head(r, bq, hq, member);
+                const float lse2 = m_ref == -INFINITY ? -INFINITY : m_ref + log2f(lr);
+                if constexpr (kShared)
+                    p.ws_lse[(member * p.Hq + hq) * p.prefix_splits + ks] = lse2;
+                else if (p.lse != nullptr)
+                    p.lse[static_cast<size_t>(bq) * p.Hq + hq] = lse2 * kDecLn2;
+            }
         }
     }
     tc_fence_before_sync();
@@ -442,11 +526,11 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
-template <int D, int BS>
+template <int D, int BS, bool kShared>
 cudaError_t launch_pp(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
                       cudaStream_t stream) {
     using Cfg = PagedPrefillCfg<D, BS>;
-    auto kernel = paged_prefill_kernel<D, BS>;
+    auto kernel = paged_prefill_kernel<D, BS, kShared>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tk, tv, kp);
@@ -457,11 +541,116 @@ cudaError_t launch_pp(const DecodeKParams &kp, const CUtensorMap &tk, const CUte
 
 cudaError_t launch_paged_prefill(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int d,
                                  int bs, dim3 grid, cudaStream_t stream) {
-    if (d == 128) return bs == 16 ? launch_pp<128, 16>(kp, tk, tv, grid, stream)
-                                  : launch_pp<128, 32>(kp, tk, tv, grid, stream);
-    if (d == 64) return bs == 16 ? launch_pp<64, 16>(kp, tk, tv, grid, stream)
-                                 : launch_pp<64, 32>(kp, tk, tv, grid, stream);
+    if (d == 128) return bs == 16 ? launch_pp<128, 16, false>(kp, tk, tv, grid, stream)
+                                  : launch_pp<128, 32, false>(kp, tk, tv, grid, stream);
+    if (d == 64) return bs == 16 ? launch_pp<64, 16, false>(kp, tk, tv, grid, stream)
+                                 : launch_pp<64, 32, false>(kp, tk, tv, grid, stream);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_shared_prefix(const DecodeKParams &kp, const CUtensorMap &tk, const CUtensorMap &tv, int d,
+                                 int bs, dim3 grid, cudaStream_t stream) {
+    if (d == 128) return bs == 16 ? launch_pp<128, 16, true>(kp, tk, tv, grid, stream)
+                                  : launch_pp<128, 32, true>(kp, tk, tv, grid, stream);
+    if (d == 64) return bs == 16 ? launch_pp<64, 16, true>(kp, tk, tv, grid, stream)
+                                 : launch_pp<64, 32, true>(kp, tk, tv, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+namespace {
+
+// One warp per (member, query head): sequence b's attention over its group's prefix (the
+// prefix kernel's partials, lse in base 2) and over its own keys after the prefix (the
+// decode's result in out, its natural-log lse in suffix_lse) merge by log-sum-exp --
+// lse = log2 sum 2^{lse_k}, out = sum 2^{lse_k - lse} o_k (plumephp.com "KV Cache 优化与注意
+// 力机制加速" §2.2-§2.3 applied to the two key sets).  The head-0 warp of each member checks
+// that the member's prefix matches the group's first member (same length, a whole number
+// of blocks below the member's last position, the same physical blocks) and raises
+// PKV_DEVERR_PREFIX otherwise.
+template <int D>
+__global__ void __launch_bounds__(256)
+    shared_prefix_merge_kernel(const DecodeKParams p, const float *suffix_lse, int bs, int n_groups, int n_members) {
+    const int lane = threadIdx.x & 31;
+    const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (wid >= static_cast<long long>(n_members) * p.Hq) return;
+    const int member = static_cast<int>(wid / p.Hq), hq = static_cast<int>(wid % p.Hq);
+    const int b = __ldg(p.group_seqs + member);
+    if (hq == 0) {
+        int lo = 0, hi = n_groups;   // the group: cu_q[g] <= member < cu_q[g + 1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(p.cu_q + mid) <= member) lo = mid;
+            else hi = mid;
+        }
+        const int first = __ldg(p.group_seqs + __ldg(p.cu_q + lo));
+        const int P = __ldg(p.kv_start + b), len = __ldg(p.context_lens + b);
+        bool good = P == __ldg(p.kv_start + first) && P >= 0 && P % bs == 0 && P <= len - 1 &&
+                    len <= p.MBS * bs;
+        for (int j = lane; good && j < P / bs; j += 32)
+            if (__ldg(p.block_table + static_cast<size_t>(b) * p.MBS + j) !=
+                __ldg(p.block_table + static_cast<size_t>(first) * p.MBS + j))
+                good = false;
+        if (!__all_sync(kFull, good) && lane == 0) raise_error(p.err, PKV_DEVERR_PREFIX);
+    }
+    const size_t row = static_cast<size_t>(b) * p.Hq + hq;
+    const size_t part = (static_cast<size_t>(member) * p.Hq + hq) * p.prefix_splits;
+    const int S = p.prefix_splits;
+    const float ls = __ldg(suffix_lse + row) * kDecLog2e;   // base 2
+    float M = ls;
+    for (int k = lane; k < S; k += 32) M = fmaxf(M, __ldcg(p.ws_lse + part + k));
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, sh));
+    constexpr int CPL = D / 32;   // columns per lane
+    float acc[CPL];
+    const float ws = M == -INFINITY ? 0.f : ex2_approx(ls - M);
+    float L = ws;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) acc[e] = ws * p.out[row * D + lane * CPL + e];
+    // four partials at a time: their loads are in flight together
+    for (int k0 = 0; k0 < S; k0 += 4) {
+        float lk[4], v[4][CPL];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = min(k0 + u, S - 1);
+            lk[u] = k0 + u < S ? __ldcg(p.ws_lse + part + k) : -INFINITY;
+            const float *po = p.ws_o + (part + k) * D + lane * CPL;
+            if constexpr (CPL == 4) {
+                const float4 x = __ldcg(reinterpret_cast<const float4 *>(po));
+                v[u][0] = x.x;
+                v[u][1] = x.y;
+                v[u][2] = x.z;
+                v[u][3] = x.w;
+            } else {
+                const float2 x = __ldcg(reinterpret_cast<const float2 *>(po));
+                v[u][0] = x.x;
+                v[u][1] = x.y;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float w = M == -INFINITY ? 0.f : ex2_approx(lk[u] - M);   // 0 past the last partial
+            L += w;
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) acc[e] += w * v[u][e];
+        }
+    }
+    const float il = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) p.out[row * D + lane * CPL + e] = acc[e] * il;
+    if (lane == 0 && p.lse != nullptr) p.lse[row] = L > 0.f ? (M + log2f(L)) * kDecLn2 : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_shared_prefix_merge(const DecodeKParams &kp, const float *suffix_lse, int d, int bs,
+                                       int n_groups, int n_members, cudaStream_t stream) {
+    const long long warps = static_cast<long long>(n_members) * kp.Hq;
+    if (warps == 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+    if (d == 128) shared_prefix_merge_kernel<128><<<blocks, 256, 0, stream>>>(kp, suffix_lse, bs, n_groups, n_members);
+    else if (d == 64) shared_prefix_merge_kernel<64><<<blocks, 256, 0, stream>>>(kp, suffix_lse, bs, n_groups, n_members);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
 }
 
 }  // namespace pkv

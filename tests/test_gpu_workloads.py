@@ -157,12 +157,13 @@ def test_long_context_varlen_prefill_writes_cache():
     check_sampled(dout, dlse, q, kc, vc, table, clens, scale, list(range(len(lens))), "decode after prefill")
 
 
-@pytest.mark.parametrize("via_step", [False, True], ids=["append_then_decode", "decode_step"])
-def test_continuous_batching_mix_with_prefix_sharing_and_cow(via_step):
+@pytest.mark.parametrize("route", ["append_then_decode", "decode_step", "shared_prefix"])
+def test_continuous_batching_mix_with_prefix_sharing_and_cow(route):
     """256 sequences, lognormal lengths; 0..63 share a 4096-token prefix and form 32 fork
     pairs sharing their whole history, so each pair's first write into a shared partial
     block triggers copy-on-write (kv_block_copy) before the appends: kv_append then the
-    decode, or, as the bench's step, pkv_decode_step writing into the blocks just copied."""
+    decode, pkv_decode_step writing into the blocks just copied, or, as the bench's step,
+    pkv_decode_step_shared_prefix reading the 64 sequences' shared prefix once."""
     spec = gen.MIX
     lay = gen.mix_layout()
     B, hq, hkv, d, bs = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim, spec.block_size
@@ -205,7 +206,20 @@ def test_continuous_batching_mix_with_prefix_sharing_and_cow(via_step):
     gk, gv = dev(kc), dev(vc)
     table, lens = bm.block_table(range(B)), bm.context_lens(range(B))
     pkv.kv_block_copy(gk, gv, dev(torch.tensor(copies, dtype=torch.int32)))
-    if via_step:
+    if route == "shared_prefix":
+        groups = bm.shared_prefix_groups(range(B))
+        assert groups.n_groups == 1 and groups.n_members == lay.prefix_seqs
+        assert groups.max_prefix_tokens == lay.prefix_tokens
+        ws = torch.zeros(pkv.decode_step_shared_prefix_workspace_bytes(B, hq, hkv, d, bs, table.shape[1], groups),
+                         dtype=torch.uint8, device="cuda")
+        gout = torch.full((B, hq, d), float("nan"), device="cuda")
+        glse = torch.full((B, hq), float("nan"), device="cuda")
+        pkv.decode_step_shared_prefix(gout, dev(lay.q), dev(lay.k_new), dev(lay.v_new), dev(torch.tensor(slots)),
+                                      gk, gv, dev(table), dev(lens), spec.scale, groups.to("cuda"), lse=glse,
+                                      workspace=ws)
+        torch.cuda.synchronize()
+        out, lse = gout.cpu(), glse.cpu()
+    elif route == "decode_step":
         out, lse = decode_step(dev(lay.q), dev(lay.k_new), dev(lay.v_new), dev(torch.tensor(slots)), gk, gv,
                                dev(table), dev(lens), spec.scale)
     else:

@@ -168,3 +168,28 @@ def test_tiny_workload_draws_a_pool_of_8_blocks_with_3_free():
     used = {b for row in table for b in row if b >= 0}
     assert len(used) == 5 and used <= set(range(8))
     assert sorted(set(range(8)) - used) == sorted(order[5:])
+
+
+def test_shared_prefix_groups_find_whole_common_blocks():
+    """Rows forked from one prompt share its whole blocks; the group's prefix stops before
+    the partial block each fork copied on write and before every member's last position."""
+    bs = 16
+    bm = BlockManager(64, bs, order=gen.permutation(gen.generator(3), 64))
+    bm.add_sequence(100, 40)                  # a prompt of 40 tokens: 2 whole blocks + 8
+    for s in (0, 1, 2):
+        bm.fork(100, s)
+    bm.add_sequence(3, 20)                     # a row in no group
+    bm.fork(100, 4)
+    bm.free_sequence(100)
+    slots, copies = bm.append_step([0, 1, 2, 3, 4])
+    assert len(copies) >= 3                    # the shared partial block is copied by its writers
+    grp = bm.shared_prefix_groups([0, 1, 2, 3, 4])
+    assert grp.n_groups == 1 and grp.n_members == 4
+    assert grp.group_seqs.tolist() == [0, 1, 2, 4] and grp.group_start.tolist() == [0, 4]
+    assert grp.prefix_tokens.tolist() == [32, 32, 32, 0, 32]
+    assert grp.max_group_size == 4 and grp.max_prefix_tokens == 32
+    for r in (0, 1, 2, 4):                     # the same physical blocks, ending before the new token
+        assert bm.tables[r][:2] == bm.tables[0][:2] and bm.lengths[r] - 1 >= 32
+    # a group needs two rows and one whole block
+    assert bm.shared_prefix_groups([0, 3]).n_groups == 0
+    assert bm.shared_prefix_groups([0, 1], min_blocks=3).n_groups == 0
