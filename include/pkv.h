@@ -252,7 +252,7 @@ int pkv_decode_step_kernel_launches(int B, int Hq, int Hkv, int d, int bs, int M
  *                  aligned, its first PKV_DECODE_COUNTER_BYTES zeroed once (as the decode's)
  *   the other arguments as pkv_decode_step.
  * The prefix path is taken for bf16 caches with d in {64, 128}, bs in {16, 32}, 16-byte aligned
- * caches and q, and at most 8 query heads per KV head; otherwise (or with n_groups = 0) the call
+ * caches and q, and at most 64 query heads per KV head; otherwise (or with n_groups = 0) the call
  * is exactly pkv_decode_step.
  */
 pkv_status pkv_decode_step_shared_prefix(float *out, float *lse, const float *q, const void *k_new,

@@ -529,7 +529,8 @@ SharedPrefixLayout shared_prefix_layout(const DecodePlan &plan, pkv_dtype dt, in
     L.decode_bytes = (plan.workspace_bytes + 255) / 256 * 256;
     L.total = plan.workspace_bytes;
     L.ok = n_groups > 0 && n_members > 0 && max_group_size > 0 && max_prefix_tokens > 0 && dt == PKV_BF16 &&
-           (d == 64 || d == 128) && (bs == 16 || bs == 32) && aligned && plan.tensor_core && !plan.umma;
+           (d == 64 || d == 128) && (bs == 16 || bs == 32) && aligned && plan.tensor_core &&
+           (!plan.group || plan.umma) && Hq / Hkv <= 64;
     if (!L.ok) return L;
     const int m = Hq / Hkv;
     L.rtiles = static_cast<int>((static_cast<long long>(max_group_size) * m + 127) / 128);

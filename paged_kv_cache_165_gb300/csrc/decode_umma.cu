@@ -135,10 +135,12 @@ __global__ void __launch_bounds__(384, 1)
     const int slots = nqt * p.m;   // 1..64 query rows x heads
     const int P0 = L - nq + q0;    // position of the tile's first query
     // keys the whole sequence's rows see (chunk boundaries) and this tile's rows see
-    const int lo_seq = p.window > 0 ? max(0, L - nq + 1 - p.window) : 0;
+    // a shared prefix attended elsewhere (decode only): keys from kv_start[b] on, the last kept
+    const int kv0 = p.kv_start != nullptr && p.cu_q == nullptr && L > 0 ? min(__ldg(p.kv_start + b), L - 1) : 0;
+    const int lo_seq = max(kv0, p.window > 0 ? max(0, L - nq + 1 - p.window) : 0);
     const int cpfirst = lo_seq / BS, cnpages = L > 0 ? (L + BS - 1) / BS - cpfirst : 0;
     const int nc = (cnpages + p.chunk_pages - 1) / p.chunk_pages;
-    const int lo_tile = p.window > 0 ? max(0, P0 + 1 - p.window) : 0;    // first query's window
+    const int lo_tile = max(kv0, p.window > 0 ? max(0, P0 + 1 - p.window) : 0);   // first query's window
     const int hi_tile = P0 + nqt;                                         // one past the last query
     const int cp0 = cpfirst + split * p.chunk_pages;                      // this chunk's pages
     const int cp1 = min(cpfirst + cnpages, cp0 + p.chunk_pages);
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(384, 1)
         const bool slot_ok = slot < slots;
         // this row's query position and visible keys [lo_r, hi_r)
         const int pos_r = P0 + (slot_ok ? slot / p.m : 0);
-        const int lo_r = p.window > 0 ? max(0, pos_r + 1 - p.window) : 0;
+        const int lo_r = max(kv0, p.window > 0 ? max(0, pos_r + 1 - p.window) : 0);
         const int hi_r = min(pos_r + 1, apg1 * BS);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4
