@@ -550,23 +550,52 @@ SharedPrefixLayout shared_prefix_layout(const DecodePlan &plan, pkv_dtype dt, in
 }
 
 // A non-blocking stream and two events per device for work that runs beside a call's
-// stream (created on first use, kept until the process exits).  The mutex keeps one call's
-// record / wait / launch / record sequence whole when several host threads call at once.
+// stream (created on first use in each CUDA context, kept until the process exits).  The
+// mutex keeps one call's record / wait / launch / record sequence whole when several host
+// threads call at once.
 struct SideStream {
+    unsigned long long ctx_id = 0;   // the CUDA context they belong to (cuCtxGetId)
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
 };
 SideStream g_side[kMaxDevices];
 std::mutex g_side_mutex;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_fn_once;
+
+// Id of the current CUDA context (0 when none is current).  A stream or event created in a
+// context that has since been destroyed (cudaDeviceReset) must not be used again.
+unsigned long long current_ctx_id() {
+    std::call_once(g_ctx_fn_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current != nullptr && g_ctx_id != nullptr && g_ctx_current(&ctx) == CUDA_SUCCESS && ctx != nullptr)
+        g_ctx_id(ctx, &id);
+    return id;
+}
 
 pkv_status side_stream(cudaStream_t *stream, cudaEvent_t *fork, cudaEvent_t *join) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    const unsigned long long ctx = current_ctx_id();
     std::lock_guard<std::mutex> lock(g_side_mutex);
     SideStream &s = g_side[dev];
+    if (s.stream != nullptr && s.ctx_id != ctx) s = SideStream{};   // made in a context since destroyed
     if (s.stream == nullptr) {
+        s.ctx_id = ctx;
         e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
@@ -676,6 +705,7 @@ pkv_status pkv_decode_step_shared_prefix(float *out, float *lse, const float *q,
         kp.kv_start = prefix_tokens;
         kp.prefix_splits = L.splits;
         kp.prefix_rtiles = L.rtiles;
+        kp.n_members = n_members;
         kp.ws_o = reinterpret_cast<float *>(ws + L.o_off);
         kp.ws_lse = reinterpret_cast<float *>(ws + L.lse_off);
         CUtensorMap tk, tv;
@@ -722,6 +752,7 @@ pkv_status pkv_decode_step_shared_prefix(float *out, float *lse, const float *q,
         kp.block_table = block_table;
         kp.context_lens = context_lens;
         kp.err = st->err;
+        kp.B = B;
         kp.Hq = Hq;
         kp.MBS = MBS;
         kp.cu_q = group_start;

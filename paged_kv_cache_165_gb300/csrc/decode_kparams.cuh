@@ -43,6 +43,7 @@ struct DecodeKParams {
     const int32_t *group_seqs;   // prefix kernel: the member sequences of each group (cu_q: offsets)
     int prefix_splits;           // prefix kernel: key splits of a group's prefix
     int prefix_rtiles;           // prefix kernel: 128-row tiles of (member, head) rows per group
+    int n_members;               // prefix kernel: entries of group_seqs (group offsets must stay within)
 };
 
 // The step's new token, written by one warp of the block that reads sequence b's last page

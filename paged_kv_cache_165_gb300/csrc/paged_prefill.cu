@@ -111,10 +111,20 @@ __global__ void __launch_bounds__(384, 1)
         const int g = blockIdx.z / p.prefix_rtiles, rt = blockIdx.z % p.prefix_rtiles;
         gs = __ldg(p.cu_q + g);
         const int nmem = __ldg(p.cu_q + g + 1) - gs;
+        if (gs < 0 || nmem < 0 || gs + nmem > p.n_members ||
+            static_cast<long long>(nmem) * p.m > static_cast<long long>(p.prefix_rtiles) * BM) {
+            // offsets outside the member list, or a group larger than the declared maximum
+            if (threadIdx.x == 0 && ks == 0 && kvh == 0 && rt == 0) raise_error(p.err, PKV_DEVERR_PREFIX);
+            return;
+        }
         r0 = rt * BM;
         nrows = min(BM, nmem * p.m - r0);
         if (nrows <= 0) return;
         const int first = __ldg(p.group_seqs + gs);
+        if (first < 0 || first >= p.B) {
+            if (threadIdx.x == 0 && ks == 0 && kvh == 0 && rt == 0) raise_error(p.err, PKV_DEVERR_PREFIX);
+            return;
+        }
         int P = __ldg(p.kv_start + first);
         if (P < 0 || P % BS != 0 || P > p.MBS * BS) P = 0;   // flagged by the merge
         const int KT = (P + TK - 1) / TK;
@@ -315,6 +325,7 @@ __global__ void __launch_bounds__(384, 1)
                 const int rho = r0 + rr;
                 member = static_cast<size_t>(gs + rho / p.m);
                 bq = __ldg(p.group_seqs + member);
+                if (bq < 0 || bq >= p.B) bq = 0;   // flagged by the merge; never read out of range
                 hq = kvh * p.m + rho % p.m;
             } else {
                 member = 0;
@@ -575,6 +586,10 @@ __global__ void __launch_bounds__(256)
     if (wid >= static_cast<long long>(n_members) * p.Hq) return;
     const int member = static_cast<int>(wid / p.Hq), hq = static_cast<int>(wid % p.Hq);
     const int b = __ldg(p.group_seqs + member);
+    if (b < 0 || b >= p.B) {   // a member that is no sequence of the batch: flagged, skipped
+        if (hq == 0 && lane == 0) raise_error(p.err, PKV_DEVERR_PREFIX);
+        return;
+    }
     if (hq == 0) {
         int lo = 0, hi = n_groups;   // the group: cu_q[g] <= member < cu_q[g + 1]
         while (hi - lo > 1) {
@@ -582,10 +597,12 @@ __global__ void __launch_bounds__(256)
             if (__ldg(p.cu_q + mid) <= member) lo = mid;
             else hi = mid;
         }
-        const int first = __ldg(p.group_seqs + __ldg(p.cu_q + lo));
+        const int g0 = __ldg(p.cu_q + lo);
+        int first = g0 >= 0 && g0 < n_members ? __ldg(p.group_seqs + g0) : -1;
+        if (first < 0 || first >= p.B) first = b;   // (flagged below: the offsets or ids are bad)
         const int P = __ldg(p.kv_start + b), len = __ldg(p.context_lens + b);
-        bool good = P == __ldg(p.kv_start + first) && P >= 0 && P % bs == 0 && P <= len - 1 &&
-                    len <= p.MBS * bs;
+        bool good = g0 >= 0 && g0 < n_members && __ldg(p.group_seqs + g0) == first &&
+                    P == __ldg(p.kv_start + first) && P >= 0 && P % bs == 0 && P <= len - 1 && len <= p.MBS * bs;
         for (int j = lane; good && j < P / bs; j += 32)
             if (__ldg(p.block_table + static_cast<size_t>(b) * p.MBS + j) !=
                 __ldg(p.block_table + static_cast<size_t>(first) * p.MBS + j))

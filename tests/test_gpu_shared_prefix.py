@@ -155,3 +155,31 @@ def test_shared_prefix_group_whose_members_differ_is_flagged():
     c["table"] = c["bm"].block_table(c["rows"])
     run_step(c, groups)
     assert pkv.get_device_error() & pkv.DEVERR["prefix"]
+
+
+def test_shared_prefix_bad_group_descriptions_are_flagged_not_read():
+    """Group offsets past the member list, a member that is no sequence of the batch and a
+    group larger than the declared maximum raise PKV_DEVERR_PREFIX; the kernels' own range
+    checks keep every access inside the arrays."""
+    c = build_case(7, 32, 8, 128, 16, ROOTS, LONERS)
+    good = c["bm"].shared_prefix_groups(c["rows"])
+    B = len(c["rows"])
+    bad_start = pkv.PrefixGroups(good.prefix_tokens, torch.tensor([0, 5, 9], dtype=torch.int32), good.group_seqs,
+                                 good.max_group_size, good.max_prefix_tokens)      # 9 > the 8 members
+    bad_seq = pkv.PrefixGroups(good.prefix_tokens, good.group_start,
+                               torch.tensor(good.group_seqs.tolist()[:-1] + [B + 5], dtype=torch.int32),
+                               good.max_group_size, good.max_prefix_tokens)        # sequence B + 5
+    for groups in (bad_start, bad_seq):
+        run_step(c, groups)
+        assert pkv.get_device_error() & pkv.DEVERR["prefix"]
+    run_step(c, good)
+    assert pkv.get_device_error() == 0
+    # 64 query heads a KV head: a group of 5 has 320 (member, head) rows, three 128-row tiles;
+    # declared as a group of at most 1 (one tile), its rows would not all be computed
+    c = build_case(8, 64, 1, 128, 16, ROOTS, LONERS)
+    good = c["bm"].shared_prefix_groups(c["rows"])
+    too_big = pkv.PrefixGroups(good.prefix_tokens, good.group_start, good.group_seqs, 1, good.max_prefix_tokens)
+    run_step(c, too_big)
+    assert pkv.get_device_error() & pkv.DEVERR["prefix"]
+    run_step(c, good)
+    assert pkv.get_device_error() == 0
