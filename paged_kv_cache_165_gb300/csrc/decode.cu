@@ -932,6 +932,7 @@ bool decode_fuses_append(const DecodePlan &plan, pkv_dtype dt, pkv_dtype new_dt,
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int bs, int MBS, int NB, pkv_dtype dt,
                        int num_splits, int sm_count, bool caches_aligned, bool q_aligned) {
     DecodePlan plan{};
+    plan.sm_count = sm_count;
     const int tiles = (Hq / Hkv + 7) / 8;
     if (dt == PKV_FP8_E4M3) {
         // E4M3 codes: the tensor-core kernel takes d = 128 and one head tile per KV head
@@ -953,6 +954,7 @@ DecodePlan plan_attention_rows(int B, int Tq, int max_q, int Hq, int Hkv, int d,
                                pkv_dtype dt, int window, int num_splits, int sm_count, bool caches_aligned,
                                bool q_aligned) {
     DecodePlan plan{};
+    plan.sm_count = sm_count;
     const int m = Hq / Hkv;
     if (dt == PKV_BF16 && (d == 64 || d == 128) && (bs == 16 || bs == 32) && caches_aligned && q_aligned &&
         window == 0 && max_q >= kPagedPrefillMinRows && static_cast<long long>(NB + 1) * Hkv * bs < (1ll << 31)) {
@@ -1037,7 +1039,13 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype
     // up to 256 lengths at its start; a 4-token verification step on ragged lengths: 4.7%
     // faster).  With many query tiles per sequence the blocks are fine-grained already and
     // the ranking cost 1%.
-    kp.longest_first = plan.umma && plan.qtiles == 1 && a.B <= 256 ? 1 : 0;
+    // ... but only when the grid has more blocks than one wave: in a single wave every block
+    // starts at once and the ranking (a load of every length at the block's start) only delays
+    // the first copies
+    kp.longest_first = plan.umma && plan.qtiles == 1 && a.B <= 256 &&
+                               static_cast<long long>(plan.splits) * a.Hkv * a.B > plan.sm_count
+                           ? 1
+                           : 0;
     if (plan.splits > 1) {
         uint8_t *ws = static_cast<uint8_t *>(a.workspace);
         kp.counters = plan.fused_merge ? reinterpret_cast<unsigned *>(ws) : nullptr;

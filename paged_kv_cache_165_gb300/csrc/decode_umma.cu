@@ -95,6 +95,15 @@ __global__ void __launch_bounds__(384, 1)
     const int split = blockIdx.x, kvh = blockIdx.y;
     const int qt = blockIdx.z % p.qtiles;
     int b = blockIdx.z / p.qtiles;
+    // Decode in launch order (one query, no window, no shared prefix): the chunk's pages start
+    // at split * chunk_pages whatever the sequence's length, so the loader warps load their
+    // first block-table entries now, while the block sets up
+    const bool early_table = !p.longest_first && p.cu_q == nullptr && p.window <= 0 && p.kv_start == nullptr &&
+                             (warp == 9 || warp == 10);
+    const int early_page0 = split * p.chunk_pages;
+    int early_tcur = -1;
+    if (early_table && early_page0 + lane < p.MBS)
+        early_tcur = __ldg(p.block_table + static_cast<size_t>(b) * p.MBS + early_page0 + lane);
     if (p.longest_first) {
         // grid z ranks the sequences by length, longest first (ties: lower index first), so
         // that with lengths that differ the long blocks start first and the short ones fill
@@ -219,7 +228,8 @@ __global__ void __launch_bounds__(384, 1)
         const int full0 = is_k ? Cfg::kKFull : Cfg::kVFull, free0 = is_k ? Cfg::kKFree : Cfg::kVFree;
         const CUtensorMap *map = is_k ? &tm_k : &tm_v;
         const int32_t *tbl = p.block_table + static_cast<size_t>(b) * p.MBS + pfirst;
-        int tcur = lane < pages ? __ldg(tbl + lane) : -1;
+        int tcur = early_table && pfirst == early_page0 ? (lane < pages ? early_tcur : -1)
+                                                        : (lane < pages ? __ldg(tbl + lane) : -1);
         int tbase = 0;
         const int oob_row = p.NB * p.Hkv * BS;
         const int pg = lane / PANELS, pn = lane % PANELS;

@@ -52,6 +52,7 @@ struct DecodePlan {
     int chunk_pages;    // blocks per chunk
     bool fused_merge;   // the last chunk of each unit merges (counters in the workspace)
     size_t counter_bytes = 0;  // bytes of arrival counters a call uses (from the start)
+    int sm_count = 0;          // the device's SMs the plan was made for
     size_t workspace_bytes;
     int q_per_tile = 1; // tcgen05 kernel: query rows per block (several queries per sequence)
     int qtiles = 1;     // tcgen05 kernel: query tiles per sequence
