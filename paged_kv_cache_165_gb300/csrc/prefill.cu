@@ -64,21 +64,24 @@ struct TcPrefillCfg {
     static constexpr int kOffK = kQBytes;
     static constexpr int kOffV = kOffK + NK * kSlotBytes;
     static constexpr int kOffBar = kOffV + NV * kSlotBytes;
-    // barriers: Q; K full / free per slot; V full / free per slot; S full x2; P full; O done;
-    // all MMAs done; drain x2 (one per MMA-issuing thread)
+    static constexpr int NSP = 3;                       // S / P buffers in tensor memory
+    // barriers: Q; K full / free per slot; V full / free per slot; per S/P buffer: S full, P
+    // full, P consumed (its P.V done); all MMAs done; drain x2 (one per MMA-issuing thread)
     static constexpr int kQ = 0, kKFull = 1, kKFree = 1 + NK, kVFull = 1 + 2 * NK, kVFree = 1 + 2 * NK + NV,
-                         kSFull = 1 + 2 * NK + 2 * NV, kPFull = kSFull + 2, kODone = kPFull + 1,
-                         kDone = kODone + 1, kDrain = kDone + 1, kNumBars = kDrain + 2;
+                         kSFull = 1 + 2 * NK + 2 * NV, kPFull = kSFull + NSP, kPFree = kPFull + NSP,
+                         kDone = kPFree + NSP, kDrain = kDone + 1, kNumBars = kDrain + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;          // TMEM slot, abort flag
     // row exchange of the two warps of a row, double-buffered by tile parity:
     // [buffer][value, ok][half][128 rows] floats
     static constexpr int kOffXch = (kOffMisc + 16 + 15) / 16 * 16;
     static constexpr int kSmemBytes = 1024 + kOffXch + 2 * 2 * 2 * kBM * 4;
-    // tensor memory: two S buffers, O, P_hi, P_lo
+    // tensor memory: NSP S buffers of 128 columns, then O.  The weights of tile j overwrite
+    // its scores: the thread that read S columns 64h .. 64h + 63 of a row writes P_hi of
+    // those keys to columns 64h .. 64h + 31 of the buffer and P_lo to 64h + 32 .. 64h + 63.
     static constexpr int kTmemCols = 512;
-    static constexpr int kSCol = 0, kOCol = 2 * kTK, kPHiCol = kOCol + D, kPLoCol = kPHiCol + kTK / 2;
+    static constexpr int kSCol = 0, kOCol = NSP * kTK;
     static constexpr int kThreads = 384;
-    static_assert(kPLoCol + kTK / 2 <= kTmemCols, "tensor memory budget");
+    static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(8 * 32 * (D / 2 + 4) * 4 <= NK * kSlotBytes, "the output staging fits the K ring");
 };
@@ -89,10 +92,11 @@ struct TcPrefillCfg {
 //     into two rings of tile slots, one {64, 1, 16} box (16 rows of one 64-column panel) per
 //     lane, so that sixteen threads issue copies at once; a K slot is free once its scores
 //     are computed, a V slot once its P.V is.
-//   warps 11 and 8 (one lane each issues tcgen05.mma): S_j = Q K_j^T (N = 128 keys) into one
-//     of two tensor-memory S buffers, once K_j has landed and, for j >= 2, P_{j-2} has been
-//     written (S_{j-2} read); and O += P_hi V_j + P_lo V_j (N = d) with P_hi and P_lo read
-//     from tensor memory.  Each issuer waits only for its own inputs.
+//   warps 11 and 8 (one lane each issues tcgen05.mma): S_j = Q K_j^T (N = 128 keys) into
+//     tensor-memory buffer j % 3, once K_j has landed and, for j >= 3, P_{j-3} V_{j-3} (which
+//     read that buffer) is done; and O += P_hi V_j + P_lo V_j (N = d) with P_hi and P_lo read
+//     from the same buffer.  Each issuer waits only for its own inputs; with three buffers
+//     the softmax of tile j never waits for a P.V unless it rescales O.
 //   warps 0-7 (softmax): row r of the query tile is tensor-memory lane r, shared by warps
 //     w and w+4 (w = r / 32); warp half h = w / 4 takes keys 64h .. 64h + 63 of each key tile.
 //     Per tile: read the row of S, apply the causal mask (key <= query) on the diagonal tile,
@@ -141,10 +145,11 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(bar(Cfg::kVFull + s), 1);
             mbar_init(bar(Cfg::kVFree + s), 1);
         }
-        mbar_init(bar(Cfg::kSFull), 1);
-        mbar_init(bar(Cfg::kSFull + 1), 1);
-        mbar_init(bar(Cfg::kPFull), 8);
-        mbar_init(bar(Cfg::kODone), 1);
+        for (int u = 0; u < Cfg::NSP; ++u) {
+            mbar_init(bar(Cfg::kSFull + u), 1);
+            mbar_init(bar(Cfg::kPFull + u), 8);
+            mbar_init(bar(Cfg::kPFree + u), 1);
+        }
         mbar_init(bar(Cfg::kDone), 1);
         mbar_init(bar(Cfg::kDrain), 1);
         mbar_init(bar(Cfg::kDrain + 1), 1);
@@ -200,8 +205,10 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 8 || warp == 11) {
         // ---- MMA issue, one lane each: warp 11 the scores, warp 8 the products with V.
         // tcgen05.commit covers the committing thread's MMAs: warp 11 signals S full and K
-        // free, warp 8 O done, V free and, after the last P.V (which follows every S), all
-        // MMAs done.
+        // free, warp 8 P consumed, V free and, after the last P.V (which follows every S),
+        // all MMAs done.  Buffer j % 3's barriers complete once per use (tiles j, j + 3, ..),
+        // and no use starts before the previous one is consumed, so each wait's phase is
+        // unambiguous.
         if (lane == 0) {
             const bool is_s = warp == 11;
             bool issued = false, alive = true;
@@ -209,7 +216,9 @@ __global__ void __launch_bounds__(384, 1)
                 const uint32_t idesc_s = umma_idesc_bf16(BM, TK, 0);
                 alive = wait_or_abort(bar(Cfg::kQ), 0, abort, p.err);
                 for (int t = 0; t < ntiles && alive; ++t) {
-                    if (t >= 2) alive = wait_or_abort(bar(Cfg::kPFull), (t - 2) & 1, abort, p.err);
+                    const int sb = t % Cfg::NSP;
+                    if (t >= Cfg::NSP)
+                        alive = wait_or_abort(bar(Cfg::kPFree + sb), ((t - Cfg::NSP) / Cfg::NSP) & 1, abort, p.err);
                     alive = alive && wait_or_abort(bar(Cfg::kKFull + t % NK), (t / NK) & 1, abort, p.err);
                     if (!alive) break;
                     tc_fence_after_sync();
@@ -218,16 +227,17 @@ __global__ void __launch_bounds__(384, 1)
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t ad = umma_desc_sw128(sQ + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
                         const uint64_t bd = umma_desc_sw128(sK(s) + (kk / 4) * TK * 128 + (kk % 4) * 32, 16, 1024);
-                        umma_bf16(tmem + Cfg::kSCol + (t & 1) * TK, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                        umma_bf16(tmem + Cfg::kSCol + sb * TK, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
                     }
-                    umma_commit(bar(Cfg::kSFull + (t & 1)));
+                    umma_commit(bar(Cfg::kSFull + sb));
                     umma_commit(bar(Cfg::kKFree + s));
                     issued = true;
                 }
             } else {
                 const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
                 for (int j = 0; j < ntiles && alive; ++j) {
-                    alive = wait_or_abort(bar(Cfg::kPFull), j & 1, abort, p.err) &&
+                    const int sb = j % Cfg::NSP;
+                    alive = wait_or_abort(bar(Cfg::kPFull + sb), (j / Cfg::NSP) & 1, abort, p.err) &&
                             wait_or_abort(bar(Cfg::kVFull + j % NV), (j / NV) & 1, abort, p.err);
                     if (!alive) break;
                     tc_fence_after_sync();
@@ -236,11 +246,13 @@ __global__ void __launch_bounds__(384, 1)
                     for (int half = 0; half < 2; ++half)
 #pragma unroll
                         for (int kk = 0; kk < TK / 16; ++kk) {
+                            // keys 16 kk .. 16 kk + 15: P_hi (half 0) or P_lo of the keys' 64-key half
+                            const uint32_t pcol = Cfg::kSCol + sb * TK + (kk / 4) * 64 + half * 32 + (kk % 4) * 8;
                             const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
-                            umma_bf16_ts(tmem + Cfg::kOCol, tmem + (half ? Cfg::kPLoCol : Cfg::kPHiCol) + kk * 8, bd,
-                                         idesc_o, (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                            umma_bf16_ts(tmem + Cfg::kOCol, tmem + pcol, bd, idesc_o,
+                                         (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
                         }
-                    umma_commit(bar(Cfg::kODone));
+                    umma_commit(bar(Cfg::kPFree + sb));
                     umma_commit(bar(Cfg::kVFree + s));
                     issued = true;
                 }
@@ -267,14 +279,17 @@ __global__ void __launch_bounds__(384, 1)
         // row: a failed wait skips the remaining work but never a named barrier
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const int sb = j & 1;
-            if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kSFull + sb), (j >> 1) & 1, abort, p.err));
+            const int sb = j & 1;              // exchange buffer
+            const int pb = j % Cfg::NSP;       // S / P buffer
+            const uint32_t scol = lane_base + Cfg::kSCol + pb * TK + h * 64;
+            if (ok)
+                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kSFull + pb), (j / Cfg::NSP) & 1, abort, p.err));
             float sc[64];
             if (ok) {
                 tc_fence_after_sync();
                 uint32_t s0[32], s1[32];
-                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64, s0);
-                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64 + 32, s1);
+                tmem_ld32(scol, s0);
+                tmem_ld32(scol + 32, s1);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -319,12 +334,14 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t phi[32], plo[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) split_bf16x2(sc[2 * e], sc[2 * e + 1], phi[e], plo[e]);
-            // P_{j-1} V_{j-1} must be done: the P columns are free and O is current
-            if (j > 0) {
-                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kODone), (j - 1) & 1, abort, p.err));
+            // a rescale of O waits for P_{j-1} V_{j-1} (and so every earlier P.V): O is then
+            // current, and P_j V_j has not started, as it waits for this tile's P
+            if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
+                const int qb = (j - 1) % Cfg::NSP;
+                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kPFree + qb), ((j - 1) / Cfg::NSP) & 1, abort, p.err));
                 if (!ok) continue;
                 tc_fence_after_sync();
-                if (__any_sync(kFull, alpha != 1.f)) {
+                {
                     // this half rescales columns D/2 h .. D/2 h + D/2 - 1 of its rows
 #pragma unroll
                     for (int cc = 0; cc < D / 64; ++cc) {
@@ -337,12 +354,13 @@ __global__ void __launch_bounds__(384, 1)
                     }
                 }
             }
-            tmem_st32(lane_base + Cfg::kPHiCol + h * 32, phi);
-            tmem_st32(lane_base + Cfg::kPLoCol + h * 32, plo);
+            // the weights over this thread's own scores (already in registers)
+            tmem_st32(scol, phi);
+            tmem_st32(scol + 32, plo);
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Cfg::kPFull));
+            if (lane == 0) mbar_arrive(bar(Cfg::kPFull + pb));
         }
         if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kDone), 0, abort, p.err));
 
