@@ -53,66 +53,105 @@ __device__ __forceinline__ bool seq_range(const PrefillKParams &p, int b, int &s
 
 // ============================================================ tcgen05 path
 
-// Tiles of the tcgen05 prefill: one 128-row query tile per CTA, 128-key K/V tiles.
+// Tiles of the tcgen05 prefill: 128-row query tiles of one head, 128-key K/V tiles.  One
+// CTA per SM works through the query tiles of the launch.
 template <int D>
 struct TcPrefillCfg {
     static constexpr int kBM = 128, kTK = 128;
     static constexpr int PANELS = D / 64;
     static constexpr int NK = D == 64 ? 6 : 3, NV = D == 64 ? 5 : 2;   // K and V ring slots
+    static constexpr int NSP = 3;                      // S / P buffers in tensor memory
     static constexpr int kQBytes = kBM * D * 2;        // the Q tile: D/64 panels of [128][128 B]
     static constexpr int kSlotBytes = kTK * D * 2;     // one K or V tile: D/64 panels of [128][128 B]
     static constexpr int kOffK = kQBytes;
     static constexpr int kOffV = kOffK + NK * kSlotBytes;
-    static constexpr int kOffBar = kOffV + NV * kSlotBytes;
-    static constexpr int NSP = 3;                       // S / P buffers in tensor memory
-    // barriers: Q; K full / free per slot; V full / free per slot; per S/P buffer: S full, P
-    // full, P consumed (its P.V done); all MMAs done; drain x2 (one per MMA-issuing thread)
-    static constexpr int kQ = 0, kKFull = 1, kKFree = 1 + NK, kVFull = 1 + 2 * NK, kVFree = 1 + 2 * NK + NV,
-                         kSFull = 1 + 2 * NK + 2 * NV, kPFull = kSFull + NSP, kPFree = kPFull + NSP,
-                         kDone = kPFree + NSP, kDrain = kDone + 1, kNumBars = kDrain + 2;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;          // TMEM slot, abort flag
-    // row exchange of the two warps of a row, double-buffered by tile parity:
+    // output staging of the epilogue warps: [warp][32 rows][32 columns + 4] floats
+    static constexpr int kPitch = 36;
+    static constexpr int kOffStage = kOffV + NV * kSlotBytes;
+    // row statistics handed to the epilogue warps, double-buffered by query tile:
+    // [buffer][m, l of half 0, l of half 1][128 rows] floats
+    static constexpr int kOffStats = kOffStage + 4 * 32 * kPitch * 4;
+    // row-maximum exchange of the two softmax warps of a row, double-buffered by key tile:
     // [buffer][value, ok][half][128 rows] floats
-    static constexpr int kOffXch = (kOffMisc + 16 + 15) / 16 * 16;
-    static constexpr int kSmemBytes = 1024 + kOffXch + 2 * 2 * 2 * kBM * 4;
-    // tensor memory: NSP S buffers of 128 columns, then O.  The weights of tile j overwrite
-    // its scores: the thread that read S columns 64h .. 64h + 63 of a row writes P_hi of
-    // those keys to columns 64h .. 64h + 31 of the buffer and P_lo to 64h + 32 .. 64h + 63.
+    static constexpr int kOffXch = kOffStats + 2 * 3 * kBM * 4;
+    static constexpr int kOffBar = kOffXch + 2 * 2 * 2 * kBM * 4;
+    // barriers: Q loaded, Q free (a query tile's scores all computed); K full / free per
+    // slot; V full / free per slot; per S/P buffer: S full, P full, P consumed (its P.V
+    // done); O done (a query tile's last P.V), O free (read by the epilogue warps); per
+    // statistics buffer: full, free; drain x2 (one per MMA-issuing thread)
+    static constexpr int kQ = 0, kQFree = 1, kKFull = 2, kKFree = 2 + NK, kVFull = 2 + 2 * NK,
+                         kVFree = 2 + 2 * NK + NV, kSFull = 2 + 2 * NK + 2 * NV, kPFull = kSFull + NSP,
+                         kPFree = kPFull + NSP, kODone = kPFree + NSP, kOFree = kODone + 1,
+                         kStFull = kOFree + 1, kStFree = kStFull + 2, kDrain = kStFree + 2,
+                         kNumBars = kDrain + 2;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // TMEM slot, abort flag
+    static constexpr int kSmemBytes = 1024 + kOffMisc + 16;
+    // tensor memory: NSP S buffers of 128 columns, then O.  The weights of a key tile
+    // overwrite its scores: the thread that read S columns 64h .. 64h + 63 of a row writes
+    // P_hi of those keys to columns 64h .. 64h + 31 of the buffer and P_lo to 64h + 32 ..
+    // 64h + 63.
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 0, kOCol = NSP * kTK;
-    static constexpr int kThreads = 384;
+    static constexpr int kThreads = 512;
     static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert(8 * 32 * (D / 2 + 4) * 4 <= NK * kSlotBytes, "the output staging fits the K ring");
 };
 
-// One CTA per (query head, sequence, 128-query tile), the tiles with the most key tiles
-// launched first across all sequences; twelve warps:
-//   warps 9 and 10 (TMA): the Q tile once (lane 0 of warp 9), then the K and the V tiles
-//     into two rings of tile slots, one {64, 1, 16} box (16 rows of one 64-column panel) per
-//     lane, so that sixteen threads issue copies at once; a K slot is free once its scores
-//     are computed, a V slot once its P.V is.
-//   warps 11 and 8 (one lane each issues tcgen05.mma): S_j = Q K_j^T (N = 128 keys) into
-//     tensor-memory buffer j % 3, once K_j has landed and, for j >= 3, P_{j-3} V_{j-3} (which
-//     read that buffer) is done; and O += P_hi V_j + P_lo V_j (N = d) with P_hi and P_lo read
-//     from the same buffer.  Each issuer waits only for its own inputs; with three buffers
-//     the softmax of tile j never waits for a P.V unless it rescales O.
+// A query tile of the launch: tile `it` in the order largest start first (across sequences),
+// then sequence, then head.  False for a tile past its sequence's end or a sequence with
+// inconsistent offsets.
+struct PrefillItem {
+    int b, head, q0, start, len, ntiles;
+};
+
+__device__ __forceinline__ bool prefill_item(const PrefillKParams &p, int it, int nqt, PrefillItem &w) {
+    const int per_tile = p.B * p.Hq;
+    const int z = it / per_tile, rem = it % per_tile;
+    w.b = rem / p.Hq;
+    w.head = rem % p.Hq;
+    w.q0 = (nqt - 1 - z) * 128;
+    if (!seq_range(p, w.b, w.start, w.len, false) || w.q0 >= w.len) return false;
+    w.ntiles = (min(w.q0 + 128, w.len) - 1) / 128 + 1;   // key tiles up to the diagonal
+    return true;
+}
+
+// One CTA per SM; CTA c takes query tiles c, c + G, c + 2G, .. of the launch order (G CTAs),
+// the longest first.  Sixteen warps, each role walking the same tiles:
+//   warps 9 and 10 (TMA): the K and the V tiles into two rings of tile slots, one
+//     {64, 1, 16} box (16 rows of one 64-column panel) per lane, so that sixteen threads
+//     issue copies at once; a K slot is free once its scores are computed, a V slot once its
+//     P.V is.  The rings run on across query tiles, so the next tile's copies start while
+//     the current one is being finished.
+//   warps 11 and 8 (one lane each issues tcgen05.mma): S = Q K_j^T (N = 128 keys) into
+//     tensor-memory buffer g % 3 (g counts key tiles over all query tiles), once K_j has
+//     landed and the P.V three key tiles back (which read that buffer) is done; and
+//     O += P_hi V_j + P_lo V_j (N = d) with P_hi and P_lo read from the same buffer, the
+//     first product of a query tile once the epilogue warps have read the previous O.
+//     The score issuer also brings each Q tile, once the previous query tile's scores
+//     have all been computed (it has nothing else to issue until then).
 //   warps 0-7 (softmax): row r of the query tile is tensor-memory lane r, shared by warps
-//     w and w+4 (w = r / 32); warp half h = w / 4 takes keys 64h .. 64h + 63 of each key tile.
-//     Per tile: read the row of S, apply the causal mask (key <= query) on the diagonal tile,
-//     share the row maximum between the two warps through shared memory, update the running
-//     maximum and sum (online softmax), rescale the O row in tensor memory when the
-//     reference maximum grew by more than 2^8 (exponentials stay <= 256 otherwise, and O and
-//     l share the reference), and write P as bf16 hi and lo parts (P = P_hi + P_lo to about
-//     2^-16 relative) into tensor memory.  At the end: O / l and the log-sum-exp.
+//     w and w+4 (w = r / 32); warp half h = w / 4 takes keys 64h .. 64h + 63 of each key
+//     tile.  Per key tile: read the row of S, apply the causal mask (key <= query) on the
+//     diagonal tile, share the row maximum between the two warps through shared memory,
+//     update the running maximum and sum (online softmax), rescale the O row in tensor
+//     memory when the reference maximum grew by more than 2^8 (exponentials stay <= 256
+//     otherwise, and O and l share the reference), and write P as bf16 hi and lo parts
+//     (P = P_hi + P_lo to about 2^-16 relative) over the scores.  At the end of a query
+//     tile the row's maximum and partial sums go to the epilogue warps, and the softmax
+//     warps go on with the next query tile.
+//   warps 12-15 (epilogue): once a query tile's last P.V is done, thread (w, lane) reads O
+//     row 32 (w % 4) + lane 32 columns at a time, frees O for the next query tile, and
+//     writes O / l (staged in shared memory, so that each store writes whole 128-byte row
+//     segments) and the log-sum-exp.
 // Every wait is bounded and shares an abort flag: on a timeout the block drains its copies
 // and MMAs, frees tensor memory and returns with PKV_DEVERR_TIMEOUT.
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillKParams p) {
     using Cfg = TcPrefillCfg<D>;
-    constexpr int BM = Cfg::kBM, TK = Cfg::kTK, PANELS = Cfg::PANELS, NK = Cfg::NK, NV = Cfg::NV;
+    constexpr int BM = Cfg::kBM, TK = Cfg::kTK, PANELS = Cfg::PANELS, NK = Cfg::NK, NV = Cfg::NV,
+                  NSP = Cfg::NSP;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -121,22 +160,21 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
     float *xch = reinterpret_cast<float *>(smem + Cfg::kOffXch);
+    float *stats = reinterpret_cast<float *>(smem + Cfg::kOffStats);
     auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = blockIdx.x, b = blockIdx.y;
-    int start = 0, len = 0;
-    if (!seq_range(p, b, start, len, threadIdx.x == 0 && blockIdx.z == 0 && i == 0)) return;
     const int nqt = (p.max_seqlen + BM - 1) / BM;
-    // grid z ranks the query tiles by start, largest first, across all sequences: a tile
-    // at q0 has q0 / 128 + 1 key tiles, so the launch order is longest first globally
-    const int q0 = (nqt - 1 - static_cast<int>(blockIdx.z)) * BM;
-    if (q0 >= len) return;
-    const int kvh = i / p.m;
-    const int ntiles = (min(q0 + BM, len) - 1) / TK + 1;   // key tiles up to the diagonal
+    const int n_items = nqt * p.B * p.Hq;
 
     if (threadIdx.x == 0) {
+        if (blockIdx.x == 0)   // inconsistent offsets are reported once; their tiles are skipped
+            for (int b = 0; b < p.B; ++b) {
+                int s0, l0;
+                seq_range(p, b, s0, l0, true);
+            }
         mbar_init(bar(Cfg::kQ), 1);
+        mbar_init(bar(Cfg::kQFree), 1);
         for (int s = 0; s < NK; ++s) {
             mbar_init(bar(Cfg::kKFull + s), 1);
             mbar_init(bar(Cfg::kKFree + s), 1);
@@ -145,12 +183,17 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(bar(Cfg::kVFull + s), 1);
             mbar_init(bar(Cfg::kVFree + s), 1);
         }
-        for (int u = 0; u < Cfg::NSP; ++u) {
+        for (int u = 0; u < NSP; ++u) {
             mbar_init(bar(Cfg::kSFull + u), 1);
             mbar_init(bar(Cfg::kPFull + u), 8);
             mbar_init(bar(Cfg::kPFree + u), 1);
         }
-        mbar_init(bar(Cfg::kDone), 1);
+        mbar_init(bar(Cfg::kODone), 1);
+        mbar_init(bar(Cfg::kOFree), 4);
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(bar(Cfg::kStFull + u), 8);
+            mbar_init(bar(Cfg::kStFree + u), 4);
+        }
         mbar_init(bar(Cfg::kDrain), 1);
         mbar_init(bar(Cfg::kDrain + 1), 1);
         *abort = 0;
@@ -169,94 +212,129 @@ __global__ void __launch_bounds__(384, 1)
     auto sV = [&](int s) { return smem_addr(smem + Cfg::kOffV + s * Cfg::kSlotBytes); };
 
     if (warp == 9 || warp == 10) {
-        // ---- TMA loaders: warp 9 the Q tile and the K tiles, warp 10 the V tiles.  Tile t
-        // (keys t*128 ..) goes to slot t % N once the slot's previous tile is consumed.  Lane
+        // ---- TMA loaders: warp 9 the K tiles, warp 10 the V tiles.  Key tile g (counted over
+        // all query tiles) goes to slot g % N once the slot's previous tile is consumed.  Lane
         // l < 8 * PANELS copies rows 16 (l / PANELS) .. + 15 of panel l % PANELS.
         const bool is_k = warp == 9;
         const int N = is_k ? NK : NV;
         const int full0 = is_k ? Cfg::kKFull : Cfg::kVFull, free0 = is_k ? Cfg::kKFree : Cfg::kVFree;
         const CUtensorMap *map = is_k ? &tm_k : &tm_v;
-        if (is_k && lane == 0) {
-            mbar_arrive_expect_tx(bar(Cfg::kQ), Cfg::kQBytes);
-#pragma unroll
-            for (int pn = 0; pn < PANELS; ++pn)
-                tma_load_3d(sQ + pn * BM * 128, &tm_q, pn * 64, i, start + q0, bar(Cfg::kQ));
-        }
         const int chunk = lane / PANELS, pn = lane % PANELS;
-        int t = 0;
-        for (; t < ntiles; ++t) {
-            bool fr = true;
-            if (lane == 0 && t >= N) fr = wait_or_abort(bar(free0 + t % N), ((t - N) / N) & 1, abort, p.err);
-            if (!__shfl_sync(kFull, fr ? 1 : 0, 0)) break;
-            const int s = t % N;
-            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), Cfg::kSlotBytes);
-            __syncwarp();
-            if (lane < 8 * PANELS) {
-                const uint32_t dst = (is_k ? sK(s) : sV(s)) + pn * TK * 128 + chunk * 16 * 128;
-                tma_load_3d(dst, map, pn * 64, kvh, start + t * TK + chunk * 16, bar(full0 + s));
+        int t = 0;   // key tiles copied
+        bool alive = true;
+        for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x) {
+            PrefillItem w;
+            if (!prefill_item(p, it, nqt, w)) continue;
+            const int kvh = w.head / p.m;
+            for (int j = 0; j < w.ntiles; ++j) {
+                bool fr = true;
+                if (lane == 0 && t >= N) fr = wait_or_abort(bar(free0 + t % N), ((t - N) / N) & 1, abort, p.err);
+                if (!__shfl_sync(kFull, fr ? 1 : 0, 0)) {
+                    alive = false;
+                    break;
+                }
+                const int s = t % N;
+                if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), Cfg::kSlotBytes);
+                __syncwarp();
+                if (lane < 8 * PANELS) {
+                    const uint32_t dst = (is_k ? sK(s) : sV(s)) + pn * TK * 128 + chunk * 16 * 128;
+                    tma_load_3d(dst, map, pn * 64, kvh, w.start + j * TK + chunk * 16, bar(full0 + s));
+                }
+                ++t;
             }
         }
         // before teardown every copy issued must have landed (bounded)
         if (lane == 0) {
-            if (is_k && !mbar_wait_bounded(bar(Cfg::kQ), 0)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
             for (int u = max(0, t - N); u < t; ++u)
                 if (!mbar_wait_bounded(bar(full0 + u % N), (u / N) & 1)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
         }
     } else if (warp == 8 || warp == 11) {
         // ---- MMA issue, one lane each: warp 11 the scores, warp 8 the products with V.
-        // tcgen05.commit covers the committing thread's MMAs: warp 11 signals S full and K
-        // free, warp 8 P consumed, V free and, after the last P.V (which follows every S),
-        // all MMAs done.  Buffer j % 3's barriers complete once per use (tiles j, j + 3, ..),
-        // and no use starts before the previous one is consumed, so each wait's phase is
-        // unambiguous.
+        // tcgen05.commit covers the committing thread's MMAs: warp 11 signals S full, K free
+        // and, after a query tile's last scores, Q free (waited by itself before it copies the
+        // next Q tile); warp 8 P consumed, V free and, after a query tile's last P.V, O done.
+        // Buffer g % 3's barriers complete once per use, no use starts before the previous
+        // one is consumed, and a query tile's barriers complete once per query tile with the
+        // next one waiting for this one's consumer, so each wait's phase is unambiguous.
         if (lane == 0) {
             const bool is_s = warp == 11;
             bool issued = false, alive = true;
+            int g = 0, cnt = 0;   // key tiles and query tiles done
             if (is_s) {
                 const uint32_t idesc_s = umma_idesc_bf16(BM, TK, 0);
-                alive = wait_or_abort(bar(Cfg::kQ), 0, abort, p.err);
-                for (int t = 0; t < ntiles && alive; ++t) {
-                    const int sb = t % Cfg::NSP;
-                    if (t >= Cfg::NSP)
-                        alive = wait_or_abort(bar(Cfg::kPFree + sb), ((t - Cfg::NSP) / Cfg::NSP) & 1, abort, p.err);
-                    alive = alive && wait_or_abort(bar(Cfg::kKFull + t % NK), (t / NK) & 1, abort, p.err);
+                bool q_in_flight = false;
+                for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x) {
+                    PrefillItem w;
+                    if (!prefill_item(p, it, nqt, w)) continue;
+                    // the Q tile, over the previous one once its scores have all been computed
+                    if (cnt > 0) alive = wait_or_abort(bar(Cfg::kQFree), (cnt - 1) & 1, abort, p.err);
                     if (!alive) break;
-                    tc_fence_after_sync();
-                    const int s = t % NK;
+                    mbar_arrive_expect_tx(bar(Cfg::kQ), Cfg::kQBytes);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t ad = umma_desc_sw128(sQ + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
-                        const uint64_t bd = umma_desc_sw128(sK(s) + (kk / 4) * TK * 128 + (kk % 4) * 32, 16, 1024);
-                        umma_bf16(tmem + Cfg::kSCol + sb * TK, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    for (int k = 0; k < PANELS; ++k)
+                        tma_load_3d(sQ + k * BM * 128, &tm_q, k * 64, w.head, w.start + w.q0, bar(Cfg::kQ));
+                    q_in_flight = true;
+                    alive = wait_or_abort(bar(Cfg::kQ), cnt & 1, abort, p.err);
+                    if (!alive) break;
+                    q_in_flight = false;
+                    for (int j = 0; j < w.ntiles && alive; ++j) {
+                        const int sb = g % NSP;
+                        if (g >= NSP) alive = wait_or_abort(bar(Cfg::kPFree + sb), ((g - NSP) / NSP) & 1, abort, p.err);
+                        alive = alive && wait_or_abort(bar(Cfg::kKFull + g % NK), (g / NK) & 1, abort, p.err);
+                        if (!alive) break;
+                        tc_fence_after_sync();
+                        const int s = g % NK;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t ad = umma_desc_sw128(sQ + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024);
+                            const uint64_t bd = umma_desc_sw128(sK(s) + (kk / 4) * TK * 128 + (kk % 4) * 32, 16, 1024);
+                            umma_bf16(tmem + Cfg::kSCol + sb * TK, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(bar(Cfg::kSFull + sb));
+                        umma_commit(bar(Cfg::kKFree + s));
+                        issued = true;
+                        ++g;
                     }
-                    umma_commit(bar(Cfg::kSFull + sb));
-                    umma_commit(bar(Cfg::kKFree + s));
-                    issued = true;
+                    if (!alive) break;
+                    umma_commit(bar(Cfg::kQFree));
+                    ++cnt;
                 }
+                // a Q copy whose wait gave up must still land before teardown (bounded)
+                if (q_in_flight && !mbar_wait_bounded(bar(Cfg::kQ), cnt & 1)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
             } else {
                 const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
-                for (int j = 0; j < ntiles && alive; ++j) {
-                    const int sb = j % Cfg::NSP;
-                    alive = wait_or_abort(bar(Cfg::kPFull + sb), (j / Cfg::NSP) & 1, abort, p.err) &&
-                            wait_or_abort(bar(Cfg::kVFull + j % NV), (j / NV) & 1, abort, p.err);
+                for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x) {
+                    PrefillItem w;
+                    if (!prefill_item(p, it, nqt, w)) continue;
+                    for (int j = 0; j < w.ntiles && alive; ++j) {
+                        const int sb = g % NSP;
+                        alive = wait_or_abort(bar(Cfg::kPFull + sb), (g / NSP) & 1, abort, p.err) &&
+                                wait_or_abort(bar(Cfg::kVFull + g % NV), (g / NV) & 1, abort, p.err);
+                        // the first product of a query tile overwrites O: the previous one read
+                        if (alive && j == 0 && cnt > 0)
+                            alive = wait_or_abort(bar(Cfg::kOFree), (cnt - 1) & 1, abort, p.err);
+                        if (!alive) break;
+                        tc_fence_after_sync();
+                        const int s = g % NV;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+#pragma unroll
+                            for (int kk = 0; kk < TK / 16; ++kk) {
+                                // keys 16 kk .. 16 kk + 15: P_hi (half 0) or P_lo of the keys' 64-key half
+                                const uint32_t pcol = Cfg::kSCol + sb * TK + (kk / 4) * 64 + half * 32 + (kk % 4) * 8;
+                                const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
+                                umma_bf16_ts(tmem + Cfg::kOCol, tmem + pcol, bd, idesc_o,
+                                             (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        umma_commit(bar(Cfg::kPFree + sb));
+                        umma_commit(bar(Cfg::kVFree + s));
+                        issued = true;
+                        ++g;
+                    }
                     if (!alive) break;
-                    tc_fence_after_sync();
-                    const int s = j % NV;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half)
-#pragma unroll
-                        for (int kk = 0; kk < TK / 16; ++kk) {
-                            // keys 16 kk .. 16 kk + 15: P_hi (half 0) or P_lo of the keys' 64-key half
-                            const uint32_t pcol = Cfg::kSCol + sb * TK + (kk / 4) * 64 + half * 32 + (kk % 4) * 8;
-                            const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
-                            umma_bf16_ts(tmem + Cfg::kOCol, tmem + pcol, bd, idesc_o,
-                                         (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
-                        }
-                    umma_commit(bar(Cfg::kPFree + sb));
-                    umma_commit(bar(Cfg::kVFree + s));
-                    issued = true;
+                    umma_commit(bar(Cfg::kODone));
+                    ++cnt;
                 }
-                if (alive) umma_commit(bar(Cfg::kDone));
             }
             if (*abort && issued) {
                 // let this thread's MMAs finish (bounded) before teardown
@@ -265,83 +343,94 @@ __global__ void __launch_bounds__(384, 1)
                 if (!mbar_wait_bounded(bar(drain), 0)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
             }
         }
-    } else {
+    } else if (warp < 8) {
         // ---- softmax: thread (w, lane) owns query row r = 32 (w % 4) + lane (tensor-memory
         // lane r) and keys 64h .. 64h + 63 of each key tile (h = w / 4)
         const int h = warp >> 2;
         const int r = ((warp & 3) << 5) | lane;
-        const int qpos = q0 + r;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4
         auto xs = [&](int buf, int kind, int hh) { return xch + ((buf * 2 + kind) * 2 + hh) * BM + r; };
-        float m_ref = -INFINITY, l = 0.f;
-        // ok is warp-uniform, and after each tile's exchange the same in both warps of a
-        // row: a failed wait skips the remaining work but never a named barrier
+        // ok is warp-uniform, and after each key tile's exchange the same in both warps of a
+        // row: a failed wait skips the remaining work but never a named barrier (the warps
+        // walk every key tile of every query tile either way)
         bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
-            const int sb = j & 1;              // exchange buffer
-            const int pb = j % Cfg::NSP;       // S / P buffer
-            const uint32_t scol = lane_base + Cfg::kSCol + pb * TK + h * 64;
-            if (ok)
-                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kSFull + pb), (j / Cfg::NSP) & 1, abort, p.err));
-            float sc[64];
-            if (ok) {
-                tc_fence_after_sync();
-                uint32_t s0[32], s1[32];
-                tmem_ld32(scol, s0);
-                tmem_ld32(scol + 32, s1);
-                tmem_ld_wait();
+        int g = 0, cnt = 0;
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+            PrefillItem w;
+            if (!prefill_item(p, it, nqt, w)) continue;
+            const int qpos = w.q0 + r;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < w.ntiles; ++j, ++g) {
+                const int sb = g & 1;              // exchange buffer
+                const int pb = g % NSP;            // S / P buffer
+                const uint32_t scol = lane_base + Cfg::kSCol + pb * TK + h * 64;
+                if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kSFull + pb), (g / NSP) & 1, abort, p.err));
+                float sc[64];
+                if (ok) {
+                    tc_fence_after_sync();
+                    uint32_t s0[32], s1[32];
+                    tmem_ld32(scol, s0);
+                    tmem_ld32(scol + 32, s1);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    sc[c] = __uint_as_float(s0[c]);
-                    sc[32 + c] = __uint_as_float(s1[c]);
+                    for (int c = 0; c < 32; ++c) {
+                        sc[c] = __uint_as_float(s0[c]);
+                        sc[32 + c] = __uint_as_float(s1[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) sc[c] = -INFINITY;
                 }
-            } else {
+                // causal mask on the diagonal tile: key <= query
+                const int key0 = j * TK + h * 64;
+                if (key0 + 63 > w.q0) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) sc[c] = -INFINITY;
-            }
-            // causal mask on the diagonal tile: key <= query
-            const int key0 = j * TK + h * 64;
-            if (key0 + 63 > q0) {
+                    for (int c = 0; c < 64; ++c)
+                        if (key0 + c > qpos) sc[c] = -INFINITY;
+                }
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (key0 + c > qpos) sc[c] = -INFINITY;
-            }
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
-            float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            // the other half's maximum of this row, and whether it is still ok; the exchange
-            // buffer alternates with the tile, so one barrier a tile suffices
-            *xs(sb, 0, h) = mx;
-            *xs(sb, 1, h) = ok ? 1.f : 0.f;
-            named_barrier(pair_bar, 64);
-            mx = fmaxf(mx, *xs(sb, 0, 1 - h)) * p.scale_log2;
-            ok = ok && *xs(sb, 1, 1 - h) != 0.f;
-            if (!ok) continue;
-            // key 0 is always visible, so the row maximum is finite from the first tile on
-            const float m_new = mx > m_ref + 8.f ? mx : m_ref;
-            const float alpha = ex2_approx(m_ref - m_new);
-            m_ref = m_new;
-            const float neg_m = -m_ref;
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                sc[c] = ex2_approx(fmaf(sc[c], p.scale_log2, neg_m));
-                l4[c & 3] += sc[c];
-            }
-            l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-            uint32_t phi[32], plo[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) split_bf16x2(sc[2 * e], sc[2 * e + 1], phi[e], plo[e]);
-            // a rescale of O waits for P_{j-1} V_{j-1} (and so every earlier P.V): O is then
-            // current, and P_j V_j has not started, as it waits for this tile's P
-            if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
-                const int qb = (j - 1) % Cfg::NSP;
-                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kPFree + qb), ((j - 1) / Cfg::NSP) & 1, abort, p.err));
+                for (int c = 0; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
+                float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                // the other half's maximum of this row, and whether it is still ok; the
+                // exchange buffer alternates with the key tile, so one barrier a tile suffices
+                *xs(sb, 0, h) = mx;
+                *xs(sb, 1, h) = ok ? 1.f : 0.f;
+                named_barrier(pair_bar, 64);
+                mx = fmaxf(mx, *xs(sb, 0, 1 - h)) * p.scale_log2;
+                ok = ok && *xs(sb, 1, 1 - h) != 0.f;
                 if (!ok) continue;
-                tc_fence_after_sync();
-                {
+                // key 0 is always visible, so the row maximum is finite from the first tile on
+                const float m_new = mx > m_ref + 8.f ? mx : m_ref;
+                const float alpha = ex2_approx(m_ref - m_new);
+                m_ref = m_new;
+                const float neg_m = -m_ref;
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    sc[c] = ex2_approx(fmaf(sc[c], p.scale_log2, neg_m));
+                    l4[c & 3] += sc[c];
+                }
+                l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+                // the weights over this thread's own scores (already in registers), 32 keys at a
+                // time: P_hi of keys 2e, 2e + 1 in column e, P_lo in column 32 + e
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t phi[16], plo[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        split_bf16x2(sc[32 * q + 2 * e], sc[32 * q + 2 * e + 1], phi[e], plo[e]);
+                    tmem_st16(scol + 16 * q, phi);
+                    tmem_st16(scol + 32 + 16 * q, plo);
+                }
+                // a rescale of O waits for the previous P.V of this query tile (and so every
+                // earlier one): O is then current, and this tile's P.V waits for its P
+                if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
+                    const int qb = (g - 1) % NSP;
+                    ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kPFree + qb), ((g - 1) / NSP) & 1, abort, p.err));
+                    if (!ok) continue;
+                    tc_fence_after_sync();
                     // this half rescales columns D/2 h .. D/2 h + D/2 - 1 of its rows
 #pragma unroll
                     for (int cc = 0; cc < D / 64; ++cc) {
@@ -353,56 +442,71 @@ __global__ void __launch_bounds__(384, 1)
                         tmem_st32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
                     }
                 }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(Cfg::kPFull + pb));
             }
-            // the weights over this thread's own scores (already in registers)
-            tmem_st32(scol, phi);
-            tmem_st32(scol + 32, plo);
-            tmem_st_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Cfg::kPFull + pb));
+            // the row's maximum and this half's sum for the epilogue warps (the buffer was
+            // read by them two query tiles ago)
+            const int sbuf = cnt & 1;
+            if (ok && cnt >= 2)
+                ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kStFree + sbuf), ((cnt - 2) >> 1) & 1, abort, p.err));
+            if (ok) {
+                if (h == 0) stats[(sbuf * 3) * BM + r] = m_ref;
+                stats[(sbuf * 3 + 1 + h) * BM + r] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(Cfg::kStFull + sbuf));
+            }
+            ++cnt;
         }
-        if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kDone), 0, abort, p.err));
-
-        // ---- the row's sum over its two threads, through the exchange buffer the last tile
-        // did not use; O / l and the log-sum-exp
-        const int fb = ntiles & 1;
-        *xs(fb, 0, h) = l;
-        named_barrier(pair_bar, 64);
-        const float lr = l + *xs(fb, 0, 1 - h);
-        if (ok) {
+    } else {
+        // ---- epilogue: thread (w, lane) writes query row r = 32 (w % 4) + lane
+        const int r = ((warp & 3) << 5) | lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        float *stage = reinterpret_cast<float *>(smem + Cfg::kOffStage) + (warp & 3) * 32 * Cfg::kPitch;
+        bool ok = true;
+        int cnt = 0;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            PrefillItem w;
+            if (!prefill_item(p, it, nqt, w)) continue;
+            const int sbuf = cnt & 1;
+            ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kStFull + sbuf), (cnt >> 1) & 1, abort, p.err)) &&
+                 __all_sync(kFull, wait_or_abort(bar(Cfg::kODone), cnt & 1, abort, p.err));
+            if (!ok) break;
             tc_fence_after_sync();
+            const float m = stats[(sbuf * 3) * BM + r];
+            const float lr = stats[(sbuf * 3 + 1) * BM + r] + stats[(sbuf * 3 + 2) * BM + r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Cfg::kStFree + sbuf));
             const float inv_l = 1.f / lr;
-            // O / l of the warp's 32 rows x D/2 columns, staged in the K ring (every MMA has
-            // completed, so it is free) so that each store writes whole row segments rather
-            // than one 16-byte piece of 32 rows; the pitch spreads the rows over the banks
-            constexpr int HW = D / 2, PITCH = HW + 4;
-            float *stage = reinterpret_cast<float *>(smem + Cfg::kOffK) + warp * 32 * PITCH;
-            fence_proxy_async_smem();
+            const int wrow0 = w.q0 + ((warp & 3) << 5);
+            const int nrows = min(32, w.len - wrow0);   // rows of the warp inside the sequence
 #pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
-                tmem_ld32(lane_base + Cfg::kOCol + h * HW + cc * 32, ov);
+                tmem_ld32(lane_base + Cfg::kOCol + c * 32, ov);
                 tmem_ld_wait();
+                if (c == D / 32 - 1) {
+                    // O has been read: the next query tile's first P.V may overwrite it
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(Cfg::kOFree));
+                }
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4 *>(stage + lane * PITCH + cc * 32 + e) =
+                    *reinterpret_cast<float4 *>(stage + lane * Cfg::kPitch + e) =
                         make_float4(__uint_as_float(ov[e]) * inv_l, __uint_as_float(ov[e + 1]) * inv_l,
                                     __uint_as_float(ov[e + 2]) * inv_l, __uint_as_float(ov[e + 3]) * inv_l);
+                __syncwarp();
+                for (int rr = 0; rr < nrows; ++rr)
+                    p.out[(static_cast<size_t>(w.start + wrow0 + rr) * p.Hq + w.head) * D + c * 32 + lane] =
+                        stage[rr * Cfg::kPitch + lane];
+                __syncwarp();
             }
-            __syncwarp();
-            const int row0 = q0 + ((warp & 3) << 5);
-            const int nrows = min(32, len - row0);   // rows of the warp inside the sequence
-            for (int rr = 0; rr < nrows; ++rr) {
-                float *dst = p.out + (static_cast<size_t>(start + row0 + rr) * p.Hq + i) * D + h * HW;
-                if constexpr (HW == 64)
-                    *reinterpret_cast<float2 *>(dst + 2 * lane) =
-                        *reinterpret_cast<const float2 *>(stage + rr * PITCH + 2 * lane);
-                else
-                    dst[lane] = stage[rr * PITCH + lane];
-            }
-            if (qpos < len && h == 0 && p.lse != nullptr)
-                p.lse[static_cast<size_t>(start + qpos) * p.Hq + i] = (m_ref + log2f(lr)) * kLn2;
+            if (w.q0 + r < w.len && p.lse != nullptr)
+                p.lse[static_cast<size_t>(w.start + w.q0 + r) * p.Hq + w.head] = (m + log2f(lr)) * kLn2;
+            ++cnt;
         }
     }
     tc_fence_before_sync();
@@ -493,7 +597,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, const PrefillKParams &kp, cu
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const dim3 grid(a.Hq, a.B, (a.max_seqlen + Cfg::kBM - 1) / Cfg::kBM);
+    // one CTA per SM (at most one per query tile)
+    const long long n_items = static_cast<long long>((a.max_seqlen + Cfg::kBM - 1) / Cfg::kBM) * a.B * a.Hq;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(min(static_cast<long long>(sms), n_items));
     kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, kp);
     return cudaGetLastError();
 }
@@ -548,11 +658,11 @@ cudaError_t launch_prefill(const PrefillArgs &a, pkv_dtype dt, cudaStream_t stre
     kp.Hkv = a.Hkv;
     kp.m = a.Hq / a.Hkv;
     kp.scale_log2 = a.scale * kLog2e;
-    // the tcgen05 grid's z counts 128-query tiles (at most 65535 of them)
+    // the tcgen05 kernel numbers the query tiles of the launch with an int
     // the tcgen05 kernel writes out in 8-byte pieces
     if (prefill_tensor_core_ok(dt, a.d, a.q, a.k, a.v, a.T, a.Hq, a.Hkv) &&
         reinterpret_cast<uintptr_t>(a.out) % 8 == 0 &&
-        static_cast<long long>(a.max_seqlen) <= 65535ll * 128)
+        static_cast<long long>((a.max_seqlen + 127) / 128) * a.B * a.Hq < (1ll << 31))
         return a.d == 64 ? launch_prefill_tc<64>(a, kp, stream) : launch_prefill_tc<128>(a, kp, stream);
     return dt == PKV_F32 ? launch_prefill_simt<float>(a, kp, stream)
                          : launch_prefill_simt<__nv_bfloat16>(a, kp, stream);
