@@ -97,26 +97,76 @@ struct TcPrefillCfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// A query tile of the launch: tile `it` in the order largest start first (across sequences),
-// then sequence, then head.  False for a tile past its sequence's end or a sequence with
-// inconsistent offsets.
+// A query tile: 128 query rows of one head of one sequence.
 struct PrefillItem {
     int b, head, q0, start, len, ntiles;
 };
 
-__device__ __forceinline__ bool prefill_item(const PrefillKParams &p, int it, int nqt, PrefillItem &w) {
-    const int per_tile = p.B * p.Hq;
-    const int z = it / per_tile, rem = it % per_tile;
-    w.b = rem / p.Hq;
-    w.head = rem % p.Hq;
-    w.q0 = (nqt - 1 - z) * 128;
-    if (!seq_range(p, w.b, w.start, w.len, false) || w.q0 >= w.len) return false;
-    w.ntiles = (min(w.q0 + 128, w.len) - 1) / 128 + 1;   // key tiles up to the diagonal
-    return true;
-}
+// The query tiles of the launch, in the order largest start first, then sequence, then
+// head (tiles past a sequence's end, and sequences with inconsistent offsets, are not in
+// it).  CTA c of G takes tile k = r G + c of round r when r is even and k = r G + G - 1 - c
+// when r is odd ("snake" order), so that every CTA gets a similar share of long and short
+// tiles.  Each role of a CTA walks the same tiles with its own walker; the walk only moves
+// forward, so finding a tile's band (its start) is amortised over the walk.
+struct PrefillWalk {
+    const PrefillKParams *p;
+    int nqt, total;        // 128-row bands of starts; query tiles of the launch
+    int r = 0;             // next round
+    int z = 0, base = 0;   // band z (start (nqt - 1 - z) 128) holds tiles base .. base + band - 1
+    int band = 0;
 
-// One CTA per SM; CTA c takes query tiles c, c + G, c + 2G, .. of the launch order (G CTAs),
-// the longest first.  Sixteen warps, each role walking the same tiles:
+    __device__ __forceinline__ int len_of(int b) const {
+        int s0, l0;
+        return seq_range(*p, b, s0, l0, false) ? l0 : 0;
+    }
+    __device__ __forceinline__ int band_size(int zz) const {
+        const int q0 = (nqt - 1 - zz) * 128;
+        int n = 0;
+        for (int b = 0; b < p->B; ++b) n += len_of(b) > q0 ? 1 : 0;
+        return n * p->Hq;
+    }
+    __device__ __forceinline__ void init(const PrefillKParams &pp) {
+        p = &pp;
+        nqt = (pp.max_seqlen + 127) / 128;
+        total = 0;   // a sequence longer than max_seqlen (flagged) has only nqt tiles
+        for (int b = 0; b < pp.B; ++b) total += min((len_of(b) + 127) / 128, nqt) * pp.Hq;
+        band = band_size(0);
+    }
+    // the CTA's next query tile; false when it has none left
+    __device__ __forceinline__ bool next(PrefillItem &w) {
+        const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+        const int k = r * G + ((r & 1) ? G - 1 - c : c);
+        ++r;
+        if (k >= total) return false;
+        while (k >= base + band) {
+            base += band;
+            ++z;
+            band = band_size(z);
+        }
+        const int idx = k - base, rank = idx / p->Hq;
+        w.b = 0;
+        w.start = 0;
+        w.len = 0;
+        w.head = idx % p->Hq;
+        w.q0 = (nqt - 1 - z) * 128;
+        int seen = 0;
+        for (int b = 0; b < p->B; ++b) {
+            int s0, l0;
+            if (!seq_range(*p, b, s0, l0, false) || l0 <= w.q0) continue;
+            if (seen++ == rank) {
+                w.b = b;
+                w.start = s0;
+                w.len = l0;
+                break;
+            }
+        }
+        w.ntiles = w.len > w.q0 ? (min(w.q0 + 128, w.len) - 1) / 128 + 1 : 0;   // key tiles up to the diagonal
+        return true;
+    }
+};
+
+// One CTA per SM, taking the query tiles of the launch in snake order (PrefillWalk), the
+// longest first.  Sixteen warps, each role walking the same tiles:
 //   warps 9 and 10 (TMA): the K and the V tiles into two rings of tile slots, one
 //     {64, 1, 16} box (16 rows of one 64-column panel) per lane, so that sixteen threads
 //     issue copies at once; a K slot is free once its scores are computed, a V slot once its
@@ -164,8 +214,8 @@ __global__ void __launch_bounds__(512, 1)
     auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nqt = (p.max_seqlen + BM - 1) / BM;
-    const int n_items = nqt * p.B * p.Hq;
+    PrefillWalk walk;
+    walk.init(p);
 
     if (threadIdx.x == 0) {
         if (blockIdx.x == 0)   // inconsistent offsets are reported once; their tiles are skipped
@@ -222,9 +272,8 @@ __global__ void __launch_bounds__(512, 1)
         const int chunk = lane / PANELS, pn = lane % PANELS;
         int t = 0;   // key tiles copied
         bool alive = true;
-        for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x) {
-            PrefillItem w;
-            if (!prefill_item(p, it, nqt, w)) continue;
+        PrefillItem w;
+        while (alive && walk.next(w)) {
             const int kvh = w.head / p.m;
             for (int j = 0; j < w.ntiles; ++j) {
                 bool fr = true;
@@ -263,9 +312,8 @@ __global__ void __launch_bounds__(512, 1)
             if (is_s) {
                 const uint32_t idesc_s = umma_idesc_bf16(BM, TK, 0);
                 bool q_in_flight = false;
-                for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x) {
-                    PrefillItem w;
-                    if (!prefill_item(p, it, nqt, w)) continue;
+                PrefillItem w;
+                while (alive && walk.next(w)) {
                     // the Q tile, over the previous one once its scores have all been computed
                     if (cnt > 0) alive = wait_or_abort(bar(Cfg::kQFree), (cnt - 1) & 1, abort, p.err);
                     if (!alive) break;
@@ -303,9 +351,8 @@ __global__ void __launch_bounds__(512, 1)
                 if (q_in_flight && !mbar_wait_bounded(bar(Cfg::kQ), cnt & 1)) raise_error(p.err, PKV_DEVERR_TIMEOUT);
             } else {
                 const uint32_t idesc_o = umma_idesc_bf16(BM, D, 1);
-                for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x) {
-                    PrefillItem w;
-                    if (!prefill_item(p, it, nqt, w)) continue;
+                PrefillItem w;
+                while (alive && walk.next(w)) {
                     for (int j = 0; j < w.ntiles && alive; ++j) {
                         const int sb = g % NSP;
                         alive = wait_or_abort(bar(Cfg::kPFull + sb), (g / NSP) & 1, abort, p.err) &&
@@ -356,9 +403,8 @@ __global__ void __launch_bounds__(512, 1)
         // walk every key tile of every query tile either way)
         bool ok = true;
         int g = 0, cnt = 0;
-        for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-            PrefillItem w;
-            if (!prefill_item(p, it, nqt, w)) continue;
+        PrefillItem w;
+        while (walk.next(w)) {
             const int qpos = w.q0 + r;
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < w.ntiles; ++j, ++g) {
@@ -467,9 +513,8 @@ __global__ void __launch_bounds__(512, 1)
         float *stage = reinterpret_cast<float *>(smem + Cfg::kOffStage) + (warp & 3) * 32 * Cfg::kPitch;
         bool ok = true;
         int cnt = 0;
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-            PrefillItem w;
-            if (!prefill_item(p, it, nqt, w)) continue;
+        PrefillItem w;
+        while (ok && walk.next(w)) {
             const int sbuf = cnt & 1;
             ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kStFull + sbuf), (cnt >> 1) & 1, abort, p.err)) &&
                  __all_sync(kFull, wait_or_abort(bar(Cfg::kODone), cnt & 1, abort, p.err));
@@ -499,9 +544,15 @@ __global__ void __launch_bounds__(512, 1)
                         make_float4(__uint_as_float(ov[e]) * inv_l, __uint_as_float(ov[e + 1]) * inv_l,
                                     __uint_as_float(ov[e + 2]) * inv_l, __uint_as_float(ov[e + 3]) * inv_l);
                 __syncwarp();
-                for (int rr = 0; rr < nrows; ++rr)
-                    p.out[(static_cast<size_t>(w.start + wrow0 + rr) * p.Hq + w.head) * D + c * 32 + lane] =
-                        stage[rr * Cfg::kPitch + lane];
+                // four rows a store: lane l writes columns 4 (l % 8) .. + 3 of row 4 i + l / 8
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = 4 * i + (lane >> 3);
+                    if (rr < nrows)
+                        *reinterpret_cast<float4 *>(p.out + (static_cast<size_t>(w.start + wrow0 + rr) * p.Hq + w.head) * D +
+                                                    c * 32 + (lane & 7) * 4) =
+                            *reinterpret_cast<const float4 *>(stage + rr * Cfg::kPitch + (lane & 7) * 4);
+                }
                 __syncwarp();
             }
             if (w.q0 + r < w.len && p.lse != nullptr)
