@@ -295,14 +295,14 @@ __global__ void __launch_bounds__(128, 4)
             for (int e = 0; e < 2; ++e) {
                 const int tok = nt * 8 + 2 * t4 + e;
                 const bool vis = tok >= first && tok < valid;
-                sc[nt][e] = vis ? (s[nt][e] + s[nt][2 + e]) * ksc[tok] * p.scale_log2 : -INFINITY;
+                sc[nt][e] = vis ? (s[nt][e] + s[nt][2 + e]) * (ksc[tok] * p.scale_log2) : -INFINITY;
                 mx = fmaxf(mx, sc[nt][e]);
             }
         }
         mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 2));
         const float m_new = fmaxf(m_run, mx);   // finite: every block holds a visible key
-        const float alpha = exp2f(m_run - m_new);
+        const float alpha = ex2_approx(m_run - m_new);
         float psum = 0.f;
         float pv[NT][2];
 #pragma unroll
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(128, 4)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int tok = nt * 8 + 2 * t4 + e;
-                const float w = exp2f(sc[nt][e] - m_new);
+                const float w = ex2_approx(sc[nt][e] - m_new);
                 psum += w;
                 pv[nt][e] = tok >= first && tok < valid ? w * vsc[tok] : 0.f;
             }
