@@ -69,12 +69,9 @@ struct TcPrefillCfg {
     static constexpr int kPitch = 36;
     static constexpr int kOffStage = kOffV + NV * kSlotBytes;
     // row statistics handed to the epilogue warps, double-buffered by query tile:
-    // [buffer][m, l of half 0, l of half 1][128 rows] floats
+    // [buffer][m, l][128 rows] floats
     static constexpr int kOffStats = kOffStage + 4 * 32 * kPitch * 4;
-    // row-maximum exchange of the two softmax warps of a row, double-buffered by key tile:
-    // [buffer][value, ok][half][128 rows] floats
-    static constexpr int kOffXch = kOffStats + 2 * 3 * kBM * 4;
-    static constexpr int kOffBar = kOffXch + 2 * 2 * 2 * kBM * 4;
+    static constexpr int kOffBar = kOffStats + 2 * 2 * kBM * 4;
     // barriers: Q loaded, Q free (a query tile's scores all computed); K full / free per
     // slot; V full / free per slot; per S/P buffer: S full, P full, P consumed (its P.V
     // done); O done (a query tile's last P.V), O free (read by the epilogue warps); per
@@ -87,9 +84,8 @@ struct TcPrefillCfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // TMEM slot, abort flag
     static constexpr int kSmemBytes = 1024 + kOffMisc + 16;
     // tensor memory: NSP S buffers of 128 columns, then O.  The weights of a key tile
-    // overwrite its scores: the thread that read S columns 64h .. 64h + 63 of a row writes
-    // P_hi of those keys to columns 64h .. 64h + 31 of the buffer and P_lo to 64h + 32 ..
-    // 64h + 63.
+    // overwrite its scores: P_hi of keys 2e, 2e + 1 (one bf16 pair) in column e of the
+    // buffer, P_lo in column 64 + e.
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 0, kOCol = NSP * kTK;
     static constexpr int kThreads = 512;
@@ -179,16 +175,18 @@ struct PrefillWalk {
 //     first product of a query tile once the epilogue warps have read the previous O.
 //     The score issuer also brings each Q tile, once the previous query tile's scores
 //     have all been computed (it has nothing else to issue until then).
-//   warps 0-7 (softmax): row r of the query tile is tensor-memory lane r, shared by warps
-//     w and w+4 (w = r / 32); warp half h = w / 4 takes keys 64h .. 64h + 63 of each key
-//     tile.  Per key tile: read the row of S, apply the causal mask (key <= query) on the
-//     diagonal tile, share the row maximum between the two warps through shared memory,
-//     update the running maximum and sum (online softmax), rescale the O row in tensor
-//     memory when the reference maximum grew by more than 2^8 (exponentials stay <= 256
-//     otherwise, and O and l share the reference), and write P as bf16 hi and lo parts
-//     (P = P_hi + P_lo to about 2^-16 relative) over the scores.  At the end of a query
-//     tile the row's maximum and partial sums go to the epilogue warps, and the softmax
-//     warps go on with the next query tile.
+//   warps 0-7 (softmax): row r of the query tile is tensor-memory lane r; warp w reads
+//     lanes 32 (w % 4) + 16 (w / 4) .. + 15 with the 16-lane shapes, thread t taking rows
+//     t / 4 and t / 4 + 8 of them and, of each key tile, the key pairs 4k + t % 4 (keys
+//     8k + 2 (t % 4), + 1; k = 0 .. 15): the four threads of a row are lanes of one warp and
+//     share its maximum and sum by shuffles, and the eight warps run independently.  Per
+//     key tile: read the rows of S, apply the causal mask (key <= query) on the diagonal
+//     tile, update the running maximum and sum (online softmax), rescale the O rows in
+//     tensor memory when the reference maximum grew by more than 2^8 (exponentials stay
+//     <= 256 otherwise, and O and l share the reference), and write P as bf16 hi and lo
+//     parts (P = P_hi + P_lo to about 2^-16 relative) over the scores.  At the end of a
+//     query tile the rows' maxima and sums go to the epilogue warps, and the softmax warps
+//     go on with the next query tile.
 //   warps 12-15 (epilogue): once a query tile's last P.V is done, thread (w, lane) reads O
 //     row 32 (w % 4) + lane 32 columns at a time, frees O for the next query tile, and
 //     writes O / l (staged in shared memory, so that each store writes whole 128-byte row
@@ -209,7 +207,6 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
-    float *xch = reinterpret_cast<float *>(smem + Cfg::kOffXch);
     float *stats = reinterpret_cast<float *>(smem + Cfg::kOffStats);
     auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
@@ -367,8 +364,8 @@ __global__ void __launch_bounds__(512, 1)
                         for (int half = 0; half < 2; ++half)
 #pragma unroll
                             for (int kk = 0; kk < TK / 16; ++kk) {
-                                // keys 16 kk .. 16 kk + 15: P_hi (half 0) or P_lo of the keys' 64-key half
-                                const uint32_t pcol = Cfg::kSCol + sb * TK + (kk / 4) * 64 + half * 32 + (kk % 4) * 8;
+                                // keys 16 kk .. 16 kk + 15: the pairs 8 kk .. 8 kk + 7 of P_hi (half 0) or P_lo
+                                const uint32_t pcol = Cfg::kSCol + sb * TK + half * 64 + kk * 8;
                                 const uint64_t bd = umma_desc_sw128(sV(s) + kk * 16 * 128, TK * 128, 1024);
                                 umma_bf16_ts(tmem + Cfg::kOCol, tmem + pcol, bd, idesc_o,
                                              (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
@@ -391,101 +388,114 @@ __global__ void __launch_bounds__(512, 1)
             }
         }
     } else if (warp < 8) {
-        // ---- softmax: thread (w, lane) owns query row r = 32 (w % 4) + lane (tensor-memory
-        // lane r) and keys 64h .. 64h + 63 of each key tile (h = w / 4)
-        const int h = warp >> 2;
-        const int r = ((warp & 3) << 5) | lane;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4
-        auto xs = [&](int buf, int kind, int hh) { return xch + ((buf * 2 + kind) * 2 + hh) * BM + r; };
-        // ok is warp-uniform, and after each key tile's exchange the same in both warps of a
-        // row: a failed wait skips the remaining work but never a named barrier (the warps
-        // walk every key tile of every query tile either way)
+        // ---- softmax: thread (w, t) owns rows ra = 32 (w % 4) + 16 (w / 4) + t / 4 and rb =
+        // ra + 8 of the query tile, and of each key tile the key pairs 4k + c4 (c4 = t % 4)
+        const int c4 = lane & 3;
+        const int ra = 32 * (warp & 3) + 16 * (warp >> 2) + (lane >> 2), rb = ra + 8;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3) + 16 * (warp >> 2)) << 16);
+        const uint32_t ocol = lane_base + Cfg::kOCol;
+        // ok is warp-uniform; a failed wait skips the remaining work of this warp
         bool ok = true;
         int g = 0, cnt = 0;
         PrefillItem w;
         while (walk.next(w)) {
-            const int qpos = w.q0 + r;
-            float m_ref = -INFINITY, l = 0.f;
+            const int qa = w.q0 + ra, qb = w.q0 + rb;   // the rows' positions
+            float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
             for (int j = 0; j < w.ntiles; ++j, ++g) {
-                const int sb = g & 1;              // exchange buffer
                 const int pb = g % NSP;            // S / P buffer
-                const uint32_t scol = lane_base + Cfg::kSCol + pb * TK + h * 64;
+                const uint32_t scol = lane_base + Cfg::kSCol + pb * TK;
                 if (ok) ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kSFull + pb), (g / NSP) & 1, abort, p.err));
+                if (!ok) continue;
+                tc_fence_after_sync();
+                // sc[4k + e]: row a, key 8k + 2 c4 + e; sc[4k + 2 + e]: row b, the same key
                 float sc[64];
-                if (ok) {
-                    tc_fence_after_sync();
+                {
                     uint32_t s0[32], s1[32];
-                    tmem_ld32(scol, s0);
-                    tmem_ld32(scol + 32, s1);
+                    tmem_ld_16x256b_x8(scol, s0);
+                    tmem_ld_16x256b_x8(scol + 64, s1);
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         sc[c] = __uint_as_float(s0[c]);
                         sc[32 + c] = __uint_as_float(s1[c]);
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) sc[c] = -INFINITY;
                 }
                 // causal mask on the diagonal tile: key <= query
-                const int key0 = j * TK + h * 64;
-                if (key0 + 63 > w.q0) {
+                const int key0 = j * TK + 2 * c4;
+                if (j * TK + TK - 1 > w.q0) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (key0 + c > qpos) sc[c] = -INFINITY;
+                    for (int k = 0; k < 16; ++k)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            if (key0 + 8 * k + e > qa) sc[4 * k + e] = -INFINITY;
+                            if (key0 + 8 * k + e > qb) sc[4 * k + 2 + e] = -INFINITY;
+                        }
                 }
-                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // the rows' maxima over the four threads of each row
+                float xa0 = -INFINITY, xa1 = -INFINITY, xb0 = -INFINITY, xb1 = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
-                float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                // the other half's maximum of this row, and whether it is still ok; the
-                // exchange buffer alternates with the key tile, so one barrier a tile suffices
-                *xs(sb, 0, h) = mx;
-                *xs(sb, 1, h) = ok ? 1.f : 0.f;
-                named_barrier(pair_bar, 64);
-                mx = fmaxf(mx, *xs(sb, 0, 1 - h)) * p.scale_log2;
-                ok = ok && *xs(sb, 1, 1 - h) != 0.f;
-                if (!ok) continue;
-                // key 0 is always visible, so the row maximum is finite from the first tile on
-                const float m_new = mx > m_ref + 8.f ? mx : m_ref;
-                const float alpha = ex2_approx(m_ref - m_new);
-                m_ref = m_new;
-                const float neg_m = -m_ref;
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    sc[c] = ex2_approx(fmaf(sc[c], p.scale_log2, neg_m));
-                    l4[c & 3] += sc[c];
+                for (int k = 0; k < 16; ++k) {
+                    xa0 = fmaxf(xa0, sc[4 * k]);
+                    xa1 = fmaxf(xa1, sc[4 * k + 1]);
+                    xb0 = fmaxf(xb0, sc[4 * k + 2]);
+                    xb1 = fmaxf(xb1, sc[4 * k + 3]);
                 }
-                l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-                // the weights over this thread's own scores (already in registers), 32 keys at a
-                // time: P_hi of keys 2e, 2e + 1 in column e, P_lo in column 32 + e
+                float mxa = fmaxf(xa0, xa1), mxb = fmaxf(xb0, xb1);
+                mxa = fmaxf(mxa, __shfl_xor_sync(kFull, mxa, 1));
+                mxb = fmaxf(mxb, __shfl_xor_sync(kFull, mxb, 1));
+                mxa = fmaxf(mxa, __shfl_xor_sync(kFull, mxa, 2)) * p.scale_log2;
+                mxb = fmaxf(mxb, __shfl_xor_sync(kFull, mxb, 2)) * p.scale_log2;
+                // key 0 is always visible, so the row maxima are finite from the first tile on
+                const float mna = mxa > m_a + 8.f ? mxa : m_a, mnb = mxb > m_b + 8.f ? mxb : m_b;
+                const float alpha_a = ex2_approx(m_a - mna), alpha_b = ex2_approx(m_b - mnb);
+                m_a = mna;
+                m_b = mnb;
+                float la4[2] = {0.f, 0.f}, lb4[2] = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        sc[4 * k + e] = ex2_approx(fmaf(sc[4 * k + e], p.scale_log2, -m_a));
+                        sc[4 * k + 2 + e] = ex2_approx(fmaf(sc[4 * k + 2 + e], p.scale_log2, -m_b));
+                        la4[e] += sc[4 * k + e];
+                        lb4[e] += sc[4 * k + 2 + e];
+                    }
+                l_a = l_a * alpha_a + (la4[0] + la4[1]);
+                l_b = l_b * alpha_b + (lb4[0] + lb4[1]);
+                // the weights over the scores (all of them in registers by now): pair 4k + c4
+                // of P_hi in column 4k + c4, of P_lo in column 64 + 4k + c4, 64 keys at a time
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    uint32_t phi[16], plo[16];
+                    uint32_t ph[16], pl[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        split_bf16x2(sc[32 * q + 2 * e], sc[32 * q + 2 * e + 1], phi[e], plo[e]);
-                    tmem_st16(scol + 16 * q, phi);
-                    tmem_st16(scol + 32 + 16 * q, plo);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int k = 8 * q + kk;
+                        split_bf16x2(sc[4 * k], sc[4 * k + 1], ph[2 * kk], pl[2 * kk]);
+                        split_bf16x2(sc[4 * k + 2], sc[4 * k + 3], ph[2 * kk + 1], pl[2 * kk + 1]);
+                    }
+                    tmem_st_16x128b_x8(scol + 32 * q, ph);
+                    tmem_st_16x128b_x8(scol + 64 + 32 * q, pl);
                 }
                 // a rescale of O waits for the previous P.V of this query tile (and so every
                 // earlier one): O is then current, and this tile's P.V waits for its P
-                if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
-                    const int qb = (g - 1) % NSP;
-                    ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kPFree + qb), ((g - 1) / NSP) & 1, abort, p.err));
+                if (j > 0 && __any_sync(kFull, alpha_a != 1.f || alpha_b != 1.f)) {
+                    const int qb2 = (g - 1) % NSP;
+                    ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kPFree + qb2), ((g - 1) / NSP) & 1, abort, p.err));
                     if (!ok) continue;
                     tc_fence_after_sync();
-                    // this half rescales columns D/2 h .. D/2 h + D/2 - 1 of its rows
 #pragma unroll
                     for (int cc = 0; cc < D / 64; ++cc) {
                         uint32_t ov[32];
-                        tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
+                        tmem_ld_16x256b_x8(ocol + cc * 64, ov);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
+                        for (int k = 0; k < 8; ++k) {
+                            ov[4 * k] = __float_as_uint(__uint_as_float(ov[4 * k]) * alpha_a);
+                            ov[4 * k + 1] = __float_as_uint(__uint_as_float(ov[4 * k + 1]) * alpha_a);
+                            ov[4 * k + 2] = __float_as_uint(__uint_as_float(ov[4 * k + 2]) * alpha_b);
+                            ov[4 * k + 3] = __float_as_uint(__uint_as_float(ov[4 * k + 3]) * alpha_b);
+                        }
+                        tmem_st_16x256b_x8(ocol + cc * 64, ov);
                     }
                 }
                 tmem_st_wait();
@@ -493,14 +503,22 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(Cfg::kPFull + pb));
             }
-            // the row's maximum and this half's sum for the epilogue warps (the buffer was
-            // read by them two query tiles ago)
+            // the rows' sums over their four threads, and the maxima, for the epilogue warps
+            // (the buffer was read by them two query tiles ago)
+            l_a += __shfl_xor_sync(kFull, l_a, 1);
+            l_b += __shfl_xor_sync(kFull, l_b, 1);
+            l_a += __shfl_xor_sync(kFull, l_a, 2);
+            l_b += __shfl_xor_sync(kFull, l_b, 2);
             const int sbuf = cnt & 1;
             if (ok && cnt >= 2)
                 ok = __all_sync(kFull, wait_or_abort(bar(Cfg::kStFree + sbuf), ((cnt - 2) >> 1) & 1, abort, p.err));
             if (ok) {
-                if (h == 0) stats[(sbuf * 3) * BM + r] = m_ref;
-                stats[(sbuf * 3 + 1 + h) * BM + r] = l;
+                if (c4 == 0) {
+                    stats[(sbuf * 2) * BM + ra] = m_a;
+                    stats[(sbuf * 2 + 1) * BM + ra] = l_a;
+                    stats[(sbuf * 2) * BM + rb] = m_b;
+                    stats[(sbuf * 2 + 1) * BM + rb] = l_b;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(Cfg::kStFull + sbuf));
             }
@@ -520,8 +538,8 @@ __global__ void __launch_bounds__(512, 1)
                  __all_sync(kFull, wait_or_abort(bar(Cfg::kODone), cnt & 1, abort, p.err));
             if (!ok) break;
             tc_fence_after_sync();
-            const float m = stats[(sbuf * 3) * BM + r];
-            const float lr = stats[(sbuf * 3 + 1) * BM + r] + stats[(sbuf * 3 + 2) * BM + r];
+            const float m = stats[(sbuf * 2) * BM + r];
+            const float lr = stats[(sbuf * 2 + 1) * BM + r];
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Cfg::kStFree + sbuf));
             const float inv_l = 1.f / lr;
