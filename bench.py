@@ -797,6 +797,7 @@ def measure(name, wl, args, device, world, rank, steps, warmup, soak, with_e2e=T
                              "achieved": ach, "peak": bf16, "unit": "TFLOP/s", "frac": ach / bf16,
                              "peak_source": "measured bf16_tflops (burst)" if peak_kind == "measured"
                              else "fallback 1.9 PFLOP/s",
+                             "frac_of_sustained": ach / bf16_sus, "peak_sustained": bf16_sus,
                              "algorithmic_flops_per_launch": flops, "avg_launch_ms": kern_avg_ms,
                              "traffic": traffic, "kernel_source_sha256_16": src},
             })
@@ -813,6 +814,8 @@ def measure(name, wl, args, device, world, rank, steps, warmup, soak, with_e2e=T
             "roofline": {"bound": "tensor", "kernel": "prefill_attention (cache write + attention)",
                          "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
                          "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                         # the step loop runs seconds under the power cap: the sustained GEMM rate
+                         "frac_of_sustained": achieved / bf16_sus, "peak_sustained": bf16_sus,
                          "avg_launch_ms": kern_avg_ms,
                          "traffic": profiled_traffic("prefill.md", src), "kernel_source_sha256_16": src},
         })
