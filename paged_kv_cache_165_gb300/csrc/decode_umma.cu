@@ -22,17 +22,17 @@
 //     S_t goes into the buffer S_{t-2} leaves once P_{t-2} is written (S_{t-2} has been
 //     read), so the tensor core computes the next scores while the softmax runs; with one
 //     issuer per kind, the waits of one overlap the MMAs of the other.
-//   warps 0-7 (softmax): row r of the 128-row tile is tensor-memory lane r, shared by
-//     warps w and w+4 (w = r / 32); warp half h = w / 4 takes keys 64h .. 64h+63 of each
-//     tile.  Row 2s holds the bf16 rounding of query slot s ("hi"), row 2s+1 the bf16
-//     rounding of the remainder ("lo"), so s = S[2s] + S[2s+1] carries q to about 2^-16
-//     relative.  The two rows sit in lanes 2s and 2s+1 of a warp: each lane takes half of
-//     its warp's 64 keys and receives the partner row's values for them by one shuffle per
-//     key; the row maximum is shared by a shuffle and, between the two warps, through
-//     shared memory.  The weights go back to tensor memory as hi (row 2s) and lo (row 2s+1)
-//     bf16 parts, so O[2s] + O[2s+1] = sum_t P_t V_t to about 2^-16 relative as well.  O
-//     rows are rescaled in tensor memory only when the running maximum grew by more than
-//     2^8.
+//   warps 0-7 (softmax): row r of the 128-row tile is tensor-memory lane r.  Query slot
+//     s = 8g + i (g = 0 .. 7, i = 0 .. 7) has two rows in lane group g (lanes 16g .. 16g +
+//     15): row 16g + i holds the bf16 rounding of the query ("hi"), row 16g + 8 + i the bf16
+//     rounding of the remainder ("lo"), so s = S_hi + S_lo carries q to about 2^-16
+//     relative.  Warp w reads lane group 2 (w % 4) + w / 4 with the 16-lane shapes: thread
+//     t holds both rows of slot 8g + t / 4 and, of each key tile, the key pairs 4k + t % 4
+//     (keys 8k + 2 (t % 4), + 1), so it adds the two parts itself; the four threads of a
+//     slot share its maximum and sum by two shuffles, and the warps run independently.  The
+//     weights go back to tensor memory as hi (the hi row) and lo (the lo row) bf16 parts,
+//     so O_hi + O_lo = sum_t P_t V_t to about 2^-16 relative as well.  O rows are rescaled
+//     in tensor memory only when the running maximum grew by more than 2^8.
 // A chunk writes a normalised partial and its base-2 log-sum-exp into the workspace,
 // merged by the merge kernel of decode.cu (or, for a single chunk, the output).  Every wait
 // is bounded and shares an abort flag: on a timeout the block drains the copies and MMAs
@@ -62,8 +62,7 @@ struct UmmaDecodeCfg {
                          kSFull = 1 + 2 * NKT + 2 * NVT, kPFull = kSFull + 2, kODone = kPFull + 1,
                          kDone = kODone + 1, kDrain = kDone + 1, kNumBars = kDrain + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;          // TMEM slot, abort flag
-    static constexpr int kOffXch = (kOffMisc + 16 + 15) / 16 * 16;   // [warp half][value, ok][128]
-    static constexpr int kSmemBytes = 1024 + kOffXch + 4 * kBM * 4;
+    static constexpr int kSmemBytes = 1024 + kOffMisc + 16;
     // tensor memory: two S buffers, O, P, Q
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 0, kOCol = 2 * kTK, kPCol = kOCol + D, kQCol = kPCol + kTK / 2;
@@ -88,7 +87,6 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::kOffMisc + 4);
-    float *xch = reinterpret_cast<float *>(smem + Cfg::kOffXch);
     auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -322,43 +320,47 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
     } else {
-        // ---- softmax: thread (w, lane) owns tensor-memory lane r = 32 (w % 4) + lane, keys
-        // 64h .. 64h + 63 of each tile (h = w / 4), of which lane parity `part` takes 32
-        const int h = warp >> 2;
-        const int r = ((warp & 3) << 5) | lane;
-        const int slot = r >> 1, part = r & 1;
-        const bool slot_ok = slot < slots;
-        // this row's query position and visible keys [lo_r, hi_r)
-        const int pos_r = P0 + (slot_ok ? slot / p.m : 0);
-        const int lo_r = max(kv0, p.window > 0 ? max(0, pos_r + 1 - p.window) : 0);
-        const int hi_r = min(pos_r + 1, apg1 * BS);
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4
-        float *xv = xch;                       // [half][128]: maxima, then sums
-        float *xo = xch + 2 * BM;              // [half][128]: the half is still ok
-
-        // Q row r in tensor memory (hi or lo part of slot r/2): warp half h writes d = D/2 h
-        // .. D/2 h + D/2 - 1, i.e. columns D/4 h .. D/4 h + D/4 - 1 (two values a column)
+        // ---- softmax.  First the queries: thread (w, lane) writes tensor-memory lane r =
+        // 32 (w % 4) + lane (the hi or lo row of one query slot), columns D/4 h .. D/4 h +
+        // D/4 - 1 (two values a column) of it for h = w / 4
         {
-            const float *qrow = p.q + row_of(slot_ok ? slot : 0) * D + h * (D / 2);
+            const int h = warp >> 2;
+            const int r = ((warp & 3) << 5) | lane;
+            const int qslot = 8 * (r >> 4) + (r & 7), qpart = (r >> 3) & 1;
+            const bool qok = qslot < slots;
+            const uint32_t qbase = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const float *qrow = p.q + row_of(qok ? qslot : 0) * D + h * (D / 2);
             uint32_t w[D / 4];
 #pragma unroll
             for (int e = 0; e < D / 8; ++e) {
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (slot_ok) x = __ldg(reinterpret_cast<const float4 *>(qrow + 4 * e));
+                if (qok) x = __ldg(reinterpret_cast<const float4 *>(qrow + 4 * e));
                 uint32_t hi, lo;
                 split_bf16x2(x.x, x.y, hi, lo);
-                w[2 * e] = part ? lo : hi;
+                w[2 * e] = qpart ? lo : hi;
                 split_bf16x2(x.z, x.w, hi, lo);
-                w[2 * e + 1] = part ? lo : hi;
+                w[2 * e + 1] = qpart ? lo : hi;
             }
-            if constexpr (D == 128) tmem_st32(lane_base + Cfg::kQCol + h * (D / 4), w);
-            else tmem_st16(lane_base + Cfg::kQCol + h * (D / 4), w);
+            if constexpr (D == 128) tmem_st32(qbase + Cfg::kQCol + h * (D / 4), w);
+            else tmem_st16(qbase + Cfg::kQCol + h * (D / 4), w);
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Cfg::kQ));
         }
+
+        // Then per key tile: thread t of warp w owns slot `slot` = 8 g + t / 4 of lane group
+        // g = 2 (w % 4) + w / 4 (its hi row is lane 16 g + t / 4 of the group's base, its lo
+        // row 8 lanes further) and the key pairs 4k + c4 (c4 = t % 4) of the tile
+        const int c4 = lane & 3;
+        const int grp = 2 * (warp & 3) + (warp >> 2);
+        const int slot = 8 * grp + (lane >> 2);
+        const bool slot_ok = slot < slots;
+        // this slot's query position and visible keys [lo_r, hi_r)
+        const int pos_r = P0 + (slot_ok ? slot / p.m : 0);
+        const int lo_r = max(kv0, p.window > 0 ? max(0, pos_r + 1 - p.window) : 0);
+        const int hi_r = min(pos_r + 1, apg1 * BS);
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(16 * grp) << 16);
 
         // The chunk's last page may end inside the sequence's last block: its V rows past
         // the end hold whatever the slots hold (NaN, Inf) and must be zero for P.V.
@@ -367,31 +369,14 @@ __global__ void __launch_bounds__(384, 1)
         const int tail_row0 = ((pages - 1) % PPT) * BS + tail_valid;
         const int tail_rows = BS - tail_valid;
         float m_ref = -INFINITY, l = 0.f;
-        // ok is warp-uniform, and after each tile's exchange the same in both warps of a
-        // pair: a failed wait skips the remaining work but never a named barrier
+        // ok is warp-uniform; a failed wait skips the remaining work of this warp
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int sb = j & 1;
             if (ok) ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kSFull + sb), (j >> 1) & 1, abort, p.err));
-            // keys 64h + 32 part .. + 31: own row plus the partner row, by one shuffle a key
-            float sc[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) sc[c] = -INFINITY;
-            if (ok) {
-                tc_fence_after_sync();
-                uint32_t s0[32], s1[32];
-                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64, s0);
-                tmem_ld32(lane_base + Cfg::kSCol + sb * TK + h * 64 + 32, s1);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float mine = __uint_as_float(part ? s1[c] : s0[c]);
-                    const float send = __uint_as_float(part ? s0[c] : s1[c]);
-                    sc[c] = mine + __shfl_xor_sync(kFullMask, send, 1);
-                }
-            }
             if (ok && j == tail_tile && tail_rows > 0) {
-                // once the V copies of this tile have landed
+                // once the V copies of this tile have landed (each softmax warp zeroes its
+                // share of the rows, so each waits)
                 ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kVFull + j % NVT), (j / NVT) & 1, abort, p.err));
                 if (ok) {
                     uint8_t *vt = smem + Cfg::kOffV + (j % NVT) * Cfg::kSlotBytes;
@@ -403,28 +388,40 @@ __global__ void __launch_bounds__(384, 1)
                     fence_proxy_async_smem();
                 }
             }
-            const int key0 = tok0 + j * TK + h * 64 + part * 32;
+            if (!ok) continue;
+            tc_fence_after_sync();
+            // sc[2k + e]: the slot's score of key 8k + 2 c4 + e of the tile (hi + lo rows)
+            float sc[32];
+            {
+                uint32_t s0[32], s1[32];
+                tmem_ld_16x256b_x8(lane_base + Cfg::kSCol + sb * TK, s0);
+                tmem_ld_16x256b_x8(lane_base + Cfg::kSCol + sb * TK + 64, s1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        sc[2 * k + e] = __uint_as_float(s0[4 * k + e]) + __uint_as_float(s0[4 * k + 2 + e]);
+                        sc[16 + 2 * k + e] = __uint_as_float(s1[4 * k + e]) + __uint_as_float(s1[4 * k + 2 + e]);
+                    }
+            }
+            const int key0 = tok0 + j * TK + 2 * c4;
             if (tok0 + j * TK < lo_r || tok0 + (j + 1) * TK > hi_r) {
-                // keys outside this row's [lo_r, hi_r): before its window, after its own
+                // keys outside this slot's [lo_r, hi_r): before its window, after its own
                 // position (causal), or past the end of the chunk
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (key0 + c < lo_r || key0 + c >= hi_r) sc[c] = -INFINITY;
+                for (int k = 0; k < 16; ++k)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (key0 + 8 * k + e < lo_r || key0 + 8 * k + e >= hi_r) sc[2 * k + e] = -INFINITY;
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
             float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
-            // the other warp half's maximum of this row, and whether it is still ok
-            xv[h * BM + r] = mx;
-            xo[h * BM + r] = ok ? 1.f : 0.f;
-            named_barrier(pair_bar, 64);
-            mx = fmaxf(mx, xv[(1 - h) * BM + r]) * p.scale_log2;
-            ok = ok && xo[(1 - h) * BM + r] != 0.f;
-            named_barrier(pair_bar, 64);   // xch is rewritten next tile
-            if (!ok) continue;
-            // a row that has seen no key yet keeps m = -inf and weight 0
+            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 2)) * p.scale_log2;
+            // a slot that has seen no key yet keeps m = -inf and weight 0
             const float m_new = mx > m_ref + 8.f ? mx : m_ref;
             const float alpha = m_new == m_ref ? 1.f : ex2_approx(m_ref - m_new);
             m_ref = m_new;
@@ -436,38 +433,31 @@ __global__ void __launch_bounds__(384, 1)
                 l4[c & 3] += sc[c];
             }
             l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-            uint32_t phi[16], plo[16];
+            // pair 4k + c4 of the weights: P_hi for the hi row, P_lo for the lo row
+            uint32_t pw[2][16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) split_bf16x2(sc[2 * e], sc[2 * e + 1], phi[e], plo[e]);
+            for (int k = 0; k < 16; ++k) split_bf16x2(sc[2 * k], sc[2 * k + 1], pw[k >> 3][2 * (k & 7)], pw[k >> 3][2 * (k & 7) + 1]);
             // P_{j-1} V_{j-1} must be done: the P columns are free and O is current
             if (j > 0) {
                 ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kODone), (j - 1) & 1, abort, p.err));
                 if (!ok) continue;
                 tc_fence_after_sync();
                 if (__any_sync(kFullMask, alpha != 1.f)) {
-                    // this warp half rescales columns D/2 h .. D/2 h + D/2 - 1 of its rows
+                    // both rows of the slot, D columns in 64-column pieces
 #pragma unroll
                     for (int cc = 0; cc < D / 64; ++cc) {
                         uint32_t ov[32];
-                        tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
+                        tmem_ld_16x256b_x8(lane_base + Cfg::kOCol + cc * 64, ov);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
+                        tmem_st_16x256b_x8(lane_base + Cfg::kOCol + cc * 64, ov);
                     }
                 }
             }
-            // row 2s gets P_hi and row 2s+1 P_lo of keys 64h .. 64h + 63 (32 columns): each
-            // lane keeps its own part of its 32 keys and trades the other part for the
-            // partner's
-            uint32_t pw[32];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const uint32_t got = __shfl_xor_sync(kFullMask, part ? phi[e] : plo[e], 1);
-                pw[e] = part ? got : phi[e];        // keys 64h + 2e, +1 (part 0's keys)
-                pw[16 + e] = part ? plo[e] : got;   // keys 64h + 32 + 2e, +1 (part 1's keys)
-            }
-            tmem_st32(lane_base + Cfg::kPCol + h * 32, pw);
+            // pair e of the hi and lo rows in column e: the 64 pairs in two 32-column stores
+            tmem_st_16x128b_x8(lane_base + Cfg::kPCol, pw[0]);
+            tmem_st_16x128b_x8(lane_base + Cfg::kPCol + 32, pw[1]);
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
@@ -475,41 +465,32 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (ok) ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kDone), 0, abort, p.err));
 
-        // ---- the row's sum over the four threads that hold it (the loop's last barrier
-        // ended every read of xch); O[2s] + O[2s+1] normalised
+        // ---- the slot's sum over its four threads; O_hi + O_lo normalised
         float lr = l + __shfl_xor_sync(kFullMask, l, 1);
-        xv[h * BM + r] = lr;
-        named_barrier(pair_bar, 64);
-        lr += xv[(1 - h) * BM + r];
-        // m = -inf: the row sees no key of this chunk (an empty partial)
+        lr += __shfl_xor_sync(kFullMask, lr, 2);
+        // m = -inf: the slot sees no key of this chunk (an empty partial)
         const bool empty = m_ref == -INFINITY;
         const float scale = empty ? 0.f : 1.f / lr;
         if (ok) {
             tc_fence_after_sync();
             const size_t bi = row_of(slot_ok ? slot : 0);
             float *dst = nc == 1 ? p.out + bi * D : p.ws_o + (bi * p.splits + split) * D;
-            // this warp half: columns D/2 h .. D/2 h + D/2 - 1, 32 at a time; lane 2s writes
-            // the first 16 of each 32, lane 2s+1 the last 16
+            // columns 8k + 2 c4, + 1 of each 64-column piece: the four threads of a slot
+            // write 32 contiguous bytes a step
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t ov[32];
-                tmem_ld32(lane_base + Cfg::kOCol + h * (D / 2) + cc * 32, ov);
+                tmem_ld_16x256b_x8(lane_base + Cfg::kOCol + cc * 64, ov);
                 tmem_ld_wait();
-                float sum[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sum[e] = __uint_as_float(ov[e]) * scale;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sum[e] += __shfl_xor_sync(kFullMask, sum[e], 1);
                 if (slot_ok) {
-                    float *o = dst + h * (D / 2) + cc * 32 + part * 16;
 #pragma unroll
-                    for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4 *>(o + e) =
-                            part ? make_float4(sum[16 + e], sum[17 + e], sum[18 + e], sum[19 + e])
-                                 : make_float4(sum[e], sum[e + 1], sum[e + 2], sum[e + 3]);
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<float2 *>(dst + cc * 64 + 8 * k + 2 * c4) =
+                            make_float2((__uint_as_float(ov[4 * k]) + __uint_as_float(ov[4 * k + 2])) * scale,
+                                        (__uint_as_float(ov[4 * k + 1]) + __uint_as_float(ov[4 * k + 3])) * scale);
                 }
             }
-            if (slot_ok && part == 0 && h == 0) {
+            if (slot_ok && c4 == 0) {
                 const float lse2 = empty ? -INFINITY : m_ref + log2f(lr);
                 if (nc == 1) {
                     if (p.lse != nullptr) p.lse[bi] = lse2 * kDecLn2;
