@@ -450,18 +450,27 @@ __global__ void __launch_bounds__(512, 1)
                 const float alpha_a = ex2_approx(m_a - mna), alpha_b = ex2_approx(m_b - mnb);
                 m_a = mna;
                 m_b = mnb;
-                float la4[2] = {0.f, 0.f}, lb4[2] = {0.f, 0.f};
+                // the key pairs of a row as packed fp32 pairs: one FMA and one add a pair
+                const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+                const float2 nma = make_float2(-m_a, -m_a), nmb = make_float2(-m_b, -m_b);
+                float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        sc[4 * k + e] = ex2_approx(fmaf(sc[4 * k + e], p.scale_log2, -m_a));
-                        sc[4 * k + 2 + e] = ex2_approx(fmaf(sc[4 * k + 2 + e], p.scale_log2, -m_b));
-                        la4[e] += sc[4 * k + e];
-                        lb4[e] += sc[4 * k + 2 + e];
-                    }
-                l_a = l_a * alpha_a + (la4[0] + la4[1]);
-                l_b = l_b * alpha_b + (lb4[0] + lb4[1]);
+                for (int k = 0; k < 16; ++k) {
+                    float2 xa = fma2(make_float2(sc[4 * k], sc[4 * k + 1]), sl2, nma);
+                    float2 xb = fma2(make_float2(sc[4 * k + 2], sc[4 * k + 3]), sl2, nmb);
+                    xa.x = ex2_approx(xa.x);
+                    xa.y = ex2_approx(xa.y);
+                    xb.x = ex2_approx(xb.x);
+                    xb.y = ex2_approx(xb.y);
+                    la = add2(la, xa);
+                    lb = add2(lb, xb);
+                    sc[4 * k] = xa.x;
+                    sc[4 * k + 1] = xa.y;
+                    sc[4 * k + 2] = xb.x;
+                    sc[4 * k + 3] = xb.y;
+                }
+                l_a = l_a * alpha_a + (la.x + la.y);
+                l_b = l_b * alpha_b + (lb.x + lb.y);
                 // the weights over the scores (all of them in registers by now): pair 4k + c4
                 // of P_hi in column 4k + c4, of P_lo in column 64 + 4k + c4, 64 keys at a time
 #pragma unroll
@@ -470,8 +479,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const int k = 8 * q + kk;
-                        split_bf16x2(sc[4 * k], sc[4 * k + 1], ph[2 * kk], pl[2 * kk]);
-                        split_bf16x2(sc[4 * k + 2], sc[4 * k + 3], ph[2 * kk + 1], pl[2 * kk + 1]);
+                        split_bf16x2_p(sc[4 * k], sc[4 * k + 1], ph[2 * kk], pl[2 * kk]);
+                        split_bf16x2_p(sc[4 * k + 2], sc[4 * k + 3], ph[2 * kk + 1], pl[2 * kk + 1]);
                     }
                     tmem_st_16x128b_x8(scol + 32 * q, ph);
                     tmem_st_16x128b_x8(scol + 64 + 32 * q, pl);
