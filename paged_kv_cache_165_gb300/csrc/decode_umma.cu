@@ -398,12 +398,16 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_ld_16x256b_x8(lane_base + Cfg::kSCol + sb * TK + 64, s1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        sc[2 * k + e] = __uint_as_float(s0[4 * k + e]) + __uint_as_float(s0[4 * k + 2 + e]);
-                        sc[16 + 2 * k + e] = __uint_as_float(s1[4 * k + e]) + __uint_as_float(s1[4 * k + 2 + e]);
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    const float2 a = add2(make_float2(__uint_as_float(s0[4 * k]), __uint_as_float(s0[4 * k + 1])),
+                                          make_float2(__uint_as_float(s0[4 * k + 2]), __uint_as_float(s0[4 * k + 3])));
+                    const float2 c = add2(make_float2(__uint_as_float(s1[4 * k]), __uint_as_float(s1[4 * k + 1])),
+                                          make_float2(__uint_as_float(s1[4 * k + 2]), __uint_as_float(s1[4 * k + 3])));
+                    sc[2 * k] = a.x;
+                    sc[2 * k + 1] = a.y;
+                    sc[16 + 2 * k] = c.x;
+                    sc[16 + 2 * k + 1] = c.y;
+                }
             }
             const int key0 = tok0 + j * TK + 2 * c4;
             if (tok0 + j * TK < lo_r || tok0 + (j + 1) * TK > hi_r) {
@@ -426,17 +430,24 @@ __global__ void __launch_bounds__(384, 1)
             const float alpha = m_new == m_ref ? 1.f : ex2_approx(m_ref - m_new);
             m_ref = m_new;
             const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            // the key pairs as packed fp32 pairs: one FMA and one add a pair
+            const float2 sl2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
+            float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                sc[c] = ex2_approx(fmaf(sc[c], p.scale_log2, neg_m));
-                l4[c & 3] += sc[c];
+            for (int k = 0; k < 16; ++k) {
+                float2 x = fma2(make_float2(sc[2 * k], sc[2 * k + 1]), sl2, nm2);
+                x.x = ex2_approx(x.x);
+                x.y = ex2_approx(x.y);
+                l2[k & 1] = add2(l2[k & 1], x);
+                sc[2 * k] = x.x;
+                sc[2 * k + 1] = x.y;
             }
-            l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+            l = l * alpha + ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y));
             // pair 4k + c4 of the weights: P_hi for the hi row, P_lo for the lo row
             uint32_t pw[2][16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) split_bf16x2(sc[2 * k], sc[2 * k + 1], pw[k >> 3][2 * (k & 7)], pw[k >> 3][2 * (k & 7) + 1]);
+            for (int k = 0; k < 16; ++k)
+                split_bf16x2_p(sc[2 * k], sc[2 * k + 1], pw[k >> 3][2 * (k & 7)], pw[k >> 3][2 * (k & 7) + 1]);
             // P_{j-1} V_{j-1} must be done: the P columns are free and O is current
             if (j > 0) {
                 ok = __all_sync(kFullMask, wait_or_abort(bar(Cfg::kODone), (j - 1) & 1, abort, p.err));

@@ -491,13 +491,19 @@ __global__ void __launch_bounds__(512, 1)
                 const float alpha = m_new == m_ref ? 1.f : ex2_approx(m_ref - m_new);
                 m_ref = m_new;
                 const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+                // the keys as packed fp32 pairs: one FMA and one add a pair
+                const float2 sl2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
+                float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    sc[c] = ex2_approx(fmaf(sc[c], p.scale_log2, neg_m));
-                    l4[c & 3] += sc[c];
+                for (int c = 0; c < 32; ++c) {
+                    float2 x = fma2(make_float2(sc[2 * c], sc[2 * c + 1]), sl2, nm2);
+                    x.x = ex2_approx(x.x);
+                    x.y = ex2_approx(x.y);
+                    l2[c & 1] = add2(l2[c & 1], x);
+                    sc[2 * c] = x.x;
+                    sc[2 * c + 1] = x.y;
                 }
-                l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+                l = l * alpha + ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y));
                 // the weights over this thread's own scores (already in registers), 32 keys at
                 // a time: P_hi of keys 2e, 2e + 1 in column e, P_lo in column 32 + e
 #pragma unroll
@@ -505,7 +511,7 @@ __global__ void __launch_bounds__(512, 1)
                     uint32_t phi[16], plo[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        split_bf16x2(sc[32 * q + 2 * e], sc[32 * q + 2 * e + 1], phi[e], plo[e]);
+                        split_bf16x2_p(sc[32 * q + 2 * e], sc[32 * q + 2 * e + 1], phi[e], plo[e]);
                     tmem_st16(scol + 16 * q, phi);
                     tmem_st16(scol + 32 + 16 * q, plo);
                 }
