@@ -674,6 +674,7 @@ __global__ void __launch_bounds__(32)
 // most one chunk were written directly by the attention kernel.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeMaxChunks = 4096;
+constexpr int kMergePrefetch = 6;   // even: the prefetched chunks keep the two sums' order
 
 __global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const DecodeKParams p, int d, int bs) {
@@ -691,6 +692,22 @@ __global__ void __launch_bounds__(kMergeThreads)
     if (nc <= 1) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *ls = p.ws_lse + bi * p.splits;
+    const float *po = p.ws_o + bi * p.splits * d;
+    const bool vec = d % 4 == 0 && (reinterpret_cast<uintptr_t>(p.ws_o) & 15) == 0;
+    const int width = vec ? d / 4 : d;          // threads per group (d <= 256)
+    const int G = kMergeThreads / width;        // groups
+    const int grp = tid / width, col = tid % width;
+    // the rows of this thread's first kMergePrefetch chunks, loaded before the weights are
+    // known so that their latency overlaps the weights' reductions
+    float4 pre[kMergePrefetch];
+    if (vec && grp < G) {
+#pragma unroll
+        for (int i = 0; i < kMergePrefetch; ++i) {
+            const int c = grp + i * G;
+            pre[i] = c < nc ? *reinterpret_cast<const float4 *>(po + static_cast<size_t>(c) * d + 4 * col)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
     float M = -INFINITY;
     for (int c = tid; c < nc; c += kMergeThreads) {
         w[c] = ls[c];
@@ -717,15 +734,20 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
     for (int i = 0; i < kMergeThreads / 32; ++i) L += red[i];
     const float il = 1.f / L;
-    const float *po = p.ws_o + bi * p.splits * d;
-    const bool vec = d % 4 == 0 && (reinterpret_cast<uintptr_t>(p.ws_o) & 15) == 0;
-    const int width = vec ? d / 4 : d;          // threads per group (d <= 256)
-    const int G = kMergeThreads / width;        // groups
-    const int grp = tid / width, col = tid % width;
     if (grp < G) {
         if (vec) {
             float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-            int c = grp;
+            // chunks grp + iG alternate between the two sums, as in the loop below
+#pragma unroll
+            for (int i = 0; i < kMergePrefetch; ++i) {
+                const int c = grp + i * G;
+                if (c < nc) {
+                    const float wx = w[c];
+                    float4 &a = (i & 1) ? a1 : a0;
+                    a.x += wx * pre[i].x; a.y += wx * pre[i].y; a.z += wx * pre[i].z; a.w += wx * pre[i].w;
+                }
+            }
+            int c = grp + kMergePrefetch * G;
             for (; c + G < nc; c += 2 * G) {
                 const float4 x = *reinterpret_cast<const float4 *>(po + static_cast<size_t>(c) * d + 4 * col);
                 const float4 y = *reinterpret_cast<const float4 *>(po + static_cast<size_t>(c + G) * d + 4 * col);
