@@ -761,13 +761,17 @@ __global__ void __launch_bounds__(256)
         int first = g0 >= 0 && g0 < n_members ? __ldg(p.group_seqs + g0) : -1;
         if (first < 0 || first >= p.B) first = b;   // (flagged below: the offsets or ids are bad)
         const int P = __ldg(p.kv_start + b), len = __ldg(p.context_lens + b);
-        bool good = g0 >= 0 && g0 < n_members && __ldg(p.group_seqs + g0) == first &&
-                    P == __ldg(p.kv_start + first) && P >= 0 && P % bs == 0 && P <= len - 1 && len <= p.MBS * bs;
-        for (int j = lane; good && j < P / bs; j += 32)
-            if (__ldg(p.block_table + static_cast<size_t>(b) * p.MBS + j) !=
-                __ldg(p.block_table + static_cast<size_t>(first) * p.MBS + j))
-                good = false;
-        if (!__all_sync(kFull, good) && lane == 0) raise_error(p.err, PKV_DEVERR_PREFIX);
+        const bool good = g0 >= 0 && g0 < n_members && __ldg(p.group_seqs + g0) == first &&
+                          P == __ldg(p.kv_start + first) && P >= 0 && P % bs == 0 && P <= len - 1 &&
+                          len <= p.MBS * bs;
+        // the leading blocks, compared without a test between loads so that they are in flight together
+        const int nb = good ? P / bs : 0;
+        const int32_t *tb = p.block_table + static_cast<size_t>(b) * p.MBS;
+        const int32_t *tf = p.block_table + static_cast<size_t>(first) * p.MBS;
+        int diff = 0;
+#pragma unroll 4
+        for (int j = lane; j < nb; j += 32) diff |= __ldg(tb + j) ^ __ldg(tf + j);
+        if (!__all_sync(kFull, good && diff == 0) && lane == 0) raise_error(p.err, PKV_DEVERR_PREFIX);
     }
     const size_t row = static_cast<size_t>(b) * p.Hq + hq;
     const size_t part = (static_cast<size_t>(member) * p.Hq + hq) * p.prefix_splits;
