@@ -9,8 +9,9 @@
 // (plumephp.com "KV Cache 优化与注意力机制加速" §4.2-§4.3), with query head i reading KV
 // head floor(i/m) (limoncc.com §3.3) and the online softmax of plumephp.com §2.2-§2.3.
 //
-// The design is the prefill kernel's (prefill.cu): one CTA per SM walking the work tiles
-// (128 query rows of one head of one sequence), 128-key tiles, sixteen warps.  What differs:
+// The design follows the prefill kernel's (prefill.cu): one CTA per SM walking the work
+// tiles (128 query rows of one head of one sequence), 128-key tiles, sixteen warps.  What
+// differs:
 //   - the queries are fp32: the epilogue warps split each into bf16 hi + lo parts and store
 //     them, 128-byte swizzled, as two shared-memory operand tiles; S = Q_hi K^T + Q_lo K^T
 //     (two passes over the head dimension) carries q to about 2^-16 relative.
@@ -185,10 +186,12 @@ __device__ __forceinline__ void pp_row(const DecodeKParams &p, const PPItem &w, 
 //     landed and the P.V three key tiles back (which read that buffer) is done; O += P_hi
 //     V_j + P_lo V_j (N = d), P read from the same buffer, the first product of a work tile
 //     once the epilogue warps have read the previous O.
-//   warps 0-7 (softmax): per key tile the prefill kernel's online softmax for row r =
-//     32 (w % 4) + lane over keys 64h .. 64h + 63 of the tile (h = w / 4), with the
-//     bottom-right causal mask; at the end of a work tile the row's maximum and partial sums
-//     go to the epilogue warps, and the softmax warps go on with the next tile.
+//   warps 0-7 (softmax): per key tile the online softmax for row r = 32 (w % 4) + lane over
+//     keys 64h .. 64h + 63 of the tile (h = w / 4; the two warps of a row share its maximum
+//     through shared memory), with the bottom-right causal mask; at the end of a work tile
+//     the row's maximum and partial sums go to the epilogue warps, and the softmax warps go
+//     on with the next tile.  (The prefill kernel's softmax on the 16-lane shapes measured
+//     slower here: this kernel's two query passes keep the tensor pipe the busier unit.)
 //   warps 12-15 (queries and epilogue): thread (w, lane) loads row r = 32 (w % 4) + lane of
 //     the next work tile's fp32 queries once the current tile's scores have all been
 //     computed, splits them into bf16 hi and lo parts and stores both as row r of the two

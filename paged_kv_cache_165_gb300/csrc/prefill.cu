@@ -6,14 +6,16 @@
 // aligned so that a query at position t sees keys 0..t, §13), with query head i reading
 // KV head floor(i/m) (limoncc.com "大语言模型研究15——注意力机制优化之KV缓存" §3.3).
 //
-// Tensor-core path (bf16, d in {64, 128}): 5th-generation tensor cores (tcgen05).  One
-// CTA per (query head, sequence, 128-query tile): TMA brings the Q tile once and 128-key
-// K/V tiles through two rings (128-byte swizzle, mbarrier completion with bounded waits);
-// one thread issues S = Q K^T into tensor memory (double-buffered), another O += P V into
-// a tensor-memory accumulator with P read from tensor memory; eight warps, two per query
-// row, run the online softmax (running max and sum, plumephp.com "KV Cache 优化与注意力
-// 机制加速" §2.2-§2.3) and write P back into tensor memory as bf16 hi + lo parts, so the
-// weights keep ~16 bits (details at prefill_tc_kernel).
+// Tensor-core path (bf16, d in {64, 128}): 5th-generation tensor cores (tcgen05), one
+// persistent CTA per SM walking the 128-query tiles of the launch, longest first.  TMA
+// brings each Q tile and 128-key K/V tiles through two rings (128-byte swizzle, mbarrier
+// completion with bounded waits); one thread issues S = Q K^T into one of three
+// tensor-memory buffers, another O += P V into a tensor-memory accumulator with P read
+// from the same buffer; eight warps, four threads per query row of one warp, run the online
+// softmax (running max and sum, plumephp.com "KV Cache 优化与注意力机制加速" §2.2-§2.3) and
+// write P over the scores as bf16 hi + lo parts, so the weights keep ~16 bits; four warps
+// write the output while the softmax goes on with the next tile (details at
+// prefill_tc_kernel).
 // Only key tiles at or below the diagonal are visited.
 // CUDA-core path (fp32 or other d): one warp per (query row, head).
 #include <math.h>
